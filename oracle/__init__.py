@@ -1,0 +1,248 @@
+"""ctypes wrapper around the C oracle (``kivi_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers; the product package never
+imports this module and shares no code with it.
+
+The oracle is built from source with the host C compiler the first time it is
+needed (or by :func:`build`), into ``oracle/_build/``.  fp16 tensors are passed
+as ``numpy.uint16`` arrays holding the IEEE binary16 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kivi_oracle.c")
+_HDR = os.path.join(_HERE, "kivi_oracle.h")
+_LIB = os.path.join(_HERE, "_build", "libkivi_oracle.so")
+# -ffp-contract=off: no fused multiply-add; -fno-fast-math: IEEE semantics,
+# no flush-to-zero, no reassociation.
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+          "-fPIC", "-shared", "-Wall", "-Wextra"]
+
+_lock = threading.Lock()
+_lib = None
+
+_u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
+_u32p = np.ctypeslib.ndpointer(np.uint32, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+_i64 = C.c_int64
+_i64p = C.POINTER(C.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library if it is missing or stale."""
+    stale = (not os.path.exists(_LIB) or
+             os.path.getmtime(_LIB) < max(os.path.getmtime(_SRC), os.path.getmtime(_HDR)))
+    if force or stale:
+        os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        cc = os.environ.get("CC", "gcc")
+        subprocess.run([cc, *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = build()
+            L = C.CDLL(path)
+            L.kivi_oracle_half_to_float.argtypes = [C.c_uint16]
+            L.kivi_oracle_half_to_float.restype = C.c_float
+            L.kivi_oracle_float_to_half.argtypes = [C.c_float]
+            L.kivi_oracle_float_to_half.restype = C.c_uint16
+            L.kivi_oracle_halves_to_floats.argtypes = [_u16p, _f32p, _i64]
+            L.kivi_oracle_halves_to_floats.restype = None
+            L.kivi_oracle_floats_to_halves.argtypes = [_f32p, _u16p, _i64]
+            L.kivi_oracle_floats_to_halves.restype = None
+            L.kivi_oracle_group_params.argtypes = [_f32p, _i64, C.c_int,
+                                                   C.POINTER(C.c_float), C.POINTER(C.c_float)]
+            L.kivi_oracle_group_params.restype = C.c_int
+            L.kivi_oracle_code.argtypes = [C.c_float, C.c_float, C.c_float, C.c_int]
+            L.kivi_oracle_code.restype = C.c_uint32
+            L.kivi_oracle_recon.argtypes = [C.c_uint32, C.c_float, C.c_float]
+            L.kivi_oracle_recon.restype = C.c_uint16
+            for name in ("kivi_oracle_quantize_keys", "kivi_oracle_quantize_values"):
+                f = getattr(L, name)
+                f.argtypes = [_u16p, _i64, _i64, _i64, C.c_int, C.c_int, _u32p, _f32p, _f32p]
+                f.restype = C.c_int
+            for name in ("kivi_oracle_dequantize_keys", "kivi_oracle_dequantize_values"):
+                f = getattr(L, name)
+                f.argtypes = [_u32p, _f32p, _f32p, _i64, _i64, _i64, C.c_int, C.c_int, _u16p]
+                f.restype = C.c_int
+            L.kivi_oracle_key_group.argtypes = [_u16p, _i64, _i64, _i64, _i64, C.c_int, C.c_int,
+                                                _u32p, C.POINTER(C.c_float), C.POINTER(C.c_float)]
+            L.kivi_oracle_key_group.restype = C.c_int
+            L.kivi_oracle_value_row.argtypes = [_u16p, _i64, C.c_int, C.c_int, _u32p, _f32p, _f32p]
+            L.kivi_oracle_value_row.restype = C.c_int
+            L.kivi_oracle_flush_size.argtypes = [_i64, C.c_int, C.c_int]
+            L.kivi_oracle_flush_size.restype = _i64
+            L.kivi_oracle_flush.argtypes = [_u16p, _u16p, _i64, _i64, _i64, _i64,
+                                            C.c_int, C.c_int, C.c_int,
+                                            _u32p, _f32p, _f32p, _u32p, _f32p, _f32p,
+                                            _i64p, _i64p, _i64p]
+            L.kivi_oracle_flush.restype = _i64
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (rc={rc})")
+
+
+def codes_per_word(bits: int) -> int:
+    return 32 // bits
+
+
+# --------------------------------------------------------------------------
+# scalar / element-wise helpers
+# --------------------------------------------------------------------------
+
+def half_to_float(h: np.ndarray) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, np.float32)
+    lib().kivi_oracle_halves_to_floats(h.reshape(-1), out.reshape(-1), h.size)
+    return out
+
+
+def float_to_half(f: np.ndarray) -> np.ndarray:
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    out = np.empty(f.shape, np.uint16)
+    lib().kivi_oracle_floats_to_halves(f.reshape(-1), out.reshape(-1), f.size)
+    return out
+
+
+def group_params(vals, bits: int):
+    v = np.ascontiguousarray(vals, dtype=np.float32).reshape(-1)
+    sc, ze = C.c_float(), C.c_float()
+    _check(lib().kivi_oracle_group_params(v, v.size, bits, C.byref(sc), C.byref(ze)),
+           "group_params")
+    return np.float32(sc.value), np.float32(ze.value)
+
+
+def code(x, scale, zero, bits: int) -> int:
+    return int(lib().kivi_oracle_code(float(x), float(scale), float(zero), bits))
+
+
+def recon(q: int, scale, zero) -> int:
+    return int(lib().kivi_oracle_recon(int(q), float(scale), float(zero)))
+
+
+# --------------------------------------------------------------------------
+# full-tensor operations
+# --------------------------------------------------------------------------
+
+def quantize_keys(x: np.ndarray, group: int, bits: int):
+    """x: uint16 [bh, s, d] -> (codes u32 [bh, ng*G/W, d], scale, zero f32 [bh, ng, d])."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    bh, s, d = x.shape
+    ng = -(-s // group)
+    codes = np.zeros((bh, ng * group // codes_per_word(bits), d), np.uint32)
+    scale = np.zeros((bh, ng, d), np.float32)
+    zero = np.zeros((bh, ng, d), np.float32)
+    _check(lib().kivi_oracle_quantize_keys(x, bh, s, d, group, bits, codes, scale, zero),
+           "quantize_keys")
+    return codes, scale, zero
+
+
+def quantize_values(x: np.ndarray, group: int, bits: int):
+    """x: uint16 [bh, s, d] -> (codes u32 [bh, s, d/W], scale, zero f32 [bh, s, d/G])."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    bh, s, d = x.shape
+    codes = np.zeros((bh, s, d // codes_per_word(bits)), np.uint32)
+    scale = np.zeros((bh, s, d // group), np.float32)
+    zero = np.zeros((bh, s, d // group), np.float32)
+    _check(lib().kivi_oracle_quantize_values(x, bh, s, d, group, bits, codes, scale, zero),
+           "quantize_values")
+    return codes, scale, zero
+
+
+def dequantize_keys(codes, scale, zero, s: int, group: int, bits: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    zero = np.ascontiguousarray(zero, dtype=np.float32)
+    bh, _, d = codes.shape
+    y = np.zeros((bh, s, d), np.uint16)
+    _check(lib().kivi_oracle_dequantize_keys(codes, scale, zero, bh, s, d, group, bits, y),
+           "dequantize_keys")
+    return y
+
+
+def dequantize_values(codes, scale, zero, group: int, bits: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    zero = np.ascontiguousarray(zero, dtype=np.float32)
+    bh, s, dw = codes.shape
+    d = dw * codes_per_word(bits)
+    y = np.zeros((bh, s, d), np.uint16)
+    _check(lib().kivi_oracle_dequantize_values(codes, scale, zero, bh, s, d, group, bits, y),
+           "dequantize_values")
+    return y
+
+
+def key_group(x_bh: np.ndarray, g: int, c: int, group: int, bits: int):
+    """One key group of a [s, d] slice: (words u32 [G/W], scale, zero)."""
+    x_bh = np.ascontiguousarray(x_bh, dtype=np.uint16)
+    s, d = x_bh.shape
+    words = np.zeros(group // codes_per_word(bits), np.uint32)
+    sc, ze = C.c_float(), C.c_float()
+    _check(lib().kivi_oracle_key_group(x_bh, s, d, g, c, group, bits, words,
+                                       C.byref(sc), C.byref(ze)), "key_group")
+    return words, np.float32(sc.value), np.float32(ze.value)
+
+
+def value_row(x_row: np.ndarray, group: int, bits: int):
+    """One value row [d]: (words u32 [d/W], scale f32 [d/G], zero f32 [d/G])."""
+    x_row = np.ascontiguousarray(x_row, dtype=np.uint16).reshape(-1)
+    d = x_row.size
+    words = np.zeros(d // codes_per_word(bits), np.uint32)
+    scale = np.zeros(d // group, np.float32)
+    zero = np.zeros(d // group, np.float32)
+    _check(lib().kivi_oracle_value_row(x_row, d, group, bits, words, scale, zero), "value_row")
+    return words, scale, zero
+
+
+def flush_size(n_res: int, residual: int, group: int) -> int:
+    return int(lib().kivi_oracle_flush_size(n_res, residual, group))
+
+
+class Store:
+    """Host-side quantized store of one layer (oracle layout, capacity ``cap`` tokens)."""
+
+    def __init__(self, bh: int, d: int, cap: int, group: int, bits: int):
+        w = codes_per_word(bits)
+        self.bh, self.d, self.cap, self.group, self.bits = bh, d, cap, group, bits
+        self.k_codes = np.zeros((bh, cap // w, d), np.uint32)
+        self.k_scale = np.zeros((bh, cap // group, d), np.float32)
+        self.k_zero = np.zeros((bh, cap // group, d), np.float32)
+        self.v_codes = np.zeros((bh, cap, d // w), np.uint32)
+        self.v_scale = np.zeros((bh, cap, d // group), np.float32)
+        self.v_zero = np.zeros((bh, cap, d // group), np.float32)
+
+
+def flush(k_res: np.ndarray, v_res: np.ndarray, store: Store, residual: int,
+          s_q: int, res_head: int, n_res: int):
+    """Flush one layer's residual ring into ``store``.
+
+    Returns ``(n_flushed, s_q, res_head, n_res)`` after the flush.
+    """
+    k_res = np.ascontiguousarray(k_res, dtype=np.uint16)
+    v_res = np.ascontiguousarray(v_res, dtype=np.uint16)
+    bh, r_cap, d = k_res.shape
+    a, b, c = C.c_int64(s_q), C.c_int64(res_head), C.c_int64(n_res)
+    n = lib().kivi_oracle_flush(k_res, v_res, bh, d, r_cap, store.cap, store.group,
+                                store.bits, residual, store.k_codes, store.k_scale,
+                                store.k_zero, store.v_codes, store.v_scale, store.v_zero,
+                                C.byref(a), C.byref(b), C.byref(c))
+    if n < 0:
+        raise ValueError(f"oracle flush rejected its arguments (rc={n})")
+    return int(n), a.value, b.value, c.value

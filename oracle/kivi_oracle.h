@@ -1,0 +1,125 @@
+/*
+ * kivi_oracle.h -- plain, single-threaded CPU oracle for the KIVI KV-cache flush.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this library: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code with the CUDA library.
+ *
+ * Sources (VeloxQuant-MLX documentation pages):
+ *   [POST]    blog post "How I fused KIVI's KV-cache quantization into two
+ *             bit-exact Metal kernels ..." (veloxquant-mlx.netlify.app/docs/blog)
+ *   [RELEASE] blog post "VeloxQuant-MLX 0.8.0 adds KIVI", section "What KIVI is"
+ *   [README]  VeloxQuant-MLX 0.24.1 project description (pypi.org),
+ *             section "KIVI -- tuning-free asymmetric 2-bit baseline"
+ *   [BITPACK] blog post on the library's Metal kernels, section
+ *             "Kernel 1: Bit-Packing" (LSB-first code order)
+ *
+ * Arithmetic: IEEE binary32 throughout, no fused multiply-add, no flush to
+ * zero, round-half-to-even.  Inputs and reconstructions are IEEE binary16,
+ * passed as raw uint16_t bit patterns.
+ *
+ * Layouts (all row-contiguous, bh = batch*kv_heads flattened):
+ *   x            fp16   [bh][s][d]
+ *   key codes    u32    [bh][ng*G/W][d]   word (bh, t/W, c) holds tokens
+ *                                         t..t+W-1 of channel c, token t at
+ *                                         bits [(t%W)*b, (t%W+1)*b)
+ *   key scale    f32    [bh][ng][d]       one (scale, zero) per channel per
+ *   key zero     f32    [bh][ng][d]       group of G tokens
+ *   value codes  u32    [bh][s][d/W]      word (bh, s, c/W) holds channels
+ *                                         c..c+W-1 of token s
+ *   value scale  f32    [bh][s][d/G]      one (scale, zero) per token per
+ *   value zero   f32    [bh][s][d/G]      group of G channels
+ * with W = 32/b codes per word and ng = ceil(s/G).
+ *
+ * Return values: 0 on success, -1 on an argument the operation does not
+ * define (bits not in {2,4,8}, G not in {32,64,128}, d not divisible as
+ * required, non-finite input).  Functions never allocate caller memory.
+ */
+#ifndef KIVI_ORACLE_H
+#define KIVI_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* binary16 <-> binary32 conversions written from the IEEE 754 format
+ * definition.  half -> float is exact; float -> half rounds to nearest,
+ * ties to even, and overflows to infinity. */
+float    kivi_oracle_half_to_float(uint16_t h);
+uint16_t kivi_oracle_float_to_half(float f);
+/* Element-wise array forms of the two conversions (n elements). */
+void kivi_oracle_halves_to_floats(const uint16_t *h, float *f, int64_t n);
+void kivi_oracle_floats_to_halves(const float *f, uint16_t *h, int64_t n);
+
+/* Asymmetric min/max parameters of one group of n fp32 values
+ * ([POST] "What we're actually optimizing"; [RELEASE] "What KIVI is"):
+ *   zero = min(group), scale = (max(group) - min(group)) / (2^bits - 1).
+ * min and max are canonicalised so that a zero extreme is +0. */
+int kivi_oracle_group_params(const float *vals, int64_t n, int bits,
+                             float *scale, float *zero);
+
+/* Code of one value: q = clip(round_half_even((x - zero) / scale), 0, 2^b-1),
+ * q = 0 when scale == 0.  Returns 0xFFFFFFFF for an invalid bit width. */
+uint32_t kivi_oracle_code(float x, float scale, float zero, int bits);
+
+/* Reconstruction of one code: fp16(round(round(q*scale) + zero)) with two
+ * separately rounded binary32 operations ([POST] "1. FMA contraction"). */
+uint16_t kivi_oracle_recon(uint32_t q, float scale, float zero);
+
+/* Full-tensor operations on contiguous buffers (layouts above). */
+int kivi_oracle_quantize_keys(const uint16_t *x, int64_t bh, int64_t s, int64_t d,
+                              int group, int bits,
+                              uint32_t *codes, float *scale, float *zero);
+int kivi_oracle_quantize_values(const uint16_t *x, int64_t bh, int64_t s, int64_t d,
+                                int group, int bits,
+                                uint32_t *codes, float *scale, float *zero);
+int kivi_oracle_dequantize_keys(const uint32_t *codes, const float *scale,
+                                const float *zero, int64_t bh, int64_t s, int64_t d,
+                                int group, int bits, uint16_t *y);
+int kivi_oracle_dequantize_values(const uint32_t *codes, const float *scale,
+                                  const float *zero, int64_t bh, int64_t s, int64_t d,
+                                  int group, int bits, uint16_t *y);
+
+/* One key group (channel c, token group g) of one bh slice x_bh [s][d]:
+ * writes G/W code words (token order), its scale and zero.  Lets tests check
+ * sampled outputs of tensors too large for the full-tensor calls. */
+int kivi_oracle_key_group(const uint16_t *x_bh, int64_t s, int64_t d,
+                          int64_t g, int64_t c, int group, int bits,
+                          uint32_t *words, float *scale, float *zero);
+/* One value row (token s of x_bh [s][d]): writes d/W words and d/G scales
+ * and zeros. */
+int kivi_oracle_value_row(const uint16_t *x_row, int64_t d, int group, int bits,
+                          uint32_t *words, float *scale, float *zero);
+
+/* Residual-window flush size ([POST] "What we're actually optimizing": the
+ * newest residual tokens stay fp16, aged-out tokens are quantized as a batch;
+ * pinned by the "flush/layer" column of the [POST] Generation 1 table):
+ *   n_flush = floor((n_res - R) / G) * G  if n_res >= R + G, else 0. */
+int64_t kivi_oracle_flush_size(int64_t n_res, int residual, int group);
+
+/* Flush of one layer (keys and values) from an fp16 residual ring into the
+ * quantized store.
+ *   k_res, v_res   fp16 [bh][r_cap][d]; logical residual token i (0 = oldest)
+ *                  sits at ring row (res_head + i) % r_cap
+ *   store          key codes [bh][cap/W][d], key scale/zero [bh][cap/G][d],
+ *                  value codes [bh][cap][d/W], value scale/zero [bh][cap][d/G]
+ *   *s_q           tokens already in the store (multiple of G); advanced
+ *   *res_head      ring row of the oldest residual token; advanced
+ *   *n_res         residual token count; reduced
+ * The oldest n_flush tokens are quantized (keys per channel, values per
+ * token) and written at store token offset *s_q.  Returns the number of
+ * tokens flushed, or -1 (invalid arguments) / -3 (store capacity exceeded). */
+int64_t kivi_oracle_flush(const uint16_t *k_res, const uint16_t *v_res,
+                          int64_t bh, int64_t d, int64_t r_cap, int64_t cap,
+                          int group, int bits, int residual,
+                          uint32_t *k_codes, float *k_scale, float *k_zero,
+                          uint32_t *v_codes, float *v_scale, float *v_zero,
+                          int64_t *s_q, int64_t *res_head, int64_t *n_res);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KIVI_ORACLE_H */
