@@ -1,0 +1,254 @@
+/*
+ * kivi.h -- C ABI of the GB300 KIVI KV-cache codec (libkivi.so).
+ *
+ * KIVI quantizes keys per channel and values per token with asymmetric
+ * min/max groups, keeps the newest tokens in fp16 and folds aged-out tokens
+ * into a compressed store (VeloxQuant-MLX blog post "How I fused KIVI's
+ * KV-cache quantization into two bit-exact Metal kernels ...", sections
+ * "What we're actually optimizing" and "The layout problem that shapes
+ * everything"; release post "VeloxQuant-MLX 0.8.0 adds KIVI", section "What
+ * KIVI is").  For every group:
+ *
+ *     zero  = min(group)                      (binary32; a zero extreme is +0)
+ *     scale = (max(group) - min(group)) / (2^bits - 1)      (IEEE division)
+ *     q     = clip(round_half_even((x - zero) / scale), 0, 2^bits - 1)
+ *             (q = 0 when scale == 0, i.e. max == min)
+ *     recon = fp16_rn( fp32(q * scale) + zero )   (two roundings, no FMA)
+ *
+ * All arithmetic is IEEE binary32 and matches the CPU oracle bit for bit.
+ *
+ * Tensors are row-contiguous [bh][s][d] IEEE binary16 (bh = batch * kv_heads,
+ * s = tokens, d = head_dim), element (b, t, c) at b*bh_stride + t*d + c.
+ * With G = group, b = bits, W = 32 / b codes per uint32 word and
+ * ng = ceil(s / G):
+ *
+ *   keys    codes  u32 [bh][ng*G/W][d]  word (b, t/W, c) holds tokens t..t+W-1
+ *                                       of channel c; token t at bits
+ *                                       [(t%W)*b, (t%W+1)*b) (LSB first)
+ *           scale  f32 [bh][ng][d]      one (scale, zero) per channel per
+ *           zero   f32 [bh][ng][d]      group of G tokens
+ *   values  codes  u32 [bh][s][d/W]     word (b, t, c/W) holds channels
+ *                                       c..c+W-1 of token t (LSB first)
+ *           scale  f32 [bh][s][d/G]     one (scale, zero) per token per
+ *           zero   f32 [bh][s][d/G]     group of G channels
+ *
+ * A key group that runs past the last token is padded by repeating the last
+ * token (fused-kernel post, "3. Padding semantics"); its padding slots hold
+ * that token's code.
+ *
+ * Common rules for every call:
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *     the library allocates no device or host memory and keeps no pointer
+ *     after the call returns.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
+ *     outputs are complete when the stream reaches that point.  Calls that
+ *     overlap on the GPU with writes to their inputs or outputs race.
+ *   - Supported: bits in {2, 4, 8}; group in {32, 64, 128}; 8 <= d <= 256
+ *     with d % 8 == 0 for keys and d % group == 0 for values.
+ *   - Alignment (KIVI_ERR_ALIGN otherwise): every base pointer 16-byte
+ *     aligned; bh strides of fp16 tensors and of key codes multiples of 16
+ *     bytes; key scale/zero bh strides multiples of 8 bytes (16 for
+ *     dequantization); value code bh strides multiples of 8 bytes at 2 bits
+ *     and 16 bytes at 4 and 8 bits; value scale/zero strides unrestricted.
+ *     The contiguous layouts above always satisfy these rules.
+ *   - Arguments are validated on the host before any launch; a call that
+ *     returns an error launched nothing and wrote nothing.  bh == 0 or
+ *     s == 0 is a valid empty call.
+ *   - Inputs must be finite; results for NaN or infinite inputs are
+ *     unspecified (but every write stays inside the stated output ranges).
+ */
+#ifndef KIVI_H
+#define KIVI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of this header are the library's only exported symbols. */
+#if defined(__GNUC__)
+#define KIVI_API __attribute__((visibility("default")))
+#else
+#define KIVI_API
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *kivi_stream_t;
+
+typedef enum {
+    KIVI_OK = 0,
+    KIVI_ERR_INVAL = 1,     /* argument outside the supported set */
+    KIVI_ERR_ALIGN = 2,     /* pointer or bh stride breaks 16-byte alignment */
+    KIVI_ERR_CAPACITY = 3,  /* flush would overrun the store */
+    KIVI_ERR_CUDA = 4       /* a CUDA runtime call failed; see kivi_last_cuda_error */
+} kivi_status;
+
+/* Most layers one batched call takes (kivi_flush, kivi_dequantize_cache). */
+#define KIVI_MAX_LAYERS 128
+
+/* ------------------------------------------------------------------------ */
+/* Full-tensor quantization                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Keys, quantized per channel over groups of `group` tokens (fused-kernel
+ * post, "The layout problem": the group runs along the strided token axis).
+ *   x        device fp16 [bh][s][d], bh stride x_bh_stride >= s*d elements
+ *   codes    device u32, bh stride codes_bh_stride >= ng*group/W*d words
+ *   scale,   device f32, bh stride sz_bh_stride >= ng*d floats
+ *   zero
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_quantize_keys(const void *x, int64_t bh, int64_t s, int64_t d,
+                               int64_t x_bh_stride, int group, int bits,
+                               uint32_t *codes, int64_t codes_bh_stride,
+                               float *scale, float *zero, int64_t sz_bh_stride,
+                               kivi_stream_t stream);
+
+/* Values, quantized per token over groups of `group` channels (the group
+ * runs along the contiguous head_dim axis).
+ *   x        device fp16 [bh][s][d], bh stride x_bh_stride >= s*d elements
+ *   codes    device u32, bh stride codes_bh_stride >= s*d/W words
+ *   scale,   device f32, bh stride sz_bh_stride >= s*d/group floats
+ *   zero
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_quantize_values(const void *x, int64_t bh, int64_t s, int64_t d,
+                                 int64_t x_bh_stride, int group, int bits,
+                                 uint32_t *codes, int64_t codes_bh_stride,
+                                 float *scale, float *zero, int64_t sz_bh_stride,
+                                 kivi_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Dequantization (fused-kernel post, "1. FMA contraction": the product is  */
+/* rounded before the add)                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Keys: codes/scale/zero in the key layout above (same strides as the
+ * quantize call) -> y device fp16 [bh][s][d], bh stride y_bh_stride >= s*d.
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_dequantize_keys(const uint32_t *codes, int64_t codes_bh_stride,
+                                 const float *scale, const float *zero,
+                                 int64_t sz_bh_stride, int64_t bh, int64_t s, int64_t d,
+                                 int group, int bits, void *y, int64_t y_bh_stride,
+                                 kivi_stream_t stream);
+
+/* Values: codes/scale/zero in the value layout above -> y fp16 [bh][s][d].
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_dequantize_values(const uint32_t *codes, int64_t codes_bh_stride,
+                                   const float *scale, const float *zero,
+                                   int64_t sz_bh_stride, int64_t bh, int64_t s, int64_t d,
+                                   int group, int bits, void *y, int64_t y_bh_stride,
+                                   kivi_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Residual window and flush                                                */
+/* ------------------------------------------------------------------------ */
+
+/* One layer's buffers (all device, caller-owned, contiguous per bh):
+ *   k_res, v_res   fp16 [bh][r_cap][d] residual rings: logical residual
+ *                  token i (0 = oldest) lives at ring row (res_head + i) % r_cap
+ *   k_codes        u32 [bh][cap/W][d]      store, key layout with s = cap
+ *   k_scale,k_zero f32 [bh][cap/G][d]
+ *   v_codes        u32 [bh][cap][d/W]      store, value layout with s = cap
+ *   v_scale,v_zero f32 [bh][cap][d/G] */
+typedef struct {
+    const void *k_res;
+    const void *v_res;
+    uint32_t *k_codes;
+    float *k_scale;
+    float *k_zero;
+    uint32_t *v_codes;
+    float *v_scale;
+    float *v_zero;
+} kivi_layer;
+
+/* Geometry and state shared by every layer of a cache (every layer flushes
+ * together).  r_cap and cap are multiples of `group`; s_q and res_head stay
+ * multiples of `group`; 0 <= n_res <= r_cap. */
+typedef struct {
+    int64_t bh, d;        /* batch * kv_heads, head_dim */
+    int64_t r_cap;        /* residual ring capacity, tokens */
+    int64_t cap;          /* store capacity, tokens */
+    int32_t group, bits;  /* group size G, code width b */
+    int32_t residual;     /* R: newest tokens kept fp16 */
+    int32_t reserved;     /* must be 0 */
+    int64_t s_q;          /* tokens in the store */
+    int64_t res_head;     /* ring row of the oldest residual token */
+    int64_t n_res;        /* tokens in the residual ring */
+} kivi_cache;
+
+/* Tokens one flush moves: floor((n_res - residual) / group) * group when
+ * n_res >= residual + group, else 0 (fused-kernel post, "What we're actually
+ * optimizing": the newest residual tokens stay fp16 and whole groups of
+ * aged-out tokens are quantized as a batch; the "flush/layer" column of its
+ * "Generation 1" table fixes the rule).  Returns -1 for a negative argument
+ * or group <= 0. */
+KIVI_API int64_t kivi_flush_size(int64_t n_res, int residual, int group);
+
+/* Flush: quantize the oldest kivi_flush_size(n_res, residual, group) residual
+ * tokens of every layer (keys per channel, values per token) into the store
+ * at token offset s_q, then advance the state: s_q += n, res_head =
+ * (res_head + n) % r_cap, n_res -= n.  The residual rings are only read; no
+ * token is copied.  `layers` is a host array of n_layers (1..KIVI_MAX_LAYERS)
+ * entries; `cache` is host memory updated in place on success; `n_flushed`
+ * (host, may be NULL) receives n.  n == 0 launches nothing.
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN, KIVI_ERR_CAPACITY (state
+ * unchanged, nothing launched) or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_flush(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                       int64_t *n_flushed, kivi_stream_t stream);
+
+/* Dequantize the first cache->s_q tokens of every layer's store into
+ * k_out[l], v_out[l] (host arrays of n_layers device pointers, each fp16
+ * [bh][s_q][d] contiguous).  Equivalent to kivi_dequantize_keys and
+ * kivi_dequantize_values on each layer's store, in two launches.
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_dequantize_cache(const kivi_layer *layers, int n_layers,
+                                  const kivi_cache *cache, void *const *k_out,
+                                  void *const *v_out, kivi_stream_t stream);
+
+/* The two batched calls with per-launch timing points: when `events` is not
+ * NULL, events[0] is recorded on `stream` before the key launch, events[1]
+ * between the key and the value launch and events[2] after the value launch
+ * (each a cudaEvent_t created by the caller; NULL entries are skipped).
+ * Otherwise identical to kivi_flush / kivi_dequantize_cache; a flush that
+ * moves nothing records nothing. */
+KIVI_API kivi_status kivi_flush_timed(const kivi_layer *layers, int n_layers,
+                                      kivi_cache *cache, int64_t *n_flushed,
+                                      kivi_stream_t stream, void *const events[3]);
+KIVI_API kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n_layers,
+                                                 const kivi_cache *cache, void *const *k_out,
+                                                 void *const *v_out, kivi_stream_t stream,
+                                                 void *const events[3]);
+
+/* ------------------------------------------------------------------------ */
+/* Sizes and diagnostics                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* uint32 words of one bh slice of key codes (ceil(s/G)*G/W*d) or value
+ * codes (s*d/W); -1 for unsupported group/bits or negative sizes. */
+KIVI_API int64_t kivi_key_code_words(int64_t s, int64_t d, int group, int bits);
+KIVI_API int64_t kivi_value_code_words(int64_t s, int64_t d, int group, int bits);
+
+/* Static description of a status code. */
+KIVI_API const char *kivi_status_string(kivi_status status);
+
+/* The cudaError_t value behind the last KIVI_ERR_CUDA returned on the calling
+ * host thread (0 if none). */
+KIVI_API int kivi_last_cuda_error(void);
+
+/* Device-side fault record.  Kernels bound every wait on an asynchronous
+ * copy (one second); a wait that runs out records a nonzero code here, the
+ * kernel stops early and its outputs are incomplete.  This call
+ * synchronizes the current device, stores the record (0 = none) in *fault
+ * and clears it.  Returns KIVI_OK or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_device_fault(uint32_t *fault);
+
+/* ABI version of this header (KIVI_ABI_VERSION). */
+#define KIVI_ABI_VERSION 1
+KIVI_API int kivi_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KIVI_H */

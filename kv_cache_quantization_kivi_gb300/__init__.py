@@ -1,0 +1,342 @@
+"""Python binding of ``libkivi`` -- the GB300 KIVI KV-cache codec.
+
+Argument marshalling only: every step of quantization, dequantization and
+flush runs in the library's CUDA kernels (``csrc/``); PyTorch supplies device
+memory and streams.  The functions carry the names of the C entry points
+declared in ``include/kivi.h`` and take ``torch`` CUDA tensors:
+
+    fp16 tensors       torch.float16, shape [bh, s, d], last two dims contiguous
+    code words         torch.int32 (bit patterns of the uint32 words)
+    scales and zeros   torch.float32
+
+If the shared library is missing it is built from ``csrc/`` with nvcc; if
+that is impossible the import of :func:`lib` raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from typing import List, Optional, Sequence, Tuple
+
+from . import _build
+
+__all__ = [
+    "KiviError", "lib", "library_path", "kivi_quantize_keys", "kivi_quantize_values",
+    "kivi_dequantize_keys", "kivi_dequantize_values", "kivi_flush", "kivi_flush_size",
+    "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
+    "kivi_device_fault", "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
+    "KIVI_MAX_LAYERS",
+]
+
+KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN, KIVI_ERR_CAPACITY, KIVI_ERR_CUDA = range(5)
+STATUS = {0: "KIVI_OK", 1: "KIVI_ERR_INVAL", 2: "KIVI_ERR_ALIGN", 3: "KIVI_ERR_CAPACITY",
+          4: "KIVI_ERR_CUDA"}
+KIVI_MAX_LAYERS = 128
+
+
+class KiviError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)}"
+        if _lib is not None:
+            msg += f" ({_lib.kivi_status_string(status).decode()})"
+            if status == KIVI_ERR_CUDA:
+                msg += f", cudaError {_lib.kivi_last_cuda_error()}"
+        super().__init__(msg)
+
+
+class kivi_layer(C.Structure):
+    _fields_ = [("k_res", C.c_void_p), ("v_res", C.c_void_p), ("k_codes", C.c_void_p),
+                ("k_scale", C.c_void_p), ("k_zero", C.c_void_p), ("v_codes", C.c_void_p),
+                ("v_scale", C.c_void_p), ("v_zero", C.c_void_p)]
+
+
+class kivi_cache(C.Structure):
+    _fields_ = [("bh", C.c_int64), ("d", C.c_int64), ("r_cap", C.c_int64), ("cap", C.c_int64),
+                ("group", C.c_int32), ("bits", C.c_int32), ("residual", C.c_int32),
+                ("reserved", C.c_int32), ("s_q", C.c_int64), ("res_head", C.c_int64),
+                ("n_res", C.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+_i64, _int, _vp = C.c_int64, C.c_int, C.c_void_p
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded ``libkivi.so`` (built from source first if missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = C.CDLL(path)
+            q_args = [_vp, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _vp, _vp, _i64, _vp]
+            dq_args = [_vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _vp]
+            for name, args in (("kivi_quantize_keys", q_args), ("kivi_quantize_values", q_args),
+                               ("kivi_dequantize_keys", dq_args),
+                               ("kivi_dequantize_values", dq_args)):
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = _int
+            L.kivi_flush.argtypes = [C.POINTER(kivi_layer), _int, C.POINTER(kivi_cache),
+                                     C.POINTER(_i64), _vp]
+            L.kivi_flush.restype = _int
+            L.kivi_dequantize_cache.argtypes = [C.POINTER(kivi_layer), _int,
+                                                C.POINTER(kivi_cache), C.POINTER(_vp),
+                                                C.POINTER(_vp), _vp]
+            L.kivi_dequantize_cache.restype = _int
+            L.kivi_flush_size.argtypes = [_i64, _int, _int]
+            L.kivi_flush_size.restype = _i64
+            L.kivi_key_code_words.argtypes = [_i64, _i64, _int, _int]
+            L.kivi_key_code_words.restype = _i64
+            L.kivi_value_code_words.argtypes = [_i64, _i64, _int, _int]
+            L.kivi_value_code_words.restype = _i64
+            L.kivi_status_string.argtypes = [_int]
+            L.kivi_status_string.restype = C.c_char_p
+            L.kivi_last_cuda_error.argtypes = []
+            L.kivi_last_cuda_error.restype = _int
+            L.kivi_device_fault.argtypes = [C.POINTER(C.c_uint32)]
+            L.kivi_device_fault.restype = _int
+            L.kivi_abi_version.argtypes = []
+            L.kivi_abi_version.restype = _int
+            _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != KIVI_OK:
+        raise KiviError(status, where)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _fp16_3d(x, what: str):
+    import torch
+    if x.dtype != torch.float16 or x.dim() != 3 or not x.is_cuda:
+        raise ValueError(f"{what}: expected a CUDA float16 tensor [bh, s, d]")
+    if x.shape[1] > 0 and x.shape[2] > 0 and (x.stride(2) != 1 or x.stride(1) != x.shape[2]):
+        raise ValueError(f"{what}: the last two dimensions must be contiguous")
+    return x
+
+
+def _bh_stride(t) -> int:
+    return int(t.stride(0)) if t.shape[0] > 1 else int(t[0].numel()) if t.numel() else 0
+
+
+def codes_per_word(bits: int) -> int:
+    return 32 // bits
+
+
+def kivi_flush_size(n_res: int, residual: int, group: int) -> int:
+    return int(lib().kivi_flush_size(n_res, residual, group))
+
+
+def kivi_key_code_words(s: int, d: int, group: int, bits: int) -> int:
+    return int(lib().kivi_key_code_words(s, d, group, bits))
+
+
+def kivi_value_code_words(s: int, d: int, group: int, bits: int) -> int:
+    return int(lib().kivi_value_code_words(s, d, group, bits))
+
+
+# ---------------------------------------------------------------------------
+# full-tensor calls
+# ---------------------------------------------------------------------------
+
+def kivi_quantize_keys(x, group: int, bits: int, codes=None, scale=None, zero=None,
+                       stream=None) -> Tuple:
+    """Per-channel key quantization of x [bh, s, d] -> (codes [bh, ng*G/W, d] int32,
+    scale [bh, ng, d] f32, zero [bh, ng, d] f32)."""
+    import torch
+    x = _fp16_3d(x, "kivi_quantize_keys")
+    bh, s, d = x.shape
+    ng = -(-s // group)
+    if codes is None:
+        codes = torch.empty((bh, ng * group // codes_per_word(bits), d), dtype=torch.int32,
+                            device=x.device)
+    if scale is None:
+        scale = torch.empty((bh, ng, d), dtype=torch.float32, device=x.device)
+    if zero is None:
+        zero = torch.empty((bh, ng, d), dtype=torch.float32, device=x.device)
+    _check(lib().kivi_quantize_keys(x.data_ptr(), bh, s, d, _bh_stride(x), group, bits,
+                                    codes.data_ptr(), _bh_stride(codes), scale.data_ptr(),
+                                    zero.data_ptr(), _bh_stride(scale), _stream_handle(stream)),
+           "kivi_quantize_keys")
+    return codes, scale, zero
+
+
+def kivi_quantize_values(x, group: int, bits: int, codes=None, scale=None, zero=None,
+                         stream=None) -> Tuple:
+    """Per-token value quantization of x [bh, s, d] -> (codes [bh, s, d/W] int32,
+    scale [bh, s, d/G] f32, zero [bh, s, d/G] f32)."""
+    import torch
+    x = _fp16_3d(x, "kivi_quantize_values")
+    bh, s, d = x.shape
+    if codes is None:
+        codes = torch.empty((bh, s, d // codes_per_word(bits)), dtype=torch.int32,
+                            device=x.device)
+    if scale is None:
+        scale = torch.empty((bh, s, max(1, d // group)), dtype=torch.float32, device=x.device)
+    if zero is None:
+        zero = torch.empty((bh, s, max(1, d // group)), dtype=torch.float32, device=x.device)
+    _check(lib().kivi_quantize_values(x.data_ptr(), bh, s, d, _bh_stride(x), group, bits,
+                                      codes.data_ptr(), _bh_stride(codes), scale.data_ptr(),
+                                      zero.data_ptr(), _bh_stride(scale), _stream_handle(stream)),
+           "kivi_quantize_values")
+    return codes, scale, zero
+
+
+def kivi_dequantize_keys(codes, scale, zero, s: int, group: int, bits: int, y=None,
+                         stream=None):
+    """Key reconstruction [bh, s, d] fp16 from the key code layout."""
+    import torch
+    bh, _, d = codes.shape
+    if y is None:
+        y = torch.empty((bh, s, d), dtype=torch.float16, device=codes.device)
+    _check(lib().kivi_dequantize_keys(codes.data_ptr(), _bh_stride(codes), scale.data_ptr(),
+                                      zero.data_ptr(), _bh_stride(scale), bh, s, d, group, bits,
+                                      y.data_ptr(), _bh_stride(y), _stream_handle(stream)),
+           "kivi_dequantize_keys")
+    return y
+
+
+def kivi_dequantize_values(codes, scale, zero, group: int, bits: int, s: Optional[int] = None,
+                           y=None, stream=None):
+    """Value reconstruction [bh, s, d] fp16 from the value code layout."""
+    import torch
+    bh, s_codes, dw = codes.shape
+    s = s_codes if s is None else s
+    d = dw * codes_per_word(bits)
+    if y is None:
+        y = torch.empty((bh, s, d), dtype=torch.float16, device=codes.device)
+    _check(lib().kivi_dequantize_values(codes.data_ptr(), _bh_stride(codes), scale.data_ptr(),
+                                        zero.data_ptr(), _bh_stride(scale), bh, s, d, group,
+                                        bits, y.data_ptr(), _bh_stride(y),
+                                        _stream_handle(stream)),
+           "kivi_dequantize_values")
+    return y
+
+
+def kivi_device_fault() -> int:
+    """Reads and clears the device fault record (synchronizes the device)."""
+    v = C.c_uint32(0)
+    _check(lib().kivi_device_fault(C.byref(v)), "kivi_device_fault")
+    return int(v.value)
+
+
+# ---------------------------------------------------------------------------
+# cache: residual ring + quantized store, flush, batched dequantization
+# ---------------------------------------------------------------------------
+
+def kivi_flush(layers, n_layers: int, cache: kivi_cache, stream=None) -> int:
+    """Raw C call: ``layers`` a ctypes array of kivi_layer, ``cache`` a kivi_cache
+    (updated in place).  Returns the number of tokens flushed."""
+    n = C.c_int64(0)
+    _check(lib().kivi_flush(layers, n_layers, C.byref(cache), C.byref(n),
+                            _stream_handle(stream)), "kivi_flush")
+    return int(n.value)
+
+
+def kivi_dequantize_cache(layers, n_layers: int, cache: kivi_cache, k_out: Sequence,
+                          v_out: Sequence, stream=None) -> None:
+    kp = (C.c_void_p * n_layers)(*[t.data_ptr() for t in k_out])
+    vp = (C.c_void_p * n_layers)(*[t.data_ptr() for t in v_out])
+    _check(lib().kivi_dequantize_cache(layers, n_layers, C.byref(cache), kp, vp,
+                                       _stream_handle(stream)), "kivi_dequantize_cache")
+
+
+class KiviCache:
+    """Device buffers and state of an ``n_layers`` KIVI cache (all torch-allocated).
+
+    Per layer: fp16 residual rings ``k_res``/``v_res`` [bh, r_cap, d] and the
+    quantized store (key codes [bh, cap/W, d], key scale/zero [bh, cap/G, d],
+    value codes [bh, cap, d/W], value scale/zero [bh, cap, d/G]).
+    """
+
+    def __init__(self, n_layers: int, bh: int, d: int, r_cap: int, cap: int, group: int = 32,
+                 bits: int = 2, residual: int = 32, device="cuda"):
+        import torch
+        if not (1 <= n_layers <= KIVI_MAX_LAYERS):
+            raise ValueError("n_layers out of range")
+        w = codes_per_word(bits)
+        self.n_layers, self.group, self.bits = n_layers, group, bits
+        dev = torch.device(device)
+        mk = lambda shape, dt: torch.zeros(shape, dtype=dt, device=dev)  # noqa: E731
+        self.k_res = [mk((bh, r_cap, d), torch.float16) for _ in range(n_layers)]
+        self.v_res = [mk((bh, r_cap, d), torch.float16) for _ in range(n_layers)]
+        self.k_codes = [mk((bh, cap // w, d), torch.int32) for _ in range(n_layers)]
+        self.k_scale = [mk((bh, cap // group, d), torch.float32) for _ in range(n_layers)]
+        self.k_zero = [mk((bh, cap // group, d), torch.float32) for _ in range(n_layers)]
+        self.v_codes = [mk((bh, cap, d // w), torch.int32) for _ in range(n_layers)]
+        self.v_scale = [mk((bh, cap, d // group), torch.float32) for _ in range(n_layers)]
+        self.v_zero = [mk((bh, cap, d // group), torch.float32) for _ in range(n_layers)]
+        self.layers = (kivi_layer * n_layers)(*[
+            kivi_layer(self.k_res[i].data_ptr(), self.v_res[i].data_ptr(),
+                       self.k_codes[i].data_ptr(), self.k_scale[i].data_ptr(),
+                       self.k_zero[i].data_ptr(), self.v_codes[i].data_ptr(),
+                       self.v_scale[i].data_ptr(), self.v_zero[i].data_ptr())
+            for i in range(n_layers)])
+        self.state = kivi_cache(bh, d, r_cap, cap, group, bits, residual, 0, 0, 0, 0)
+
+    # state ------------------------------------------------------------------
+    @property
+    def s_q(self) -> int:
+        return int(self.state.s_q)
+
+    @property
+    def n_res(self) -> int:
+        return int(self.state.n_res)
+
+    @property
+    def res_head(self) -> int:
+        return int(self.state.res_head)
+
+    def reset(self, s_q: int = 0, res_head: int = 0, n_res: int = 0) -> None:
+        self.state.s_q, self.state.res_head, self.state.n_res = s_q, res_head, n_res
+
+    def ring_rows(self, start: int, n: int):
+        """Ring rows of logical residual tokens start .. start+n-1."""
+        import torch
+        r_cap = int(self.state.r_cap)
+        return (torch.arange(start, start + n, device=self.k_res[0].device) + self.res_head) % r_cap
+
+    def append(self, layer: int, k_new, v_new) -> None:
+        """Writes new tokens [bh, n, d] behind the residual of one layer (a
+        caller-side copy; call :meth:`advance` once every layer has its tokens)."""
+        rows = self.ring_rows(self.n_res, k_new.shape[1])
+        self.k_res[layer].index_copy_(1, rows, k_new)
+        self.v_res[layer].index_copy_(1, rows, v_new)
+
+    def advance(self, n: int) -> None:
+        if self.n_res + n > int(self.state.r_cap):
+            raise ValueError("residual ring overflow")
+        self.state.n_res += n
+
+    # hot path --------------------------------------------------------------
+    def flush(self, stream=None) -> int:
+        return kivi_flush(self.layers, self.n_layers, self.state, stream)
+
+    def dequantize(self, k_out: Optional[List] = None, v_out: Optional[List] = None,
+                   stream=None):
+        import torch
+        bh, d, s = int(self.state.bh), int(self.state.d), self.s_q
+        dev = self.k_res[0].device
+        if k_out is None:
+            k_out = [torch.empty((bh, s, d), dtype=torch.float16, device=dev)
+                     for _ in range(self.n_layers)]
+        if v_out is None:
+            v_out = [torch.empty((bh, s, d), dtype=torch.float16, device=dev)
+                     for _ in range(self.n_layers)]
+        kivi_dequantize_cache(self.layers, self.n_layers, self.state, k_out, v_out, stream)
+        return k_out, v_out

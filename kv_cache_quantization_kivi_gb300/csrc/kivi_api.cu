@@ -1,0 +1,361 @@
+// kivi_api.cu -- the extern "C" entry points declared in include/kivi.h:
+// host-side validation, parameter blocks, launches and flush bookkeeping.
+//
+// Every check happens before the first CUDA call, so an invalid call
+// launches nothing and touches no memory.  Launch failures are reported as
+// KIVI_ERR_CUDA with the cudaError_t kept per host thread.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/kivi.h"
+#include "kivi_launch.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+bool valid_bits(int bits) { return bits == 2 || bits == 4 || bits == 8; }
+bool valid_group(int g) { return g == 32 || g == 64 || g == 128; }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool bytes16(int64_t n_elems, int64_t elem_bytes) { return (n_elems * elem_bytes) % 16 == 0; }
+bool bytes_mult(int64_t n_elems, int64_t elem_bytes, int64_t m) {
+  return (n_elems * elem_bytes) % m == 0;
+}
+// Value code rows are written and read in pieces of 4*bits bytes per 32
+// channels (8 bytes at 2 bits, 16 bytes otherwise).
+int64_t value_code_align(int bits) { return bits == 2 ? 8 : 16; }
+
+constexpr int64_t kMaxUnits = (int64_t{1} << 31) - 1;
+
+bool valid_key_dim(int64_t d) { return d >= 8 && d <= 256 && d % 8 == 0; }
+bool valid_value_dim(int64_t d, int group) { return d >= 32 && d <= 256 && d % group == 0; }
+
+int64_t groups_of(int64_t s, int group) { return (s + group - 1) / group; }
+
+kivi_status cuda_status(cudaError_t err) {
+  if (err == cudaSuccess) return KIVI_OK;
+  t_last_cuda_error = static_cast<int>(err);
+  return KIVI_ERR_CUDA;
+}
+
+struct KeyGeom {
+  int64_t code_words;  // per bh slice
+  int64_t sz;          // per bh slice
+};
+
+KeyGeom key_geom(int64_t s, int64_t d, int group, int bits) {
+  const int64_t ng = groups_of(s, group);
+  return {ng * group / (32 / bits) * d, ng * d};
+}
+
+}  // namespace
+
+extern "C" {
+
+int kivi_abi_version(void) { return KIVI_ABI_VERSION; }
+
+const char *kivi_status_string(kivi_status status) {
+  switch (status) {
+    case KIVI_OK: return "ok";
+    case KIVI_ERR_INVAL: return "invalid argument";
+    case KIVI_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case KIVI_ERR_CAPACITY: return "store capacity exceeded";
+    case KIVI_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+int kivi_last_cuda_error(void) { return t_last_cuda_error; }
+
+int64_t kivi_flush_size(int64_t n_res, int residual, int group) {
+  if (n_res < 0 || residual < 0 || group <= 0) return -1;
+  if (n_res < static_cast<int64_t>(residual) + group) return 0;
+  return (n_res - residual) / group * group;
+}
+
+int64_t kivi_key_code_words(int64_t s, int64_t d, int group, int bits) {
+  if (!valid_bits(bits) || !valid_group(group) || s < 0 || d < 0) return -1;
+  return key_geom(s, d, group, bits).code_words;
+}
+
+int64_t kivi_value_code_words(int64_t s, int64_t d, int group, int bits) {
+  if (!valid_bits(bits) || !valid_group(group) || s < 0 || d < 0) return -1;
+  return s * (d / (32 / bits));
+}
+
+// ---------------------------------------------------------------------------
+// full-tensor calls
+// ---------------------------------------------------------------------------
+
+kivi_status kivi_quantize_keys(const void *x, int64_t bh, int64_t s, int64_t d,
+                               int64_t x_bh_stride, int group, int bits, uint32_t *codes,
+                               int64_t codes_bh_stride, float *scale, float *zero,
+                               int64_t sz_bh_stride, kivi_stream_t stream) {
+  if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_key_dim(d))
+    return KIVI_ERR_INVAL;
+  if (bh == 0 || s == 0) return KIVI_OK;
+  if (!x || !codes || !scale || !zero) return KIVI_ERR_INVAL;
+  const KeyGeom kg = key_geom(s, d, group, bits);
+  if (x_bh_stride < s * d || codes_bh_stride < kg.code_words || sz_bh_stride < kg.sz)
+    return KIVI_ERR_INVAL;
+  if (bh * groups_of(s, group) > kMaxUnits || bh > kMaxUnits) return KIVI_ERR_INVAL;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scale) || !aligned16(zero) ||
+      !bytes16(x_bh_stride, 2) || !bytes16(codes_bh_stride, 4) || !bytes_mult(sz_bh_stride, 4, 8))
+    return KIVI_ERR_ALIGN;
+
+  kivi_impl::QuantParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_jobs = 1;
+  p.d = static_cast<int32_t>(d);
+  p.bh = bh;
+  p.rows = s;
+  p.x_bh_stride = x_bh_stride;
+  p.codes_bh_stride = codes_bh_stride;
+  p.sz_bh_stride = sz_bh_stride;
+  p.jobs[0] = {x, codes, scale, zero};
+  return cuda_status(kivi_impl::launch_key_quant(p, group, bits, stream));
+}
+
+kivi_status kivi_quantize_values(const void *x, int64_t bh, int64_t s, int64_t d,
+                                 int64_t x_bh_stride, int group, int bits, uint32_t *codes,
+                                 int64_t codes_bh_stride, float *scale, float *zero,
+                                 int64_t sz_bh_stride, kivi_stream_t stream) {
+  if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_value_dim(d, group))
+    return KIVI_ERR_INVAL;
+  if (bh == 0 || s == 0) return KIVI_OK;
+  if (!x || !codes || !scale || !zero) return KIVI_ERR_INVAL;
+  if (x_bh_stride < s * d || codes_bh_stride < s * (d / (32 / bits)) ||
+      sz_bh_stride < s * (d / group))
+    return KIVI_ERR_INVAL;
+  if (bh * s * (d / 32) > kMaxUnits) return KIVI_ERR_INVAL;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scale) || !aligned16(zero) ||
+      !bytes16(x_bh_stride, 2) || !bytes_mult(codes_bh_stride, 4, value_code_align(bits)))
+    return KIVI_ERR_ALIGN;
+
+  kivi_impl::QuantParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_jobs = 1;
+  p.d = static_cast<int32_t>(d);
+  p.bh = bh;
+  p.rows = s;
+  p.x_bh_stride = x_bh_stride;
+  p.codes_bh_stride = codes_bh_stride;
+  p.sz_bh_stride = sz_bh_stride;
+  p.jobs[0] = {x, codes, scale, zero};
+  return cuda_status(kivi_impl::launch_value_quant(p, group, bits, stream));
+}
+
+kivi_status kivi_dequantize_keys(const uint32_t *codes, int64_t codes_bh_stride,
+                                 const float *scale, const float *zero, int64_t sz_bh_stride,
+                                 int64_t bh, int64_t s, int64_t d, int group, int bits, void *y,
+                                 int64_t y_bh_stride, kivi_stream_t stream) {
+  if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_key_dim(d))
+    return KIVI_ERR_INVAL;
+  if (bh == 0 || s == 0) return KIVI_OK;
+  if (!codes || !scale || !zero || !y) return KIVI_ERR_INVAL;
+  const KeyGeom kg = key_geom(s, d, group, bits);
+  if (codes_bh_stride < kg.code_words || sz_bh_stride < kg.sz || y_bh_stride < s * d)
+    return KIVI_ERR_INVAL;
+  if (!aligned16(codes) || !aligned16(scale) || !aligned16(zero) || !aligned16(y) ||
+      !bytes16(codes_bh_stride, 4) || !bytes16(sz_bh_stride, 4) || !bytes16(y_bh_stride, 2))
+    return KIVI_ERR_ALIGN;
+
+  kivi_impl::DequantParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_jobs = 1;
+  p.d = static_cast<int32_t>(d);
+  p.bh = bh;
+  p.rows = s;
+  p.codes_bh_stride = codes_bh_stride;
+  p.sz_bh_stride = sz_bh_stride;
+  p.y_bh_stride = y_bh_stride;
+  p.jobs[0] = {codes, scale, zero, y};
+  return cuda_status(kivi_impl::launch_key_dequant(p, group, bits, stream));
+}
+
+kivi_status kivi_dequantize_values(const uint32_t *codes, int64_t codes_bh_stride,
+                                   const float *scale, const float *zero, int64_t sz_bh_stride,
+                                   int64_t bh, int64_t s, int64_t d, int group, int bits,
+                                   void *y, int64_t y_bh_stride, kivi_stream_t stream) {
+  if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_value_dim(d, group))
+    return KIVI_ERR_INVAL;
+  if (bh == 0 || s == 0) return KIVI_OK;
+  if (!codes || !scale || !zero || !y) return KIVI_ERR_INVAL;
+  if (codes_bh_stride < s * (d / (32 / bits)) || sz_bh_stride < s * (d / group) ||
+      y_bh_stride < s * d)
+    return KIVI_ERR_INVAL;
+  if (bh * s * (d / 32) > kMaxUnits) return KIVI_ERR_INVAL;
+  if (!aligned16(codes) || !aligned16(scale) || !aligned16(zero) || !aligned16(y) ||
+      !bytes_mult(codes_bh_stride, 4, value_code_align(bits)) || !bytes16(y_bh_stride, 2))
+    return KIVI_ERR_ALIGN;
+
+  kivi_impl::DequantParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_jobs = 1;
+  p.d = static_cast<int32_t>(d);
+  p.bh = bh;
+  p.rows = s;
+  p.codes_bh_stride = codes_bh_stride;
+  p.sz_bh_stride = sz_bh_stride;
+  p.y_bh_stride = y_bh_stride;
+  p.jobs[0] = {codes, scale, zero, y};
+  return cuda_status(kivi_impl::launch_value_dequant(p, group, bits, stream));
+}
+
+// ---------------------------------------------------------------------------
+// cache: flush and batched dequantization
+// ---------------------------------------------------------------------------
+
+static kivi_status check_cache(const kivi_layer *layers, int n_layers, const kivi_cache *c) {
+  if (!layers || !c || n_layers < 1 || n_layers > KIVI_MAX_LAYERS) return KIVI_ERR_INVAL;
+  if (!valid_bits(c->bits) || !valid_group(c->group) || c->residual < 0 || c->reserved != 0)
+    return KIVI_ERR_INVAL;
+  const int64_t G = c->group;
+  if (c->bh < 0 || !valid_key_dim(c->d) || !valid_value_dim(c->d, c->group)) return KIVI_ERR_INVAL;
+  if (c->r_cap <= 0 || c->r_cap % G != 0 || c->cap < 0 || c->cap % G != 0) return KIVI_ERR_INVAL;
+  if (c->s_q < 0 || c->s_q % G != 0 || c->s_q > c->cap) return KIVI_ERR_INVAL;
+  if (c->res_head < 0 || c->res_head >= c->r_cap || c->res_head % G != 0) return KIVI_ERR_INVAL;
+  if (c->n_res < 0 || c->n_res > c->r_cap) return KIVI_ERR_INVAL;
+  if (c->bh * c->cap * (c->d / 32) * n_layers > kMaxUnits) return KIVI_ERR_INVAL;
+  for (int l = 0; l < n_layers; ++l) {
+    const kivi_layer &L = layers[l];
+    const void *ptrs[8] = {L.k_res, L.v_res, L.k_codes, L.k_scale,
+                           L.k_zero, L.v_codes, L.v_scale, L.v_zero};
+    for (const void *q : ptrs) {
+      if (!q) return KIVI_ERR_INVAL;
+    }
+    for (const void *q : ptrs) {
+      if (!aligned16(q)) return KIVI_ERR_ALIGN;
+    }
+  }
+  return KIVI_OK;
+}
+
+static cudaError_t record(void *const *events, int i, cudaStream_t s) {
+  if (!events || !events[i]) return cudaSuccess;
+  return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
+}
+
+kivi_status kivi_flush(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                       int64_t *n_flushed, kivi_stream_t stream) {
+  return kivi_flush_timed(layers, n_layers, cache, n_flushed, stream, nullptr);
+}
+
+kivi_status kivi_flush_timed(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                             int64_t *n_flushed, kivi_stream_t stream, void *const events[3]) {
+  const kivi_status st = check_cache(layers, n_layers, cache);
+  if (st != KIVI_OK) return st;
+  const int64_t G = cache->group;
+  const int W = 32 / cache->bits;
+  const int64_t n = kivi_flush_size(cache->n_res, cache->residual, cache->group);
+  if (n > 0 && cache->s_q + n > cache->cap) return KIVI_ERR_CAPACITY;
+  if (n == 0 || cache->bh == 0) {
+    if (n_flushed) *n_flushed = 0;
+    if (n > 0) {  // bh == 0: nothing to move, but the state advances
+      cache->s_q += n;
+      cache->res_head = (cache->res_head + n) % cache->r_cap;
+      cache->n_res -= n;
+      if (n_flushed) *n_flushed = n;
+    }
+    return KIVI_OK;
+  }
+
+  const int64_t d = cache->d;
+  kivi_impl::QuantParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.n_jobs = n_layers;
+  kp.d = static_cast<int32_t>(d);
+  kp.bh = cache->bh;
+  kp.rows = n;
+  kp.x_bh_stride = cache->r_cap * d;
+  kp.ring = cache->r_cap;
+  kp.head = cache->res_head;
+
+  kivi_impl::QuantParams vp = kp;
+  kp.codes_bh_stride = cache->cap / W * d;
+  kp.sz_bh_stride = cache->cap / G * d;
+  kp.out0 = cache->s_q / G;
+  vp.codes_bh_stride = cache->cap * (d / W);
+  vp.sz_bh_stride = cache->cap * (d / G);
+  vp.out0 = cache->s_q;
+  for (int l = 0; l < n_layers; ++l) {
+    const kivi_layer &L = layers[l];
+    kp.jobs[l] = {L.k_res, L.k_codes, L.k_scale, L.k_zero};
+    vp.jobs[l] = {L.v_res, L.v_codes, L.v_scale, L.v_zero};
+  }
+  cudaStream_t s = stream;
+  kivi_status r = cuda_status(record(events, 0, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(kivi_impl::launch_key_quant(kp, cache->group, cache->bits, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(record(events, 1, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(kivi_impl::launch_value_quant(vp, cache->group, cache->bits, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(record(events, 2, s));
+  if (r != KIVI_OK) return r;
+
+  cache->s_q += n;
+  cache->res_head = (cache->res_head + n) % cache->r_cap;
+  cache->n_res -= n;
+  if (n_flushed) *n_flushed = n;
+  return KIVI_OK;
+}
+
+kivi_status kivi_dequantize_cache(const kivi_layer *layers, int n_layers, const kivi_cache *cache,
+                                  void *const *k_out, void *const *v_out, kivi_stream_t stream) {
+  return kivi_dequantize_cache_timed(layers, n_layers, cache, k_out, v_out, stream, nullptr);
+}
+
+kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n_layers,
+                                        const kivi_cache *cache, void *const *k_out,
+                                        void *const *v_out, kivi_stream_t stream,
+                                        void *const events[3]) {
+  const kivi_status st = check_cache(layers, n_layers, cache);
+  if (st != KIVI_OK) return st;
+  if (!k_out || !v_out) return KIVI_ERR_INVAL;
+  if (cache->s_q == 0 || cache->bh == 0) return KIVI_OK;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!k_out[l] || !v_out[l]) return KIVI_ERR_INVAL;
+    if (!aligned16(k_out[l]) || !aligned16(v_out[l])) return KIVI_ERR_ALIGN;
+  }
+  const int64_t G = cache->group;
+  const int W = 32 / cache->bits;
+  const int64_t d = cache->d;
+  kivi_impl::DequantParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.n_jobs = n_layers;
+  kp.d = static_cast<int32_t>(d);
+  kp.bh = cache->bh;
+  kp.rows = cache->s_q;
+  kp.y_bh_stride = cache->s_q * d;
+  kivi_impl::DequantParams vp = kp;
+  kp.codes_bh_stride = cache->cap / W * d;
+  kp.sz_bh_stride = cache->cap / G * d;
+  vp.codes_bh_stride = cache->cap * (d / W);
+  vp.sz_bh_stride = cache->cap * (d / G);
+  for (int l = 0; l < n_layers; ++l) {
+    const kivi_layer &L = layers[l];
+    kp.jobs[l] = {L.k_codes, L.k_scale, L.k_zero, k_out[l]};
+    vp.jobs[l] = {L.v_codes, L.v_scale, L.v_zero, v_out[l]};
+  }
+  cudaStream_t s = stream;
+  kivi_status r = cuda_status(record(events, 0, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(kivi_impl::launch_key_dequant(kp, cache->group, cache->bits, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(record(events, 1, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(kivi_impl::launch_value_dequant(vp, cache->group, cache->bits, s));
+  if (r != KIVI_OK) return r;
+  return cuda_status(record(events, 2, s));
+}
+
+kivi_status kivi_device_fault(uint32_t *fault) {
+  if (!fault) return KIVI_ERR_INVAL;
+  return cuda_status(kivi_impl::read_and_clear_key_fault(fault));
+}
+
+}  // extern "C"

@@ -1,0 +1,233 @@
+// kivi_device.cuh -- device helpers shared by the KIVI kernels: the group
+// quantizer with its exact rounding decision, code packing, and the
+// mbarrier / bulk-copy (TMA) primitives written as inline PTX.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace kivi_dev {
+
+// ---------------------------------------------------------------------------
+// Group quantizer
+// ---------------------------------------------------------------------------
+//
+// Definition (per group, IEEE binary32; the VeloxQuant-MLX KIVI fused-kernel
+// post, "What we're actually optimizing" and "2. Rounding mode"):
+//   zero = min, scale = (max - min) / Q with Q = 2^b - 1,
+//   q = clip(rint((x - zero) / scale), 0, Q), q = 0 when scale == 0,
+// where both the subtraction and the division are rounded to binary32 and
+// rint rounds half to even.
+//
+// Fast path.  Dividing every element costs a correctly rounded division.
+// Instead each group precomputes r = RN(1/scale) and c = RN(-zero * r), and
+// each element evaluates v = RN(x * r + c) with one fused multiply-add.
+// With eps = 2^-24, T = RN(x - zero) / scale (the exact quotient of the
+// rounded difference) and u = RN(T) (the quotient the definition rounds):
+//   x*r + c = T (1+a)/(1+g) + e_c,  |a|,|g| <= eps,  |e_c| <= eps |zero*r|
+//   v = (x*r + c)(1+h),             |h| <= eps
+//   |T| <= Q (1 + 2 eps)            (x - zero <= max - min and monotone rounding)
+// so |v - u| <= eps (4.001 Q + 1.001 |c|) =: E.  Let n = rint(v).  If
+// |v - n| < 1/2 - E then u lies strictly within 1/2 of the integer n, so
+// rint(u) = n and no tie is possible: the fast code is the defined code.
+// Otherwise (v within E of a half-integer, about one element in 10^5 for
+// b = 2) the caller recomputes the element with the exact division.  The
+// group constants below use a threshold 1/2 - 2E, which also absorbs the
+// rounding of the threshold's own computation.
+//
+// rint(v) for 0 <= v < 2^22 is read from y = RN(v + 1.5*2^23): y lies in
+// [2^23, 2^24) where the binary32 spacing is 1, so the addition itself
+// rounds v to an integer with ties to even, and the low mantissa bits of y
+// hold that integer (y's bit pattern is 0x4B400000 + n).
+
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+
+template <int BITS>
+struct CodeFmt {
+  static constexpr int W = 32 / BITS;            // codes per uint32 word
+  static constexpr uint32_t Q = (1u << BITS) - 1u;
+  // sum over the W slots of (kRoundMagicBits << slot*BITS) modulo 2^32: the
+  // offset to subtract after packing raw y bit patterns (see pack below)
+  __host__ __device__ static constexpr uint32_t magic_sum() {
+    uint32_t s = 0;
+    for (int i = 0; i < W; ++i) s += kRoundMagicBits << (i * BITS);
+    return s;
+  }
+};
+
+struct GroupQ {
+  float scale;  // binary32 scale (0 when max == min)
+  float zero;   // binary32 zero point (min, canonical +0)
+  float r;      // RN(1/scale), 0 when scale == 0
+  float c;      // RN(-zero * r)
+  float thr;    // fast-path acceptance threshold on |v - rint(v)|
+};
+
+__device__ __forceinline__ GroupQ make_group(float mn, float mx, float qf) {
+  GroupQ g;
+  // A zero extreme may arrive as -0 or +0; adding +0 gives +0 either way.
+  mn = __fadd_rn(mn, 0.0f);
+  mx = __fadd_rn(mx, 0.0f);
+  g.zero = mn;
+  g.scale = __fdiv_rn(__fsub_rn(mx, mn), qf);
+  if (g.scale > 0.0f) {
+    g.r = __frcp_rn(g.scale);
+    g.c = __fmul_rn(-mn, g.r);
+    // 2E = 2^-23 (4.01 Q + 1.01 |c|)
+    const float two_e = __fmul_rn(__fmaf_rn(1.01f, fabsf(g.c), __fmul_rn(4.01f, qf)), 0x1p-23f);
+    g.thr = __fsub_rn(0.5f, two_e);
+  } else {
+    g.r = 0.0f;     // v = 0 for every element: code 0, exact
+    g.c = 0.0f;
+    g.thr = 1.0f;
+  }
+  return g;
+}
+
+// Fast code of x: returns the bit pattern of y = RN(v + 1.5*2^23), i.e.
+// kRoundMagicBits + q, and sets `bad` when the decision needs the exact path.
+__device__ __forceinline__ uint32_t fast_code_bits(float x, const GroupQ &g, bool &bad) {
+  const float v = __fmaf_rn(x, g.r, g.c);
+  const float y = __fadd_rn(v, kRoundMagic);
+  const float n = __fsub_rn(y, kRoundMagic);
+  const float dist = __fsub_rn(v, n);
+  bad |= !(fabsf(dist) < g.thr);
+  return __float_as_uint(y);
+}
+
+// The defined code, computed literally (used when the fast path declines).
+__device__ __forceinline__ uint32_t exact_code(float x, const GroupQ &g, float qf) {
+  if (g.scale == 0.0f) return 0u;
+  const float t = __fsub_rn(x, g.zero);
+  const float u = __fdiv_rn(t, g.scale);
+  float r = rintf(u);
+  r = fminf(fmaxf(r, 0.0f), qf);
+  return static_cast<uint32_t>(r);
+}
+
+// ---------------------------------------------------------------------------
+// Reconstruction: fp16(RN(RN(q * scale) + zero))  (fused-kernel post,
+// "1. FMA contraction": the product is rounded before the add).
+//
+// q is turned into a float without a conversion instruction: m = the float
+// with bits 0x4B000000 | q equals 2^23 + q.  Then RN(m*scale - 2^23*scale)
+// with one fused multiply-add equals RN(q*scale) exactly: 2^23*scale is an
+// exact power-of-two multiple, the real value m*scale - 2^23*scale is q*scale,
+// and the fused operation rounds it once.  The add of zero is a separate,
+// separately rounded operation.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float recon_f32(uint32_t q, float scale, float neg_scale_2p23,
+                                           float zero) {
+  const float m = __uint_as_float(0x4B000000u | q);
+  const float prod = __fmaf_rn(m, scale, neg_scale_2p23);
+  return __fadd_rn(prod, zero);
+}
+
+// ---------------------------------------------------------------------------
+// Half-precision min / max.  binary16 -> binary32 conversion is exact and
+// monotone, so min/max taken in binary16 equal min/max of the converted
+// values; only the sign of a zero extreme can differ, and make_group
+// canonicalises it.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
+  __half2 h;
+  memcpy(&h, &u, 4);
+  return h;
+}
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk asynchronous copy (TMA, non-tensor form)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete, giving up
+// after `limit_ns` nanoseconds of wall-clock time.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+#pragma unroll 1
+  for (int i = 0; i < 16; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// L2 policy for data read exactly once.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completion is signalled on
+// the mbarrier as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Streaming global loads / stores (data touched once)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_stream(void *p, uint4 v) {
+  __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+__device__ __forceinline__ void st_stream(void *p, uint2 v) {
+  __stcs(reinterpret_cast<uint2 *>(p), v);
+}
+
+}  // namespace kivi_dev

@@ -1,0 +1,299 @@
+// kivi_values.cu -- per-token value quantization and value dequantization.
+//
+// Values are grouped along the contiguous head_dim axis: one (scale, zero)
+// per token per group of G channels (VeloxQuant-MLX KIVI fused-kernel post,
+// "The layout problem that shapes everything").  One thread owns 32
+// consecutive channels of one token (four 16-byte loads); a group of G
+// channels is a sub-warp of G/32 lanes, reduced with __shfl_xor_sync on the
+// packed half2 {min, -max} (one shuffle per step carries both extremes).
+// Codes are packed along channels in registers and written with one 8- or
+// 16-byte store per word group.
+//
+// The grid is persistent (a multiple of the SM count times the resident
+// blocks per SM) and every warp walks the units in warp-aligned steps, so
+// the lanes of a group are always together and inactive tail lanes still
+// take part in the shuffles.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "kivi_device.cuh"
+#include "kivi_launch.h"
+
+namespace kivi_impl {
+namespace {
+
+using namespace kivi_dev;
+
+struct RowRef {
+  int job;
+  uint32_t b;
+  uint32_t r;
+  uint32_t k;  // 32-channel chunk within the row
+};
+
+// unit = ((job * bh + b) * rows + r) * chunks + k   (all < 2^31, host-checked)
+__device__ __forceinline__ RowRef decode_unit(uint32_t u, uint32_t chunks, uint32_t rows,
+                                              uint32_t bh) {
+  RowRef t;
+  const uint32_t row = u / chunks;
+  t.k = u - row * chunks;
+  const uint32_t jb = row / rows;
+  t.r = row - jb * rows;
+  t.job = static_cast<int>(jb / bh);
+  t.b = jb - static_cast<uint32_t>(t.job) * bh;
+  return t;
+}
+
+__device__ __forceinline__ float h2lo(__half2 h) { return __low2float(h); }
+__device__ __forceinline__ float h2hi(__half2 h) { return __high2float(h); }
+
+template <int BITS, int G>
+__global__ void __launch_bounds__(256) value_quant_kernel(const __grid_constant__ QuantParams p) {
+  constexpr int L = G / 32;               // lanes per group
+  constexpr int W = CodeFmt<BITS>::W;
+  constexpr uint32_t Q = CodeFmt<BITS>::Q;
+  constexpr uint32_t MAGIC_SUM = CodeFmt<BITS>::magic_sum();
+  const float qf = static_cast<float>(Q);
+
+  const int D = p.d;
+  const uint32_t chunks = static_cast<uint32_t>(D / 32);
+  const uint32_t rows = static_cast<uint32_t>(p.rows);
+  const uint32_t bh = static_cast<uint32_t>(p.bh);
+  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * bh * rows * chunks;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t stride = gridDim.x * blockDim.x;
+
+#pragma unroll 1
+  for (uint32_t base = (blockIdx.x * blockDim.x + threadIdx.x) & ~31u; base < total;
+       base += stride) {
+    const uint32_t u = base + lane;
+    const bool active = u < total;
+    const RowRef t = decode_unit(active ? u : base, chunks, rows, bh);
+    const QuantJob &job = p.jobs[t.job];
+
+    uint4 v[4] = {};
+    if (active) {
+      int64_t phys = t.r;
+      if (p.ring > 0) phys = (p.head + phys) % p.ring;
+      const __half *src = static_cast<const __half *>(job.x) + t.b * p.x_bh_stride + phys * D +
+                          t.k * 32;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = ld_stream(src + 8 * i);
+    }
+    __half2 h[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      h[4 * i + 0] = u32_as_h2(v[i].x);
+      h[4 * i + 1] = u32_as_h2(v[i].y);
+      h[4 * i + 2] = u32_as_h2(v[i].z);
+      h[4 * i + 3] = u32_as_h2(v[i].w);
+    }
+
+    // min / max of the 32 channels (tree in half2, then the two halves)
+    __half2 mn2[8], mx2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      mn2[i] = __hmin2(h[2 * i], h[2 * i + 1]);
+      mx2[i] = __hmax2(h[2 * i], h[2 * i + 1]);
+    }
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        mn2[i] = __hmin2(mn2[i], mn2[i + w]);
+        mx2[i] = __hmax2(mx2[i], mx2[i + w]);
+      }
+    }
+    const __half mn = __hmin(__low2half(mn2[0]), __high2half(mn2[0]));
+    const __half mx = __hmax(__low2half(mx2[0]), __high2half(mx2[0]));
+    // {min, -max}: a single element-wise min combines both extremes
+    __half2 ext = __halves2half2(mn, __hneg(mx));
+    if (L > 1) {
+#pragma unroll
+      for (int off = 1; off < L; off <<= 1) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, h2_as_u32(ext), off);
+        ext = __hmin2(ext, u32_as_h2(other));
+      }
+    }
+    if (!active) continue;
+
+    const GroupQ g = make_group(__low2float(ext), -__high2float(ext), qf);
+
+    uint32_t w[BITS];
+    bool bad = false;
+#pragma unroll
+    for (int wi = 0; wi < BITS; ++wi) {
+      uint32_t acc = 0u;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const int e = wi * W + k;  // channel within the chunk
+        const float x = (e & 1) ? h2hi(h[e >> 1]) : h2lo(h[e >> 1]);
+        acc += fast_code_bits(x, g, bad) << (k * BITS);
+      }
+      w[wi] = acc - MAGIC_SUM;
+    }
+    if (bad) {  // rare: some element needs the exact division
+#pragma unroll
+      for (int wi = 0; wi < BITS; ++wi) {
+        uint32_t acc = 0u;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const int e = wi * W + k;
+          const float x = (e & 1) ? h2hi(h[e >> 1]) : h2lo(h[e >> 1]);
+          acc |= exact_code(x, g, qf) << (k * BITS);
+        }
+        w[wi] = acc;
+      }
+    }
+
+    const int64_t out_row = p.out0 + t.r;
+    uint32_t *dst = job.codes + t.b * p.codes_bh_stride + out_row * (D / W) + t.k * BITS;
+    if (BITS == 2) {
+      st_stream(dst, make_uint2(w[0], w[1 % BITS]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < BITS; i += 4)
+        st_stream(dst + i, make_uint4(w[i % BITS], w[(i + 1) % BITS], w[(i + 2) % BITS],
+                                      w[(i + 3) % BITS]));
+    }
+    if (t.k % L == 0) {
+      const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k / L;
+      __stcs(job.scale + so, g.scale);
+      __stcs(job.zero + so, g.zero);
+    }
+  }
+}
+
+template <int BITS, int G>
+__global__ void __launch_bounds__(256)
+    value_dequant_kernel(const __grid_constant__ DequantParams p) {
+  constexpr int L = G / 32;
+  constexpr int W = CodeFmt<BITS>::W;
+  constexpr uint32_t Q = CodeFmt<BITS>::Q;
+  const int D = p.d;
+  const uint32_t chunks = static_cast<uint32_t>(D / 32);
+  const uint32_t rows = static_cast<uint32_t>(p.rows);
+  const uint32_t bh = static_cast<uint32_t>(p.bh);
+  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * bh * rows * chunks;
+  const uint32_t stride = gridDim.x * blockDim.x;
+
+#pragma unroll 1
+  for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
+    const RowRef t = decode_unit(u, chunks, rows, bh);
+    const DequantJob &J = p.jobs[t.job];
+    const uint32_t *src = J.codes + t.b * p.codes_bh_stride + static_cast<int64_t>(t.r) * (D / W) +
+                          t.k * BITS;
+    uint32_t w[BITS];
+    if (BITS == 2) {
+      const uint2 a = __ldcs(reinterpret_cast<const uint2 *>(src));
+      w[0] = a.x;
+      w[1 % BITS] = a.y;
+    } else {
+#pragma unroll
+      for (int i = 0; i < BITS; i += 4) {
+        const uint4 a = ld_stream(src + i);
+        w[i % BITS] = a.x;
+        w[(i + 1) % BITS] = a.y;
+        w[(i + 2) % BITS] = a.z;
+        w[(i + 3) % BITS] = a.w;
+      }
+    }
+    const int64_t so = t.b * p.sz_bh_stride + static_cast<int64_t>(t.r) * (D / G) + t.k / L;
+    const float sc = __ldcs(J.scale + so);
+    const float ze = __ldcs(J.zero + so);
+    const float nsc = __fmul_rn(sc, -8388608.0f);  // -2^23 * scale, exact
+
+    uint32_t out[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const uint32_t q0 = (w[e / W] >> ((e % W) * BITS)) & Q;
+      const uint32_t q1 = (w[(e + 1) / W] >> (((e + 1) % W) * BITS)) & Q;
+      const float r0 = recon_f32(q0, sc, nsc, ze);
+      const float r1 = recon_f32(q1, sc, nsc, ze);
+      out[e >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
+    }
+    __half *y = static_cast<__half *>(J.y) + t.b * p.y_bh_stride + static_cast<int64_t>(t.r) * D +
+                t.k * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      st_stream(y + 8 * i, make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]));
+  }
+}
+
+int g_num_sms = 0;
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_num_sms = n > 0 ? n : 1;
+  }
+  return g_num_sms;
+}
+
+template <typename K>
+cudaError_t persistent_grid(K kern, int threads, int64_t units, int64_t *grid) {
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t blocks = (units + threads - 1) / threads;
+  *grid = std::max<int64_t>(1, std::min<int64_t>(blocks, static_cast<int64_t>(num_sms()) * per_sm));
+  return cudaSuccess;
+}
+
+template <int BITS, int G>
+cudaError_t value_quant_launch(const QuantParams &p, cudaStream_t stream) {
+  const int threads = 256;
+  auto kern = value_quant_kernel<BITS, G>;
+  const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
+  int64_t grid = 0;
+  cudaError_t err = persistent_grid(kern, threads, units, &grid);
+  if (err != cudaSuccess) return err;
+  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int BITS, int G>
+cudaError_t value_dequant_launch(const DequantParams &p, cudaStream_t stream) {
+  const int threads = 256;
+  auto kern = value_dequant_kernel<BITS, G>;
+  const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
+  int64_t grid = 0;
+  cudaError_t err = persistent_grid(kern, threads, units, &grid);
+  if (err != cudaSuccess) return err;
+  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+#define KIVI_DISPATCH(FN, P, GROUP, BITS, STREAM)                                   \
+  do {                                                                              \
+    switch ((BITS) * 1000 + (GROUP)) {                                              \
+      case 2032: return FN<2, 32>(P, STREAM);                                       \
+      case 2064: return FN<2, 64>(P, STREAM);                                       \
+      case 2128: return FN<2, 128>(P, STREAM);                                      \
+      case 4032: return FN<4, 32>(P, STREAM);                                       \
+      case 4064: return FN<4, 64>(P, STREAM);                                       \
+      case 4128: return FN<4, 128>(P, STREAM);                                      \
+      case 8032: return FN<8, 32>(P, STREAM);                                       \
+      case 8064: return FN<8, 64>(P, STREAM);                                       \
+      case 8128: return FN<8, 128>(P, STREAM);                                      \
+      default: return cudaErrorInvalidValue;                                        \
+    }                                                                               \
+  } while (0)
+
+cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, cudaStream_t stream) {
+  KIVI_DISPATCH(value_quant_launch, p, group, bits, stream);
+}
+
+cudaError_t launch_value_dequant(const DequantParams &p, int group, int bits,
+                                 cudaStream_t stream) {
+  KIVI_DISPATCH(value_dequant_launch, p, group, bits, stream);
+}
+
+}  // namespace kivi_impl

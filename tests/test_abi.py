@@ -1,0 +1,191 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry
+point declared in include/kivi.h, and its host-side logic (argument
+validation, sizes, flush-size rule, empty calls) behaves as documented --
+none of these paths makes a CUDA call."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import kv_cache_quantization_kivi_gb300 as K
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kivi.h")
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kivi_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    L = K.lib()
+    names = declared_functions()
+    assert {"kivi_quantize_keys", "kivi_quantize_values", "kivi_dequantize_keys",
+            "kivi_dequantize_values", "kivi_flush"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.kivi_abi_version() == 1
+
+
+def test_library_is_the_in_tree_build():
+    assert os.path.exists(K.library_path())
+    assert os.path.commonpath([K.library_path(), ROOT]) == ROOT
+
+
+def test_status_strings():
+    L = K.lib()
+    for s in range(5):
+        assert L.kivi_status_string(s)
+    assert L.kivi_last_cuda_error() == 0
+
+
+def test_flush_size_rule_matches_oracle():
+    L = K.lib()
+    for n_res in list(range(0, 300, 7)) + [559, 2059, 8209]:
+        for r, g in [(32, 32), (64, 64), (0, 32), (32, 128), (5, 64)]:
+            assert L.kivi_flush_size(n_res, r, g) == O.flush_size(n_res, r, g)
+    assert L.kivi_flush_size(-1, 32, 32) == -1
+    assert L.kivi_flush_size(10, 32, 0) == -1
+
+
+def test_code_word_counts():
+    assert K.kivi_key_code_words(100, 128, 32, 2) == 128 // 16 * 128
+    assert K.kivi_key_code_words(4096, 128, 64, 4) == 4096 // 8 * 128
+    assert K.kivi_value_code_words(100, 128, 32, 8) == 100 * 32
+    assert K.kivi_value_code_words(7, 64, 64, 2) == 7 * 4
+    assert K.kivi_key_code_words(10, 128, 48, 2) == -1
+    assert K.kivi_value_code_words(10, 128, 32, 3) == -1
+
+
+def _qk(**kw):
+    a = dict(x=FAKE, bh=2, s=64, d=128, xs=64 * 128, group=32, bits=2, codes=FAKE,
+             cs=64 // 16 * 128, scale=FAKE, zero=FAKE, ss=2 * 128, stream=None)
+    a.update(kw)
+    return K.lib().kivi_quantize_keys(a["x"], a["bh"], a["s"], a["d"], a["xs"], a["group"],
+                                      a["bits"], a["codes"], a["cs"], a["scale"], a["zero"],
+                                      a["ss"], a["stream"])
+
+
+def _qv(**kw):
+    a = dict(x=FAKE, bh=2, s=10, d=128, xs=10 * 128, group=32, bits=2, codes=FAKE,
+             cs=10 * 8, scale=FAKE, zero=FAKE, ss=10 * 4, stream=None)
+    a.update(kw)
+    return K.lib().kivi_quantize_values(a["x"], a["bh"], a["s"], a["d"], a["xs"], a["group"],
+                                        a["bits"], a["codes"], a["cs"], a["scale"], a["zero"],
+                                        a["ss"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bits=3), 1), (dict(bits=16), 1), (dict(group=48), 1), (dict(group=16), 1),
+    (dict(d=100), 1), (dict(d=264), 1), (dict(d=0), 1), (dict(bh=-1), 1), (dict(s=-3), 1),
+    (dict(x=None), 1), (dict(codes=None), 1), (dict(zero=None), 1),
+    (dict(xs=64 * 128 - 8), 1), (dict(cs=100), 1), (dict(ss=128), 1),
+    (dict(x=FAKE + 8), 2), (dict(codes=FAKE + 4), 2), (dict(scale=FAKE + 8), 2),
+    (dict(xs=64 * 128 + 4), 2), (dict(cs=64 // 16 * 128 + 1), 2), (dict(ss=2 * 128 + 1), 2),
+    (dict(bh=0, x=None), 0), (dict(s=0, codes=None), 0),
+])
+def test_quantize_keys_validation(kw, status):
+    assert _qk(**kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bits=5), 1), (dict(group=64, d=96), 1), (dict(d=16), 1), (dict(d=48), 1),
+    (dict(scale=None), 1), (dict(cs=10 * 8 - 1), 1), (dict(ss=10 * 4 - 1), 1),
+    (dict(xs=10 * 128 + 4), 2), (dict(bits=4, cs=10 * 16 + 2), 2), (dict(zero=FAKE + 4), 2),
+    (dict(bh=0), 0), (dict(s=0), 0),
+])
+def test_quantize_values_validation(kw, status):
+    assert _qv(**kw) == status
+
+
+def test_dequantize_validation():
+    L = K.lib()
+    # keys: y stride too small, then misaligned y
+    assert L.kivi_dequantize_keys(FAKE, 512, FAKE, FAKE, 256, 2, 64, 128, 32, 2, FAKE,
+                                  64 * 128 - 8, None) == 1
+    assert L.kivi_dequantize_keys(FAKE, 512, FAKE, FAKE, 256, 2, 64, 128, 32, 2, FAKE + 2,
+                                  64 * 128, None) == 2
+    assert L.kivi_dequantize_keys(FAKE, 512, FAKE, FAKE, 256, 0, 64, 128, 32, 2, None,
+                                  64 * 128, None) == 0
+    assert L.kivi_dequantize_values(FAKE, 80, FAKE, FAKE, 40, 2, 10, 128, 32, 3, FAKE,
+                                    1280, None) == 1
+    assert L.kivi_dequantize_values(FAKE, 80, FAKE, FAKE, 40, 2, 0, 128, 32, 2, FAKE,
+                                    1280, None) == 0
+
+
+def _cache(**kw):
+    c = K.kivi_cache(bh=4, d=128, r_cap=128, cap=256, group=32, bits=2, residual=32,
+                     reserved=0, s_q=0, res_head=0, n_res=40)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _layers(n=2, **kw):
+    arr = (K.kivi_layer * n)()
+    for i in range(n):
+        for f, _ in K.kivi_layer._fields_:
+            setattr(arr[i], f, FAKE + 4096 * i)
+        for f, v in kw.items():
+            setattr(arr[i], f, v)
+    return arr
+
+
+def _flush(layers, n, cache):
+    out = C.c_int64(-7)
+    rc = K.lib().kivi_flush(layers, n, C.byref(cache), C.byref(out), None)
+    return rc, out.value
+
+
+def test_flush_nothing_to_move_launches_nothing():
+    c = _cache(n_res=63)
+    rc, n = _flush(_layers(), 2, c)
+    assert (rc, n) == (0, 0) and (c.s_q, c.res_head, c.n_res) == (0, 0, 63)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(bits=3), dict(group=16), dict(residual=-1), dict(reserved=1), dict(d=80),
+    dict(r_cap=100), dict(cap=250), dict(s_q=16), dict(s_q=288), dict(res_head=16),
+    dict(res_head=128), dict(n_res=129), dict(n_res=-1), dict(bh=-2),
+])
+def test_flush_rejects_bad_cache_state(kw):
+    c = _cache(**kw)
+    before = (c.s_q, c.res_head, c.n_res)
+    rc, _ = _flush(_layers(), 2, c)
+    assert rc == 1
+    assert (c.s_q, c.res_head, c.n_res) == before
+
+
+def test_flush_rejects_bad_layers():
+    c = _cache(n_res=100)
+    assert _flush(_layers(), 0, c)[0] == 1
+    assert _flush(_layers(), K.KIVI_MAX_LAYERS + 1, c)[0] == 1
+    assert _flush(_layers(v_zero=None), 2, c)[0] == 1
+    assert _flush(_layers(k_scale=FAKE + 4), 2, c)[0] == 2
+
+
+def test_flush_capacity_error_leaves_state():
+    c = _cache(cap=64, s_q=32, n_res=128)    # would move 96 tokens into 32 free
+    rc, _ = _flush(_layers(), 2, c)
+    assert rc == 3
+    assert (c.s_q, c.res_head, c.n_res) == (32, 0, 128)
+
+
+def test_flush_with_no_sequences_advances_state_only():
+    c = _cache(bh=0, n_res=100)
+    rc, n = _flush(_layers(), 2, c)
+    assert (rc, n) == (0, 64) and (c.s_q, c.res_head, c.n_res) == (64, 64, 36)
+
+
+def test_dequantize_cache_empty_store_is_a_noop():
+    c = _cache(s_q=0)
+    ptrs = (C.c_void_p * 2)(FAKE, FAKE)
+    assert K.lib().kivi_dequantize_cache(_layers(), 2, C.byref(c), ptrs, ptrs, None) == 0
