@@ -236,13 +236,6 @@ KIVI_API const char *kivi_status_string(kivi_status status);
  * host thread (0 if none). */
 KIVI_API int kivi_last_cuda_error(void);
 
-/* Device-side fault record.  Kernels bound every wait on an asynchronous
- * copy (one second); a wait that runs out records a nonzero code here, the
- * kernel stops early and its outputs are incomplete.  This call
- * synchronizes the current device, stores the record (0 = none) in *fault
- * and clears it.  Returns KIVI_OK or KIVI_ERR_CUDA. */
-KIVI_API kivi_status kivi_device_fault(uint32_t *fault);
-
 /* ABI version of this header (KIVI_ABI_VERSION). */
 #define KIVI_ABI_VERSION 1
 KIVI_API int kivi_abi_version(void);

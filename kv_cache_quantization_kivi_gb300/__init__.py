@@ -25,8 +25,8 @@ __all__ = [
     "KiviError", "lib", "library_path", "kivi_quantize_keys", "kivi_quantize_values",
     "kivi_dequantize_keys", "kivi_dequantize_values", "kivi_flush", "kivi_flush_size",
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
-    "kivi_device_fault", "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
-    "KIVI_MAX_LAYERS",
+    "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
+    "KIVI_MAX_LAYERS", "event_handles",
 ]
 
 KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN, KIVI_ERR_CAPACITY, KIVI_ERR_CUDA = range(5)
@@ -91,6 +91,13 @@ def lib():
                                                 C.POINTER(kivi_cache), C.POINTER(_vp),
                                                 C.POINTER(_vp), _vp]
             L.kivi_dequantize_cache.restype = _int
+            L.kivi_flush_timed.argtypes = [C.POINTER(kivi_layer), _int, C.POINTER(kivi_cache),
+                                           C.POINTER(_i64), _vp, C.POINTER(_vp)]
+            L.kivi_flush_timed.restype = _int
+            L.kivi_dequantize_cache_timed.argtypes = [C.POINTER(kivi_layer), _int,
+                                                      C.POINTER(kivi_cache), C.POINTER(_vp),
+                                                      C.POINTER(_vp), _vp, C.POINTER(_vp)]
+            L.kivi_dequantize_cache_timed.restype = _int
             L.kivi_flush_size.argtypes = [_i64, _int, _int]
             L.kivi_flush_size.restype = _i64
             L.kivi_key_code_words.argtypes = [_i64, _i64, _int, _int]
@@ -101,8 +108,6 @@ def lib():
             L.kivi_status_string.restype = C.c_char_p
             L.kivi_last_cuda_error.argtypes = []
             L.kivi_last_cuda_error.restype = _int
-            L.kivi_device_fault.argtypes = [C.POINTER(C.c_uint32)]
-            L.kivi_device_fault.restype = _int
             L.kivi_abi_version.argtypes = []
             L.kivi_abi_version.restype = _int
             _lib = L
@@ -228,32 +233,49 @@ def kivi_dequantize_values(codes, scale, zero, group: int, bits: int, s: Optiona
     return y
 
 
-def kivi_device_fault() -> int:
-    """Reads and clears the device fault record (synchronizes the device)."""
-    v = C.c_uint32(0)
-    _check(lib().kivi_device_fault(C.byref(v)), "kivi_device_fault")
-    return int(v.value)
-
-
 # ---------------------------------------------------------------------------
 # cache: residual ring + quantized store, flush, batched dequantization
 # ---------------------------------------------------------------------------
 
-def kivi_flush(layers, n_layers: int, cache: kivi_cache, stream=None) -> int:
+def event_handles(events) -> "C.Array":
+    """ctypes array of three cudaEvent_t handles from torch.cuda.Event objects
+    (each must have been recorded once so that the CUDA event exists)."""
+    return (C.c_void_p * 3)(*[e.cuda_event if e is not None else None for e in events])
+
+
+def kivi_flush(layers, n_layers: int, cache: kivi_cache, stream=None, events=None) -> int:
     """Raw C call: ``layers`` a ctypes array of kivi_layer, ``cache`` a kivi_cache
-    (updated in place).  Returns the number of tokens flushed."""
+    (updated in place).  ``events``: optional (ctypes array of) three event
+    handles recorded around the two launches.  Returns the tokens flushed."""
     n = C.c_int64(0)
-    _check(lib().kivi_flush(layers, n_layers, C.byref(cache), C.byref(n),
-                            _stream_handle(stream)), "kivi_flush")
+    if events is None:
+        st = lib().kivi_flush(layers, n_layers, C.byref(cache), C.byref(n),
+                              _stream_handle(stream))
+    else:
+        if not isinstance(events, C.Array):
+            events = event_handles(events)
+        st = lib().kivi_flush_timed(layers, n_layers, C.byref(cache), C.byref(n),
+                                    _stream_handle(stream), events)
+    _check(st, "kivi_flush")
     return int(n.value)
 
 
-def kivi_dequantize_cache(layers, n_layers: int, cache: kivi_cache, k_out: Sequence,
-                          v_out: Sequence, stream=None) -> None:
-    kp = (C.c_void_p * n_layers)(*[t.data_ptr() for t in k_out])
-    vp = (C.c_void_p * n_layers)(*[t.data_ptr() for t in v_out])
-    _check(lib().kivi_dequantize_cache(layers, n_layers, C.byref(cache), kp, vp,
-                                       _stream_handle(stream)), "kivi_dequantize_cache")
+def kivi_dequantize_cache(layers, n_layers: int, cache: kivi_cache, k_out, v_out,
+                          stream=None, events=None) -> None:
+    """``k_out``/``v_out``: sequences of fp16 tensors, or prepared ctypes pointer arrays."""
+    kp = k_out if isinstance(k_out, C.Array) else (C.c_void_p * n_layers)(
+        *[t.data_ptr() for t in k_out])
+    vp = v_out if isinstance(v_out, C.Array) else (C.c_void_p * n_layers)(
+        *[t.data_ptr() for t in v_out])
+    if events is None:
+        st = lib().kivi_dequantize_cache(layers, n_layers, C.byref(cache), kp, vp,
+                                         _stream_handle(stream))
+    else:
+        if not isinstance(events, C.Array):
+            events = event_handles(events)
+        st = lib().kivi_dequantize_cache_timed(layers, n_layers, C.byref(cache), kp, vp,
+                                               _stream_handle(stream), events)
+    _check(st, "kivi_dequantize_cache")
 
 
 class KiviCache:
@@ -272,15 +294,24 @@ class KiviCache:
         w = codes_per_word(bits)
         self.n_layers, self.group, self.bits = n_layers, group, bits
         dev = torch.device(device)
-        mk = lambda shape, dt: torch.zeros(shape, dtype=dt, device=dev)  # noqa: E731
-        self.k_res = [mk((bh, r_cap, d), torch.float16) for _ in range(n_layers)]
-        self.v_res = [mk((bh, r_cap, d), torch.float16) for _ in range(n_layers)]
-        self.k_codes = [mk((bh, cap // w, d), torch.int32) for _ in range(n_layers)]
-        self.k_scale = [mk((bh, cap // group, d), torch.float32) for _ in range(n_layers)]
-        self.k_zero = [mk((bh, cap // group, d), torch.float32) for _ in range(n_layers)]
-        self.v_codes = [mk((bh, cap, d // w), torch.int32) for _ in range(n_layers)]
-        self.v_scale = [mk((bh, cap, d // group), torch.float32) for _ in range(n_layers)]
-        self.v_zero = [mk((bh, cap, d // group), torch.float32) for _ in range(n_layers)]
+        # one contiguous allocation per buffer kind, one view per layer
+        mk = lambda shape, dt: torch.zeros((n_layers,) + shape, dtype=dt, device=dev)  # noqa
+        self.k_res_all = mk((bh, r_cap, d), torch.float16)
+        self.v_res_all = mk((bh, r_cap, d), torch.float16)
+        self.k_codes_all = mk((bh, cap // w, d), torch.int32)
+        self.k_scale_all = mk((bh, cap // group, d), torch.float32)
+        self.k_zero_all = mk((bh, cap // group, d), torch.float32)
+        self.v_codes_all = mk((bh, cap, d // w), torch.int32)
+        self.v_scale_all = mk((bh, cap, d // group), torch.float32)
+        self.v_zero_all = mk((bh, cap, d // group), torch.float32)
+        self.k_res = list(self.k_res_all.unbind(0))
+        self.v_res = list(self.v_res_all.unbind(0))
+        self.k_codes = list(self.k_codes_all.unbind(0))
+        self.k_scale = list(self.k_scale_all.unbind(0))
+        self.k_zero = list(self.k_zero_all.unbind(0))
+        self.v_codes = list(self.v_codes_all.unbind(0))
+        self.v_scale = list(self.v_scale_all.unbind(0))
+        self.v_zero = list(self.v_zero_all.unbind(0))
         self.layers = (kivi_layer * n_layers)(*[
             kivi_layer(self.k_res[i].data_ptr(), self.v_res[i].data_ptr(),
                        self.k_codes[i].data_ptr(), self.k_scale[i].data_ptr(),
@@ -324,19 +355,22 @@ class KiviCache:
         self.state.n_res += n
 
     # hot path --------------------------------------------------------------
-    def flush(self, stream=None) -> int:
-        return kivi_flush(self.layers, self.n_layers, self.state, stream)
+    def flush(self, stream=None, events=None) -> int:
+        return kivi_flush(self.layers, self.n_layers, self.state, stream, events)
 
-    def dequantize(self, k_out: Optional[List] = None, v_out: Optional[List] = None,
-                   stream=None):
+    def dequantize(self, k_out=None, v_out=None, stream=None, events=None):
+        """fp16 reconstructions of the first s_q store tokens of every layer;
+        ``k_out``/``v_out`` default to new [n_layers, bh, s_q, d] tensors
+        (returned as per-layer lists)."""
         import torch
         bh, d, s = int(self.state.bh), int(self.state.d), self.s_q
         dev = self.k_res[0].device
         if k_out is None:
-            k_out = [torch.empty((bh, s, d), dtype=torch.float16, device=dev)
-                     for _ in range(self.n_layers)]
+            k_out = list(torch.empty((self.n_layers, bh, s, d), dtype=torch.float16,
+                                     device=dev).unbind(0))
         if v_out is None:
-            v_out = [torch.empty((bh, s, d), dtype=torch.float16, device=dev)
-                     for _ in range(self.n_layers)]
-        kivi_dequantize_cache(self.layers, self.n_layers, self.state, k_out, v_out, stream)
+            v_out = list(torch.empty((self.n_layers, bh, s, d), dtype=torch.float16,
+                                     device=dev).unbind(0))
+        kivi_dequantize_cache(self.layers, self.n_layers, self.state, k_out, v_out, stream,
+                              events)
         return k_out, v_out

@@ -158,6 +158,7 @@ kivi_status kivi_dequantize_keys(const uint32_t *codes, int64_t codes_bh_stride,
   const KeyGeom kg = key_geom(s, d, group, bits);
   if (codes_bh_stride < kg.code_words || sz_bh_stride < kg.sz || y_bh_stride < s * d)
     return KIVI_ERR_INVAL;
+  if (bh * groups_of(s, group) * (d / 8) > kMaxUnits) return KIVI_ERR_INVAL;
   if (!aligned16(codes) || !aligned16(scale) || !aligned16(zero) || !aligned16(y) ||
       !bytes16(codes_bh_stride, 4) || !bytes16(sz_bh_stride, 4) || !bytes16(y_bh_stride, 2))
     return KIVI_ERR_ALIGN;
@@ -351,11 +352,6 @@ kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n_layers,
   r = cuda_status(kivi_impl::launch_value_dequant(vp, cache->group, cache->bits, s));
   if (r != KIVI_OK) return r;
   return cuda_status(record(events, 2, s));
-}
-
-kivi_status kivi_device_fault(uint32_t *fault) {
-  if (!fault) return KIVI_ERR_INVAL;
-  return cuda_status(kivi_impl::read_and_clear_key_fault(fault));
 }
 
 }  // extern "C"

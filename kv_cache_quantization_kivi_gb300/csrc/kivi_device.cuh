@@ -1,6 +1,6 @@
 // kivi_device.cuh -- device helpers shared by the KIVI kernels: the group
-// quantizer with its exact rounding decision, code packing, and the
-// mbarrier / bulk-copy (TMA) primitives written as inline PTX.
+// quantizer with its exact rounding decision, packed binary32 (f32x2)
+// arithmetic written as inline PTX, and streaming loads / stores.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -107,6 +107,98 @@ __device__ __forceinline__ uint32_t exact_code(float x, const GroupQ &g, float q
 }
 
 // ---------------------------------------------------------------------------
+// Packed binary32 pairs (Blackwell f32x2 arithmetic: two IEEE operations,
+// each rounded on its own, per instruction).  A pair is a 64-bit value with
+// the first element in the low 32 bits.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint32_t f2_lo_bits(uint64_t v) { return static_cast<uint32_t>(v); }
+__device__ __forceinline__ uint32_t f2_hi_bits(uint64_t v) {
+  return static_cast<uint32_t>(v >> 32);
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t h2_to_f2(__half2 h) {
+  const float2 f = __half22float2(h);
+  return f2_pack(f.x, f.y);
+}
+
+// Constants of two groups (one per element of a pair) for the packed fast path.
+struct GroupQ2 {
+  uint64_t r;        // (r0, r1)
+  uint64_t c;        // (c0, c1)
+  uint64_t neg_thr2; // -(thr'^2) with thr' slightly below thr (see fast_codes2)
+};
+
+__device__ __forceinline__ float thr_sq_below(float thr) {
+  // thr' = thr (1 - 2^-20) and RN(thr'^2) <= thr^2, so d^2 < RN(thr'^2)
+  // implies |d| < thr.  A non-positive threshold rejects everything.
+  if (!(thr > 0.0f)) return 0.0f;
+  const float t = __fmul_rn(thr, 0.99999904632568359375f);
+  return __fmul_rn(t, t);
+}
+
+__device__ __forceinline__ GroupQ2 make_group2(const GroupQ &a, const GroupQ &b) {
+  GroupQ2 g;
+  g.r = f2_pack(a.r, b.r);
+  g.c = f2_pack(a.c, b.c);
+  g.neg_thr2 = f2_pack(-thr_sq_below(a.thr), -thr_sq_below(b.thr));
+  return g;
+}
+
+// The defined codes of a pair, computed literally; returned in the same
+// encoding as the fast path (0x4B400000 + q per element).  Out of line: it
+// runs only for the rare pairs the fast path declines (mostly exact .5 ties,
+// which fp16 data produce often).
+template <int BITS>
+__device__ __noinline__ uint64_t exact_codes2(float x0, float x1, float mn0, float mx0,
+                                              float mn1, float mx1) {
+  const float qf = static_cast<float>((1u << BITS) - 1u);
+  const GroupQ g0 = make_group(mn0, mx0, qf);
+  const GroupQ g1 = make_group(mn1, mx1, qf);
+  const uint32_t q0 = exact_code(x0, g0, qf);
+  const uint32_t q1 = exact_code(x1, g1, qf);
+  return (static_cast<uint64_t>(kRoundMagicBits + q1) << 32) | (kRoundMagicBits + q0);
+}
+
+// Codes of a pair: y = RN(v + 1.5*2^23) for both elements (bit patterns
+// 0x4B400000 + q).  The acceptance test of fast_code_bits, |v - rint(v)| <
+// thr, is evaluated as RN(d*d - RN(thr'^2)) < 0 (sign bit set); a pair with an
+// element outside it is recomputed by exact_codes2.  (mn0, mx0) and (mn1, mx1)
+// are the extremes of the two elements' groups.
+template <int BITS>
+__device__ __forceinline__ uint64_t codes2(uint64_t x, const GroupQ2 &g, float mn0, float mx0,
+                                           float mn1, float mx1) {
+  const uint64_t magic = f2_pack(kRoundMagic, kRoundMagic);
+  const uint64_t v = f2_fma(x, g.r, g.c);
+  const uint64_t y = f2_add(v, magic);
+  const uint64_t n = f2_sub(y, magic);
+  const uint64_t d = f2_sub(v, n);
+  const uint64_t e = f2_fma(d, d, g.neg_thr2);
+  if ((f2_lo_bits(e) & f2_hi_bits(e)) >> 31) return y;
+  return exact_codes2<BITS>(__uint_as_float(f2_lo_bits(x)), __uint_as_float(f2_hi_bits(x)),
+                            mn0, mx0, mn1, mx1);
+}
+
+// ---------------------------------------------------------------------------
 // Reconstruction: fp16(RN(RN(q * scale) + zero))  (fused-kernel post,
 // "1. FMA contraction": the product is rounded before the add).
 //
@@ -141,79 +233,6 @@ __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
   uint32_t u;
   memcpy(&u, &h, 4);
   return u;
-}
-
-// ---------------------------------------------------------------------------
-// mbarrier + bulk asynchronous copy (TMA, non-tensor form)
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Wait for the phase of `bar` with the given parity to complete, giving up
-// after `limit_ns` nanoseconds of wall-clock time.  Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  uint64_t limit_ns) {
-#pragma unroll 1
-  for (int i = 0; i < 16; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-#pragma unroll 1
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  }
-}
-
-// L2 policy for data read exactly once.
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
-// Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) from
-// global memory into this CTA's shared memory; completion is signalled on
-// the mbarrier as transaction bytes.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -3,24 +3,22 @@
 // Keys are grouped along the token axis: one (scale, zero) per channel per
 // group of G tokens (VeloxQuant-MLX KIVI fused-kernel post, "The layout
 // problem that shapes everything": the group runs along the strided axis,
-// consecutive group elements are d apart).  In the row-contiguous [bh][s][d]
-// layout the G rows of one group are one contiguous block of G*d fp16 values,
-// so a whole group tile is fetched with a single bulk asynchronous copy into
-// shared memory -- no transpose is ever materialised.
+// consecutive group elements are d apart).
 //
-// Quantize kernel (persistent, one tile = one (layer, bh, token group)):
-//   * thread 0 keeps NS tiles in flight: mbarrier.arrive.expect_tx +
-//     cp.async.bulk per stage, L2 evict-first;
-//   * thread (col, split) owns channel pair (2col, 2col+1) and the 32 tokens
-//     [32 split, 32 split + 32) of the group: it reads them from shared
-//     memory as half2 (a warp reads 128 consecutive bytes of one row: no bank
-//     conflicts), reduces min/max in half2 registers, exchanges the partial
-//     extremes of the G/32 splits through a small shared buffer, then
-//     quantizes its 64 values and packs its codes along tokens;
-//   * one __syncthreads per tile both publishes the partial extremes and
-//     frees the stage for the next bulk copy.
-// Dequantize kernel: one thread per (layer, bh, group, 8 channels); 16-byte
-// loads of codes, scales and zeros, 16-byte streaming stores.
+// Quantize: as in the post's "Kernel A", a thread owns whole columns of a
+// group, so the reduction over tokens happens in registers and a warp's loads
+// are coalesced along d; no transpose is materialised and no shared memory or
+// barrier is needed.  Here a thread owns a channel pair (half2) and 32 tokens;
+// for G = 64 and 128 the G/32 threads of a column are adjacent lanes that
+// combine their extremes with two-step shuffles.  The arithmetic is the
+// packed binary32 fast path of kivi_device.cuh with the exact-division
+// fallback; codes are packed along tokens in registers and stored as 8-byte
+// words pairs.  (A variant that staged each G x d tile into shared memory with
+// bulk asynchronous copies ran at a third of this throughput: its per-tile
+// CTA barrier and waits cost more than the copies saved.)
+//
+// Dequantize: one thread per (layer, bh, group, 8 channels); 16-byte loads of
+// codes, scales and zeros, 16-byte streaming stores.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -34,233 +32,206 @@ namespace {
 
 using namespace kivi_dev;
 
-// Fault record of the quantize kernel: the first timed-out wait stores
-// (1 << 31) | (block index & 0x7FFFFFFF).
-__device__ unsigned int g_key_fault = 0u;
-
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
-
-template <int G>
-struct KeyTileCfg;
-template <>
-struct KeyTileCfg<32> { static constexpr int NS = 4; };
-template <>
-struct KeyTileCfg<64> { static constexpr int NS = 3; };
-template <>
-struct KeyTileCfg<128> { static constexpr int NS = 2; };
-
-__host__ __device__ constexpr int key_threads(int g, int d) { return (d / 2) * (g / 32); }
-
-template <int G>
-__host__ __device__ constexpr size_t key_smem_bytes(int d) {
-  // stages | mbarriers | partial extremes [2][G/32][d/2] (uint2)
-  return static_cast<size_t>(KeyTileCfg<G>::NS) * G * d * 2 +
-         KeyTileCfg<G>::NS * sizeof(uint64_t) + 2ull * (G / 32) * (d / 2) * sizeof(uint2);
-}
-
-struct TileRef {
+// Work unit of the quantize kernel: u = ((job * bh + b) * ng + g) * (C * T)
+// + col * T + split, with C = d/2 channel pairs and T = G/32 token splits.
+// Thread u owns channels (2 col, 2 col + 1) and tokens [32 split, 32 split +
+// 32) of group g.  Consecutive lanes take consecutive splits, then columns,
+// so every warp load reads T rows x (32/T) columns x 4 bytes: whole 32-byte
+// sectors, and the T threads of one column are adjacent lanes that combine
+// their partial extremes with __shfl_xor_sync.
+struct KeyUnit {
   int job;
-  int64_t b;
-  int64_t g;
-  int rows_valid;
+  int b, g;
+  int col, split;
 };
 
-__device__ __forceinline__ TileRef decode_tile(const QuantParams &p, int64_t tile, int64_t ng,
-                                               int group) {
-  TileRef t;
-  const int64_t per_job = p.bh * ng;
-  t.job = static_cast<int>(tile / per_job);
-  const int64_t rem = tile - t.job * per_job;
-  t.b = rem / ng;
-  t.g = rem - t.b * ng;
-  const int64_t left = p.rows - t.g * group;
-  t.rows_valid = static_cast<int>(left < group ? left : group);
-  return t;
+template <int T>
+__device__ __forceinline__ KeyUnit decode_key_unit(uint32_t u, const QuantParams &p) {
+  KeyUnit k;
+  k.split = static_cast<int>(u & (T - 1));
+  const uint32_t cu = u / T;
+  const uint32_t tile = p.div_chunks.div(cu);            // divide by C
+  k.col = static_cast<int>(cu - tile * p.div_chunks.d);
+  const uint32_t jb = p.div_rows.div(tile);              // divide by ng
+  k.g = static_cast<int>(tile - jb * p.div_rows.d);
+  const uint32_t job = p.div_bh.div(jb);                 // divide by bh
+  k.b = static_cast<int>(jb - job * p.div_bh.d);
+  k.job = static_cast<int>(job);
+  return k;
 }
 
-template <int BITS, int G>
-__global__ void __launch_bounds__(512) key_quant_kernel(const __grid_constant__ QuantParams p) {
-  constexpr int NS = KeyTileCfg<G>::NS;
+// Rare paths, kept out of line so that they do not weigh on the register
+// allocation of the main loop.
+
+// Token t (0..31) of a split with `rows_here` valid rows, padded by repeating
+// the group's last row (which is row rows_here - 1 of the split, or lies in
+// an earlier split when rows_here <= 0).
+__device__ __forceinline__ int padded_row(int t, int rows_here) {
+  return t < rows_here ? t : rows_here - 1;
+}
+
+// Partial (min, max) of a split of a ragged group.
+__device__ __noinline__ uint2 key_partial_ragged(const __half2 *src, int rows_here, int D) {
+  __half2 mn = __ldcs(src + static_cast<int64_t>(padded_row(0, rows_here)) * (D / 2));
+  __half2 mx = mn;
+#pragma unroll 1
+  for (int t = 1; t < 32; ++t) {
+    const __half2 h = __ldcs(src + static_cast<int64_t>(padded_row(t, rows_here)) * (D / 2));
+    mn = __hmin2(mn, h);
+    mx = __hmax2(mx, h);
+  }
+  return make_uint2(h2_as_u32(mn), h2_as_u32(mx));
+}
+
+// Exact codes of one thread's 32 tokens x 2 channels (rows padded as above),
+// computed from global memory with the literal division, and stored.
+template <int BITS>
+__device__ __noinline__ void key_exact_store(const __half2 *src, int rows_here, int D,
+                                             uint32_t ext_mn, uint32_t ext_mx, uint32_t *cdst) {
+  constexpr int W = CodeFmt<BITS>::W;
+  const float qf = static_cast<float>(CodeFmt<BITS>::Q);
+  const float2 mnf = __half22float2(u32_as_h2(ext_mn));
+  const float2 mxf = __half22float2(u32_as_h2(ext_mx));
+  const GroupQ g0 = make_group(mnf.x, mxf.x, qf);
+  const GroupQ g1 = make_group(mnf.y, mxf.y, qf);
+#pragma unroll 1
+  for (int wr = 0; wr < 32 / W; ++wr) {
+    uint32_t a0 = 0u, a1 = 0u;
+#pragma unroll 1
+    for (int k = 0; k < W; ++k) {
+      const int r = padded_row(wr * W + k, rows_here);
+      const float2 xf = __half22float2(__ldcs(src + static_cast<int64_t>(r) * (D / 2)));
+      a0 |= exact_code(xf.x, g0, qf) << (k * BITS);
+      a1 |= exact_code(xf.y, g1, qf) << (k * BITS);
+    }
+    st_stream(cdst + static_cast<int64_t>(wr) * D, make_uint2(a0, a1));
+  }
+}
+
+template <int BITS, int G, int DC>
+__global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr int T = G / 32;                  // token splits per group
   constexpr int W = CodeFmt<BITS>::W;        // codes per word
+  constexpr int WPT = 32 / W;                // words per channel per thread (= BITS)
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
   constexpr uint32_t MAGIC_SUM = CodeFmt<BITS>::magic_sum();
   const float qf = static_cast<float>(Q);
 
-  const int D = p.d;
-  const int C = D >> 1;                      // half2 columns
-  const int tid = threadIdx.x;
-  const int col = tid % C;
-  const int split = tid / C;
+  const int D = DC > 0 ? DC : p.d;           // head_dim, compile-time when DC > 0
+  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * p.div_bh.d * p.div_rows.d *
+                         p.div_chunks.d * T;
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t stride = gridDim.x * blockDim.x;
 
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int stage_bytes = G * D * 2;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(NS) * stage_bytes);
-  uint2 *red = reinterpret_cast<uint2 *>(bars + NS);
-
-  const int64_t ng = (p.rows + G - 1) / G;
-  const int64_t n_tiles = static_cast<int64_t>(p.n_jobs) * p.bh * ng;
-  if (static_cast<int64_t>(blockIdx.x) >= n_tiles) return;
-  const int64_t my_tiles = (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
-
-  uint64_t policy = 0;
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&bars[s]), 1u);
-    fence_mbar_init();
-    policy = policy_evict_first();
-  }
-  __syncthreads();
-
-  auto issue = [&](int64_t i) {  // thread 0 only
-    const int64_t tile = blockIdx.x + i * static_cast<int64_t>(gridDim.x);
-    const TileRef t = decode_tile(p, tile, ng, G);
-    int64_t row0 = t.g * G;
-    if (p.ring > 0) row0 = (p.head + row0) % p.ring;
-    const __half *src = static_cast<const __half *>(p.jobs[t.job].x) + t.b * p.x_bh_stride +
-                        row0 * D;
-    const int s = static_cast<int>(i % NS);
-    const uint32_t bytes = static_cast<uint32_t>(t.rows_valid) * D * 2u;
-    const uint32_t bar = smem_addr(&bars[s]);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(smem_addr(smem + static_cast<size_t>(s) * stage_bytes), src, bytes, bar, policy);
-  };
-
-  if (tid == 0) {
-    const int64_t pre = my_tiles < NS ? my_tiles : NS;
-    for (int64_t i = 0; i < pre; ++i) issue(i);
-  }
-
-  int64_t i = 0;
-  bool faulted = false;
 #pragma unroll 1
-  for (; i < my_tiles; ++i) {
-    const int s = static_cast<int>(i % NS);
-    const uint32_t parity = static_cast<uint32_t>((i / NS) & 1);
-    const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), parity, kWaitLimitNs);
+  for (uint32_t base = (blockIdx.x * blockDim.x + threadIdx.x) & ~31u; base < total;
+       base += stride) {
+    const uint32_t u = base + lane;
+    const bool active = u < total;
+    const KeyUnit k = decode_key_unit<T>(active ? u : base, p);
+    const QuantJob &job = p.jobs[k.job];
+    int64_t row0 = static_cast<int64_t>(k.g) * G;  // first stored row of the group
+    const int rows_here = static_cast<int>(p.rows - row0) - k.split * 32;  // valid rows of the split
+    if (p.ring > 0) {
+      row0 += p.head;
+      if (row0 >= p.ring) row0 -= p.ring;    // head < ring and g*G < ring
+    }
+    // column (2 col, 2 col + 1) of the first row of this thread's split
+    const __half2 *src = reinterpret_cast<const __half2 *>(
+                             static_cast<const __half *>(job.x) +
+                             static_cast<int64_t>(k.b) * p.x_bh_stride + row0 * D) +
+                         k.col + static_cast<int64_t>(k.split) * 32 * (D / 2);
+    const bool full = active && rows_here >= 32;
 
-    const int64_t tile = blockIdx.x + i * static_cast<int64_t>(gridDim.x);
-    const TileRef t = decode_tile(p, tile, ng, G);
-    const __half2 *tile_h2 =
-        reinterpret_cast<const __half2 *>(smem + static_cast<size_t>(s) * stage_bytes);
-
-    // 32 tokens of this thread's channel pair; rows past the end of a ragged
-    // group repeat the last row (edge padding).
+    // 32 tokens of this thread's channel pair; min / max in four chains
     __half2 h[32];
+    __half2 gmn, gmx;
+    if (full) {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      int r = split * 32 + k;
-      r = r < t.rows_valid ? r : t.rows_valid - 1;
-      h[k] = tile_h2[r * C + col];
-    }
-    __half2 mn = h[0], mx = h[0];
+      for (int t = 0; t < 32; ++t) h[t] = __ldcs(src + t * (D / 2));
+      __half2 mn[4] = {h[0], h[1], h[2], h[3]};
+      __half2 mx[4] = {h[0], h[1], h[2], h[3]};
 #pragma unroll
-    for (int k = 1; k < 32; ++k) {
-      mn = __hmin2(mn, h[k]);
-      mx = __hmax2(mx, h[k]);
+      for (int t = 4; t < 32; ++t) {
+        mn[t & 3] = __hmin2(mn[t & 3], h[t]);
+        mx[t & 3] = __hmax2(mx[t & 3], h[t]);
+      }
+      gmn = __hmin2(__hmin2(mn[0], mn[1]), __hmin2(mn[2], mn[3]));
+      gmx = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
+    } else if (active) {  // ragged last group: padded by repeating the last row
+      const uint2 e = key_partial_ragged(src, rows_here, D);
+      gmn = u32_as_h2(e.x);
+      gmx = u32_as_h2(e.y);
+    } else {
+      gmn = gmx = __float2half2_rn(0.0f);
     }
-    uint2 *red_buf = red + (i & 1) * (T * C);
-    if (T > 1) red_buf[split * C + col] = make_uint2(h2_as_u32(mn), h2_as_u32(mx));
-
-    // Publishes the partial extremes, certifies that every thread has read
-    // this stage, and agrees on a timed-out wait.
-    if (__syncthreads_or(!ok)) {
-      faulted = true;
-      break;
-    }
-    if (tid == 0 && i + NS < my_tiles) issue(i + NS);
-
     if (T > 1) {
+      // partners of inactive lanes are inactive too (whole groups per lane set)
 #pragma unroll
-      for (int j = 0; j < T; ++j) {
-        if (j == split) continue;
-        const uint2 o = red_buf[j * C + col];
-        mn = __hmin2(mn, u32_as_h2(o.x));
-        mx = __hmax2(mx, u32_as_h2(o.y));
+      for (int off = 1; off < T; off <<= 1) {
+        gmn = __hmin2(gmn, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(gmn), off)));
+        gmx = __hmax2(gmx, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(gmx), off)));
       }
     }
-    const float2 mnf = __half22float2(mn);
-    const float2 mxf = __half22float2(mx);
-    const GroupQ g0 = make_group(mnf.x, mxf.x, qf);
-    const GroupQ g1 = make_group(mnf.y, mxf.y, qf);
+    if (!active) continue;
 
-    // Quantize and pack along tokens: BITS words per channel, word wi holds
+    const int64_t out_g = p.out0 + k.g;
+    uint32_t *cdst = job.codes + static_cast<int64_t>(k.b) * p.codes_bh_stride +
+                     (out_g * (G / W) + k.split * WPT) * D + 2 * k.col;
+    GroupQ2 gq;
+    const float2 mnf = __half22float2(gmn);
+    const float2 mxf = __half22float2(gmx);
+    {
+      const GroupQ g0 = make_group(mnf.x, mxf.x, qf);
+      const GroupQ g1 = make_group(mnf.y, mxf.y, qf);
+      gq = make_group2(g0, g1);
+      if (k.split == 0) {
+        const int64_t o = static_cast<int64_t>(k.b) * p.sz_bh_stride + out_g * D + 2 * k.col;
+        __stcs(reinterpret_cast<float2 *>(job.scale + o), make_float2(g0.scale, g1.scale));
+        __stcs(reinterpret_cast<float2 *>(job.zero + o), make_float2(g0.zero, g1.zero));
+      }
+    }
+    if (!full) {
+      key_exact_store<BITS>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst);
+      continue;
+    }
+
+    // Quantize and pack along tokens: WPT words per channel, word wi holds
     // tokens [wi*W, wi*W + W) of this thread's 32.
-    uint32_t w0[BITS], w1[BITS];
-    bool bad = false;
 #pragma unroll
-    for (int wi = 0; wi < BITS; ++wi) {
+    for (int wi = 0; wi < WPT; ++wi) {
       uint32_t a0 = 0u, a1 = 0u;
 #pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const float2 xf = __half22float2(h[wi * W + k]);
-        a0 += fast_code_bits(xf.x, g0, bad) << (k * BITS);
-        a1 += fast_code_bits(xf.y, g1, bad) << (k * BITS);
+      for (int t = 0; t < W; ++t) {
+        const uint64_t y = codes2<BITS>(h2_to_f2(h[wi * W + t]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
+        // raw terms (0x4B400000 + q) << slot; the constant part is removed below
+        a0 += f2_lo_bits(y) << (t * BITS);
+        a1 += f2_hi_bits(y) << (t * BITS);
       }
-      // each raw term is (0x4B400000 + q) << slot; removing the constant part
-      // of all W terms leaves the packed codes
-      w0[wi] = a0 - MAGIC_SUM;
-      w1[wi] = a1 - MAGIC_SUM;
-    }
-    if (bad) {  // rare: some element needs the exact division
-#pragma unroll
-      for (int wi = 0; wi < BITS; ++wi) {
-        uint32_t a0 = 0u, a1 = 0u;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const float2 xf = __half22float2(h[wi * W + k]);
-          a0 |= exact_code(xf.x, g0, qf) << (k * BITS);
-          a1 |= exact_code(xf.y, g1, qf) << (k * BITS);
-        }
-        w0[wi] = a0;
-        w1[wi] = a1;
-      }
-    }
-
-    const QuantJob &job = p.jobs[t.job];
-    const int64_t out_g = p.out0 + t.g;
-    uint32_t *cdst = job.codes + t.b * p.codes_bh_stride +
-                     (out_g * (G / W) + split * BITS) * D + 2 * col;
-#pragma unroll
-    for (int wi = 0; wi < BITS; ++wi)
-      st_stream(cdst + static_cast<int64_t>(wi) * D, make_uint2(w0[wi], w1[wi]));
-    if (split == 0) {
-      const int64_t o = t.b * p.sz_bh_stride + out_g * D + 2 * col;
-      __stcs(reinterpret_cast<float2 *>(job.scale + o), make_float2(g0.scale, g1.scale));
-      __stcs(reinterpret_cast<float2 *>(job.zero + o), make_float2(g0.zero, g1.zero));
-    }
-  }
-
-  if (faulted && tid == 0) {
-    atomicCAS(&g_key_fault, 0u, 0x80000000u | (blockIdx.x & 0x7FFFFFFFu));
-    // Let every copy still in flight land before the CTA exits.
-    const int64_t end = (i + NS < my_tiles) ? i + NS : my_tiles;
-    for (int64_t k = i; k < end; ++k) {
-      (void)mbar_wait_bounded(smem_addr(&bars[k % NS]), static_cast<uint32_t>((k / NS) & 1),
-                              kWaitLimitNs);
+      st_stream(cdst + static_cast<int64_t>(wi) * D, make_uint2(a0 - MAGIC_SUM, a1 - MAGIC_SUM));
     }
   }
 }
 
 // One thread: channels [8*chunk, 8*chunk + 8) of group g of one bh slice.
-template <int BITS, int G>
+// unit = ((job * bh + b) * ng + g) * (d/8) + chunk  (< 2^31, host-checked);
+// p.div_chunks, p.div_rows and p.div_bh divide by d/8, ng and bh.
+template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant__ DequantParams p) {
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
-  const int D = p.d;
-  const int chunks = D >> 3;
-  const int64_t ng = (p.rows + G - 1) / G;
-  const int64_t per_job = p.bh * ng * chunks;
-  const int64_t total = per_job * p.n_jobs;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int D = DC > 0 ? DC : p.d;
+  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * p.div_bh.d * p.div_rows.d *
+                         p.div_chunks.d;
+  const uint32_t stride = gridDim.x * blockDim.x;
 #pragma unroll 1
-  for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total;
-       u += stride) {
-    const int job = static_cast<int>(u / per_job);
-    int64_t rem = u - job * per_job;
-    const int64_t bg = rem / chunks;
-    const int ch = static_cast<int>(rem - bg * chunks);
-    const int64_t b = bg / ng;
-    const int64_t g = bg - b * ng;
+  for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
+    const uint32_t bg_all = p.div_chunks.div(u);
+    const int ch = static_cast<int>(u - bg_all * p.div_chunks.d);
+    const uint32_t jb = p.div_rows.div(bg_all);
+    const int64_t g = bg_all - jb * p.div_rows.d;
+    const uint32_t job = p.div_bh.div(jb);
+    const int64_t b = jb - job * p.div_bh.d;
     const DequantJob &J = p.jobs[job];
 
     const int64_t so = b * p.sz_bh_stride + g * D + ch * 8;
@@ -315,29 +286,30 @@ int num_sms() {
   return g_num_sms;
 }
 
-template <int BITS, int G>
+template <int BITS, int G, int DC>
 cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
-  const int threads = key_threads(G, p.d);
-  const size_t smem = key_smem_bytes<G>(p.d);
-  auto kern = key_quant_kernel<BITS, G>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
+  const int threads = 256;
+  auto kern = key_quant_kernel<BITS, G, DC>;
   int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const int64_t ng = (p.rows + G - 1) / G;
-  const int64_t tiles = static_cast<int64_t>(p.n_jobs) * p.bh * ng;
-  const int64_t grid = std::min<int64_t>(tiles, static_cast<int64_t>(num_sms()) * per_sm);
-  kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(p);
+  const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 2) * (G / 32);
+  const int64_t blocks = (units + threads - 1) / threads;
+  const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(num_sms()) * per_sm);
+  QuantParams q = p;
+  q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 2));
+  q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));
+  q.div_bh = FastDiv::make(static_cast<uint32_t>(p.bh));
+  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(q);
   return cudaGetLastError();
 }
 
-template <int BITS, int G>
+template <int BITS, int G, int DC>
 cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   const int threads = 256;
-  auto kern = key_dequant_kernel<BITS, G>;
+  auto kern = key_dequant_kernel<BITS, G, DC>;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
   if (err != cudaSuccess) return err;
@@ -346,27 +318,17 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 8);
   const int64_t blocks = (units + threads - 1) / threads;
   const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(num_sms()) * per_sm);
-  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(p);
+  DequantParams q = p;
+  q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 8));
+  q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));
+  q.div_bh = FastDiv::make(static_cast<uint32_t>(p.bh));
+  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(q);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-#define KIVI_DISPATCH(FN, P, GROUP, BITS, STREAM)                                   \
-  do {                                                                              \
-    switch ((BITS) * 1000 + (GROUP)) {                                              \
-      case 2032: return FN<2, 32>(P, STREAM);                                       \
-      case 2064: return FN<2, 64>(P, STREAM);                                       \
-      case 2128: return FN<2, 128>(P, STREAM);                                      \
-      case 4032: return FN<4, 32>(P, STREAM);                                       \
-      case 4064: return FN<4, 64>(P, STREAM);                                       \
-      case 4128: return FN<4, 128>(P, STREAM);                                      \
-      case 8032: return FN<8, 32>(P, STREAM);                                       \
-      case 8064: return FN<8, 64>(P, STREAM);                                       \
-      case 8128: return FN<8, 128>(P, STREAM);                                      \
-      default: return cudaErrorInvalidValue;                                        \
-    }                                                                               \
-  } while (0)
+#include "kivi_dispatch.h"
 
 cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, cudaStream_t stream) {
   KIVI_DISPATCH(key_quant_launch, p, group, bits, stream);
@@ -375,19 +337,6 @@ cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, cudaStre
 cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits,
                                cudaStream_t stream) {
   KIVI_DISPATCH(key_dequant_launch, p, group, bits, stream);
-}
-
-cudaError_t read_and_clear_key_fault(uint32_t *fault) {
-  cudaError_t err = cudaDeviceSynchronize();
-  if (err != cudaSuccess) return err;
-  unsigned int v = 0;
-  err = cudaMemcpyFromSymbol(&v, g_key_fault, sizeof(v));
-  if (err != cudaSuccess) return err;
-  const unsigned int zero = 0;
-  err = cudaMemcpyToSymbol(g_key_fault, &zero, sizeof(zero));
-  if (err != cudaSuccess) return err;
-  *fault = v;
-  return cudaSuccess;
 }
 
 }  // namespace kivi_impl

@@ -12,6 +12,28 @@
 
 namespace kivi_impl {
 
+// Division of unsigned n < 2^31 by a fixed divisor d >= 1 without a divide:
+// with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (umulhi(n, m) + n) >> l  (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994).  n + umulhi(n, m) stays
+// below 2^32 because n < 2^31.
+struct FastDiv {
+  uint32_t d, m, l;
+  static FastDiv make(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.l = 0;
+    while ((uint64_t{1} << f.l) < d) ++f.l;
+    f.m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << f.l) - d)) / d + 1);
+    return f;
+  }
+#ifdef __CUDACC__
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    return (__umulhi(n, m) + n) >> l;
+  }
+#endif
+};
+
 // One fp16 tensor quantized into one code/scale/zero set.
 struct QuantJob {
   const void *x;
@@ -37,6 +59,8 @@ struct QuantParams {
   int64_t ring;
   int64_t head;
   int64_t out0;
+  // filled by the launchers: divisors of the kernels' unit index
+  FastDiv div_chunks, div_rows, div_bh;
   QuantJob jobs[KIVI_MAX_LAYERS];
 };
 
@@ -56,6 +80,7 @@ struct DequantParams {
   int64_t codes_bh_stride;
   int64_t sz_bh_stride;
   int64_t y_bh_stride;
+  FastDiv div_chunks, div_rows, div_bh;  // filled by the launcher
   DequantJob jobs[KIVI_MAX_LAYERS];
 };
 
@@ -67,8 +92,5 @@ cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, cudaSt
 cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits, cudaStream_t stream);
 cudaError_t launch_value_dequant(const DequantParams &p, int group, int bits,
                                  cudaStream_t stream);
-
-// Reads and clears the key kernel's fault record (synchronous).
-cudaError_t read_and_clear_key_fault(uint32_t *fault);
 
 }  // namespace kivi_impl

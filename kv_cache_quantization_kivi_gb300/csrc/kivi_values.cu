@@ -34,34 +34,33 @@ struct RowRef {
 };
 
 // unit = ((job * bh + b) * rows + r) * chunks + k   (all < 2^31, host-checked)
-__device__ __forceinline__ RowRef decode_unit(uint32_t u, uint32_t chunks, uint32_t rows,
-                                              uint32_t bh) {
+template <typename P>
+__device__ __forceinline__ RowRef decode_unit(uint32_t u, const P &p) {
   RowRef t;
-  const uint32_t row = u / chunks;
-  t.k = u - row * chunks;
-  const uint32_t jb = row / rows;
-  t.r = row - jb * rows;
-  t.job = static_cast<int>(jb / bh);
-  t.b = jb - static_cast<uint32_t>(t.job) * bh;
+  const uint32_t row = p.div_chunks.div(u);
+  t.k = u - row * p.div_chunks.d;
+  const uint32_t jb = p.div_rows.div(row);
+  t.r = row - jb * p.div_rows.d;
+  const uint32_t job = p.div_bh.div(jb);
+  t.b = jb - job * p.div_bh.d;
+  t.job = static_cast<int>(job);
   return t;
 }
 
 __device__ __forceinline__ float h2lo(__half2 h) { return __low2float(h); }
 __device__ __forceinline__ float h2hi(__half2 h) { return __high2float(h); }
 
-template <int BITS, int G>
-__global__ void __launch_bounds__(256) value_quant_kernel(const __grid_constant__ QuantParams p) {
+template <int BITS, int G, int DC>
+__global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr int L = G / 32;               // lanes per group
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
   constexpr uint32_t MAGIC_SUM = CodeFmt<BITS>::magic_sum();
   const float qf = static_cast<float>(Q);
 
-  const int D = p.d;
-  const uint32_t chunks = static_cast<uint32_t>(D / 32);
-  const uint32_t rows = static_cast<uint32_t>(p.rows);
-  const uint32_t bh = static_cast<uint32_t>(p.bh);
-  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * bh * rows * chunks;
+  const int D = DC > 0 ? DC : p.d;          // head_dim, compile-time when DC > 0
+  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * static_cast<uint32_t>(p.bh) *
+                         static_cast<uint32_t>(p.rows) * p.div_chunks.d;
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t stride = gridDim.x * blockDim.x;
 
@@ -70,15 +69,18 @@ __global__ void __launch_bounds__(256) value_quant_kernel(const __grid_constant_
        base += stride) {
     const uint32_t u = base + lane;
     const bool active = u < total;
-    const RowRef t = decode_unit(active ? u : base, chunks, rows, bh);
+    const RowRef t = decode_unit(active ? u : base, p);
     const QuantJob &job = p.jobs[t.job];
 
+    int64_t phys = t.r;
+    if (p.ring > 0) {
+      phys += p.head;
+      if (phys >= p.ring) phys -= p.ring;  // head < ring and r < ring
+    }
+    const __half *src = static_cast<const __half *>(job.x) + t.b * p.x_bh_stride + phys * D +
+                        t.k * 32;
     uint4 v[4] = {};
     if (active) {
-      int64_t phys = t.r;
-      if (p.ring > 0) phys = (p.head + phys) % p.ring;
-      const __half *src = static_cast<const __half *>(job.x) + t.b * p.x_bh_stride + phys * D +
-                          t.k * 32;
 #pragma unroll
       for (int i = 0; i < 4; ++i) v[i] = ld_stream(src + 8 * i);
     }
@@ -119,36 +121,33 @@ __global__ void __launch_bounds__(256) value_quant_kernel(const __grid_constant_
     }
     if (!active) continue;
 
-    const GroupQ g = make_group(__low2float(ext), -__high2float(ext), qf);
+    const float gmn = __low2float(ext), gmx = -__high2float(ext);
+    const int64_t out_row = p.out0 + t.r;
+    GroupQ2 gq;
+    {
+      const GroupQ g = make_group(gmn, gmx, qf);
+      gq = make_group2(g, g);
+      if (t.k % L == 0) {
+        const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k / L;
+        __stcs(job.scale + so, g.scale);
+        __stcs(job.zero + so, g.zero);
+      }
+    }
 
     uint32_t w[BITS];
-    bool bad = false;
 #pragma unroll
     for (int wi = 0; wi < BITS; ++wi) {
       uint32_t acc = 0u;
 #pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const int e = wi * W + k;  // channel within the chunk
-        const float x = (e & 1) ? h2hi(h[e >> 1]) : h2lo(h[e >> 1]);
-        acc += fast_code_bits(x, g, bad) << (k * BITS);
+      for (int k = 0; k < W; k += 2) {
+        const int e = wi * W + k;  // even channel within the chunk
+        const uint64_t y = codes2<BITS>(h2_to_f2(h[e >> 1]), gq, gmn, gmx, gmn, gmx);
+        acc += f2_lo_bits(y) << (k * BITS);
+        acc += f2_hi_bits(y) << ((k + 1) * BITS);
       }
       w[wi] = acc - MAGIC_SUM;
     }
-    if (bad) {  // rare: some element needs the exact division
-#pragma unroll
-      for (int wi = 0; wi < BITS; ++wi) {
-        uint32_t acc = 0u;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const int e = wi * W + k;
-          const float x = (e & 1) ? h2hi(h[e >> 1]) : h2lo(h[e >> 1]);
-          acc |= exact_code(x, g, qf) << (k * BITS);
-        }
-        w[wi] = acc;
-      }
-    }
 
-    const int64_t out_row = p.out0 + t.r;
     uint32_t *dst = job.codes + t.b * p.codes_bh_stride + out_row * (D / W) + t.k * BITS;
     if (BITS == 2) {
       st_stream(dst, make_uint2(w[0], w[1 % BITS]));
@@ -158,30 +157,23 @@ __global__ void __launch_bounds__(256) value_quant_kernel(const __grid_constant_
         st_stream(dst + i, make_uint4(w[i % BITS], w[(i + 1) % BITS], w[(i + 2) % BITS],
                                       w[(i + 3) % BITS]));
     }
-    if (t.k % L == 0) {
-      const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k / L;
-      __stcs(job.scale + so, g.scale);
-      __stcs(job.zero + so, g.zero);
-    }
   }
 }
 
-template <int BITS, int G>
+template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(256)
     value_dequant_kernel(const __grid_constant__ DequantParams p) {
   constexpr int L = G / 32;
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
-  const int D = p.d;
-  const uint32_t chunks = static_cast<uint32_t>(D / 32);
-  const uint32_t rows = static_cast<uint32_t>(p.rows);
-  const uint32_t bh = static_cast<uint32_t>(p.bh);
-  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * bh * rows * chunks;
+  const int D = DC > 0 ? DC : p.d;
+  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * static_cast<uint32_t>(p.bh) *
+                         static_cast<uint32_t>(p.rows) * p.div_chunks.d;
   const uint32_t stride = gridDim.x * blockDim.x;
 
 #pragma unroll 1
   for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
-    const RowRef t = decode_unit(u, chunks, rows, bh);
+    const RowRef t = decode_unit(u, p);
     const DequantJob &J = p.jobs[t.job];
     const uint32_t *src = J.codes + t.b * p.codes_bh_stride + static_cast<int64_t>(t.r) * (D / W) +
                           t.k * BITS;
@@ -245,47 +237,42 @@ cudaError_t persistent_grid(K kern, int threads, int64_t units, int64_t *grid) {
   return cudaSuccess;
 }
 
-template <int BITS, int G>
+template <typename P>
+P with_dividers(const P &p) {
+  P q = p;
+  q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 32));
+  q.div_rows = FastDiv::make(static_cast<uint32_t>(p.rows));
+  q.div_bh = FastDiv::make(static_cast<uint32_t>(p.bh));
+  return q;
+}
+
+template <int BITS, int G, int DC>
 cudaError_t value_quant_launch(const QuantParams &p, cudaStream_t stream) {
   const int threads = 256;
-  auto kern = value_quant_kernel<BITS, G>;
+  auto kern = value_quant_kernel<BITS, G, DC>;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
   int64_t grid = 0;
   cudaError_t err = persistent_grid(kern, threads, units, &grid);
   if (err != cudaSuccess) return err;
-  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(p);
+  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(with_dividers(p));
   return cudaGetLastError();
 }
 
-template <int BITS, int G>
+template <int BITS, int G, int DC>
 cudaError_t value_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   const int threads = 256;
-  auto kern = value_dequant_kernel<BITS, G>;
+  auto kern = value_dequant_kernel<BITS, G, DC>;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
   int64_t grid = 0;
   cudaError_t err = persistent_grid(kern, threads, units, &grid);
   if (err != cudaSuccess) return err;
-  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(p);
+  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(with_dividers(p));
   return cudaGetLastError();
 }
 
 }  // namespace
 
-#define KIVI_DISPATCH(FN, P, GROUP, BITS, STREAM)                                   \
-  do {                                                                              \
-    switch ((BITS) * 1000 + (GROUP)) {                                              \
-      case 2032: return FN<2, 32>(P, STREAM);                                       \
-      case 2064: return FN<2, 64>(P, STREAM);                                       \
-      case 2128: return FN<2, 128>(P, STREAM);                                      \
-      case 4032: return FN<4, 32>(P, STREAM);                                       \
-      case 4064: return FN<4, 64>(P, STREAM);                                       \
-      case 4128: return FN<4, 128>(P, STREAM);                                      \
-      case 8032: return FN<8, 32>(P, STREAM);                                       \
-      case 8064: return FN<8, 64>(P, STREAM);                                       \
-      case 8128: return FN<8, 128>(P, STREAM);                                      \
-      default: return cudaErrorInvalidValue;                                        \
-    }                                                                               \
-  } while (0)
+#include "kivi_dispatch.h"
 
 cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, cudaStream_t stream) {
   KIVI_DISPATCH(value_quant_launch, p, group, bits, stream);

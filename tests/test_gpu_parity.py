@@ -220,7 +220,6 @@ def test_tiny_flush_config_end_to_end():
     assert_same("value recon", host_u16(vy[0]),
                 O.dequantize_values(st.v_codes[:, :96], st.v_scale[:, :96], st.v_zero[:, :96],
                                     w.group, w.bits))
-    assert K.kivi_device_fault() == 0
 
 
 def compare_store(cache, layer: int, st) -> None:
@@ -346,7 +345,6 @@ def test_prefill_flush_full_size_sampled(name):
         sample_values(np.ascontiguousarray(v[:, :n]), host_u32(cache.v_codes[l]),
                       host_f32_bits(cache.v_scale[l]), host_f32_bits(cache.v_zero[l]),
                       host_u16(vy[l]), w.group, w.bits, 200, rng)
-    assert K.kivi_device_fault() == 0
 
 
 @pytest.mark.slow
@@ -370,7 +368,6 @@ def test_large_store_sweep_full_size_sampled():
             sample_values(v, host_u32(c), host_f32_bits(s), host_f32_bits(z), host_u16(y),
                           group, bits, 60, rng)
             del c, s, z, y
-    assert K.kivi_device_fault() == 0
 
 
 @pytest.mark.slow
@@ -413,4 +410,3 @@ def test_batched_decode_flushes_full_size_sampled():
                           host_f32_bits(cache.v_zero[l]), None, w.group, w.bits, 100, rng,
                           out_r0=s_q0)
     assert cache.s_q == w.store_prefill + steps * w.new_per_step
-    assert K.kivi_device_fault() == 0
