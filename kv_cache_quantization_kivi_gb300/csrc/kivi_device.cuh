@@ -35,25 +35,18 @@ namespace kivi_dev {
 // group constants below use a threshold 1/2 - 2E, which also absorbs the
 // rounding of the threshold's own computation.
 //
-// rint(v) for 0 <= v < 2^22 is read from y = RN(v + 1.5*2^23): y lies in
+// rint(v) for |v| < 2^22 comes from y = RN(v + 1.5*2^23): y lies in
 // [2^23, 2^24) where the binary32 spacing is 1, so the addition itself
-// rounds v to an integer with ties to even, and the low mantissa bits of y
-// hold that integer (y's bit pattern is 0x4B400000 + n).
+// rounds v to an integer with ties to even, and n = y - 1.5*2^23 is that
+// integer, exactly.  codes2 below evaluates this for a pair of elements with
+// packed f32x2 operations.
 
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
-constexpr uint32_t kRoundMagicBits = 0x4B400000u;
 
 template <int BITS>
 struct CodeFmt {
   static constexpr int W = 32 / BITS;            // codes per uint32 word
   static constexpr uint32_t Q = (1u << BITS) - 1u;
-  // sum over the W slots of (kRoundMagicBits << slot*BITS) modulo 2^32: the
-  // offset to subtract after packing raw y bit patterns (see pack below)
-  __host__ __device__ static constexpr uint32_t magic_sum() {
-    uint32_t s = 0;
-    for (int i = 0; i < W; ++i) s += kRoundMagicBits << (i * BITS);
-    return s;
-  }
 };
 
 struct GroupQ {
@@ -83,17 +76,6 @@ __device__ __forceinline__ GroupQ make_group(float mn, float mx, float qf) {
     g.thr = 1.0f;
   }
   return g;
-}
-
-// Fast code of x: returns the bit pattern of y = RN(v + 1.5*2^23), i.e.
-// kRoundMagicBits + q, and sets `bad` when the decision needs the exact path.
-__device__ __forceinline__ uint32_t fast_code_bits(float x, const GroupQ &g, bool &bad) {
-  const float v = __fmaf_rn(x, g.r, g.c);
-  const float y = __fadd_rn(v, kRoundMagic);
-  const float n = __fsub_rn(y, kRoundMagic);
-  const float dist = __fsub_rn(v, n);
-  bad |= !(fabsf(dist) < g.thr);
-  return __float_as_uint(y);
 }
 
 // The defined code, computed literally (used when the fast path declines).
@@ -164,26 +146,25 @@ __device__ __forceinline__ GroupQ2 make_group2(const GroupQ &a, const GroupQ &b)
   return g;
 }
 
-// The defined codes of a pair, computed literally; returned in the same
-// encoding as the fast path (0x4B400000 + q per element).  Out of line: it
-// runs only for the rare pairs the fast path declines (mostly exact .5 ties,
-// which fp16 data produce often).
+// The defined codes of a pair, computed literally, as an f32x2 pair of
+// integer-valued floats.  Out of line: it runs only for the rare pairs the
+// fast path declines (mostly exact .5 ties, which fp16 data produce often).
 template <int BITS>
 __device__ __noinline__ uint64_t exact_codes2(float x0, float x1, float mn0, float mx0,
                                               float mn1, float mx1) {
   const float qf = static_cast<float>((1u << BITS) - 1u);
   const GroupQ g0 = make_group(mn0, mx0, qf);
   const GroupQ g1 = make_group(mn1, mx1, qf);
-  const uint32_t q0 = exact_code(x0, g0, qf);
-  const uint32_t q1 = exact_code(x1, g1, qf);
-  return (static_cast<uint64_t>(kRoundMagicBits + q1) << 32) | (kRoundMagicBits + q0);
+  return f2_pack(static_cast<float>(exact_code(x0, g0, qf)),
+                 static_cast<float>(exact_code(x1, g1, qf)));
 }
 
-// Codes of a pair: y = RN(v + 1.5*2^23) for both elements (bit patterns
-// 0x4B400000 + q).  The acceptance test of fast_code_bits, |v - rint(v)| <
-// thr, is evaluated as RN(d*d - RN(thr'^2)) < 0 (sign bit set); a pair with an
-// element outside it is recomputed by exact_codes2.  (mn0, mx0) and (mn1, mx1)
-// are the extremes of the two elements' groups.
+// Codes of a pair as integer-valued floats (q0, q1).  y = RN(v + 1.5*2^23)
+// rounds v to an integer, n = y - 1.5*2^23 is that integer exactly, and the
+// acceptance test |v - n| < thr is evaluated as RN(d*d - RN(thr'^2)) < 0
+// (sign bit set); a pair with an element outside it is recomputed by
+// exact_codes2.  (mn0, mx0) and (mn1, mx1) are the extremes
+// of the two elements' groups.
 template <int BITS>
 __device__ __forceinline__ uint64_t codes2(uint64_t x, const GroupQ2 &g, float mn0, float mx0,
                                            float mn1, float mx1) {
@@ -193,9 +174,30 @@ __device__ __forceinline__ uint64_t codes2(uint64_t x, const GroupQ2 &g, float m
   const uint64_t n = f2_sub(y, magic);
   const uint64_t d = f2_sub(v, n);
   const uint64_t e = f2_fma(d, d, g.neg_thr2);
-  if ((f2_lo_bits(e) & f2_hi_bits(e)) >> 31) return y;
+  if ((f2_lo_bits(e) & f2_hi_bits(e)) >> 31) return n;
   return exact_codes2<BITS>(__uint_as_float(f2_lo_bits(x)), __uint_as_float(f2_hi_bits(x)),
                             mn0, mx0, mn1, mx1);
+}
+
+// Packing.  Codes are small integers held exactly in binary32, so sums
+// q_a + q_b * 2^k (k a multiple of the code width) below 2^24 are exact; a
+// binary tree of such fused multiply-adds assembles a 16-bit half-word of
+// codes, y = half + 2^23 then holds it in its low 16 mantissa bits, and one
+// byte permute joins two half-words into a 32-bit code word (LSB first).
+__device__ __forceinline__ uint64_t f2_const(float c) { return f2_pack(c, c); }
+
+// Two 16-bit halves (as integer-valued floats) -> one word: lo | hi << 16.
+__device__ __forceinline__ uint32_t join_halves(float lo, float hi) {
+  const uint64_t b = f2_add(f2_pack(lo, hi), f2_const(8388608.0f));  // + 2^23
+  return __byte_perm(f2_lo_bits(b), f2_hi_bits(b), 0x5410);
+}
+// The same for two pairs of halves (elementwise): returns (lo.x | hi.x << 16,
+// lo.y | hi.y << 16).
+__device__ __forceinline__ uint2 join_halves2(uint64_t lo, uint64_t hi) {
+  const uint64_t a = f2_add(lo, f2_const(8388608.0f));
+  const uint64_t b = f2_add(hi, f2_const(8388608.0f));
+  return make_uint2(__byte_perm(f2_lo_bits(a), f2_lo_bits(b), 0x5410),
+                    __byte_perm(f2_hi_bits(a), f2_hi_bits(b), 0x5410));
 }
 
 // ---------------------------------------------------------------------------

@@ -114,7 +114,6 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
   constexpr int W = CodeFmt<BITS>::W;        // codes per word
   constexpr int WPT = 32 / W;                // words per channel per thread (= BITS)
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
-  constexpr uint32_t MAGIC_SUM = CodeFmt<BITS>::magic_sum();
   const float qf = static_cast<float>(Q);
 
   const int D = DC > 0 ? DC : p.d;           // head_dim, compile-time when DC > 0
@@ -197,18 +196,23 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
     }
 
     // Quantize and pack along tokens: WPT words per channel, word wi holds
-    // tokens [wi*W, wi*W + W) of this thread's 32.
+    // tokens [wi*W, wi*W + W) of this thread's 32 (token wi*W + j at bits
+    // [j*BITS, (j+1)*BITS)).  Each half-word (H = 16/BITS tokens) accumulates
+    // the code pairs of both channels with packed FMAs by powers of two.
+    constexpr int H = 16 / BITS;
 #pragma unroll
     for (int wi = 0; wi < WPT; ++wi) {
-      uint32_t a0 = 0u, a1 = 0u;
+      uint64_t half[2];
 #pragma unroll
-      for (int t = 0; t < W; ++t) {
-        const uint64_t y = codes2<BITS>(h2_to_f2(h[wi * W + t]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
-        // raw terms (0x4B400000 + q) << slot; the constant part is removed below
-        a0 += f2_lo_bits(y) << (t * BITS);
-        a1 += f2_hi_bits(y) << (t * BITS);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int t0 = wi * W + hh * H;
+        half[hh] = codes2<BITS>(h2_to_f2(h[t0]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
+#pragma unroll
+        for (int j = 1; j < H; ++j)
+          half[hh] = f2_fma(codes2<BITS>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y, mxf.y),
+                            f2_const(static_cast<float>(1u << (BITS * j))), half[hh]);
       }
-      st_stream(cdst + static_cast<int64_t>(wi) * D, make_uint2(a0 - MAGIC_SUM, a1 - MAGIC_SUM));
+      st_stream(cdst + static_cast<int64_t>(wi) * D, join_halves2(half[0], half[1]));
     }
   }
 }

@@ -55,7 +55,6 @@ __global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_consta
   constexpr int L = G / 32;               // lanes per group
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
-  constexpr uint32_t MAGIC_SUM = CodeFmt<BITS>::magic_sum();
   const float qf = static_cast<float>(Q);
 
   const int D = DC > 0 ? DC : p.d;          // head_dim, compile-time when DC > 0
@@ -134,18 +133,29 @@ __global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_consta
       }
     }
 
+    // Pack along channels: word wi holds channels [wi*W, wi*W + W) of this
+    // thread's 32.  A half-word (H = 16/BITS channels) accumulates its H/2
+    // channel pairs with packed FMAs by powers of two, which leaves even
+    // channels in the low and odd channels in the high element; one more FMA
+    // interleaves them.
+    constexpr int H = 16 / BITS;
     uint32_t w[BITS];
 #pragma unroll
     for (int wi = 0; wi < BITS; ++wi) {
-      uint32_t acc = 0u;
+      float half[2];
 #pragma unroll
-      for (int k = 0; k < W; k += 2) {
-        const int e = wi * W + k;  // even channel within the chunk
-        const uint64_t y = codes2<BITS>(h2_to_f2(h[e >> 1]), gq, gmn, gmx, gmn, gmx);
-        acc += f2_lo_bits(y) << (k * BITS);
-        acc += f2_hi_bits(y) << ((k + 1) * BITS);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int p0 = (wi * W + hh * H) / 2;   // first channel pair of the half
+        uint64_t acc = codes2<BITS>(h2_to_f2(h[p0]), gq, gmn, gmx, gmn, gmx);
+#pragma unroll
+        for (int j = 1; j < H / 2; ++j)
+          acc = f2_fma(codes2<BITS>(h2_to_f2(h[p0 + j]), gq, gmn, gmx, gmn, gmx),
+                       f2_const(static_cast<float>(1u << (2 * BITS * j))), acc);
+        // even channels (low) + odd channels (high) shifted by one code
+        half[hh] = __fmaf_rn(__uint_as_float(f2_hi_bits(acc)), static_cast<float>(1u << BITS),
+                             __uint_as_float(f2_lo_bits(acc)));
       }
-      w[wi] = acc - MAGIC_SUM;
+      w[wi] = join_halves(half[0], half[1]);
     }
 
     uint32_t *dst = job.codes + t.b * p.codes_bh_stride + out_row * (D / W) + t.k * BITS;
@@ -160,6 +170,15 @@ __global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_consta
   }
 }
 
+// Dequantize: a thread reconstructs the 32 channels of one (row, chunk) unit
+// (codes, scale and zero read with 8/16-byte and 4-byte loads).  Its 64 bytes
+// of fp16 output are then exchanged through a per-warp shared-memory block
+// (32 units x 64 bytes, 16 bytes of padding per unit against bank conflicts)
+// so that each 16-byte store instruction of the warp writes 512 consecutive
+// bytes: lane l stores chunk l + 32 i of the block, whose destination is that
+// of unit (l + 32 i) / 4, taken from the owning lane by a shuffle.
+constexpr int kDqUnitWords = 20;   // 64 bytes of data + 16 bytes of padding
+
 template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(256)
     value_dequant_kernel(const __grid_constant__ DequantParams p) {
@@ -169,48 +188,70 @@ __global__ void __launch_bounds__(256)
   const int D = DC > 0 ? DC : p.d;
   const uint32_t total = static_cast<uint32_t>(p.n_jobs) * static_cast<uint32_t>(p.bh) *
                          static_cast<uint32_t>(p.rows) * p.div_chunks.d;
+  const uint32_t lane = threadIdx.x & 31u;
   const uint32_t stride = gridDim.x * blockDim.x;
+  __shared__ __align__(16) uint32_t stage[256 / 32][32 * kDqUnitWords];
+  uint32_t *blk = stage[threadIdx.x >> 5];
 
 #pragma unroll 1
-  for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
-    const RowRef t = decode_unit(u, p);
+  for (uint32_t base = (blockIdx.x * blockDim.x + threadIdx.x) & ~31u; base < total;
+       base += stride) {
+    const uint32_t u = base + lane;
+    const bool active = u < total;
+    const RowRef t = decode_unit(active ? u : base, p);
     const DequantJob &J = p.jobs[t.job];
-    const uint32_t *src = J.codes + t.b * p.codes_bh_stride + static_cast<int64_t>(t.r) * (D / W) +
-                          t.k * BITS;
-    uint32_t w[BITS];
-    if (BITS == 2) {
-      const uint2 a = __ldcs(reinterpret_cast<const uint2 *>(src));
-      w[0] = a.x;
-      w[1 % BITS] = a.y;
-    } else {
-#pragma unroll
-      for (int i = 0; i < BITS; i += 4) {
-        const uint4 a = ld_stream(src + i);
-        w[i % BITS] = a.x;
-        w[(i + 1) % BITS] = a.y;
-        w[(i + 2) % BITS] = a.z;
-        w[(i + 3) % BITS] = a.w;
-      }
-    }
-    const int64_t so = t.b * p.sz_bh_stride + static_cast<int64_t>(t.r) * (D / G) + t.k / L;
-    const float sc = __ldcs(J.scale + so);
-    const float ze = __ldcs(J.zero + so);
-    const float nsc = __fmul_rn(sc, -8388608.0f);  // -2^23 * scale, exact
-
-    uint32_t out[16];
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const uint32_t q0 = (w[e / W] >> ((e % W) * BITS)) & Q;
-      const uint32_t q1 = (w[(e + 1) / W] >> (((e + 1) % W) * BITS)) & Q;
-      const float r0 = recon_f32(q0, sc, nsc, ze);
-      const float r1 = recon_f32(q1, sc, nsc, ze);
-      out[e >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
-    }
     __half *y = static_cast<__half *>(J.y) + t.b * p.y_bh_stride + static_cast<int64_t>(t.r) * D +
                 t.k * 32;
+    if (active) {
+      const uint32_t *src = J.codes + t.b * p.codes_bh_stride +
+                            static_cast<int64_t>(t.r) * (D / W) + t.k * BITS;
+      uint32_t w[BITS];
+      if (BITS == 2) {
+        const uint2 a = __ldcs(reinterpret_cast<const uint2 *>(src));
+        w[0] = a.x;
+        w[1 % BITS] = a.y;
+      } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      st_stream(y + 8 * i, make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]));
+        for (int i = 0; i < BITS; i += 4) {
+          const uint4 a = ld_stream(src + i);
+          w[i % BITS] = a.x;
+          w[(i + 1) % BITS] = a.y;
+          w[(i + 2) % BITS] = a.z;
+          w[(i + 3) % BITS] = a.w;
+        }
+      }
+      const int64_t so = t.b * p.sz_bh_stride + static_cast<int64_t>(t.r) * (D / G) + t.k / L;
+      const float sc = __ldcs(J.scale + so);
+      const float ze = __ldcs(J.zero + so);
+      const float nsc = __fmul_rn(sc, -8388608.0f);  // -2^23 * scale, exact
+
+      uint32_t out[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const uint32_t q0 = (w[e / W] >> ((e % W) * BITS)) & Q;
+        const uint32_t q1 = (w[(e + 1) / W] >> (((e + 1) % W) * BITS)) & Q;
+        const float r0 = recon_f32(q0, sc, nsc, ze);
+        const float r1 = recon_f32(q1, sc, nsc, ze);
+        out[e >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4 *>(blk + lane * kDqUnitWords + 4 * i) =
+            make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+    }
+    __syncwarp();
+    const unsigned long long ybits = reinterpret_cast<unsigned long long>(y);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t j = lane + 32u * i;      // chunk of the warp block
+      const uint32_t owner = j >> 2;          // unit (lane) that produced it
+      const unsigned long long dst = __shfl_sync(0xffffffffu, ybits, owner);
+      if (base + owner < total) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(blk + owner * kDqUnitWords + 4 * (j & 3));
+        st_stream(reinterpret_cast<__half *>(dst) + 8 * (j & 3), v);
+      }
+    }
+    __syncwarp();
   }
 }
 
