@@ -47,9 +47,6 @@ __device__ __forceinline__ RowRef decode_unit(uint32_t u, const P &p) {
   return t;
 }
 
-__device__ __forceinline__ float h2lo(__half2 h) { return __low2float(h); }
-__device__ __forceinline__ float h2hi(__half2 h) { return __high2float(h); }
-
 template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr int L = G / 32;               // lanes per group
