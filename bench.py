@@ -44,7 +44,6 @@ if ROOT not in sys.path:
 METRIC = "quantize+dequant HBM GB/s (bytes in+out) and % of GB300 HBM peak"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNELS = ("key_quant", "value_quant", "key_dequant", "value_dequant")
 CSRC_FILES = ("kivi_api.cu", "kivi_keys.cu", "kivi_values.cu", "kivi_device.cuh", "kivi_launch.h",
               "kivi_dispatch.h")
 
@@ -174,9 +173,14 @@ def pinned_u16(shape):
 
 
 class PrefillFlush:
-    """All layers' residual rings hold the prompt; flush + dequantize."""
+    """All layers' residual rings hold the prompt; one step = flush (all
+    layers, keys then values) + dequantization of the store (all layers)."""
+
+    kernels = ("key_quant", "value_quant", "key_dequant", "value_dequant")
+    events_per_step = 6
 
     def __init__(self, w, device):
+        import ctypes as C
         import torch
         import kv_cache_quantization_kivi_gb300 as K
         import workloads as W
@@ -195,22 +199,37 @@ class PrefillFlush:
         self.cache.v_res_all.copy_(self.v_host_t.to(device))
         self.k_out = torch.empty((L, bh, self.n, d), dtype=torch.float16, device=device)
         self.v_out = torch.empty((L, bh, self.n, d), dtype=torch.float16, device=device)
-        import ctypes as C
         self.k_ptrs = (C.c_void_p * L)(*[t.data_ptr() for t in self.k_out.unbind(0)])
         self.v_ptrs = (C.c_void_p * L)(*[t.data_ptr() for t in self.v_out.unbind(0)])
         elems = L * bh * self.n * d
         bpe = bytes_per_elem(w.bits, w.group)
-        self.kernel_bytes = {k: elems * bpe for k in KERNELS}
+        self.kernel_bytes = {k: elems * bpe for k in self.kernels}
         self.step_bytes = 4 * elems * bpe
         self.launches_per_step = 4
 
-    def step(self, stream, ev_q=None, ev_dq=None):
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "layers": w.layers, "bh": w.bh, "seq": w.seq,
+                "head_dim": w.head_dim, "bits": w.bits, "group": w.group,
+                "residual": w.residual, "tokens_flushed_per_layer": self.n,
+                "step": "flush (per-channel key + per-token value quantize, pack, bookkeeping) "
+                        "+ dequantize of the store, all layers"}
+
+    def step(self, stream, ev=None):
         c = self.cache
         c.reset(s_q=0, res_head=0, n_res=self.w.seq)
-        n = c.flush(stream, ev_q)
+        n = c.flush(stream, None if ev is None else ev[0])
         assert n == self.n
         self.K.kivi_dequantize_cache(c.layers, c.n_layers, c.state, self.k_ptrs, self.v_ptrs,
-                                     stream, ev_dq)
+                                     stream, None if ev is None else ev[1])
+
+    def step_events(self, evs):
+        """Event handles for one step from its events_per_step torch events."""
+        return (self.K.event_handles(evs[0:3]), self.K.event_handles(evs[3:6]))
+
+    def kernel_times(self, e):
+        return {"key_quant": e[0].elapsed_time(e[1]), "value_quant": e[1].elapsed_time(e[2]),
+                "key_dequant": e[3].elapsed_time(e[4]), "value_dequant": e[4].elapsed_time(e[5])}
 
     def e2e_setup(self):
         import torch
@@ -261,7 +280,213 @@ class PrefillFlush:
         return done_bytes, t_total, f"{layers} of {w.layers} layers (flush + dequantize, keys and values)"
 
 
-def make_workload(name, device, layers=None):
+class DecodeFlush:
+    """Batched decode: every layer's store already holds 2048 tokens per
+    sequence; a step flushes the 32 oldest of the 64 residual tokens of every
+    layer (keys and values) into the store.  The residual ring holds 64
+    tokens (written by the attention layer, untimed); the flushed half
+    alternates, and the store offset cycles over 100 consecutive flushes."""
+
+    kernels = ("key_quant", "value_quant")
+    events_per_step = 3
+
+    def __init__(self, w, device):
+        import torch
+        import kv_cache_quantization_kivi_gb300 as K
+        import workloads as W
+        self.w, self.K = w, K
+        L, bh, d, G = w.layers, w.bh, w.head_dim, w.group
+        self.r_cap = 2 * w.residual
+        self.cycle = w.steps
+        cap = w.store_prefill + w.new_per_step * self.cycle
+        self.cache = K.KiviCache(L, bh, d, r_cap=self.r_cap, cap=cap, group=G, bits=w.bits,
+                                 residual=w.residual, device=device)
+        self.k_host_t, self.k_host = pinned_u16((L, bh, self.r_cap, d))
+        self.v_host_t, self.v_host = pinned_u16((L, bh, self.r_cap, d))
+        for l in range(L):
+            W.fill(w, l, "k", self.k_host[l], tok0=w.store_prefill)
+            W.fill(w, l, "v", self.v_host[l], tok0=w.store_prefill)
+        self.cache.k_res_all.copy_(self.k_host_t.to(device))
+        self.cache.v_res_all.copy_(self.v_host_t.to(device))
+        self.i = 0
+        elems = L * bh * w.new_per_step * d
+        bpe = bytes_per_elem(w.bits, G)
+        self.kernel_bytes = {k: elems * bpe for k in self.kernels}
+        self.step_bytes = 2 * elems * bpe
+        self.launches_per_step = 2
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "layers": w.layers, "bh": w.bh, "head_dim": w.head_dim,
+                "bits": w.bits, "group": w.group, "residual": w.residual,
+                "store_tokens": w.store_prefill, "tokens_flushed_per_step": w.new_per_step,
+                "consecutive_flushes": self.cycle,
+                "step": "one decode flush of every layer (keys and values)"}
+
+    def step(self, stream, ev=None):
+        w, c = self.w, self.cache
+        j = self.i % self.cycle
+        c.reset(s_q=w.store_prefill + w.new_per_step * j,
+                res_head=(w.new_per_step * self.i) % self.r_cap, n_res=self.r_cap)
+        self.i += 1
+        n = c.flush(stream, ev)
+        assert n == w.new_per_step
+
+    def step_events(self, evs):
+        return self.K.event_handles(evs[0:3])
+
+    def kernel_times(self, e):
+        return {"key_quant": e[0].elapsed_time(e[1]), "value_quant": e[1].elapsed_time(e[2])}
+
+    def e2e_setup(self):
+        import torch
+        w = self.w
+        # per step: the 32 new tokens of every layer in, the flushed store slice out
+        L, bh, d, G = w.layers, w.bh, w.head_dim, w.group
+        n = w.new_per_step
+        self.new_k = self.k_host_t[:, :, :n].clone().pin_memory()
+        self.new_v = self.v_host_t[:, :, :n].clone().pin_memory()
+        Wd = 32 // w.bits
+        self.back = [torch.empty((L, bh, n // Wd, d), dtype=torch.int32, pin_memory=True),
+                     torch.empty((L, bh, n // G, d), dtype=torch.float32, pin_memory=True),
+                     torch.empty((L, bh, n // G, d), dtype=torch.float32, pin_memory=True),
+                     torch.empty((L, bh, n, d // Wd), dtype=torch.int32, pin_memory=True),
+                     torch.empty((L, bh, n, d // G), dtype=torch.float32, pin_memory=True),
+                     torch.empty((L, bh, n, d // G), dtype=torch.float32, pin_memory=True)]
+        h2d = 2 * self.new_k.numel() * 2
+        d2h = sum(t.numel() * t.element_size() for t in self.back)
+        return h2d, d2h
+
+    def e2e_step(self, stream):
+        w, c = self.w, self.cache
+        n, G = w.new_per_step, w.group
+        Wd = 32 // w.bits
+        head_new = (w.new_per_step * (self.i + 1)) % self.r_cap  # the half not flushed now
+        c.k_res_all[:, :, head_new:head_new + n].copy_(self.new_k, non_blocking=True)
+        c.v_res_all[:, :, head_new:head_new + n].copy_(self.new_v, non_blocking=True)
+        s_q = w.store_prefill + n * (self.i % self.cycle)
+        self.step(stream)
+        srcs = [c.k_codes_all[:, :, s_q // Wd:(s_q + n) // Wd], c.k_scale_all[:, :, s_q // G:(s_q + n) // G],
+                c.k_zero_all[:, :, s_q // G:(s_q + n) // G], c.v_codes_all[:, :, s_q:s_q + n],
+                c.v_scale_all[:, :, s_q:s_q + n], c.v_zero_all[:, :, s_q:s_q + n]]
+        for dst, src in zip(self.back, srcs):
+            dst.copy_(src, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        import oracle as O
+        w = self.w
+        done, t_total, layers = 0.0, 0.0, 0
+        cap = w.store_prefill + w.new_per_step
+        for l in range(w.layers):
+            st = O.Store(w.bh, w.head_dim, cap, w.group, w.bits)
+            t0 = time.perf_counter()
+            n, _, _, _ = O.flush(self.k_host[l], self.v_host[l], st, w.residual,
+                                 w.store_prefill, 0, self.r_cap)
+            t_total += time.perf_counter() - t0
+            done += 2 * w.bh * n * w.head_dim * bytes_per_elem(w.bits, w.group)
+            layers += 1
+            if t_total >= budget_s:
+                break
+        return done, t_total, f"{layers} of {w.layers} layers (one decode flush, keys and values)"
+
+
+class StoreSweep:
+    """Full-tensor quantize of keys and values, then full dequantize, of a
+    [bh, S, d] store at one (bits, group) point of the sweep."""
+
+    kernels = ("key_quant", "value_quant", "key_dequant", "value_dequant")
+    events_per_step = 5
+
+    def __init__(self, w, device, bits, group):
+        import torch
+        import kv_cache_quantization_kivi_gb300 as K
+        import workloads as W
+        self.w, self.K, self.bits, self.group = w, K, bits, group
+        bh, S, d = w.bh, w.seq, w.head_dim
+        self.k_host_t, self.k_host = pinned_u16((bh, S, d))
+        self.v_host_t, self.v_host = pinned_u16((bh, S, d))
+        W.fill(w, 0, "k", self.k_host)
+        W.fill(w, 0, "v", self.v_host)
+        self.k = self.k_host_t.to(device)
+        self.v = self.v_host_t.to(device)
+        self.kc, self.ks, self.kz = K.kivi_quantize_keys(self.k, group, bits)
+        self.vc, self.vs, self.vz = K.kivi_quantize_values(self.v, group, bits)
+        self.ky = torch.empty_like(self.k)
+        self.vy = torch.empty_like(self.v)
+        elems = bh * S * d
+        bpe = bytes_per_elem(bits, group)
+        self.kernel_bytes = {k: elems * bpe for k in self.kernels}
+        self.step_bytes = 4 * elems * bpe
+        self.launches_per_step = 4
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "bh": w.bh, "seq": w.seq, "head_dim": w.head_dim,
+                "bits": self.bits, "group": self.group,
+                "step": "full quantize of keys and values, then full dequantize"}
+
+    def step(self, stream, ev=None):
+        K, S, g, b = self.K, self.w.seq, self.group, self.bits
+        if ev is not None:
+            ev[0].record(stream)
+        K.kivi_quantize_keys(self.k, g, b, self.kc, self.ks, self.kz, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        K.kivi_quantize_values(self.v, g, b, self.vc, self.vs, self.vz, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        K.kivi_dequantize_keys(self.kc, self.ks, self.kz, S, g, b, self.ky, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        K.kivi_dequantize_values(self.vc, self.vs, self.vz, g, b, y=self.vy, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    def step_events(self, evs):
+        return evs
+
+    def kernel_times(self, e):
+        return {"key_quant": e[0].elapsed_time(e[1]), "value_quant": e[1].elapsed_time(e[2]),
+                "key_dequant": e[2].elapsed_time(e[3]), "value_dequant": e[3].elapsed_time(e[4])}
+
+    def e2e_setup(self):
+        import torch
+        self.back = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                     for t in (self.ky, self.vy, self.kc, self.ks, self.kz, self.vc, self.vs,
+                               self.vz)]
+        h2d = 2 * self.k_host_t.numel() * 2
+        d2h = sum(t.numel() * t.element_size() for t in self.back)
+        return h2d, d2h
+
+    def e2e_step(self, stream):
+        self.k.copy_(self.k_host_t, non_blocking=True)
+        self.v.copy_(self.v_host_t, non_blocking=True)
+        self.step(stream)
+        for dst, src in zip(self.back, (self.ky, self.vy, self.kc, self.ks, self.kz, self.vc,
+                                        self.vs, self.vz)):
+            dst.copy_(src, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        import oracle as O
+        w, g, b = self.w, self.group, self.bits
+        done, t_total, rows = 0.0, 0.0, 0
+        for i in range(w.bh):
+            k = self.k_host[i:i + 1]
+            v = self.v_host[i:i + 1]
+            t0 = time.perf_counter()
+            c, s, z = O.quantize_keys(k, g, b)
+            O.dequantize_keys(c, s, z, w.seq, g, b)
+            c, s, z = O.quantize_values(v, g, b)
+            O.dequantize_values(c, s, z, g, b)
+            t_total += time.perf_counter() - t0
+            done += 4 * w.seq * w.head_dim * bytes_per_elem(b, g)
+            rows += 1
+            if t_total >= budget_s:
+                break
+        return done, t_total, f"{rows} of {w.bh} bh slices (quantize + dequantize, keys and values)"
+
+
+def make_workload(name, device, layers=None, bits=None, group=None):
     import dataclasses
     import workloads as W
     w = W.CONFIGS[name]
@@ -269,8 +494,11 @@ def make_workload(name, device, layers=None):
         w = dataclasses.replace(w, layers=int(layers))
     if name in ("llama3_2_3b_prefill", "qwen2_5_7b_long", "tiny_flush"):
         return PrefillFlush(w, device)
-    raise SystemExit(f"workload {name!r} is not a bench line (parity-test case); "
-                     f"choose llama3_2_3b_prefill or qwen2_5_7b_long")
+    if name == "batched_decode":
+        return DecodeFlush(w, device)
+    if name == "large_store_sweep":
+        return StoreSweep(w, device, bits or 2, group or 32)
+    raise SystemExit(f"unknown workload {name!r}")
 
 
 # ---------------------------------------------------------------------------
@@ -324,7 +552,7 @@ def run_kivi(args):
     torch.cuda.set_device(device)
     import kv_cache_quantization_kivi_gb300 as K
     K.lib()
-    wl = make_workload(args.workload, device, args.layers)
+    wl = make_workload(args.workload, device, args.layers, args.bits, args.group)
     stream = torch.cuda.current_stream(device)
 
     def new_events(n):
@@ -337,9 +565,8 @@ def run_kivi(args):
         wl.step(stream)
     torch.cuda.synchronize(device)
 
-    # per-launch events: [q0, q1, q2, dq0, dq1, dq2] per step
-    evs = [new_events(6) for _ in range(args.steps)]
-    handles = [(K.event_handles(e[0:3]), K.event_handles(e[3:6])) for e in evs]
+    evs = [new_events(wl.events_per_step) for _ in range(args.steps)]
+    handles = [wl.step_events(e) for e in evs]
     start, end = new_events(2)
     torch.cuda.synchronize(device)
 
@@ -351,7 +578,7 @@ def run_kivi(args):
     torch.cuda.synchronize(device)
     start.record(stream)
     for i in range(args.steps):
-        wl.step(stream, handles[i][0], handles[i][1])
+        wl.step(stream, handles[i])
     end.record(stream)
     torch.cuda.synchronize(device)
     barrier()
@@ -363,21 +590,20 @@ def run_kivi(args):
     total_bytes = reduce_sum(wl.step_bytes * args.steps, device)
     value = total_bytes / (elapsed_ms * 1e-3) / 1e9
 
-    k_ms = {k: [] for k in KERNELS}
+    k_ms = {k: [] for k in wl.kernels}
     for e in evs:
-        k_ms["key_quant"].append(e[0].elapsed_time(e[1]))
-        k_ms["value_quant"].append(e[1].elapsed_time(e[2]))
-        k_ms["key_dequant"].append(e[3].elapsed_time(e[4]))
-        k_ms["value_dequant"].append(e[4].elapsed_time(e[5]))
+        for k, t in wl.kernel_times(e).items():
+            k_ms[k].append(t)
     peak, peak_kind = measured_peaks()
+    total_kernel_ms = sum(sum(v) for v in k_ms.values())
     kernels = {}
-    for k in KERNELS:
+    for k in wl.kernels:
         avg = sum(k_ms[k]) / len(k_ms[k])
         gbs = wl.kernel_bytes[k] / (avg * 1e-3) / 1e9
         kernels[k] = {"avg_us": round(avg * 1e3, 2), "gbs": round(gbs, 1),
                       "frac_of_measured": round(gbs / peak, 4),
-                      "share": round(sum(k_ms[k]) / sum(sum(v) for v in k_ms.values()), 4)}
-    dom = max(KERNELS, key=lambda k: sum(k_ms[k]))
+                      "share": round(sum(k_ms[k]) / total_kernel_ms, 4)}
+    dom = max(wl.kernels, key=lambda k: sum(k_ms[k]))
     dom_avg_s = sum(k_ms[dom]) / len(k_ms[dom]) * 1e-3
     achieved = wl.kernel_bytes[dom] / dom_avg_s / 1e9
     traffic = ncu_traffic(args.workload, dom)
@@ -387,7 +613,7 @@ def run_kivi(args):
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "algorithmic_bytes_per_launch": wl.kernel_bytes[dom], "traffic": traffic}
 
-    # end to end: pinned host inputs -> device -> flush + dequantize -> host
+    # end to end: pinned host inputs -> device -> kernels -> host
     e2e = None
     if args.e2e_steps > 0:
         h2d, d2h = wl.e2e_setup()
@@ -413,21 +639,17 @@ def run_kivi(args):
         cpu = {"value": round(cb / cs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{what}; {cs:.1f} s single-threaded on the host"}
 
-    w = wl.w
+    config = wl.config()
+    config["bytes_per_step"] = wl.step_bytes
+    config["l2"] = ("no flush: each step reads and writes ~%.2f GB, more than the 129 MB L2"
+                    % (wl.step_bytes / 1e9))
+    config["parallelism"] = f"independent replicas x{ws}" if ws > 1 else "single GPU"
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded counter-based generator, shapes of the pages' models)",
-        "config": {"workload": w.name, "layers": w.layers, "bh": w.bh, "seq": w.seq,
-                   "head_dim": w.head_dim, "bits": w.bits, "group": w.group,
-                   "residual": w.residual, "tokens_flushed_per_layer": wl.n,
-                   "step": "flush (per-channel key + per-token value quantize, pack, "
-                           "bookkeeping) + dequantize of the store, all layers",
-                   "bytes_per_step": wl.step_bytes,
-                   "l2": "no flush: each step reads and writes ~%.2f GB, more than the 129 MB L2"
-                         % (wl.step_bytes / 1e9),
-                   "parallelism": f"independent replicas x{ws}" if ws > 1 else "single GPU"},
+        "config": config,
         "pct_of_hbm_peak": {"measured_copy": round(value / ws / peak * 100, 2),
                             "nominal_8tbs": round(value / ws / NOMINAL_HBM_GBS * 100, 2)},
         "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
@@ -519,6 +741,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--json-out", default=None)
+    ap.add_argument("--bits", type=int, default=None, help="large_store_sweep: code width")
+    ap.add_argument("--group", type=int, default=None, help="large_store_sweep: group size")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (profiling runs only; "
                          "the reported config says so)")

@@ -147,25 +147,31 @@ __device__ __forceinline__ GroupQ2 make_group2(const GroupQ &a, const GroupQ &b)
 }
 
 // The defined codes of a pair, computed literally, as an f32x2 pair of
-// integer-valued floats.  Out of line: it runs only for the rare pairs the
-// fast path declines (mostly exact .5 ties, which fp16 data produce often).
+// integer-valued floats.  It runs only for the rare pairs the fast path
+// declines (mostly exact .5 ties, which fp16 data produce often).
 template <int BITS>
-__device__ __noinline__ uint64_t exact_codes2(float x0, float x1, float mn0, float mx0,
-                                              float mn1, float mx1) {
+__device__ __forceinline__ uint64_t exact_codes2_inline(float x0, float x1, float mn0, float mx0,
+                                                     float mn1, float mx1) {
   const float qf = static_cast<float>((1u << BITS) - 1u);
   const GroupQ g0 = make_group(mn0, mx0, qf);
   const GroupQ g1 = make_group(mn1, mx1, qf);
   return f2_pack(static_cast<float>(exact_code(x0, g0, qf)),
                  static_cast<float>(exact_code(x1, g1, qf)));
 }
+template <int BITS>
+__device__ __noinline__ uint64_t exact_codes2_outline(float x0, float x1, float mn0, float mx0,
+                                                      float mn1, float mx1) {
+  return exact_codes2_inline<BITS>(x0, x1, mn0, mx0, mn1, mx1);
+}
 
 // Codes of a pair as integer-valued floats (q0, q1).  y = RN(v + 1.5*2^23)
 // rounds v to an integer, n = y - 1.5*2^23 is that integer exactly, and the
 // acceptance test |v - n| < thr is evaluated as RN(d*d - RN(thr'^2)) < 0
-// (sign bit set); a pair with an element outside it is recomputed by
-// exact_codes2.  (mn0, mx0) and (mn1, mx1) are the extremes
-// of the two elements' groups.
-template <int BITS>
+// (sign bit set); a pair with an element outside it is recomputed by the
+// literal division (out of line when OUTLINE, where register pressure makes
+// inlined copies spill).  (mn0, mx0) and (mn1, mx1) are the extremes of the
+// two elements' groups.
+template <int BITS, bool OUTLINE>
 __device__ __forceinline__ uint64_t codes2(uint64_t x, const GroupQ2 &g, float mn0, float mx0,
                                            float mn1, float mx1) {
   const uint64_t magic = f2_pack(kRoundMagic, kRoundMagic);
@@ -175,8 +181,25 @@ __device__ __forceinline__ uint64_t codes2(uint64_t x, const GroupQ2 &g, float m
   const uint64_t d = f2_sub(v, n);
   const uint64_t e = f2_fma(d, d, g.neg_thr2);
   if ((f2_lo_bits(e) & f2_hi_bits(e)) >> 31) return n;
-  return exact_codes2<BITS>(__uint_as_float(f2_lo_bits(x)), __uint_as_float(f2_hi_bits(x)),
-                            mn0, mx0, mn1, mx1);
+  const float x0 = __uint_as_float(f2_lo_bits(x)), x1 = __uint_as_float(f2_hi_bits(x));
+  return OUTLINE ? exact_codes2_outline<BITS>(x0, x1, mn0, mx0, mn1, mx1)
+                 : exact_codes2_inline<BITS>(x0, x1, mn0, mx0, mn1, mx1);
+}
+
+// The same without a branch: the sign bits of the acceptance test are AND-ed
+// into neg_acc (its top bit ends clear if some element needs the exact path),
+// so a whole word of pairs is one basic block and its instructions
+// interleave; a word whose flag is clear is recomputed with codes2.
+__device__ __forceinline__ uint64_t codes2_nobranch(uint64_t x, const GroupQ2 &g,
+                                                    uint32_t &neg_acc) {
+  const uint64_t magic = f2_pack(kRoundMagic, kRoundMagic);
+  const uint64_t v = f2_fma(x, g.r, g.c);
+  const uint64_t y = f2_add(v, magic);
+  const uint64_t n = f2_sub(y, magic);
+  const uint64_t d = f2_sub(v, n);
+  const uint64_t e = f2_fma(d, d, g.neg_thr2);
+  neg_acc &= f2_lo_bits(e) & f2_hi_bits(e);
+  return n;
 }
 
 // Packing.  Codes are small integers held exactly in binary32, so sums

@@ -202,14 +202,18 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
     constexpr int H = 16 / BITS;
 #pragma unroll
     for (int wi = 0; wi < WPT; ++wi) {
+      // (a pair the fast path declines is recomputed on the spot.  Measured
+      // alternatives -- a branch-free check per half with a redo of the half
+      // from registers or from global memory -- were slower here: the 32
+      // tokens a thread holds leave no registers for the longer live ranges.)
       uint64_t half[2];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int t0 = wi * W + hh * H;
-        half[hh] = codes2<BITS>(h2_to_f2(h[t0]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
+        half[hh] = codes2<BITS, true>(h2_to_f2(h[t0]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
 #pragma unroll
         for (int j = 1; j < H; ++j)
-          half[hh] = f2_fma(codes2<BITS>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y, mxf.y),
+          half[hh] = f2_fma(codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y, mxf.y),
                             f2_const(static_cast<float>(1u << (BITS * j))), half[hh]);
       }
       st_stream(cdst + static_cast<int64_t>(wi) * D, join_halves2(half[0], half[1]));

@@ -139,19 +139,30 @@ __global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_consta
     uint32_t w[BITS];
 #pragma unroll
     for (int wi = 0; wi < BITS; ++wi) {
-      float half[2];
+      uint64_t acc[2];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int p0 = (wi * W + hh * H) / 2;   // first channel pair of the half
-        uint64_t acc = codes2<BITS>(h2_to_f2(h[p0]), gq, gmn, gmx, gmn, gmx);
+        uint32_t neg_acc = 0xFFFFFFFFu;
+        acc[hh] = codes2_nobranch(h2_to_f2(h[p0]), gq, neg_acc);
 #pragma unroll
         for (int j = 1; j < H / 2; ++j)
-          acc = f2_fma(codes2<BITS>(h2_to_f2(h[p0 + j]), gq, gmn, gmx, gmn, gmx),
-                       f2_const(static_cast<float>(1u << (2 * BITS * j))), acc);
-        // even channels (low) + odd channels (high) shifted by one code
-        half[hh] = __fmaf_rn(__uint_as_float(f2_hi_bits(acc)), static_cast<float>(1u << BITS),
-                             __uint_as_float(f2_lo_bits(acc)));
+          acc[hh] = f2_fma(codes2_nobranch(h2_to_f2(h[p0 + j]), gq, neg_acc),
+                           f2_const(static_cast<float>(1u << (2 * BITS * j))), acc[hh]);
+        if (!(neg_acc >> 31)) {  // rare: redo this half pair by pair, exactly where needed
+          acc[hh] = codes2<BITS, false>(h2_to_f2(h[p0]), gq, gmn, gmx, gmn, gmx);
+#pragma unroll
+          for (int j = 1; j < H / 2; ++j)
+            acc[hh] = f2_fma(codes2<BITS, false>(h2_to_f2(h[p0 + j]), gq, gmn, gmx, gmn, gmx),
+                             f2_const(static_cast<float>(1u << (2 * BITS * j))), acc[hh]);
+        }
       }
+      // even channels (low) + odd channels (high) shifted by one code
+      float half[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        half[hh] = __fmaf_rn(__uint_as_float(f2_hi_bits(acc[hh])), static_cast<float>(1u << BITS),
+                             __uint_as_float(f2_lo_bits(acc[hh])));
       w[wi] = join_halves(half[0], half[1]);
     }
 
