@@ -141,6 +141,37 @@ KIVI_API kivi_status kivi_dequantize_values(const uint32_t *codes, int64_t codes
                                    kivi_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Fused fake quantization: quantize and dequantize in one pass             */
+/* ------------------------------------------------------------------------ */
+
+/* The fp16 reconstruction y = dequantize(quantize(x)) written in the same
+ * pass that makes the codes, with no round trip of the codes through memory
+ * (fused-kernel post, "What we're actually optimizing" and "1. FMA
+ * contraction": its kernels quantize and dequantize in one dispatch and
+ * return the reconstruction).  y is bit-identical to kivi_quantize_* followed
+ * by kivi_dequantize_* on the same arguments.  For keys of a ragged last
+ * group only the real tokens are written (the padding exists only inside
+ * the group's statistics).
+ *   x      device fp16 [bh][s][d], bh stride x_bh_stride >= s*d
+ *   y      device fp16 [bh][s][d], bh stride y_bh_stride >= s*d; must not
+ *          overlap x
+ *   codes, scale, zero, codes_bh_stride, sz_bh_stride
+ *          as for kivi_quantize_keys / kivi_quantize_values, written too; or
+ *          all three NULL (strides ignored) for the reconstruction alone
+ * Returns KIVI_OK, KIVI_ERR_INVAL (also when only some of codes, scale,
+ * zero are NULL), KIVI_ERR_ALIGN or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_fakequant_keys(const void *x, int64_t bh, int64_t s, int64_t d,
+                                         int64_t x_bh_stride, int group, int bits, void *y,
+                                         int64_t y_bh_stride, uint32_t *codes,
+                                         int64_t codes_bh_stride, float *scale, float *zero,
+                                         int64_t sz_bh_stride, kivi_stream_t stream);
+KIVI_API kivi_status kivi_fakequant_values(const void *x, int64_t bh, int64_t s, int64_t d,
+                                           int64_t x_bh_stride, int group, int bits, void *y,
+                                           int64_t y_bh_stride, uint32_t *codes,
+                                           int64_t codes_bh_stride, float *scale, float *zero,
+                                           int64_t sz_bh_stride, kivi_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Residual window and flush                                                */
 /* ------------------------------------------------------------------------ */
 
@@ -196,6 +227,23 @@ KIVI_API int64_t kivi_flush_size(int64_t n_res, int residual, int group);
  * unchanged, nothing launched) or KIVI_ERR_CUDA. */
 KIVI_API kivi_status kivi_flush(const kivi_layer *layers, int n_layers, kivi_cache *cache,
                        int64_t *n_flushed, kivi_stream_t stream);
+
+/* Fused fake-quant flush: kivi_flush that also writes the fp16
+ * reconstruction of the n flushed tokens of every layer into k_hat[l],
+ * v_hat[l] (host arrays of n_layers device pointers, each fp16
+ * [bh][cap][d] contiguous), at token rows s_q .. s_q + n - 1: the
+ * dequantized store kept as fp16, filled in the flush's own pass (the
+ * post's cache holds exactly this reconstruction).  A layer's three key
+ * store pointers (k_codes, k_scale, k_zero) may all be NULL, and likewise
+ * its three value store pointers: that store is then not written.  The rows
+ * written equal those kivi_dequantize_cache would produce from the store.
+ * events: as for kivi_flush_timed (may be NULL).
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN, KIVI_ERR_CAPACITY or
+ * KIVI_ERR_CUDA, with the state rules of kivi_flush. */
+KIVI_API kivi_status kivi_flush_fakequant(const kivi_layer *layers, int n_layers,
+                                          kivi_cache *cache, void *const *k_hat,
+                                          void *const *v_hat, int64_t *n_flushed,
+                                          kivi_stream_t stream, void *const events[3]);
 
 /* Dequantize the first cache->s_q tokens of every layer's store into
  * k_out[l], v_out[l] (host arrays of n_layers device pointers, each fp16

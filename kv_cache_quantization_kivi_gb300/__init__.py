@@ -25,6 +25,7 @@ __all__ = [
     "KiviError", "lib", "library_path", "kivi_quantize_keys", "kivi_quantize_values",
     "kivi_dequantize_keys", "kivi_dequantize_values", "kivi_flush", "kivi_flush_size",
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
+    "kivi_fakequant_keys", "kivi_fakequant_values", "kivi_flush_fakequant",
     "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
     "KIVI_MAX_LAYERS", "event_handles",
 ]
@@ -78,7 +79,11 @@ def lib():
             L = C.CDLL(path)
             q_args = [_vp, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _vp, _vp, _i64, _vp]
             dq_args = [_vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _vp]
+            fq_args = [_vp, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _vp, _i64, _vp, _vp,
+                       _i64, _vp]
             for name, args in (("kivi_quantize_keys", q_args), ("kivi_quantize_values", q_args),
+                               ("kivi_fakequant_keys", fq_args),
+                               ("kivi_fakequant_values", fq_args),
                                ("kivi_dequantize_keys", dq_args),
                                ("kivi_dequantize_values", dq_args)):
                 f = getattr(L, name)
@@ -98,6 +103,10 @@ def lib():
                                                       C.POINTER(kivi_cache), C.POINTER(_vp),
                                                       C.POINTER(_vp), _vp, C.POINTER(_vp)]
             L.kivi_dequantize_cache_timed.restype = _int
+            L.kivi_flush_fakequant.argtypes = [C.POINTER(kivi_layer), _int, C.POINTER(kivi_cache),
+                                               C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_i64),
+                                               _vp, C.POINTER(_vp)]
+            L.kivi_flush_fakequant.restype = _int
             L.kivi_flush_size.argtypes = [_i64, _int, _int]
             L.kivi_flush_size.restype = _i64
             L.kivi_key_code_words.argtypes = [_i64, _i64, _int, _int]
@@ -233,6 +242,49 @@ def kivi_dequantize_values(codes, scale, zero, group: int, bits: int, s: Optiona
     return y
 
 
+def _fakequant(name: str, x, group: int, bits: int, y, store: bool, codes, scale, zero,
+               stream, shapes):
+    import torch
+    x = _fp16_3d(x, name)
+    if y is None:
+        y = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    y = _fp16_3d(y, name + " (y)")
+    if store:
+        cs, ss = shapes
+        codes = torch.empty(cs, dtype=torch.int32, device=x.device) if codes is None else codes
+        scale = torch.empty(ss, dtype=torch.float32, device=x.device) if scale is None else scale
+        zero = torch.empty(ss, dtype=torch.float32, device=x.device) if zero is None else zero
+        cp, cst, sp, zp, sst = (codes.data_ptr(), _bh_stride(codes), scale.data_ptr(),
+                                zero.data_ptr(), _bh_stride(scale))
+    else:
+        codes = scale = zero = None
+        cp, cst, sp, zp, sst = None, 0, None, None, 0
+    bh, s, d = x.shape
+    _check(getattr(lib(), name)(x.data_ptr(), bh, s, d, _bh_stride(x), group, bits, y.data_ptr(),
+                                _bh_stride(y), cp, cst, sp, zp, sst, _stream_handle(stream)), name)
+    return y, codes, scale, zero
+
+
+def kivi_fakequant_keys(x, group: int, bits: int, y=None, store: bool = True, codes=None,
+                        scale=None, zero=None, stream=None) -> Tuple:
+    """Fused per-channel key quantize + dequantize of x [bh, s, d] in one pass ->
+    (y [bh, s, d] fp16, codes, scale, zero); with ``store=False`` only y is
+    written and the last three are None."""
+    bh, s, d = x.shape
+    ng = -(-s // group)
+    return _fakequant("kivi_fakequant_keys", x, group, bits, y, store, codes, scale, zero, stream,
+                      ((bh, ng * group // codes_per_word(bits), d), (bh, ng, d)))
+
+
+def kivi_fakequant_values(x, group: int, bits: int, y=None, store: bool = True, codes=None,
+                          scale=None, zero=None, stream=None) -> Tuple:
+    """Fused per-token value quantize + dequantize of x [bh, s, d] in one pass ->
+    (y [bh, s, d] fp16, codes, scale, zero); with ``store=False`` only y."""
+    bh, s, d = x.shape
+    return _fakequant("kivi_fakequant_values", x, group, bits, y, store, codes, scale, zero,
+                      stream, ((bh, s, d // codes_per_word(bits)), (bh, s, max(1, d // group))))
+
+
 # ---------------------------------------------------------------------------
 # cache: residual ring + quantized store, flush, batched dequantization
 # ---------------------------------------------------------------------------
@@ -260,13 +312,31 @@ def kivi_flush(layers, n_layers: int, cache: kivi_cache, stream=None, events=Non
     return int(n.value)
 
 
+def _ptr_array(ts, n: int):
+    return ts if isinstance(ts, C.Array) else (C.c_void_p * n)(*[t.data_ptr() for t in ts])
+
+
+def kivi_flush_fakequant(layers, n_layers: int, cache: kivi_cache, k_hat, v_hat, stream=None,
+                         events=None) -> int:
+    """Raw C call of the fused fake-quant flush: as :func:`kivi_flush`, and the
+    fp16 reconstruction of the flushed tokens goes to rows s_q .. of
+    ``k_hat[l]``/``v_hat[l]`` (fp16 [bh, cap, d] tensors or ctypes pointer
+    arrays).  Returns the tokens flushed."""
+    n = C.c_int64(0)
+    if events is not None and not isinstance(events, C.Array):
+        events = event_handles(events)
+    st = lib().kivi_flush_fakequant(layers, n_layers, C.byref(cache), _ptr_array(k_hat, n_layers),
+                                    _ptr_array(v_hat, n_layers), C.byref(n),
+                                    _stream_handle(stream), events)
+    _check(st, "kivi_flush_fakequant")
+    return int(n.value)
+
+
 def kivi_dequantize_cache(layers, n_layers: int, cache: kivi_cache, k_out, v_out,
                           stream=None, events=None) -> None:
     """``k_out``/``v_out``: sequences of fp16 tensors, or prepared ctypes pointer arrays."""
-    kp = k_out if isinstance(k_out, C.Array) else (C.c_void_p * n_layers)(
-        *[t.data_ptr() for t in k_out])
-    vp = v_out if isinstance(v_out, C.Array) else (C.c_void_p * n_layers)(
-        *[t.data_ptr() for t in v_out])
+    kp = _ptr_array(k_out, n_layers)
+    vp = _ptr_array(v_out, n_layers)
     if events is None:
         st = lib().kivi_dequantize_cache(layers, n_layers, C.byref(cache), kp, vp,
                                          _stream_handle(stream))
@@ -283,11 +353,16 @@ class KiviCache:
 
     Per layer: fp16 residual rings ``k_res``/``v_res`` [bh, r_cap, d] and the
     quantized store (key codes [bh, cap/W, d], key scale/zero [bh, cap/G, d],
-    value codes [bh, cap, d/W], value scale/zero [bh, cap, d/G]).
+    value codes [bh, cap, d/W], value scale/zero [bh, cap, d/G]).  With
+    ``recon=True`` also fp16 reconstructions ``k_hat``/``v_hat`` [bh, cap, d]
+    that :meth:`flush_fakequant` fills; ``store=False`` (only with recon)
+    leaves the quantized store out: the cache then holds the reconstruction
+    alone.
     """
 
     def __init__(self, n_layers: int, bh: int, d: int, r_cap: int, cap: int, group: int = 32,
-                 bits: int = 2, residual: int = 32, device="cuda"):
+                 bits: int = 2, residual: int = 32, device="cuda", recon: bool = False,
+                 store: bool = True):
         import torch
         if not (1 <= n_layers <= KIVI_MAX_LAYERS):
             raise ValueError("n_layers out of range")
@@ -295,29 +370,38 @@ class KiviCache:
         self.n_layers, self.group, self.bits = n_layers, group, bits
         dev = torch.device(device)
         # one contiguous allocation per buffer kind, one view per layer
+        if not store and not recon:
+            raise ValueError("a cache without a store needs recon=True")
         mk = lambda shape, dt: torch.zeros((n_layers,) + shape, dtype=dt, device=dev)  # noqa
         self.k_res_all = mk((bh, r_cap, d), torch.float16)
         self.v_res_all = mk((bh, r_cap, d), torch.float16)
-        self.k_codes_all = mk((bh, cap // w, d), torch.int32)
-        self.k_scale_all = mk((bh, cap // group, d), torch.float32)
-        self.k_zero_all = mk((bh, cap // group, d), torch.float32)
-        self.v_codes_all = mk((bh, cap, d // w), torch.int32)
-        self.v_scale_all = mk((bh, cap, d // group), torch.float32)
-        self.v_zero_all = mk((bh, cap, d // group), torch.float32)
         self.k_res = list(self.k_res_all.unbind(0))
         self.v_res = list(self.v_res_all.unbind(0))
-        self.k_codes = list(self.k_codes_all.unbind(0))
-        self.k_scale = list(self.k_scale_all.unbind(0))
-        self.k_zero = list(self.k_zero_all.unbind(0))
-        self.v_codes = list(self.v_codes_all.unbind(0))
-        self.v_scale = list(self.v_scale_all.unbind(0))
-        self.v_zero = list(self.v_zero_all.unbind(0))
+        names = ("k_codes", "k_scale", "k_zero", "v_codes", "v_scale", "v_zero")
+        if store:
+            shapes = ((bh, cap // w, d), (bh, cap // group, d), (bh, cap // group, d),
+                      (bh, cap, d // w), (bh, cap, d // group), (bh, cap, d // group))
+            dts = (torch.int32, torch.float32, torch.float32) * 2
+            for name, shape, dt in zip(names, shapes, dts):
+                setattr(self, name + "_all", mk(shape, dt))
+                setattr(self, name, list(getattr(self, name + "_all").unbind(0)))
+        else:
+            for name in names:
+                setattr(self, name + "_all", None)
+                setattr(self, name, [None] * n_layers)
+        self.recon = recon
+        self.k_hat_all = mk((bh, cap, d), torch.float16) if recon else None
+        self.v_hat_all = mk((bh, cap, d), torch.float16) if recon else None
+        self.k_hat = list(self.k_hat_all.unbind(0)) if recon else None
+        self.v_hat = list(self.v_hat_all.unbind(0)) if recon else None
+        ptr = lambda t: t.data_ptr() if t is not None else None  # noqa
         self.layers = (kivi_layer * n_layers)(*[
             kivi_layer(self.k_res[i].data_ptr(), self.v_res[i].data_ptr(),
-                       self.k_codes[i].data_ptr(), self.k_scale[i].data_ptr(),
-                       self.k_zero[i].data_ptr(), self.v_codes[i].data_ptr(),
-                       self.v_scale[i].data_ptr(), self.v_zero[i].data_ptr())
+                       *[ptr(getattr(self, name)[i]) for name in names])
             for i in range(n_layers)])
+        if recon:
+            self._k_hat_ptrs = _ptr_array(self.k_hat, n_layers)
+            self._v_hat_ptrs = _ptr_array(self.v_hat, n_layers)
         self.state = kivi_cache(bh, d, r_cap, cap, group, bits, residual, 0, 0, 0, 0)
 
     # state ------------------------------------------------------------------
@@ -357,6 +441,14 @@ class KiviCache:
     # hot path --------------------------------------------------------------
     def flush(self, stream=None, events=None) -> int:
         return kivi_flush(self.layers, self.n_layers, self.state, stream, events)
+
+    def flush_fakequant(self, stream=None, events=None) -> int:
+        """Flush that also writes the fp16 reconstruction of the flushed tokens
+        into ``k_hat``/``v_hat`` (needs ``recon=True``)."""
+        if not self.recon:
+            raise ValueError("flush_fakequant needs a cache built with recon=True")
+        return kivi_flush_fakequant(self.layers, self.n_layers, self.state, self._k_hat_ptrs,
+                                    self._v_hat_ptrs, stream, events)
 
     def dequantize(self, k_out=None, v_out=None, stream=None, events=None):
         """fp16 reconstructions of the first s_q store tokens of every layer;

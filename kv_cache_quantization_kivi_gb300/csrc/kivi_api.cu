@@ -32,7 +32,13 @@ constexpr int64_t kMaxUnits = (int64_t{1} << 31) - 1;
 bool valid_key_dim(int64_t d) { return d >= 8 && d <= 256 && d % 8 == 0; }
 bool valid_value_dim(int64_t d, int group) { return d >= 32 && d <= 256 && d % group == 0; }
 
-int64_t groups_of(int64_t s, int group) { return (s + group - 1) / group; }
+int64_t groups_of(int64_t s, int group) { return s / group + (s % group != 0); }
+
+// a * b for a, b >= 0, saturated at INT64_MAX (sizes are validated with it
+// before any product that could overflow is formed).
+int64_t sat_mul(int64_t a, int64_t b) {
+  return a != 0 && b > INT64_MAX / a ? INT64_MAX : a * b;
+}
 
 kivi_status cuda_status(cudaError_t err) {
   if (err == cudaSuccess) return KIVI_OK;
@@ -49,6 +55,17 @@ KeyGeom key_geom(int64_t s, int64_t d, int group, int bits) {
   const int64_t ng = groups_of(s, group);
   return {ng * group / (32 / bits) * d, ng * d};
 }
+
+// Threads of the key quantize kernel: one per (bh, group, channel pair,
+// 32-token split); of the value kernels and the key dequantize kernel: one
+// per 32 (values) or 8 (keys) channels of a row or group.
+int64_t key_quant_units(int64_t bh, int64_t s, int64_t d, int group) {
+  return sat_mul(sat_mul(bh, groups_of(s, group)), (d / 2) * (group / 32));
+}
+int64_t key_dequant_units(int64_t bh, int64_t s, int64_t d, int group) {
+  return sat_mul(sat_mul(bh, groups_of(s, group)), d / 8);
+}
+int64_t value_units(int64_t bh, int64_t s, int64_t d) { return sat_mul(sat_mul(bh, s), d / 32); }
 
 }  // namespace
 
@@ -96,11 +113,11 @@ kivi_status kivi_quantize_keys(const void *x, int64_t bh, int64_t s, int64_t d,
   if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_key_dim(d))
     return KIVI_ERR_INVAL;
   if (bh == 0 || s == 0) return KIVI_OK;
+  if (key_quant_units(bh, s, d, group) > kMaxUnits) return KIVI_ERR_INVAL;  // also bounds s * d
   if (!x || !codes || !scale || !zero) return KIVI_ERR_INVAL;
   const KeyGeom kg = key_geom(s, d, group, bits);
   if (x_bh_stride < s * d || codes_bh_stride < kg.code_words || sz_bh_stride < kg.sz)
     return KIVI_ERR_INVAL;
-  if (bh * groups_of(s, group) > kMaxUnits || bh > kMaxUnits) return KIVI_ERR_INVAL;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scale) || !aligned16(zero) ||
       !bytes16(x_bh_stride, 2) || !bytes16(codes_bh_stride, 4) || !bytes_mult(sz_bh_stride, 4, 8))
     return KIVI_ERR_ALIGN;
@@ -115,7 +132,7 @@ kivi_status kivi_quantize_keys(const void *x, int64_t bh, int64_t s, int64_t d,
   p.codes_bh_stride = codes_bh_stride;
   p.sz_bh_stride = sz_bh_stride;
   p.jobs[0] = {x, codes, scale, zero};
-  return cuda_status(kivi_impl::launch_key_quant(p, group, bits, stream));
+  return cuda_status(kivi_impl::launch_key_quant(p, group, bits, false, stream));
 }
 
 kivi_status kivi_quantize_values(const void *x, int64_t bh, int64_t s, int64_t d,
@@ -125,11 +142,11 @@ kivi_status kivi_quantize_values(const void *x, int64_t bh, int64_t s, int64_t d
   if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_value_dim(d, group))
     return KIVI_ERR_INVAL;
   if (bh == 0 || s == 0) return KIVI_OK;
+  if (value_units(bh, s, d) > kMaxUnits) return KIVI_ERR_INVAL;  // also bounds s * d
   if (!x || !codes || !scale || !zero) return KIVI_ERR_INVAL;
   if (x_bh_stride < s * d || codes_bh_stride < s * (d / (32 / bits)) ||
       sz_bh_stride < s * (d / group))
     return KIVI_ERR_INVAL;
-  if (bh * s * (d / 32) > kMaxUnits) return KIVI_ERR_INVAL;
   if (!aligned16(x) || !aligned16(codes) || !aligned16(scale) || !aligned16(zero) ||
       !bytes16(x_bh_stride, 2) || !bytes_mult(codes_bh_stride, 4, value_code_align(bits)))
     return KIVI_ERR_ALIGN;
@@ -144,7 +161,79 @@ kivi_status kivi_quantize_values(const void *x, int64_t bh, int64_t s, int64_t d
   p.codes_bh_stride = codes_bh_stride;
   p.sz_bh_stride = sz_bh_stride;
   p.jobs[0] = {x, codes, scale, zero};
-  return cuda_status(kivi_impl::launch_value_quant(p, group, bits, stream));
+  return cuda_status(kivi_impl::launch_value_quant(p, group, bits, false, stream));
+}
+
+// Fused quantize + dequantize: the same kernels with the reconstruction
+// written as each code is made.  codes/scale/zero are all given or all NULL.
+kivi_status kivi_fakequant_keys(const void *x, int64_t bh, int64_t s, int64_t d,
+                                int64_t x_bh_stride, int group, int bits, void *y,
+                                int64_t y_bh_stride, uint32_t *codes, int64_t codes_bh_stride,
+                                float *scale, float *zero, int64_t sz_bh_stride,
+                                kivi_stream_t stream) {
+  if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_key_dim(d))
+    return KIVI_ERR_INVAL;
+  if (bh == 0 || s == 0) return KIVI_OK;
+  if (key_quant_units(bh, s, d, group) > kMaxUnits) return KIVI_ERR_INVAL;  // also bounds s * d
+  const bool store = codes != nullptr;
+  if (!x || !y || (scale != nullptr) != store || (zero != nullptr) != store)
+    return KIVI_ERR_INVAL;
+  const KeyGeom kg = key_geom(s, d, group, bits);
+  if (x_bh_stride < s * d || y_bh_stride < s * d) return KIVI_ERR_INVAL;
+  if (store && (codes_bh_stride < kg.code_words || sz_bh_stride < kg.sz)) return KIVI_ERR_INVAL;
+  if (!aligned16(x) || !aligned16(y) || !bytes16(x_bh_stride, 2) || !bytes16(y_bh_stride, 2))
+    return KIVI_ERR_ALIGN;
+  if (store && (!aligned16(codes) || !aligned16(scale) || !aligned16(zero) ||
+                !bytes16(codes_bh_stride, 4) || !bytes_mult(sz_bh_stride, 4, 8)))
+    return KIVI_ERR_ALIGN;
+
+  kivi_impl::QuantParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_jobs = 1;
+  p.d = static_cast<int32_t>(d);
+  p.bh = bh;
+  p.rows = s;
+  p.x_bh_stride = x_bh_stride;
+  p.codes_bh_stride = store ? codes_bh_stride : 0;
+  p.sz_bh_stride = store ? sz_bh_stride : 0;
+  p.y_bh_stride = y_bh_stride;
+  p.jobs[0] = {x, codes, scale, zero, y};
+  return cuda_status(kivi_impl::launch_key_quant(p, group, bits, true, stream));
+}
+
+kivi_status kivi_fakequant_values(const void *x, int64_t bh, int64_t s, int64_t d,
+                                  int64_t x_bh_stride, int group, int bits, void *y,
+                                  int64_t y_bh_stride, uint32_t *codes, int64_t codes_bh_stride,
+                                  float *scale, float *zero, int64_t sz_bh_stride,
+                                  kivi_stream_t stream) {
+  if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_value_dim(d, group))
+    return KIVI_ERR_INVAL;
+  if (bh == 0 || s == 0) return KIVI_OK;
+  if (value_units(bh, s, d) > kMaxUnits) return KIVI_ERR_INVAL;  // also bounds s * d
+  const bool store = codes != nullptr;
+  if (!x || !y || (scale != nullptr) != store || (zero != nullptr) != store)
+    return KIVI_ERR_INVAL;
+  if (x_bh_stride < s * d || y_bh_stride < s * d) return KIVI_ERR_INVAL;
+  if (store && (codes_bh_stride < s * (d / (32 / bits)) || sz_bh_stride < s * (d / group)))
+    return KIVI_ERR_INVAL;
+  if (!aligned16(x) || !aligned16(y) || !bytes16(x_bh_stride, 2) || !bytes16(y_bh_stride, 2))
+    return KIVI_ERR_ALIGN;
+  if (store && (!aligned16(codes) || !aligned16(scale) || !aligned16(zero) ||
+                !bytes_mult(codes_bh_stride, 4, value_code_align(bits))))
+    return KIVI_ERR_ALIGN;
+
+  kivi_impl::QuantParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_jobs = 1;
+  p.d = static_cast<int32_t>(d);
+  p.bh = bh;
+  p.rows = s;
+  p.x_bh_stride = x_bh_stride;
+  p.codes_bh_stride = store ? codes_bh_stride : 0;
+  p.sz_bh_stride = store ? sz_bh_stride : 0;
+  p.y_bh_stride = y_bh_stride;
+  p.jobs[0] = {x, codes, scale, zero, y};
+  return cuda_status(kivi_impl::launch_value_quant(p, group, bits, true, stream));
 }
 
 kivi_status kivi_dequantize_keys(const uint32_t *codes, int64_t codes_bh_stride,
@@ -154,11 +243,11 @@ kivi_status kivi_dequantize_keys(const uint32_t *codes, int64_t codes_bh_stride,
   if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_key_dim(d))
     return KIVI_ERR_INVAL;
   if (bh == 0 || s == 0) return KIVI_OK;
+  if (key_dequant_units(bh, s, d, group) > kMaxUnits) return KIVI_ERR_INVAL;  // also bounds s * d
   if (!codes || !scale || !zero || !y) return KIVI_ERR_INVAL;
   const KeyGeom kg = key_geom(s, d, group, bits);
   if (codes_bh_stride < kg.code_words || sz_bh_stride < kg.sz || y_bh_stride < s * d)
     return KIVI_ERR_INVAL;
-  if (bh * groups_of(s, group) * (d / 8) > kMaxUnits) return KIVI_ERR_INVAL;
   if (!aligned16(codes) || !aligned16(scale) || !aligned16(zero) || !aligned16(y) ||
       !bytes16(codes_bh_stride, 4) || !bytes16(sz_bh_stride, 4) || !bytes16(y_bh_stride, 2))
     return KIVI_ERR_ALIGN;
@@ -183,11 +272,11 @@ kivi_status kivi_dequantize_values(const uint32_t *codes, int64_t codes_bh_strid
   if (!valid_bits(bits) || !valid_group(group) || bh < 0 || s < 0 || !valid_value_dim(d, group))
     return KIVI_ERR_INVAL;
   if (bh == 0 || s == 0) return KIVI_OK;
+  if (value_units(bh, s, d) > kMaxUnits) return KIVI_ERR_INVAL;  // also bounds s * d
   if (!codes || !scale || !zero || !y) return KIVI_ERR_INVAL;
   if (codes_bh_stride < s * (d / (32 / bits)) || sz_bh_stride < s * (d / group) ||
       y_bh_stride < s * d)
     return KIVI_ERR_INVAL;
-  if (bh * s * (d / 32) > kMaxUnits) return KIVI_ERR_INVAL;
   if (!aligned16(codes) || !aligned16(scale) || !aligned16(zero) || !aligned16(y) ||
       !bytes_mult(codes_bh_stride, 4, value_code_align(bits)) || !bytes16(y_bh_stride, 2))
     return KIVI_ERR_ALIGN;
@@ -209,7 +298,10 @@ kivi_status kivi_dequantize_values(const uint32_t *codes, int64_t codes_bh_strid
 // cache: flush and batched dequantization
 // ---------------------------------------------------------------------------
 
-static kivi_status check_cache(const kivi_layer *layers, int n_layers, const kivi_cache *c) {
+// allow_no_store: a layer's key (or value) store pointers may all be NULL
+// (fake-quant flush that keeps only the reconstruction).
+static kivi_status check_cache(const kivi_layer *layers, int n_layers, const kivi_cache *c,
+                               bool allow_no_store = false) {
   if (!layers || !c || n_layers < 1 || n_layers > KIVI_MAX_LAYERS) return KIVI_ERR_INVAL;
   if (!valid_bits(c->bits) || !valid_group(c->group) || c->residual < 0 || c->reserved != 0)
     return KIVI_ERR_INVAL;
@@ -219,16 +311,21 @@ static kivi_status check_cache(const kivi_layer *layers, int n_layers, const kiv
   if (c->s_q < 0 || c->s_q % G != 0 || c->s_q > c->cap) return KIVI_ERR_INVAL;
   if (c->res_head < 0 || c->res_head >= c->r_cap || c->res_head % G != 0) return KIVI_ERR_INVAL;
   if (c->n_res < 0 || c->n_res > c->r_cap) return KIVI_ERR_INVAL;
-  if (c->bh * c->cap * (c->d / 32) * n_layers > kMaxUnits) return KIVI_ERR_INVAL;
+  if (sat_mul(value_units(c->bh, c->cap, c->d), n_layers) > kMaxUnits ||
+      value_units(c->bh, c->r_cap, c->d) > kMaxUnits)
+    return KIVI_ERR_INVAL;
   for (int l = 0; l < n_layers; ++l) {
     const kivi_layer &L = layers[l];
     const void *ptrs[8] = {L.k_res, L.v_res, L.k_codes, L.k_scale,
                            L.k_zero, L.v_codes, L.v_scale, L.v_zero};
-    for (const void *q : ptrs) {
-      if (!q) return KIVI_ERR_INVAL;
+    if (!L.k_res || !L.v_res) return KIVI_ERR_INVAL;
+    for (int t = 0; t < 2; ++t) {  // key store, value store
+      const int nn = (ptrs[2 + 3 * t] != nullptr) + (ptrs[3 + 3 * t] != nullptr) +
+                     (ptrs[4 + 3 * t] != nullptr);
+      if (nn != 3 && !(allow_no_store && nn == 0)) return KIVI_ERR_INVAL;
     }
     for (const void *q : ptrs) {
-      if (!aligned16(q)) return KIVI_ERR_ALIGN;
+      if (!aligned16(q)) return KIVI_ERR_ALIGN;  // NULL is aligned
     }
   }
   return KIVI_OK;
@@ -244,10 +341,18 @@ kivi_status kivi_flush(const kivi_layer *layers, int n_layers, kivi_cache *cache
   return kivi_flush_timed(layers, n_layers, cache, n_flushed, stream, nullptr);
 }
 
-kivi_status kivi_flush_timed(const kivi_layer *layers, int n_layers, kivi_cache *cache,
-                             int64_t *n_flushed, kivi_stream_t stream, void *const events[3]) {
-  const kivi_status st = check_cache(layers, n_layers, cache);
+static kivi_status flush_impl(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                              void *const *k_hat, void *const *v_hat, int64_t *n_flushed,
+                              kivi_stream_t stream, void *const *events) {
+  const bool recon = k_hat != nullptr;
+  const kivi_status st = check_cache(layers, n_layers, cache, recon);
   if (st != KIVI_OK) return st;
+  if (recon) {
+    for (int l = 0; l < n_layers; ++l) {
+      if (!k_hat[l] || !v_hat[l]) return KIVI_ERR_INVAL;
+      if (!aligned16(k_hat[l]) || !aligned16(v_hat[l])) return KIVI_ERR_ALIGN;
+    }
+  }
   const int64_t G = cache->group;
   const int W = 32 / cache->bits;
   const int64_t n = kivi_flush_size(cache->n_res, cache->residual, cache->group);
@@ -273,6 +378,8 @@ kivi_status kivi_flush_timed(const kivi_layer *layers, int n_layers, kivi_cache 
   kp.x_bh_stride = cache->r_cap * d;
   kp.ring = cache->r_cap;
   kp.head = cache->res_head;
+  kp.y_bh_stride = cache->cap * d;  // reconstruction [bh][cap][d], rows s_q ..
+  kp.y_row0 = cache->s_q;
 
   kivi_impl::QuantParams vp = kp;
   kp.codes_bh_stride = cache->cap / W * d;
@@ -283,17 +390,17 @@ kivi_status kivi_flush_timed(const kivi_layer *layers, int n_layers, kivi_cache 
   vp.out0 = cache->s_q;
   for (int l = 0; l < n_layers; ++l) {
     const kivi_layer &L = layers[l];
-    kp.jobs[l] = {L.k_res, L.k_codes, L.k_scale, L.k_zero};
-    vp.jobs[l] = {L.v_res, L.v_codes, L.v_scale, L.v_zero};
+    kp.jobs[l] = {L.k_res, L.k_codes, L.k_scale, L.k_zero, recon ? k_hat[l] : nullptr};
+    vp.jobs[l] = {L.v_res, L.v_codes, L.v_scale, L.v_zero, recon ? v_hat[l] : nullptr};
   }
   cudaStream_t s = stream;
   kivi_status r = cuda_status(record(events, 0, s));
   if (r != KIVI_OK) return r;
-  r = cuda_status(kivi_impl::launch_key_quant(kp, cache->group, cache->bits, s));
+  r = cuda_status(kivi_impl::launch_key_quant(kp, cache->group, cache->bits, recon, s));
   if (r != KIVI_OK) return r;
   r = cuda_status(record(events, 1, s));
   if (r != KIVI_OK) return r;
-  r = cuda_status(kivi_impl::launch_value_quant(vp, cache->group, cache->bits, s));
+  r = cuda_status(kivi_impl::launch_value_quant(vp, cache->group, cache->bits, recon, s));
   if (r != KIVI_OK) return r;
   r = cuda_status(record(events, 2, s));
   if (r != KIVI_OK) return r;
@@ -303,6 +410,18 @@ kivi_status kivi_flush_timed(const kivi_layer *layers, int n_layers, kivi_cache 
   cache->n_res -= n;
   if (n_flushed) *n_flushed = n;
   return KIVI_OK;
+}
+
+kivi_status kivi_flush_timed(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                             int64_t *n_flushed, kivi_stream_t stream, void *const events[3]) {
+  return flush_impl(layers, n_layers, cache, nullptr, nullptr, n_flushed, stream, events);
+}
+
+kivi_status kivi_flush_fakequant(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                                 void *const *k_hat, void *const *v_hat, int64_t *n_flushed,
+                                 kivi_stream_t stream, void *const events[3]) {
+  if (!k_hat || !v_hat) return KIVI_ERR_INVAL;
+  return flush_impl(layers, n_layers, cache, k_hat, v_hat, n_flushed, stream, events);
 }
 
 kivi_status kivi_dequantize_cache(const kivi_layer *layers, int n_layers, const kivi_cache *cache,

@@ -118,6 +118,11 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
 __device__ __forceinline__ uint64_t h2_to_f2(__half2 h) {
   const float2 f = __half22float2(h);
   return f2_pack(f.x, f.y);
@@ -240,6 +245,18 @@ __device__ __forceinline__ float recon_f32(uint32_t q, float scale, float neg_sc
   const float m = __uint_as_float(0x4B000000u | q);
   const float prod = __fmaf_rn(m, scale, neg_scale_2p23);
   return __fadd_rn(prod, zero);
+}
+
+// Reconstruction of a pair of integer-valued float codes n = (q0, q1) with
+// per-element (scale, zero) pairs: fp16(RN(RN(q*scale) + zero)), the product
+// and the sum rounded separately (n is exact, so RN(n*scale) = RN(q*scale)).
+__device__ __forceinline__ uint32_t recon_pair(uint64_t n, uint64_t scale2, uint64_t zero2) {
+  const uint64_t r = f2_add(f2_mul(n, scale2), zero2);
+  const __half2 h = __floats2half2_rn(__uint_as_float(static_cast<uint32_t>(r)),
+                                      __uint_as_float(static_cast<uint32_t>(r >> 32)));
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
 }
 
 // ---------------------------------------------------------------------------

@@ -22,3 +22,37 @@
       default: return cudaErrorInvalidValue;                          \
     }                                                                 \
   } while (0)
+
+// The same for kernels with a compile-time reconstruction flag R.
+#define KIVI_DISPATCH_DR(FN, B, G, R, P, STREAM) \
+  return (P).d == 128 ? FN<B, G, 128, R>(P, STREAM) : FN<B, G, 0, R>(P, STREAM)
+
+#define KIVI_DISPATCH_R(FN, P, GROUP, BITS, RECON, STREAM)                              \
+  do {                                                                                  \
+    if (RECON) {                                                                        \
+      switch ((BITS) * 1000 + (GROUP)) {                                                \
+        case 2032: KIVI_DISPATCH_DR(FN, 2, 32, true, P, STREAM);                        \
+        case 2064: KIVI_DISPATCH_DR(FN, 2, 64, true, P, STREAM);                        \
+        case 2128: KIVI_DISPATCH_DR(FN, 2, 128, true, P, STREAM);                       \
+        case 4032: KIVI_DISPATCH_DR(FN, 4, 32, true, P, STREAM);                        \
+        case 4064: KIVI_DISPATCH_DR(FN, 4, 64, true, P, STREAM);                        \
+        case 4128: KIVI_DISPATCH_DR(FN, 4, 128, true, P, STREAM);                       \
+        case 8032: KIVI_DISPATCH_DR(FN, 8, 32, true, P, STREAM);                        \
+        case 8064: KIVI_DISPATCH_DR(FN, 8, 64, true, P, STREAM);                        \
+        case 8128: KIVI_DISPATCH_DR(FN, 8, 128, true, P, STREAM);                       \
+        default: return cudaErrorInvalidValue;                                          \
+      }                                                                                 \
+    }                                                                                   \
+    switch ((BITS) * 1000 + (GROUP)) {                                                  \
+      case 2032: KIVI_DISPATCH_DR(FN, 2, 32, false, P, STREAM);                         \
+      case 2064: KIVI_DISPATCH_DR(FN, 2, 64, false, P, STREAM);                         \
+      case 2128: KIVI_DISPATCH_DR(FN, 2, 128, false, P, STREAM);                        \
+      case 4032: KIVI_DISPATCH_DR(FN, 4, 32, false, P, STREAM);                         \
+      case 4064: KIVI_DISPATCH_DR(FN, 4, 64, false, P, STREAM);                         \
+      case 4128: KIVI_DISPATCH_DR(FN, 4, 128, false, P, STREAM);                        \
+      case 8032: KIVI_DISPATCH_DR(FN, 8, 32, false, P, STREAM);                         \
+      case 8064: KIVI_DISPATCH_DR(FN, 8, 64, false, P, STREAM);                         \
+      case 8128: KIVI_DISPATCH_DR(FN, 8, 128, false, P, STREAM);                        \
+      default: return cudaErrorInvalidValue;                                            \
+    }                                                                                   \
+  } while (0)

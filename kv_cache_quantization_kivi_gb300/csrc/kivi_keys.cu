@@ -87,7 +87,8 @@ __device__ __noinline__ uint2 key_partial_ragged(const __half2 *src, int rows_he
 // computed from global memory with the literal division, and stored.
 template <int BITS>
 __device__ __noinline__ void key_exact_store(const __half2 *src, int rows_here, int D,
-                                             uint32_t ext_mn, uint32_t ext_mx, uint32_t *cdst) {
+                                             uint32_t ext_mn, uint32_t ext_mx, uint32_t *cdst,
+                                             __half *ycol) {
   constexpr int W = CodeFmt<BITS>::W;
   const float qf = static_cast<float>(CodeFmt<BITS>::Q);
   const float2 mnf = __half22float2(u32_as_h2(ext_mn));
@@ -99,16 +100,22 @@ __device__ __noinline__ void key_exact_store(const __half2 *src, int rows_here, 
     uint32_t a0 = 0u, a1 = 0u;
 #pragma unroll 1
     for (int k = 0; k < W; ++k) {
-      const int r = padded_row(wr * W + k, rows_here);
+      const int t = wr * W + k;
+      const int r = padded_row(t, rows_here);
       const float2 xf = __half22float2(__ldcs(src + static_cast<int64_t>(r) * (D / 2)));
-      a0 |= exact_code(xf.x, g0, qf) << (k * BITS);
-      a1 |= exact_code(xf.y, g1, qf) << (k * BITS);
+      const uint32_t q0 = exact_code(xf.x, g0, qf), q1 = exact_code(xf.y, g1, qf);
+      a0 |= q0 << (k * BITS);
+      a1 |= q1 << (k * BITS);
+      if (ycol != nullptr && t < rows_here)  // reconstruction of real tokens only
+        __stcs(reinterpret_cast<unsigned int *>(ycol + static_cast<int64_t>(t) * D),
+               recon_pair(f2_pack(static_cast<float>(q0), static_cast<float>(q1)),
+                          f2_pack(g0.scale, g1.scale), f2_pack(g0.zero, g1.zero)));
     }
-    st_stream(cdst + static_cast<int64_t>(wr) * D, make_uint2(a0, a1));
+    if (cdst != nullptr) st_stream(cdst + static_cast<int64_t>(wr) * D, make_uint2(a0, a1));
   }
 }
 
-template <int BITS, int G, int DC>
+template <int BITS, int G, int DC, bool RECON>
 __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr int T = G / 32;                  // token splits per group
   constexpr int W = CodeFmt<BITS>::W;        // codes per word
@@ -175,23 +182,35 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
     if (!active) continue;
 
     const int64_t out_g = p.out0 + k.g;
-    uint32_t *cdst = job.codes + static_cast<int64_t>(k.b) * p.codes_bh_stride +
-                     (out_g * (G / W) + k.split * WPT) * D + 2 * k.col;
+    const bool codes_out = !RECON || job.codes != nullptr;
+    uint32_t *cdst = codes_out ? job.codes + static_cast<int64_t>(k.b) * p.codes_bh_stride +
+                                     (out_g * (G / W) + k.split * WPT) * D + 2 * k.col
+                               : nullptr;
+    // reconstruction: column (2 col, 2 col + 1) of the first token of the split
+    __half *ycol = RECON ? static_cast<__half *>(job.y) + static_cast<int64_t>(k.b) * p.y_bh_stride +
+                               (p.y_row0 + static_cast<int64_t>(k.g) * G + k.split * 32) * D +
+                               2 * k.col
+                         : nullptr;
     GroupQ2 gq;
+    uint64_t sc2 = 0, ze2 = 0;
     const float2 mnf = __half22float2(gmn);
     const float2 mxf = __half22float2(gmx);
     {
       const GroupQ g0 = make_group(mnf.x, mxf.x, qf);
       const GroupQ g1 = make_group(mnf.y, mxf.y, qf);
       gq = make_group2(g0, g1);
-      if (k.split == 0) {
+      if (RECON) {
+        sc2 = f2_pack(g0.scale, g1.scale);
+        ze2 = f2_pack(g0.zero, g1.zero);
+      }
+      if (k.split == 0 && codes_out) {
         const int64_t o = static_cast<int64_t>(k.b) * p.sz_bh_stride + out_g * D + 2 * k.col;
         __stcs(reinterpret_cast<float2 *>(job.scale + o), make_float2(g0.scale, g1.scale));
         __stcs(reinterpret_cast<float2 *>(job.zero + o), make_float2(g0.zero, g1.zero));
       }
     }
     if (!full) {
-      key_exact_store<BITS>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst);
+      key_exact_store<BITS>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst, ycol);
       continue;
     }
 
@@ -210,13 +229,19 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int t0 = wi * W + hh * H;
-        half[hh] = codes2<BITS, true>(h2_to_f2(h[t0]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
 #pragma unroll
-        for (int j = 1; j < H; ++j)
-          half[hh] = f2_fma(codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y, mxf.y),
-                            f2_const(static_cast<float>(1u << (BITS * j))), half[hh]);
+        for (int j = 0; j < H; ++j) {
+          const uint64_t n = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y,
+                                                mxf.y);
+          half[hh] = j == 0 ? n
+                            : f2_fma(n, f2_const(static_cast<float>(1u << (BITS * j))), half[hh]);
+          if (RECON)
+            __stcs(reinterpret_cast<unsigned int *>(ycol + static_cast<int64_t>(t0 + j) * D),
+                   recon_pair(n, sc2, ze2));
+        }
       }
-      st_stream(cdst + static_cast<int64_t>(wi) * D, join_halves2(half[0], half[1]));
+      if (codes_out)
+        st_stream(cdst + static_cast<int64_t>(wi) * D, join_halves2(half[0], half[1]));
     }
   }
 }
@@ -294,10 +319,10 @@ int num_sms() {
   return g_num_sms;
 }
 
-template <int BITS, int G, int DC>
+template <int BITS, int G, int DC, bool RECON>
 cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
   const int threads = 256;
-  auto kern = key_quant_kernel<BITS, G, DC>;
+  auto kern = key_quant_kernel<BITS, G, DC, RECON>;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
   if (err != cudaSuccess) return err;
@@ -338,8 +363,9 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
 
 #include "kivi_dispatch.h"
 
-cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, cudaStream_t stream) {
-  KIVI_DISPATCH(key_quant_launch, p, group, bits, stream);
+cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, bool recon,
+                             cudaStream_t stream) {
+  KIVI_DISPATCH_R(key_quant_launch, p, group, bits, recon, stream);
 }
 
 cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits,

@@ -34,12 +34,15 @@ struct FastDiv {
 #endif
 };
 
-// One fp16 tensor quantized into one code/scale/zero set.
+// One fp16 tensor quantized into one code/scale/zero set, and (fused
+// fake-quant calls) its fp16 reconstruction y.  codes/scale/zero may be null
+// in the fake-quant full-tensor calls (then only y is written).
 struct QuantJob {
   const void *x;
   uint32_t *codes;
   float *scale;
   float *zero;
+  void *y;
 };
 
 // Quantization of n_jobs tensors [bh][*][d].
@@ -59,6 +62,8 @@ struct QuantParams {
   int64_t ring;
   int64_t head;
   int64_t out0;
+  int64_t y_bh_stride;      // fp16 elements (reconstruction)
+  int64_t y_row0;           // row of the reconstruction of logical row 0
   // filled by the launchers: divisors of the kernels' unit index
   FastDiv div_chunks, div_rows, div_bh;
   QuantJob jobs[KIVI_MAX_LAYERS];
@@ -87,8 +92,12 @@ struct DequantParams {
 // Launchers (one per kernel family); they pick the template instance for
 // (group, bits), size the grid from the device's SM count and occupancy,
 // and return the launch's cudaError_t.
-cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, cudaStream_t stream);
-cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, cudaStream_t stream);
+// recon: also write the fp16 reconstruction of every quantized element
+// (jobs[i].y, p.y_bh_stride, p.y_row0).
+cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, bool recon,
+                             cudaStream_t stream);
+cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, bool recon,
+                               cudaStream_t stream);
 cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits, cudaStream_t stream);
 cudaError_t launch_value_dequant(const DequantParams &p, int group, int bits,
                                  cudaStream_t stream);

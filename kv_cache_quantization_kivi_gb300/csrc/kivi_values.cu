@@ -47,8 +47,43 @@ __device__ __forceinline__ RowRef decode_unit(uint32_t u, const P &p) {
   return t;
 }
 
-template <int BITS, int G, int DC>
-__global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_constant__ QuantParams p) {
+// Coalesced store of a warp's 32 units of 64 bytes (32 fp16 each): each lane
+// parks its unit in a per-warp shared-memory block (16 bytes of padding per
+// unit against bank conflicts), and each 16-byte store instruction of the
+// warp then writes 512 consecutive bytes: lane l stores chunk l + 32 i of the
+// block, whose destination is that of unit (l + 32 i) / 4, taken from the
+// owning lane by a shuffle.  All 32 lanes must call it; `valid` marks lanes
+// whose unit exists (their `out` and `dst` are used).
+constexpr int kUnitWords = 20;   // 64 bytes of data + 16 bytes of padding
+constexpr int kBlockThreads = 256;
+
+__device__ __forceinline__ void warp_store_units(uint32_t *blk, uint32_t lane, bool valid,
+                                                 const uint32_t (&out)[16], __half *dst,
+                                                 uint32_t base, uint32_t total) {
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<uint4 *>(blk + lane * kUnitWords + 4 * i) =
+          make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+  }
+  __syncwarp();
+  const unsigned long long dbits = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t j = lane + 32u * i;      // chunk of the warp block
+    const uint32_t owner = j >> 2;          // unit (lane) that produced it
+    const unsigned long long d = __shfl_sync(0xffffffffu, dbits, owner);
+    if (base + owner < total) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(blk + owner * kUnitWords + 4 * (j & 3));
+      st_stream(reinterpret_cast<__half *>(d) + 8 * (j & 3), v);
+    }
+  }
+  __syncwarp();
+}
+
+template <int BITS, int G, int DC, bool RECON>
+__global__ void __launch_bounds__(kBlockThreads, 4)
+    value_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr int L = G / 32;               // lanes per group
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
@@ -59,6 +94,9 @@ __global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_consta
                          static_cast<uint32_t>(p.rows) * p.div_chunks.d;
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t stride = gridDim.x * blockDim.x;
+  __shared__ __align__(16) uint32_t stage[RECON ? kBlockThreads / 32 : 1]
+                                         [RECON ? 32 * kUnitWords : 4];
+  uint32_t *blk = stage[RECON ? (threadIdx.x >> 5) : 0];
 
 #pragma unroll 1
   for (uint32_t base = (blockIdx.x * blockDim.x + threadIdx.x) & ~31u; base < total;
@@ -115,80 +153,92 @@ __global__ void __launch_bounds__(256, 4) value_quant_kernel(const __grid_consta
         ext = __hmin2(ext, u32_as_h2(other));
       }
     }
-    if (!active) continue;
-
-    const float gmn = __low2float(ext), gmx = -__high2float(ext);
-    const int64_t out_row = p.out0 + t.r;
-    GroupQ2 gq;
-    {
-      const GroupQ g = make_group(gmn, gmx, qf);
-      gq = make_group2(g, g);
-      if (t.k % L == 0) {
-        const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k / L;
-        __stcs(job.scale + so, g.scale);
-        __stcs(job.zero + so, g.zero);
-      }
-    }
-
-    // Pack along channels: word wi holds channels [wi*W, wi*W + W) of this
-    // thread's 32.  A half-word (H = 16/BITS channels) accumulates its H/2
-    // channel pairs with packed FMAs by powers of two, which leaves even
-    // channels in the low and odd channels in the high element; one more FMA
-    // interleaves them.
-    constexpr int H = 16 / BITS;
-    uint32_t w[BITS];
-#pragma unroll
-    for (int wi = 0; wi < BITS; ++wi) {
-      uint64_t acc[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int p0 = (wi * W + hh * H) / 2;   // first channel pair of the half
-        uint32_t neg_acc = 0xFFFFFFFFu;
-        acc[hh] = codes2_nobranch(h2_to_f2(h[p0]), gq, neg_acc);
-#pragma unroll
-        for (int j = 1; j < H / 2; ++j)
-          acc[hh] = f2_fma(codes2_nobranch(h2_to_f2(h[p0 + j]), gq, neg_acc),
-                           f2_const(static_cast<float>(1u << (2 * BITS * j))), acc[hh]);
-        if (!(neg_acc >> 31)) {  // rare: redo this half pair by pair, exactly where needed
-          acc[hh] = codes2<BITS, false>(h2_to_f2(h[p0]), gq, gmn, gmx, gmn, gmx);
-#pragma unroll
-          for (int j = 1; j < H / 2; ++j)
-            acc[hh] = f2_fma(codes2<BITS, false>(h2_to_f2(h[p0 + j]), gq, gmn, gmx, gmn, gmx),
-                             f2_const(static_cast<float>(1u << (2 * BITS * j))), acc[hh]);
+    __half *ydst = RECON ? static_cast<__half *>(job.y) + t.b * p.y_bh_stride +
+                               (p.y_row0 + static_cast<int64_t>(t.r)) * D + t.k * 32
+                         : nullptr;
+    if (!RECON && !active) continue;
+    uint32_t out[16];  // reconstruction of the 32 channels (RECON)
+    if (active) {
+      const float gmn = __low2float(ext), gmx = -__high2float(ext);
+      const int64_t out_row = p.out0 + t.r;
+      const bool codes_out = !RECON || job.codes != nullptr;
+      GroupQ2 gq;
+      uint64_t sc2 = 0, ze2 = 0;
+      {
+        const GroupQ g = make_group(gmn, gmx, qf);
+        gq = make_group2(g, g);
+        if (RECON) {
+          sc2 = f2_pack(g.scale, g.scale);
+          ze2 = f2_pack(g.zero, g.zero);
+        }
+        if (t.k % L == 0 && codes_out) {
+          const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k / L;
+          __stcs(job.scale + so, g.scale);
+          __stcs(job.zero + so, g.zero);
         }
       }
-      // even channels (low) + odd channels (high) shifted by one code
-      float half[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-        half[hh] = __fmaf_rn(__uint_as_float(f2_hi_bits(acc[hh])), static_cast<float>(1u << BITS),
-                             __uint_as_float(f2_lo_bits(acc[hh])));
-      w[wi] = join_halves(half[0], half[1]);
-    }
 
-    uint32_t *dst = job.codes + t.b * p.codes_bh_stride + out_row * (D / W) + t.k * BITS;
-    if (BITS == 2) {
-      st_stream(dst, make_uint2(w[0], w[1 % BITS]));
-    } else {
+      // Pack along channels: word wi holds channels [wi*W, wi*W + W) of this
+      // thread's 32.  A half-word (H = 16/BITS channels) accumulates its H/2
+      // channel pairs with packed FMAs by powers of two, which leaves even
+      // channels in the low and odd channels in the high element; one more FMA
+      // interleaves them.
+      constexpr int H = 16 / BITS;
+      uint32_t w[BITS];
 #pragma unroll
-      for (int i = 0; i < BITS; i += 4)
-        st_stream(dst + i, make_uint4(w[i % BITS], w[(i + 1) % BITS], w[(i + 2) % BITS],
-                                      w[(i + 3) % BITS]));
-    }
+      for (int wi = 0; wi < BITS; ++wi) {
+        uint64_t acc[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int p0 = (wi * W + hh * H) / 2;   // first channel pair of the half
+          uint32_t neg_acc = 0xFFFFFFFFu;
+          uint64_t n[H / 2];
+#pragma unroll
+          for (int j = 0; j < H / 2; ++j) n[j] = codes2_nobranch(h2_to_f2(h[p0 + j]), gq, neg_acc);
+          if (!(neg_acc >> 31)) {  // rare: redo this half pair by pair, exactly where needed
+#pragma unroll
+            for (int j = 0; j < H / 2; ++j)
+              n[j] = codes2<BITS, false>(h2_to_f2(h[p0 + j]), gq, gmn, gmx, gmn, gmx);
+          }
+          acc[hh] = n[0];
+#pragma unroll
+          for (int j = 1; j < H / 2; ++j)
+            acc[hh] = f2_fma(n[j], f2_const(static_cast<float>(1u << (2 * BITS * j))), acc[hh]);
+          if (RECON) {
+#pragma unroll
+            for (int j = 0; j < H / 2; ++j) out[p0 + j] = recon_pair(n[j], sc2, ze2);
+          }
+        }
+        // even channels (low) + odd channels (high) shifted by one code
+        float half[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          half[hh] = __fmaf_rn(__uint_as_float(f2_hi_bits(acc[hh])), static_cast<float>(1u << BITS),
+                               __uint_as_float(f2_lo_bits(acc[hh])));
+        w[wi] = join_halves(half[0], half[1]);
+      }
+
+      if (codes_out) {
+        uint32_t *dst = job.codes + t.b * p.codes_bh_stride + out_row * (D / W) + t.k * BITS;
+        if (BITS == 2) {
+          st_stream(dst, make_uint2(w[0], w[1 % BITS]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < BITS; i += 4)
+            st_stream(dst + i, make_uint4(w[i % BITS], w[(i + 1) % BITS], w[(i + 2) % BITS],
+                                          w[(i + 3) % BITS]));
+        }
+      }
+    }  // active
+    if (RECON) warp_store_units(blk, lane, active, out, ydst, base, total);
   }
 }
 
 // Dequantize: a thread reconstructs the 32 channels of one (row, chunk) unit
-// (codes, scale and zero read with 8/16-byte and 4-byte loads).  Its 64 bytes
-// of fp16 output are then exchanged through a per-warp shared-memory block
-// (32 units x 64 bytes, 16 bytes of padding per unit against bank conflicts)
-// so that each 16-byte store instruction of the warp writes 512 consecutive
-// bytes: lane l stores chunk l + 32 i of the block, whose destination is that
-// of unit (l + 32 i) / 4, taken from the owning lane by a shuffle.
-constexpr int kDqUnitWords = 20;   // 64 bytes of data + 16 bytes of padding
-
+// (codes, scale and zero read with 8/16-byte and 4-byte loads) and the warp
+// writes its 32 units with warp_store_units.
 template <int BITS, int G, int DC>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kBlockThreads)
     value_dequant_kernel(const __grid_constant__ DequantParams p) {
   constexpr int L = G / 32;
   constexpr int W = CodeFmt<BITS>::W;
@@ -198,7 +248,7 @@ __global__ void __launch_bounds__(256)
                          static_cast<uint32_t>(p.rows) * p.div_chunks.d;
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t stride = gridDim.x * blockDim.x;
-  __shared__ __align__(16) uint32_t stage[256 / 32][32 * kDqUnitWords];
+  __shared__ __align__(16) uint32_t stage[kBlockThreads / 32][32 * kUnitWords];
   uint32_t *blk = stage[threadIdx.x >> 5];
 
 #pragma unroll 1
@@ -210,6 +260,7 @@ __global__ void __launch_bounds__(256)
     const DequantJob &J = p.jobs[t.job];
     __half *y = static_cast<__half *>(J.y) + t.b * p.y_bh_stride + static_cast<int64_t>(t.r) * D +
                 t.k * 32;
+    uint32_t out[16];
     if (active) {
       const uint32_t *src = J.codes + t.b * p.codes_bh_stride +
                             static_cast<int64_t>(t.r) * (D / W) + t.k * BITS;
@@ -232,8 +283,6 @@ __global__ void __launch_bounds__(256)
       const float sc = __ldcs(J.scale + so);
       const float ze = __ldcs(J.zero + so);
       const float nsc = __fmul_rn(sc, -8388608.0f);  // -2^23 * scale, exact
-
-      uint32_t out[16];
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         const uint32_t q0 = (w[e / W] >> ((e % W) * BITS)) & Q;
@@ -242,24 +291,8 @@ __global__ void __launch_bounds__(256)
         const float r1 = recon_f32(q1, sc, nsc, ze);
         out[e >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<uint4 *>(blk + lane * kDqUnitWords + 4 * i) =
-            make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
     }
-    __syncwarp();
-    const unsigned long long ybits = reinterpret_cast<unsigned long long>(y);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t j = lane + 32u * i;      // chunk of the warp block
-      const uint32_t owner = j >> 2;          // unit (lane) that produced it
-      const unsigned long long dst = __shfl_sync(0xffffffffu, ybits, owner);
-      if (base + owner < total) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(blk + owner * kDqUnitWords + 4 * (j & 3));
-        st_stream(reinterpret_cast<__half *>(dst) + 8 * (j & 3), v);
-      }
-    }
-    __syncwarp();
+    warp_store_units(blk, lane, active, out, y, base, total);
   }
 }
 
@@ -295,10 +328,10 @@ P with_dividers(const P &p) {
   return q;
 }
 
-template <int BITS, int G, int DC>
+template <int BITS, int G, int DC, bool RECON>
 cudaError_t value_quant_launch(const QuantParams &p, cudaStream_t stream) {
-  const int threads = 256;
-  auto kern = value_quant_kernel<BITS, G, DC>;
+  const int threads = kBlockThreads;
+  auto kern = value_quant_kernel<BITS, G, DC, RECON>;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
   int64_t grid = 0;
   cudaError_t err = persistent_grid(kern, threads, units, &grid);
@@ -309,7 +342,7 @@ cudaError_t value_quant_launch(const QuantParams &p, cudaStream_t stream) {
 
 template <int BITS, int G, int DC>
 cudaError_t value_dequant_launch(const DequantParams &p, cudaStream_t stream) {
-  const int threads = 256;
+  const int threads = kBlockThreads;
   auto kern = value_dequant_kernel<BITS, G, DC>;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
   int64_t grid = 0;
@@ -323,8 +356,9 @@ cudaError_t value_dequant_launch(const DequantParams &p, cudaStream_t stream) {
 
 #include "kivi_dispatch.h"
 
-cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, cudaStream_t stream) {
-  KIVI_DISPATCH(value_quant_launch, p, group, bits, stream);
+cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, bool recon,
+                               cudaStream_t stream) {
+  KIVI_DISPATCH_R(value_quant_launch, p, group, bits, recon, stream);
 }
 
 cudaError_t launch_value_dequant(const DequantParams &p, int group, int bits,

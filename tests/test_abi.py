@@ -189,3 +189,75 @@ def test_dequantize_cache_empty_store_is_a_noop():
     c = _cache(s_q=0)
     ptrs = (C.c_void_p * 2)(FAKE, FAKE)
     assert K.lib().kivi_dequantize_cache(_layers(), 2, C.byref(c), ptrs, ptrs, None) == 0
+
+
+def _fq(fn, **kw):
+    a = dict(x=FAKE, bh=2, s=64, d=128, xs=64 * 128, group=32, bits=2, y=FAKE + 65536,
+             ys=64 * 128, codes=FAKE, cs=64 // 16 * 128, scale=FAKE, zero=FAKE, ss=2 * 128,
+             stream=None)
+    a.update(kw)
+    return getattr(K.lib(), fn)(a["x"], a["bh"], a["s"], a["d"], a["xs"], a["group"], a["bits"],
+                                a["y"], a["ys"], a["codes"], a["cs"], a["scale"], a["zero"],
+                                a["ss"], a["stream"])
+
+
+@pytest.mark.parametrize("fn", ["kivi_fakequant_keys", "kivi_fakequant_values"])
+@pytest.mark.parametrize("kw,status", [
+    (dict(y=None), 1), (dict(x=None), 1), (dict(bits=3), 1), (dict(group=16), 1),
+    (dict(codes=None), 1), (dict(scale=None), 1), (dict(codes=None, zero=None), 1),
+    (dict(ys=64 * 128 - 8), 1), (dict(xs=64 * 128 - 8), 1),
+    (dict(y=FAKE + 2), 2), (dict(ys=64 * 128 + 4), 2), (dict(codes=FAKE + 4), 2),
+    (dict(bh=0, x=None, y=None), 0), (dict(s=0), 0),
+    (dict(s=1 << 62), 1), (dict(bh=1 << 40), 1), (dict(bh=1 << 62, s=1 << 62), 1),
+])
+def test_fakequant_validation(fn, kw, status):
+    assert _fq(fn, **kw) == status
+
+
+@pytest.mark.parametrize("kw", [dict(s=1 << 62), dict(bh=1 << 40), dict(bh=1 << 62, s=1 << 62)])
+def test_huge_sizes_rejected_without_overflow(kw):
+    assert _qk(**kw) == 1
+    assert _qv(**kw) == 1
+    L = K.lib()
+    a = dict(bh=2, s=64)
+    a.update(kw)
+    assert L.kivi_dequantize_keys(FAKE, 512, FAKE, FAKE, 256, a["bh"], a["s"], 128, 32, 2,
+                                  FAKE, 64 * 128, None) == 1
+    assert L.kivi_dequantize_values(FAKE, 80, FAKE, FAKE, 40, a["bh"], a["s"], 128, 32, 2,
+                                    FAKE, 1280, None) == 1
+
+
+def test_flush_rejects_huge_ring():
+    c = _cache(r_cap=1 << 40, n_res=100)
+    assert _flush(_layers(), 2, c)[0] == 1
+
+
+def _flush_fq(layers, n, cache, k_hat, v_hat):
+    out = C.c_int64(-7)
+    rc = K.lib().kivi_flush_fakequant(layers, n, C.byref(cache), k_hat, v_hat, C.byref(out),
+                                      None, None)
+    return rc, out.value
+
+
+def test_fused_flush_validation():
+    hat = (C.c_void_p * 2)(FAKE + (1 << 20), FAKE + (2 << 20))
+    c = _cache(n_res=63)          # nothing to move: validated, then no launch
+    assert _flush_fq(_layers(), 2, c, hat, hat) == (0, 0)
+    # store pointers may be all NULL for a tensor kind (reconstruction only)
+    c = _cache(n_res=63)
+    assert _flush_fq(_layers(k_codes=None, k_scale=None, k_zero=None), 2, c, hat, hat)[0] == 0
+    assert _flush_fq(_layers(v_codes=None, v_scale=None, v_zero=None), 2, c, hat, hat)[0] == 0
+    # ... but not partly, and never for the plain flush
+    assert _flush_fq(_layers(k_codes=None), 2, c, hat, hat)[0] == 1
+    assert _flush(_layers(k_codes=None, k_scale=None, k_zero=None), 2, c)[0] == 1
+    assert _flush_fq(_layers(k_res=None), 2, c, hat, hat)[0] == 1
+    # reconstruction arrays
+    assert _flush_fq(_layers(), 2, c, None, hat)[0] == 1
+    assert _flush_fq(_layers(), 2, c, (C.c_void_p * 2)(FAKE, None), hat)[0] == 1
+    assert _flush_fq(_layers(), 2, c, (C.c_void_p * 2)(FAKE, FAKE + 8), hat)[0] == 2
+    # capacity and state rules are those of the flush
+    c = _cache(cap=64, s_q=32, n_res=128)
+    assert _flush_fq(_layers(), 2, c, hat, hat)[0] == 3
+    assert (c.s_q, c.res_head, c.n_res) == (32, 0, 128)
+    c = _cache(bh=0, n_res=100)
+    assert _flush_fq(_layers(), 2, c, hat, hat) == (0, 64)
