@@ -118,11 +118,6 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 __device__ __forceinline__ uint64_t h2_to_f2(__half2 h) {
   const float2 f = __half22float2(h);
   return f2_pack(f.x, f.y);
@@ -248,15 +243,26 @@ __device__ __forceinline__ float recon_f32(uint32_t q, float scale, float neg_sc
 }
 
 // Reconstruction of a pair of integer-valued float codes n = (q0, q1) with
-// per-element (scale, zero) pairs: fp16(RN(RN(q*scale) + zero)), the product
-// and the sum rounded separately (n is exact, so RN(n*scale) = RN(q*scale)).
-__device__ __forceinline__ uint32_t recon_pair(uint64_t n, uint64_t scale2, uint64_t zero2) {
-  const uint64_t r = f2_add(f2_mul(n, scale2), zero2);
+// per-element (scale, zero) pairs: fp16(RN(RN(q*scale) + zero)).  The product
+// is formed as in recon_f32, inside an explicit fused multiply-add on
+// m = 2^23 + q with the exact addend -2^23*scale (neg_scale2_2p23), because a
+// packed multiply followed by a packed add may be contracted by the compiler
+// into one fused multiply-add that rounds once (it was, and the result then
+// differs in the last fp16 bit for about 3 in 10^4 elements).  An FMA result
+// followed by an add offers nothing to contract.
+__device__ __forceinline__ uint32_t recon_pair(uint64_t n, uint64_t scale2,
+                                               uint64_t neg_scale2_2p23, uint64_t zero2) {
+  const uint64_t m = f2_add(n, f2_pack(8388608.0f, 8388608.0f));  // 2^23 + q, exact
+  const uint64_t r = f2_add(f2_fma(m, scale2, neg_scale2_2p23), zero2);
   const __half2 h = __floats2half2_rn(__uint_as_float(static_cast<uint32_t>(r)),
                                       __uint_as_float(static_cast<uint32_t>(r >> 32)));
   uint32_t u;
   memcpy(&u, &h, 4);
   return u;
+}
+// (-2^23 * s0, -2^23 * s1): exact, a power-of-two multiple.
+__device__ __forceinline__ uint64_t neg_scale_2p23_pair(float s0, float s1) {
+  return f2_pack(__fmul_rn(s0, -8388608.0f), __fmul_rn(s1, -8388608.0f));
 }
 
 // ---------------------------------------------------------------------------

@@ -109,7 +109,8 @@ __device__ __noinline__ void key_exact_store(const __half2 *src, int rows_here, 
       if (ycol != nullptr && t < rows_here)  // reconstruction of real tokens only
         __stcs(reinterpret_cast<unsigned int *>(ycol + static_cast<int64_t>(t) * D),
                recon_pair(f2_pack(static_cast<float>(q0), static_cast<float>(q1)),
-                          f2_pack(g0.scale, g1.scale), f2_pack(g0.zero, g1.zero)));
+                          f2_pack(g0.scale, g1.scale), neg_scale_2p23_pair(g0.scale, g1.scale),
+                          f2_pack(g0.zero, g1.zero)));
     }
     if (cdst != nullptr) st_stream(cdst + static_cast<int64_t>(wr) * D, make_uint2(a0, a1));
   }
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
                                2 * k.col
                          : nullptr;
     GroupQ2 gq;
-    uint64_t sc2 = 0, ze2 = 0;
+    uint64_t sc2 = 0, nsc2 = 0, ze2 = 0;
     const float2 mnf = __half22float2(gmn);
     const float2 mxf = __half22float2(gmx);
     {
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
       gq = make_group2(g0, g1);
       if (RECON) {
         sc2 = f2_pack(g0.scale, g1.scale);
+        nsc2 = neg_scale_2p23_pair(g0.scale, g1.scale);
         ze2 = f2_pack(g0.zero, g1.zero);
       }
       if (k.split == 0 && codes_out) {
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
                             : f2_fma(n, f2_const(static_cast<float>(1u << (BITS * j))), half[hh]);
           if (RECON)
             __stcs(reinterpret_cast<unsigned int *>(ycol + static_cast<int64_t>(t0 + j) * D),
-                   recon_pair(n, sc2, ze2));
+                   recon_pair(n, sc2, nsc2, ze2));
         }
       }
       if (codes_out)

@@ -163,12 +163,13 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
       const int64_t out_row = p.out0 + t.r;
       const bool codes_out = !RECON || job.codes != nullptr;
       GroupQ2 gq;
-      uint64_t sc2 = 0, ze2 = 0;
+      uint64_t sc2 = 0, nsc2 = 0, ze2 = 0;
       {
         const GroupQ g = make_group(gmn, gmx, qf);
         gq = make_group2(g, g);
         if (RECON) {
           sc2 = f2_pack(g.scale, g.scale);
+          nsc2 = neg_scale_2p23_pair(g.scale, g.scale);
           ze2 = f2_pack(g.zero, g.zero);
         }
         if (t.k % L == 0 && codes_out) {
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
             acc[hh] = f2_fma(n[j], f2_const(static_cast<float>(1u << (2 * BITS * j))), acc[hh]);
           if (RECON) {
 #pragma unroll
-            for (int j = 0; j < H / 2; ++j) out[p0 + j] = recon_pair(n[j], sc2, ze2);
+            for (int j = 0; j < H / 2; ++j) out[p0 + j] = recon_pair(n[j], sc2, nsc2, ze2);
           }
         }
         // even channels (low) + odd channels (high) shifted by one code
