@@ -116,26 +116,59 @@ __device__ __noinline__ void key_exact_store(const __half2 *src, int rows_here, 
   }
 }
 
+constexpr int kKeyThreads = 256;
+
+// Head_dim 128 with G = 64 or 128 (T = 2 or 4 token splits per group): the
+// units are ordered split-major within a group, u = tile * 64 T + split * 64
+// + col, so a warp holds 32 consecutive channel pairs of one split and every
+// warp load reads, and every store writes, whole 128-byte rows (a lane order
+// with the splits adjacent leaves rows of 128 / T bytes per warp, and
+// isolated 32-byte row pieces halve the write bandwidth of the fused
+// reconstruction).  A block's 256 units are whole groups (64 T divides 256);
+// the T partial extremes of a column meet in shared memory across one block
+// barrier, double-buffered by iteration parity so that one barrier per
+// iteration suffices.
+template <int T>
+__device__ __forceinline__ KeyUnit decode_key_unit_xch(uint32_t u, const QuantParams &p) {
+  KeyUnit k;
+  constexpr int kShift = T == 2 ? 7 : 8;       // log2(64 T)
+  const uint32_t tile = u >> kShift;
+  const uint32_t rem = u & ((1u << kShift) - 1u);
+  k.split = static_cast<int>(rem >> 6);
+  k.col = static_cast<int>(rem & 63u);
+  const uint32_t jb = p.div_rows.div(tile);    // divide by ng
+  k.g = static_cast<int>(tile - jb * p.div_rows.d);
+  const uint32_t job = p.div_bh.div(jb);       // divide by bh
+  k.b = static_cast<int>(jb - job * p.div_bh.d);
+  k.job = static_cast<int>(job);
+  return k;
+}
+
 template <int BITS, int G, int DC, bool RECON>
-__global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant__ QuantParams p) {
+__global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr int T = G / 32;                  // token splits per group
   constexpr int W = CodeFmt<BITS>::W;        // codes per word
   constexpr int WPT = 32 / W;                // words per channel per thread (= BITS)
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
+  constexpr bool XCH = DC == 128 && T > 1;   // split-major units, shared-memory exchange
   const float qf = static_cast<float>(Q);
+  __shared__ uint2 xch[XCH ? 2 : 1][XCH ? kKeyThreads : 1];
+  int parity = 0;
 
   const int D = DC > 0 ? DC : p.d;           // head_dim, compile-time when DC > 0
   const uint32_t total = static_cast<uint32_t>(p.n_jobs) * p.div_bh.d * p.div_rows.d *
                          p.div_chunks.d * T;
-  const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t stride = gridDim.x * blockDim.x;
 
+  // Block-uniform loop (every thread of a block runs the same iterations, so
+  // the exchange barrier is reached by all of them).
 #pragma unroll 1
-  for (uint32_t base = (blockIdx.x * blockDim.x + threadIdx.x) & ~31u; base < total;
-       base += stride) {
-    const uint32_t u = base + lane;
+  for (uint32_t blk = blockIdx.x * kKeyThreads; blk < total; blk += gridDim.x * kKeyThreads) {
+    const uint32_t base = blk + (threadIdx.x & ~31u);
+    const uint32_t u = blk + threadIdx.x;
     const bool active = u < total;
-    const KeyUnit k = decode_key_unit<T>(active ? u : base, p);
+    // inactive lanes decode a valid unit (their warp's first, else the block's)
+    const uint32_t ud = active ? u : base < total ? base : blk;
+    const KeyUnit k = XCH ? decode_key_unit_xch<T>(ud, p) : decode_key_unit<T>(ud, p);
     const QuantJob &job = p.jobs[k.job];
     int64_t row0 = static_cast<int64_t>(k.g) * G;  // first stored row of the group
     const int rows_here = static_cast<int>(p.rows - row0) - k.split * 32;  // valid rows of the split
@@ -172,7 +205,19 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
     } else {
       gmn = gmx = __float2half2_rn(0.0f);
     }
-    if (T > 1) {
+    if (XCH) {
+      // the T partials of this column: units split * 64 + col of this group
+      xch[parity][threadIdx.x] = make_uint2(h2_as_u32(gmn), h2_as_u32(gmx));
+      __syncthreads();
+      const int g0 = static_cast<int>(threadIdx.x) & ~(64 * T - 1);
+#pragma unroll
+      for (int sp = 0; sp < T; ++sp) {
+        const uint2 e = xch[parity][g0 + sp * 64 + k.col];
+        gmn = __hmin2(gmn, u32_as_h2(e.x));
+        gmx = __hmax2(gmx, u32_as_h2(e.y));
+      }
+      parity ^= 1;
+    } else if (T > 1) {
       // partners of inactive lanes are inactive too (whole groups per lane set)
 #pragma unroll
       for (int off = 1; off < T; off <<= 1) {
@@ -180,71 +225,77 @@ __global__ void __launch_bounds__(256, 4) key_quant_kernel(const __grid_constant
         gmx = __hmax2(gmx, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(gmx), off)));
       }
     }
-    if (!active) continue;
 
-    const int64_t out_g = p.out0 + k.g;
-    const bool codes_out = !RECON || job.codes != nullptr;
-    uint32_t *cdst = codes_out ? job.codes + static_cast<int64_t>(k.b) * p.codes_bh_stride +
-                                     (out_g * (G / W) + k.split * WPT) * D + 2 * k.col
-                               : nullptr;
-    // reconstruction: column (2 col, 2 col + 1) of the first token of the split
-    __half *ycol = RECON ? static_cast<__half *>(job.y) + static_cast<int64_t>(k.b) * p.y_bh_stride +
-                               (p.y_row0 + static_cast<int64_t>(k.g) * G + k.split * 32) * D +
-                               2 * k.col
-                         : nullptr;
-    GroupQ2 gq;
-    uint64_t sc2 = 0, nsc2 = 0, ze2 = 0;
-    const float2 mnf = __half22float2(gmn);
-    const float2 mxf = __half22float2(gmx);
-    {
-      const GroupQ g0 = make_group(mnf.x, mxf.x, qf);
-      const GroupQ g1 = make_group(mnf.y, mxf.y, qf);
-      gq = make_group2(g0, g1);
-      if (RECON) {
-        sc2 = f2_pack(g0.scale, g1.scale);
-        nsc2 = neg_scale_2p23_pair(g0.scale, g1.scale);
-        ze2 = f2_pack(g0.zero, g1.zero);
-      }
-      if (k.split == 0 && codes_out) {
-        const int64_t o = static_cast<int64_t>(k.b) * p.sz_bh_stride + out_g * D + 2 * k.col;
-        __stcs(reinterpret_cast<float2 *>(job.scale + o), make_float2(g0.scale, g1.scale));
-        __stcs(reinterpret_cast<float2 *>(job.zero + o), make_float2(g0.zero, g1.zero));
-      }
-    }
-    if (!full) {
-      key_exact_store<BITS>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst, ycol);
-      continue;
-    }
-
-    // Quantize and pack along tokens: WPT words per channel, word wi holds
-    // tokens [wi*W, wi*W + W) of this thread's 32 (token wi*W + j at bits
-    // [j*BITS, (j+1)*BITS)).  Each half-word (H = 16/BITS tokens) accumulates
-    // the code pairs of both channels with packed FMAs by powers of two.
-    constexpr int H = 16 / BITS;
-#pragma unroll
-    for (int wi = 0; wi < WPT; ++wi) {
-      // (a pair the fast path declines is recomputed on the spot.  Measured
-      // alternatives -- a branch-free check per half with a redo of the half
-      // from registers or from global memory -- were slower here: the 32
-      // tokens a thread holds leave no registers for the longer live ranges.)
-      uint64_t half[2];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int t0 = wi * W + hh * H;
-#pragma unroll
-        for (int j = 0; j < H; ++j) {
-          const uint64_t n = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y,
-                                                mxf.y);
-          half[hh] = j == 0 ? n
-                            : f2_fma(n, f2_const(static_cast<float>(1u << (BITS * j))), half[hh]);
-          if (RECON)
-            __stcs(reinterpret_cast<unsigned int *>(ycol + static_cast<int64_t>(t0 + j) * D),
-                   recon_pair(n, sc2, nsc2, ze2));
+    if (active) {
+      const int64_t out_g = p.out0 + k.g;
+      const bool codes_out = !RECON || job.codes != nullptr;
+      uint32_t *cdst = codes_out ? job.codes + static_cast<int64_t>(k.b) * p.codes_bh_stride +
+                                       (out_g * (G / W) + k.split * WPT) * D + 2 * k.col
+                                 : nullptr;
+      // reconstruction: column (2 col, 2 col + 1) of the first token of the split
+      __half *ycol = RECON ? static_cast<__half *>(job.y) +
+                                 static_cast<int64_t>(k.b) * p.y_bh_stride +
+                                 (p.y_row0 + static_cast<int64_t>(k.g) * G + k.split * 32) * D +
+                                 2 * k.col
+                           : nullptr;
+      GroupQ2 gq;
+      uint64_t sc2 = 0, nsc2 = 0, ze2 = 0;
+      const float2 mnf = __half22float2(gmn);
+      const float2 mxf = __half22float2(gmx);
+      {
+        const GroupQ g0 = make_group(mnf.x, mxf.x, qf);
+        const GroupQ g1 = make_group(mnf.y, mxf.y, qf);
+        gq = make_group2(g0, g1);
+        if (RECON) {
+          sc2 = f2_pack(g0.scale, g1.scale);
+          nsc2 = neg_scale_2p23_pair(g0.scale, g1.scale);
+          ze2 = f2_pack(g0.zero, g1.zero);
+        }
+        if (k.split == 0 && codes_out) {
+          const int64_t o = static_cast<int64_t>(k.b) * p.sz_bh_stride + out_g * D + 2 * k.col;
+          __stcs(reinterpret_cast<float2 *>(job.scale + o), make_float2(g0.scale, g1.scale));
+          __stcs(reinterpret_cast<float2 *>(job.zero + o), make_float2(g0.zero, g1.zero));
         }
       }
-      if (codes_out)
-        st_stream(cdst + static_cast<int64_t>(wi) * D, join_halves2(half[0], half[1]));
+      if (!full) {
+        // ragged group: literal division, rows read again from memory
+        key_exact_store<BITS>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst, ycol);
+      } else {
+        // Quantize and pack along tokens: WPT words per channel, word wi holds
+        // tokens [wi*W, wi*W + W) of this thread's 32 (token wi*W + j at bits
+        // [j*BITS, (j+1)*BITS)).  Each half-word (H = 16/BITS tokens)
+        // accumulates the code pairs of both channels with packed FMAs by
+        // powers of two.
+        constexpr int H = 16 / BITS;
+#pragma unroll
+        for (int wi = 0; wi < WPT; ++wi) {
+          // (a pair the fast path declines is recomputed on the spot.  Measured
+          // alternatives -- a branch-free check per half with a redo of the
+          // half from registers or from global memory -- were slower here: the
+          // 32 tokens a thread holds leave no registers for the longer live
+          // ranges.)
+          uint64_t half[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int t0 = wi * W + hh * H;
+#pragma unroll
+            for (int j = 0; j < H; ++j) {
+              const uint64_t n = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x,
+                                                    mnf.y, mxf.y);
+              half[hh] = j == 0 ? n
+                                : f2_fma(n, f2_const(static_cast<float>(1u << (BITS * j))),
+                                         half[hh]);
+              if (RECON)
+                __stcs(reinterpret_cast<unsigned int *>(ycol + static_cast<int64_t>(t0 + j) * D),
+                       recon_pair(n, sc2, nsc2, ze2));
+            }
+          }
+          if (codes_out)
+            st_stream(cdst + static_cast<int64_t>(wi) * D, join_halves2(half[0], half[1]));
+        }
+      }
     }
+
   }
 }
 
@@ -323,7 +374,7 @@ int num_sms() {
 
 template <int BITS, int G, int DC, bool RECON>
 cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
-  const int threads = 256;
+  const int threads = kKeyThreads;
   auto kern = key_quant_kernel<BITS, G, DC, RECON>;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
