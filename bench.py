@@ -52,6 +52,12 @@ def bytes_per_elem(bits: int, group: int) -> float:
     return 2.0 + bits / 8.0 + 8.0 / group
 
 
+def fused_bytes_per_elem(bits: int, group: int) -> float:
+    """Fused fake-quant pass: read fp16, write codes + scale + zero, write the
+    fp16 reconstruction."""
+    return 4.0 + bits / 8.0 + 8.0 / group
+
+
 # ---------------------------------------------------------------------------
 # distributed helpers (timing reduction only; the data path has no collective)
 # ---------------------------------------------------------------------------
@@ -205,6 +211,7 @@ class PrefillFlush:
         bpe = bytes_per_elem(w.bits, w.group)
         self.kernel_bytes = {k: elems * bpe for k in self.kernels}
         self.step_bytes = 4 * elems * bpe
+        self.step_elems = 2 * elems      # fp16 elements flushed (keys and values)
         self.launches_per_step = 4
 
     def config(self):
@@ -280,6 +287,103 @@ class PrefillFlush:
         return done_bytes, t_total, f"{layers} of {w.layers} layers (flush + dequantize, keys and values)"
 
 
+class FusedPrefillFlush(PrefillFlush):
+    """The prefill flush in its fused fake-quant form: one launch per tensor
+    kind over all layers quantizes the flushed tokens into the store and
+    writes their fp16 reconstruction in the same pass (no dequantize pass
+    re-reading the codes)."""
+
+    kernels = ("key_fakequant", "value_fakequant")
+    events_per_step = 3
+
+    def __init__(self, w, device):
+        import torch
+        import kv_cache_quantization_kivi_gb300 as K
+        import workloads as W
+        self.w, self.K = w, K
+        L, bh, S, d = w.layers, w.bh, w.seq, w.head_dim
+        self.n = K.kivi_flush_size(S, w.residual, w.group)
+        self.cache = K.KiviCache(L, bh, d, r_cap=S, cap=S, group=w.group, bits=w.bits,
+                                 residual=w.residual, device=device, recon=True)
+        self.k_host_t, self.k_host = pinned_u16((L, bh, S, d))
+        self.v_host_t, self.v_host = pinned_u16((L, bh, S, d))
+        for l in range(L):
+            W.fill(w, l, "k", self.k_host[l])
+            W.fill(w, l, "v", self.v_host[l])
+        self.cache.k_res_all.copy_(self.k_host_t.to(device))
+        self.cache.v_res_all.copy_(self.v_host_t.to(device))
+        elems = L * bh * self.n * d
+        bpe = fused_bytes_per_elem(w.bits, w.group)
+        self.kernel_bytes = {k: elems * bpe for k in self.kernels}
+        self.step_bytes = 2 * elems * bpe
+        self.step_elems = 2 * elems
+        self.launches_per_step = 2
+
+    def config(self):
+        c = super().config()
+        c["step"] = ("fused fake-quant flush: per-channel key + per-token value quantize, "
+                     "pack, bookkeeping and the fp16 reconstruction in one pass, all layers")
+        c["bytes_per_elem"] = fused_bytes_per_elem(self.w.bits, self.w.group)
+        return c
+
+    def step(self, stream, ev=None):
+        c = self.cache
+        c.reset(s_q=0, res_head=0, n_res=self.w.seq)
+        n = c.flush_fakequant(stream, ev)
+        assert n == self.n
+
+    def step_events(self, evs):
+        return self.K.event_handles(evs[0:3])
+
+    def kernel_times(self, e):
+        return {"key_fakequant": e[0].elapsed_time(e[1]),
+                "value_fakequant": e[1].elapsed_time(e[2])}
+
+    def e2e_setup(self):
+        import torch
+        c, n = self.cache, self.n
+        self.hat_dev = [c.k_hat_all[:, :, :n], c.v_hat_all[:, :, :n]]
+        self.store_dev = [c.k_codes_all, c.k_scale_all, c.k_zero_all, c.v_codes_all,
+                          c.v_scale_all, c.v_zero_all]
+        self.back = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                     for t in self.hat_dev + self.store_dev]
+        h2d = 2 * self.k_host_t.numel() * 2
+        d2h = sum(t.numel() * t.element_size() for t in self.back)
+        return h2d, d2h
+
+    def e2e_step(self, stream):
+        c = self.cache
+        c.k_res_all.copy_(self.k_host_t, non_blocking=True)
+        c.v_res_all.copy_(self.v_host_t, non_blocking=True)
+        self.step(stream)
+        for dst, src in zip(self.back, self.hat_dev + self.store_dev):
+            dst.copy_(src, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        """The oracle (flush, then dequantization of the flushed tokens) on whole
+        layers, counted in the fused pass's bytes."""
+        import oracle as O
+        w = self.w
+        done_bytes, t_total, layers = 0.0, 0.0, 0
+        elems = w.bh * self.n * w.head_dim
+        W_ = 32 // w.bits
+        for l in range(w.layers):
+            st = O.Store(w.bh, w.head_dim, w.seq, w.group, w.bits)
+            t0 = time.perf_counter()
+            n, _, _, _ = O.flush(self.k_host[l], self.v_host[l], st, w.residual, 0, 0, w.seq)
+            O.dequantize_keys(st.k_codes[:, :n // W_], st.k_scale[:, :n // w.group],
+                              st.k_zero[:, :n // w.group], n, w.group, w.bits)
+            O.dequantize_values(st.v_codes[:, :n], st.v_scale[:, :n], st.v_zero[:, :n],
+                                w.group, w.bits)
+            t_total += time.perf_counter() - t0
+            done_bytes += 2 * elems * fused_bytes_per_elem(w.bits, w.group)
+            layers += 1
+            if t_total >= budget_s:
+                break
+        return done_bytes, t_total, (f"{layers} of {w.layers} layers (flush + dequantize of the "
+                                     "flushed tokens, keys and values)")
+
+
 class DecodeFlush:
     """Batched decode: every layer's store already holds 2048 tokens per
     sequence; a step flushes the 32 oldest of the 64 residual tokens of every
@@ -313,6 +417,7 @@ class DecodeFlush:
         bpe = bytes_per_elem(w.bits, G)
         self.kernel_bytes = {k: elems * bpe for k in self.kernels}
         self.step_bytes = 2 * elems * bpe
+        self.step_elems = 2 * elems
         self.launches_per_step = 2
 
     def config(self):
@@ -417,6 +522,7 @@ class StoreSweep:
         bpe = bytes_per_elem(bits, group)
         self.kernel_bytes = {k: elems * bpe for k in self.kernels}
         self.step_bytes = 4 * elems * bpe
+        self.step_elems = 2 * elems
         self.launches_per_step = 4
 
     def config(self):
@@ -486,14 +592,16 @@ class StoreSweep:
         return done, t_total, f"{rows} of {w.bh} bh slices (quantize + dequantize, keys and values)"
 
 
-def make_workload(name, device, layers=None, bits=None, group=None):
+def make_workload(name, device, layers=None, bits=None, group=None, fused=False):
     import dataclasses
     import workloads as W
     w = W.CONFIGS[name]
     if layers:
         w = dataclasses.replace(w, layers=int(layers))
     if name in ("llama3_2_3b_prefill", "qwen2_5_7b_long", "tiny_flush"):
-        return PrefillFlush(w, device)
+        return FusedPrefillFlush(w, device) if fused else PrefillFlush(w, device)
+    if fused:
+        raise SystemExit("--fused applies to the prefill flush workloads")
     if name == "batched_decode":
         return DecodeFlush(w, device)
     if name == "large_store_sweep":
@@ -552,7 +660,7 @@ def run_kivi(args):
     torch.cuda.set_device(device)
     import kv_cache_quantization_kivi_gb300 as K
     K.lib()
-    wl = make_workload(args.workload, device, args.layers, args.bits, args.group)
+    wl = make_workload(args.workload, device, args.layers, args.bits, args.group, args.fused)
     stream = torch.cuda.current_stream(device)
 
     def new_events(n):
@@ -606,7 +714,7 @@ def run_kivi(args):
     dom = max(wl.kernels, key=lambda k: sum(k_ms[k]))
     dom_avg_s = sum(k_ms[dom]) / len(k_ms[dom]) * 1e-3
     achieved = wl.kernel_bytes[dom] / dom_avg_s / 1e9
-    traffic = ncu_traffic(args.workload, dom)
+    traffic = ncu_traffic(args.workload + ("+fused" if args.fused else ""), dom)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -641,6 +749,7 @@ def run_kivi(args):
 
     config = wl.config()
     config["bytes_per_step"] = wl.step_bytes
+    config["fp16_elements_per_step"] = wl.step_elems
     config["l2"] = ("no flush: each step reads and writes ~%.2f GB, more than the 129 MB L2"
                     % (wl.step_bytes / 1e9))
     config["parallelism"] = f"independent replicas x{ws}" if ws > 1 else "single GPU"
@@ -652,6 +761,8 @@ def run_kivi(args):
         "config": config,
         "pct_of_hbm_peak": {"measured_copy": round(value / ws / peak * 100, 2),
                             "nominal_8tbs": round(value / ws / NOMINAL_HBM_GBS * 100, 2)},
+        "elements_per_s": round(reduce_sum(wl.step_elems * args.steps, device)
+                                / (elapsed_ms * 1e-3), 1),
         "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
     }
@@ -743,6 +854,9 @@ def main(argv=None):
     ap.add_argument("--json-out", default=None)
     ap.add_argument("--bits", type=int, default=None, help="large_store_sweep: code width")
     ap.add_argument("--group", type=int, default=None, help="large_store_sweep: group size")
+    ap.add_argument("--fused", action="store_true",
+                    help="prefill workloads: time the fused fake-quant flush (store and fp16 "
+                         "reconstruction in one pass) instead of flush + dequantize")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (profiling runs only; "
                          "the reported config says so)")
