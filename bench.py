@@ -495,6 +495,103 @@ class DecodeFlush:
         return done, t_total, f"{layers} of {w.layers} layers (one decode flush, keys and values)"
 
 
+class FusedDecodeFlush(DecodeFlush):
+    """The batched decode flush in its fused fake-quant form: each step
+    quantizes the 32 oldest residual tokens of every layer into the store and
+    writes their fp16 reconstruction into the fp16 cache [bh, cap, d] in the
+    same pass."""
+
+    kernels = ("key_fakequant", "value_fakequant")
+
+    def __init__(self, w, device):
+        import torch
+        import kv_cache_quantization_kivi_gb300 as K
+        import workloads as W
+        self.w, self.K = w, K
+        L, bh, d, G = w.layers, w.bh, w.head_dim, w.group
+        self.r_cap = 2 * w.residual
+        self.cycle = w.steps
+        cap = w.store_prefill + w.new_per_step * self.cycle
+        self.cache = K.KiviCache(L, bh, d, r_cap=self.r_cap, cap=cap, group=G, bits=w.bits,
+                                 residual=w.residual, device=device, recon=True)
+        self.k_host_t, self.k_host = pinned_u16((L, bh, self.r_cap, d))
+        self.v_host_t, self.v_host = pinned_u16((L, bh, self.r_cap, d))
+        for l in range(L):
+            W.fill(w, l, "k", self.k_host[l], tok0=w.store_prefill)
+            W.fill(w, l, "v", self.v_host[l], tok0=w.store_prefill)
+        self.cache.k_res_all.copy_(self.k_host_t.to(device))
+        self.cache.v_res_all.copy_(self.v_host_t.to(device))
+        self.i = 0
+        elems = L * bh * w.new_per_step * d
+        bpe = fused_bytes_per_elem(w.bits, G)
+        self.kernel_bytes = {k: elems * bpe for k in self.kernels}
+        self.step_bytes = 2 * elems * bpe
+        self.step_elems = 2 * elems
+        self.launches_per_step = 2
+
+    def config(self):
+        c = super().config()
+        c["step"] = ("one fused fake-quant decode flush of every layer: store and fp16 "
+                     "reconstruction of the flushed tokens in one pass")
+        c["bytes_per_elem"] = fused_bytes_per_elem(self.w.bits, self.w.group)
+        return c
+
+    def step(self, stream, ev=None):
+        w, c = self.w, self.cache
+        j = self.i % self.cycle
+        c.reset(s_q=w.store_prefill + w.new_per_step * j,
+                res_head=(w.new_per_step * self.i) % self.r_cap, n_res=self.r_cap)
+        self.i += 1
+        n = c.flush_fakequant(stream, ev)
+        assert n == w.new_per_step
+
+    def kernel_times(self, e):
+        return {"key_fakequant": e[0].elapsed_time(e[1]),
+                "value_fakequant": e[1].elapsed_time(e[2])}
+
+    def e2e_setup(self):
+        import torch
+        h2d, d2h = super().e2e_setup()
+        w = self.w
+        shape = (w.layers, w.bh, w.new_per_step, w.head_dim)
+        self.hat_back = [torch.empty(shape, dtype=torch.float16, pin_memory=True)
+                         for _ in range(2)]
+        return h2d, d2h + sum(t.numel() * 2 for t in self.hat_back)
+
+    def e2e_step(self, stream):
+        w, c = self.w, self.cache
+        n = w.new_per_step
+        s_q = w.store_prefill + n * (self.i % self.cycle)
+        super().e2e_step(stream)
+        self.hat_back[0].copy_(c.k_hat_all[:, :, s_q:s_q + n], non_blocking=True)
+        self.hat_back[1].copy_(c.v_hat_all[:, :, s_q:s_q + n], non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        import oracle as O
+        w = self.w
+        done, t_total, layers = 0.0, 0.0, 0
+        cap = w.store_prefill + w.new_per_step
+        Wd = 32 // w.bits
+        s0 = w.store_prefill
+        for l in range(w.layers):
+            st = O.Store(w.bh, w.head_dim, cap, w.group, w.bits)
+            t0 = time.perf_counter()
+            n, _, _, _ = O.flush(self.k_host[l], self.v_host[l], st, w.residual, s0, 0,
+                                 self.r_cap)
+            O.dequantize_keys(st.k_codes[:, s0 // Wd:(s0 + n) // Wd],
+                              st.k_scale[:, s0 // w.group:(s0 + n) // w.group],
+                              st.k_zero[:, s0 // w.group:(s0 + n) // w.group], n, w.group, w.bits)
+            O.dequantize_values(st.v_codes[:, s0:s0 + n], st.v_scale[:, s0:s0 + n],
+                                st.v_zero[:, s0:s0 + n], w.group, w.bits)
+            t_total += time.perf_counter() - t0
+            done += 2 * w.bh * n * w.head_dim * fused_bytes_per_elem(w.bits, w.group)
+            layers += 1
+            if t_total >= budget_s:
+                break
+        return done, t_total, (f"{layers} of {w.layers} layers (one decode flush + "
+                               "dequantize of the flushed tokens, keys and values)")
+
+
 class StoreSweep:
     """Full-tensor quantize of keys and values, then full dequantize, of a
     [bh, S, d] store at one (bits, group) point of the sweep."""
@@ -592,6 +689,51 @@ class StoreSweep:
         return done, t_total, f"{rows} of {w.bh} bh slices (quantize + dequantize, keys and values)"
 
 
+class FusedStoreSweep(StoreSweep):
+    """Full-tensor fused fake quantization of keys and values (codes, scales,
+    zeros and the fp16 reconstruction in one pass each) at one sweep point."""
+
+    kernels = ("key_fakequant", "value_fakequant")
+    events_per_step = 3
+
+    def __init__(self, w, device, bits, group):
+        super().__init__(w, device, bits, group)
+        elems = w.bh * w.seq * w.head_dim
+        bpe = fused_bytes_per_elem(bits, group)
+        self.kernel_bytes = {k: elems * bpe for k in self.kernels}
+        self.step_bytes = 2 * elems * bpe
+        self.launches_per_step = 2
+
+    def config(self):
+        c = super().config()
+        c["step"] = "fused fake quantization of keys and values (store + fp16 reconstruction)"
+        c["bytes_per_elem"] = fused_bytes_per_elem(self.bits, self.group)
+        return c
+
+    def step(self, stream, ev=None):
+        K, g, b = self.K, self.group, self.bits
+        if ev is not None:
+            ev[0].record(stream)
+        K.kivi_fakequant_keys(self.k, g, b, self.ky, True, self.kc, self.ks, self.kz,
+                              stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        K.kivi_fakequant_values(self.v, g, b, self.vy, True, self.vc, self.vs, self.vz,
+                                stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def kernel_times(self, e):
+        return {"key_fakequant": e[0].elapsed_time(e[1]),
+                "value_fakequant": e[1].elapsed_time(e[2])}
+
+    def cpu_sample(self, budget_s: float):
+        done, t, what = super().cpu_sample(budget_s)
+        # same oracle work (quantize + dequantize), counted in the fused pass's bytes
+        return (done * fused_bytes_per_elem(self.bits, self.group) /
+                (2 * bytes_per_elem(self.bits, self.group)), t, what)
+
+
 def make_workload(name, device, layers=None, bits=None, group=None, fused=False):
     import dataclasses
     import workloads as W
@@ -600,12 +742,10 @@ def make_workload(name, device, layers=None, bits=None, group=None, fused=False)
         w = dataclasses.replace(w, layers=int(layers))
     if name in ("llama3_2_3b_prefill", "qwen2_5_7b_long", "tiny_flush"):
         return FusedPrefillFlush(w, device) if fused else PrefillFlush(w, device)
-    if fused:
-        raise SystemExit("--fused applies to the prefill flush workloads")
     if name == "batched_decode":
-        return DecodeFlush(w, device)
+        return FusedDecodeFlush(w, device) if fused else DecodeFlush(w, device)
     if name == "large_store_sweep":
-        return StoreSweep(w, device, bits or 2, group or 32)
+        return (FusedStoreSweep if fused else StoreSweep)(w, device, bits or 2, group or 32)
     raise SystemExit(f"unknown workload {name!r}")
 
 
@@ -855,8 +995,8 @@ def main(argv=None):
     ap.add_argument("--bits", type=int, default=None, help="large_store_sweep: code width")
     ap.add_argument("--group", type=int, default=None, help="large_store_sweep: group size")
     ap.add_argument("--fused", action="store_true",
-                    help="prefill workloads: time the fused fake-quant flush (store and fp16 "
-                         "reconstruction in one pass) instead of flush + dequantize")
+                    help="time the fused fake-quant form (store and fp16 reconstruction in "
+                         "one pass) instead of quantize + dequantize")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (profiling runs only; "
                          "the reported config says so)")
