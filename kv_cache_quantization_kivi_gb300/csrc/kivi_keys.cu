@@ -118,13 +118,13 @@ __device__ __noinline__ void key_exact_store(const __half2 *src, int rows_here, 
 
 constexpr int kKeyThreads = 256;
 
-// Head_dim 128 with G = 64 or 128 (T = 2 or 4 token splits per group): the
-// units are ordered split-major within a group, u = tile * 64 T + split * 64
-// + col, so a warp holds 32 consecutive channel pairs of one split and every
-// warp load reads, and every store writes, whole 128-byte rows (a lane order
-// with the splits adjacent leaves rows of 128 / T bytes per warp, and
-// isolated 32-byte row pieces halve the write bandwidth of the fused
-// reconstruction).  A block's 256 units are whole groups (64 T divides 256);
+// Fused reconstruction at head_dim 128 with G = 64 or 128 (T = 2 or 4 token
+// splits per group): the units are ordered split-major within a group,
+// u = tile * 64 T + split * 64 + col, so a warp holds 32 consecutive channel
+// pairs of one split and every warp load reads, and every store writes,
+// whole 128-byte rows (a lane order with the splits adjacent leaves rows of
+// 128 / T bytes per warp, and isolated 32-byte row pieces halve the write
+// bandwidth of the fused reconstruction).  A block's 256 units are whole groups (64 T divides 256);
 // the T partial extremes of a column meet in shared memory across one block
 // barrier, double-buffered by iteration parity so that one barrier per
 // iteration suffices.
@@ -150,7 +150,10 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
   constexpr int W = CodeFmt<BITS>::W;        // codes per word
   constexpr int WPT = 32 / W;                // words per channel per thread (= BITS)
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
-  constexpr bool XCH = DC == 128 && T > 1;   // split-major units, shared-memory exchange
+  // split-major units with the shared-memory exchange: with the fused
+  // reconstruction (whose row pieces would otherwise be 128 / T bytes); the
+  // plain quantize keeps the shuffle order, measured 2-7% faster without it
+  constexpr bool XCH = RECON && DC == 128 && T > 1;
   const float qf = static_cast<float>(Q);
   __shared__ uint2 xch[XCH ? 2 : 1][XCH ? kKeyThreads : 1];
   int parity = 0;
