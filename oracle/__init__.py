@@ -32,6 +32,7 @@ _lib = None
 _u16p = np.ctypeslib.ndpointer(np.uint16, flags="C_CONTIGUOUS")
 _u32p = np.ctypeslib.ndpointer(np.uint32, flags="C_CONTIGUOUS")
 _f32p = np.ctypeslib.ndpointer(np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(np.float64, flags="C_CONTIGUOUS")
 _i64 = C.c_int64
 _i64p = C.POINTER(C.c_int64)
 
@@ -90,6 +91,9 @@ def lib():
                                             _u32p, _f32p, _f32p, _u32p, _f32p, _f32p,
                                             _i64p, _i64p, _i64p]
             L.kivi_oracle_flush.restype = _i64
+            L.kivi_oracle_attention.argtypes = [_u16p, _i64, _u16p, _u16p, _i64, _i64,
+                                                C.c_double, _f64p]
+            L.kivi_oracle_attention.restype = C.c_int
             _lib = L
     return _lib
 
@@ -246,3 +250,62 @@ def flush(k_res: np.ndarray, v_res: np.ndarray, store: Store, residual: int,
     if n < 0:
         raise ValueError(f"oracle flush rejected its arguments (rc={n})")
     return int(n), a.value, b.value, c.value
+
+
+# ---------------------------------------------------------------------------
+# decode attention over the reconstructed cache
+# ---------------------------------------------------------------------------
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
+    """Attention of the query rows q [r, d] (fp16 bits) over the tokens of one
+    KV head, keys k and values v [n, d] (fp16 bits), in binary64 -> [r, d]."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    r, d = q.shape
+    n = k.shape[0]
+    if k.shape != (n, d) or v.shape != (n, d):
+        raise ValueError("k and v must be [n, d] with the query's d")
+    out = np.zeros((r, d), np.float64)
+    _check(lib().kivi_oracle_attention(q, r, k, v, n, d, float(scale), out), "attention")
+    return out
+
+
+def decode_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
+    """Grouped-query decode attention: q [batch, h_q, d]; k, v [batch*h_kv, n, d]
+    (fp16 bits).  Query head h of sequence b attends KV head b*h_kv + h // (h_q/h_kv)
+    (consecutive query heads share a KV head).  Returns [batch, h_q, d] binary64."""
+    batch, h_q, d = q.shape
+    bh = k.shape[0]
+    h_kv = bh // batch
+    if h_kv * batch != bh or h_q % h_kv:
+        raise ValueError("inconsistent head counts")
+    r = h_q // h_kv
+    out = np.zeros((batch, h_q, d), np.float64)
+    for b in range(batch):
+        for j in range(h_kv):
+            out[b, j * r:(j + 1) * r] = attention(q[b, j * r:(j + 1) * r], k[b * h_kv + j],
+                                                  v[b * h_kv + j], scale)
+    return out
+
+
+def cache_kv(store: Store, s_q: int, k_ring: np.ndarray, v_ring: np.ndarray, res_head: int,
+             n_res: int):
+    """The fp16 keys and values a cache holds, in token order: the first s_q
+    store tokens dequantized, then the n_res residual tokens of the rings
+    [bh, r_cap, d] read from ring row res_head on.  Returns (k, v), each
+    [bh, s_q + n_res, d] fp16 bits."""
+    w = codes_per_word(store.bits)
+    g = store.group
+    parts_k, parts_v = [], []
+    if s_q:
+        parts_k.append(dequantize_keys(store.k_codes[:, :s_q // w], store.k_scale[:, :s_q // g],
+                                       store.k_zero[:, :s_q // g], s_q, g, store.bits))
+        parts_v.append(dequantize_values(store.v_codes[:, :s_q], store.v_scale[:, :s_q],
+                                         store.v_zero[:, :s_q], g, store.bits))
+    if n_res:
+        rows = (res_head + np.arange(n_res)) % k_ring.shape[1]
+        parts_k.append(k_ring[:, rows])
+        parts_v.append(v_ring[:, rows])
+    return (np.ascontiguousarray(np.concatenate(parts_k, axis=1)),
+            np.ascontiguousarray(np.concatenate(parts_v, axis=1)))

@@ -19,6 +19,7 @@
 
 #include <fenv.h>
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define KIVI_ORACLE_MAX_GROUP 128
@@ -349,4 +350,43 @@ int64_t kivi_oracle_flush(const uint16_t *k_res, const uint16_t *v_res,
     *res_head = (head + n) % r_cap;
     *n_res -= n;
     return n;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention over the reconstructed cache (binary64)                  */
+/* ------------------------------------------------------------------------ */
+
+int kivi_oracle_attention(const uint16_t *q, int64_t r, const uint16_t *k,
+                          const uint16_t *v, int64_t n, int64_t d, double scale,
+                          double *out) {
+    if (n < 1 || r < 1 || d < 1) return -1;
+    double *s = (double *)malloc((size_t)n * sizeof(double));
+    if (!s) return -1;
+    for (int64_t h = 0; h < r; ++h) {
+        /* scores */
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < n; ++t) {
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dot += (double)kivi_oracle_half_to_float(q[h * d + c]) *
+                       (double)kivi_oracle_half_to_float(k[t * d + c]);
+            s[t] = scale * dot;
+            if (s[t] > mx) mx = s[t];
+        }
+        /* softmax weights */
+        double den = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            s[t] = exp(s[t] - mx);
+            den += s[t];
+        }
+        /* weighted sum of the values */
+        for (int64_t c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < n; ++t)
+                acc += (s[t] / den) * (double)kivi_oracle_half_to_float(v[t * d + c]);
+            out[h * d + c] = acc;
+        }
+    }
+    free(s);
+    return 0;
 }

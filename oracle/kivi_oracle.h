@@ -118,6 +118,22 @@ int64_t kivi_oracle_flush(const uint16_t *k_res, const uint16_t *v_res,
                           uint32_t *v_codes, float *v_scale, float *v_zero,
                           int64_t *s_q, int64_t *res_head, int64_t *n_res);
 
+/* Decode attention of r query heads against the n cached tokens of one KV
+ * head, reading the keys and values as the fp16 values the cache holds
+ * (dequantized store tokens followed by the fp16 residual tokens; [POST]
+ * last section: attention that reads the packed codes expands them in
+ * registers, so what it computes is attention over the reconstruction):
+ *   s[h][t] = scale * sum_c q[h][c] * k[t][c]
+ *   p[h][t] = exp(s[h][t] - max_t s[h][t]) / sum_t exp(s[h][t] - max_t s[h][t])
+ *   out[h][c] = sum_t p[h][t] * v[t][c]
+ * q fp16 [r][d], k and v fp16 [n][d], out binary64 [r][d].  Every product,
+ * sum, exponential and quotient is binary64 (the fp16 inputs convert
+ * exactly).  Subtracting the maximum leaves the softmax unchanged in exact
+ * arithmetic and keeps exp() finite.  Returns -1 for n < 1, r < 1 or d < 1. */
+int kivi_oracle_attention(const uint16_t *q, int64_t r, const uint16_t *k,
+                          const uint16_t *v, int64_t n, int64_t d, double scale,
+                          double *out);
+
 #ifdef __cplusplus
 }
 #endif
