@@ -269,6 +269,60 @@ KIVI_API kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n
                                                  void *const events[3]);
 
 /* ------------------------------------------------------------------------ */
+/* Decode attention over the packed cache                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Attention of one new query token per sequence over everything a cache
+ * holds, reading the packed store directly: the codes are expanded in
+ * registers and never written out as fp16 (fused-kernel post, closing
+ * section: packed storage plus attention that reads the packed codes is
+ * where the memory and speed win of the method lives).  For every layer l,
+ * sequence b and query head h (r = h_q / h_kv query heads share KV head
+ * j = h / r, h_kv = cache->bh / batch):
+ *     out[l][b][h] = sum_t softmax_t(sm_scale * q[l][b][h] . k_t) v_t
+ * over t = the cache->s_q store tokens, whose keys and values are exactly
+ * the fp16 reconstructions kivi_dequantize_cache produces, followed by the
+ * cache->n_res residual tokens of the fp16 rings (bh slice b*h_kv + j).
+ * The arithmetic is binary32 with the scores and the value products on
+ * tensor cores (fp16 inputs, binary32 accumulation; the probabilities enter
+ * as a high and a low fp16 part), so results agree with an exact evaluation
+ * to a relative error of about 1e-5 of the softmax-weighted value magnitudes.
+ *   layers, cache   as for kivi_flush (store and rings); cache is only read
+ *   batch           sequences (cache->bh must be a multiple)
+ *   h_q             query heads per sequence; h_q / h_kv in 1..8
+ *   q, out          host arrays of n_layers device pointers: q fp16
+ *                   [batch][h_q][d], out fp32 [batch][h_q][d], contiguous
+ *   n_split         1..64: token ranges per (layer, bh) processed by separate
+ *                   blocks (kivi_decode_attention_splits suggests one); with
+ *                   n_split > 1 the partial results go to `workspace`
+ *                   (device, kivi_decode_attention_workspace floats) and a
+ *                   second launch combines them
+ * Supported: d == 128.  s_q + n_res must be at least 1.
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_decode_attention(const kivi_layer *layers, int n_layers,
+                                           const kivi_cache *cache, int64_t batch, int32_t h_q,
+                                           float sm_scale, const void *const *q,
+                                           float *const *out, int32_t n_split,
+                                           float *workspace, int64_t workspace_floats,
+                                           kivi_stream_t stream);
+
+/* A split count for kivi_decode_attention that fills the current device
+ * (about two waves of blocks); 1 when the (layer, bh) pairs alone do. */
+KIVI_API int32_t kivi_decode_attention_splits(const kivi_cache *cache, int n_layers,
+                                              int64_t batch);
+
+/* Workspace floats kivi_decode_attention needs with n_split splits (0 for
+ * n_split == 1); -1 for arguments it would reject. */
+KIVI_API int64_t kivi_decode_attention_workspace(const kivi_cache *cache, int n_layers,
+                                                 int64_t batch, int32_t h_q, int32_t n_split);
+
+/* The device word in which kernels record that a pipeline wait (a bulk copy
+ * that never arrived) gave up after its time limit (bit 0: decode
+ * attention); read and cleared by this call (synchronous).  Results of a
+ * call that set it are unspecified. */
+KIVI_API kivi_status kivi_device_fault(uint32_t *fault);
+
+/* ------------------------------------------------------------------------ */
 /* Sizes and diagnostics                                                    */
 /* ------------------------------------------------------------------------ */
 

@@ -26,6 +26,8 @@ __all__ = [
     "kivi_dequantize_keys", "kivi_dequantize_values", "kivi_flush", "kivi_flush_size",
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
     "kivi_fakequant_keys", "kivi_fakequant_values", "kivi_flush_fakequant",
+    "kivi_decode_attention", "kivi_decode_attention_splits", "kivi_decode_attention_workspace",
+    "kivi_device_fault",
     "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
     "KIVI_MAX_LAYERS", "event_handles",
 ]
@@ -107,6 +109,18 @@ def lib():
                                                C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_i64),
                                                _vp, C.POINTER(_vp)]
             L.kivi_flush_fakequant.restype = _int
+            L.kivi_decode_attention.argtypes = [C.POINTER(kivi_layer), _int,
+                                                C.POINTER(kivi_cache), _i64, C.c_int32,
+                                                C.c_float, C.POINTER(_vp), C.POINTER(_vp),
+                                                C.c_int32, _vp, _i64, _vp]
+            L.kivi_decode_attention.restype = _int
+            L.kivi_decode_attention_splits.argtypes = [C.POINTER(kivi_cache), _int, _i64]
+            L.kivi_decode_attention_splits.restype = C.c_int32
+            L.kivi_decode_attention_workspace.argtypes = [C.POINTER(kivi_cache), _int, _i64,
+                                                          C.c_int32, C.c_int32]
+            L.kivi_decode_attention_workspace.restype = _i64
+            L.kivi_device_fault.argtypes = [C.POINTER(C.c_uint32)]
+            L.kivi_device_fault.restype = _int
             L.kivi_flush_size.argtypes = [_i64, _int, _int]
             L.kivi_flush_size.restype = _i64
             L.kivi_key_code_words.argtypes = [_i64, _i64, _int, _int]
@@ -348,6 +362,39 @@ def kivi_dequantize_cache(layers, n_layers: int, cache: kivi_cache, k_out, v_out
     _check(st, "kivi_dequantize_cache")
 
 
+def kivi_decode_attention_splits(cache: kivi_cache, n_layers: int, batch: int) -> int:
+    return int(lib().kivi_decode_attention_splits(C.byref(cache), n_layers, batch))
+
+
+def kivi_decode_attention_workspace(cache: kivi_cache, n_layers: int, batch: int, h_q: int,
+                                    n_split: int) -> int:
+    return int(lib().kivi_decode_attention_workspace(C.byref(cache), n_layers, batch, h_q,
+                                                     n_split))
+
+
+def kivi_decode_attention(layers, n_layers: int, cache: kivi_cache, batch: int, h_q: int,
+                          sm_scale: float, q, out, n_split: int = 1, workspace=None,
+                          stream=None) -> None:
+    """Raw C call: ``q``/``out`` sequences of per-layer tensors (fp16 / fp32
+    [batch, h_q, d]) or prepared ctypes pointer arrays; ``workspace`` a float32
+    tensor of at least :func:`kivi_decode_attention_workspace` elements when
+    ``n_split > 1``."""
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() if workspace is not None else 0
+    _check(lib().kivi_decode_attention(layers, n_layers, C.byref(cache), batch, h_q,
+                                       float(sm_scale), _ptr_array(q, n_layers),
+                                       _ptr_array(out, n_layers), n_split, wp, wn,
+                                       _stream_handle(stream)),
+           "kivi_decode_attention")
+
+
+def kivi_device_fault() -> int:
+    """Reads and clears the device fault word (nonzero: a pipeline wait gave up)."""
+    v = C.c_uint32(0)
+    _check(lib().kivi_device_fault(C.byref(v)), "kivi_device_fault")
+    return int(v.value)
+
+
 class KiviCache:
     """Device buffers and state of an ``n_layers`` KIVI cache (all torch-allocated).
 
@@ -449,6 +496,30 @@ class KiviCache:
             raise ValueError("flush_fakequant needs a cache built with recon=True")
         return kivi_flush_fakequant(self.layers, self.n_layers, self.state, self._k_hat_ptrs,
                                     self._v_hat_ptrs, stream, events)
+
+    def decode_attention(self, q, batch: int, sm_scale: Optional[float] = None, out=None,
+                         n_split: Optional[int] = None, workspace=None, stream=None):
+        """Attention of the new query tokens over everything the cache holds
+        (packed store + fp16 residual).  ``q``: fp16 [n_layers, batch, h_q, d]
+        (or a per-layer list); returns fp32 [n_layers, batch, h_q, d]."""
+        import math
+        import torch
+        qs = list(q.unbind(0)) if hasattr(q, "unbind") else list(q)
+        h_q, d = int(qs[0].shape[1]), int(qs[0].shape[2])
+        if out is None:
+            out = torch.empty((self.n_layers, batch, h_q, d), dtype=torch.float32,
+                              device=qs[0].device)
+        outs = list(out.unbind(0)) if hasattr(out, "unbind") else list(out)
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(d)
+        if n_split is None:
+            n_split = kivi_decode_attention_splits(self.state, self.n_layers, batch)
+        if n_split > 1 and workspace is None:
+            need = kivi_decode_attention_workspace(self.state, self.n_layers, batch, h_q, n_split)
+            workspace = torch.empty(max(need, 1), dtype=torch.float32, device=qs[0].device)
+        kivi_decode_attention(self.layers, self.n_layers, self.state, batch, h_q, sm_scale, qs,
+                              outs, n_split, workspace, stream)
+        return out
 
     def dequantize(self, k_out=None, v_out=None, stream=None, events=None):
         """fp16 reconstructions of the first s_q store tokens of every layer;

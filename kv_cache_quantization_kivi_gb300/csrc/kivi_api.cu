@@ -473,4 +473,97 @@ kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n_layers,
   return cuda_status(record(events, 2, s));
 }
 
+// ---------------------------------------------------------------------------
+// decode attention over the packed cache
+// ---------------------------------------------------------------------------
+
+static constexpr int kAttnD = 128;
+static constexpr int kAttnTile = 32;
+static constexpr int kAttnMaxSplit = 64;
+
+struct AttnGeom {
+  int64_t h_kv, r, tiles_store, tiles_res;
+};
+
+static kivi_status attn_geom(const kivi_cache *c, int64_t batch, int32_t h_q, AttnGeom *g) {
+  if (c->d != kAttnD || batch < 1 || c->bh % batch != 0) return KIVI_ERR_INVAL;
+  g->h_kv = c->bh / batch;
+  if (g->h_kv < 1 || h_q < 1 || h_q % g->h_kv != 0) return KIVI_ERR_INVAL;
+  g->r = h_q / g->h_kv;
+  if (g->r > 8) return KIVI_ERR_INVAL;
+  g->tiles_store = c->s_q / kAttnTile;
+  g->tiles_res = (c->n_res + kAttnTile - 1) / kAttnTile;
+  return KIVI_OK;
+}
+
+int32_t kivi_decode_attention_splits(const kivi_cache *cache, int n_layers, int64_t batch) {
+  if (!cache || n_layers < 1 || batch < 1 || cache->bh < 0) return 1;
+  const int64_t items = sat_mul(n_layers, cache->bh);
+  const int64_t tiles = cache->s_q > 0 ? cache->s_q / kAttnTile : 0;
+  return kivi_impl::attention_splits(items, tiles, cache->group, cache->bits);
+}
+
+int64_t kivi_decode_attention_workspace(const kivi_cache *cache, int n_layers, int64_t batch,
+                                        int32_t h_q, int32_t n_split) {
+  AttnGeom g;
+  if (!cache || n_layers < 1 || n_split < 1 || n_split > kAttnMaxSplit) return -1;
+  if (attn_geom(cache, batch, h_q, &g) != KIVI_OK) return -1;
+  if (n_split == 1) return 0;
+  return sat_mul(sat_mul(sat_mul(n_layers, cache->bh), n_split), g.r * (kAttnD + 2));
+}
+
+kivi_status kivi_decode_attention(const kivi_layer *layers, int n_layers, const kivi_cache *cache,
+                                  int64_t batch, int32_t h_q, float sm_scale,
+                                  const void *const *q, float *const *out, int32_t n_split,
+                                  float *workspace, int64_t workspace_floats,
+                                  kivi_stream_t stream) {
+  const kivi_status st = check_cache(layers, n_layers, cache);
+  if (st != KIVI_OK) return st;
+  AttnGeom g;
+  if (attn_geom(cache, batch, h_q, &g) != KIVI_OK) return KIVI_ERR_INVAL;
+  if (!q || !out || !(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f)
+    return KIVI_ERR_INVAL;
+  if (n_split < 1 || n_split > kAttnMaxSplit) return KIVI_ERR_INVAL;
+  if (cache->s_q + cache->n_res < 1 && cache->bh > 0) return KIVI_ERR_INVAL;  // nothing to attend
+  for (int l = 0; l < n_layers; ++l) {
+    if (!q[l] || !out[l]) return KIVI_ERR_INVAL;
+    if (!aligned16(q[l]) || !aligned16(out[l])) return KIVI_ERR_ALIGN;
+  }
+  const int64_t need = kivi_decode_attention_workspace(cache, n_layers, batch, h_q, n_split);
+  if (n_split > 1) {
+    if (!workspace || workspace_floats < need) return KIVI_ERR_INVAL;
+    if (!aligned16(workspace)) return KIVI_ERR_ALIGN;
+  }
+  if (sat_mul(sat_mul(n_layers, cache->bh), n_split) > kMaxUnits) return KIVI_ERR_INVAL;
+  if (cache->bh == 0) return KIVI_OK;
+
+  kivi_impl::AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.n_jobs = n_layers;
+  p.r = static_cast<int32_t>(g.r);
+  p.h_kv = static_cast<int32_t>(g.h_kv);
+  p.n_split = n_split;
+  p.tiles_store = static_cast<int32_t>(g.tiles_store);
+  p.tiles_res = static_cast<int32_t>(g.tiles_res);
+  p.tiles_per_split = static_cast<int32_t>((g.tiles_store + n_split - 1) / n_split);
+  p.bh = cache->bh;
+  p.cap = cache->cap;
+  p.r_cap = cache->r_cap;
+  p.res_head = cache->res_head;
+  p.n_res = cache->n_res;
+  p.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+  p.ws = n_split > 1 ? workspace : nullptr;
+  for (int l = 0; l < n_layers; ++l) {
+    const kivi_layer &L = layers[l];
+    p.jobs[l] = {L.k_codes, L.k_scale, L.k_zero, L.v_codes, L.v_scale, L.v_zero,
+                 L.k_res, L.v_res, q[l], out[l]};
+  }
+  return cuda_status(kivi_impl::launch_decode_attention(p, cache->group, cache->bits, stream));
+}
+
+kivi_status kivi_device_fault(uint32_t *fault) {
+  if (!fault) return KIVI_ERR_INVAL;
+  return cuda_status(kivi_impl::read_and_clear_fault(fault));
+}
+
 }  // extern "C"

@@ -89,6 +89,44 @@ struct DequantParams {
   DequantJob jobs[KIVI_MAX_LAYERS];
 };
 
+// Decode attention over one layer's cache: the packed store (key and value
+// codes, scales, zeros) and the fp16 residual rings, queries fp16
+// [batch][h_q][d], output fp32 [batch][h_q][d].
+struct AttnJob {
+  const uint32_t *k_codes;
+  const float *k_scale;
+  const float *k_zero;
+  const uint32_t *v_codes;
+  const float *v_scale;
+  const float *v_zero;
+  const void *k_res;
+  const void *v_res;
+  const void *q;
+  float *out;
+};
+
+// Work item = (job, bh, split): split s covers store tiles [s*tps, (s+1)*tps)
+// (tiles of 32 tokens) and the last split also the residual tiles.
+struct AttnParams {
+  int32_t n_jobs;
+  int32_t r;          // query heads per KV head
+  int32_t h_kv;       // KV heads per sequence (bh = batch * h_kv)
+  int32_t n_split;
+  int32_t tiles_store;
+  int32_t tiles_res;
+  int32_t tiles_per_split;
+  int32_t pad0;
+  int64_t bh;
+  int64_t cap;        // store capacity (tokens)
+  int64_t r_cap;      // ring capacity (tokens)
+  int64_t res_head;
+  int64_t n_res;
+  float scale_log2;   // softmax scale * log2(e)
+  float pad1;
+  float *ws;          // n_split > 1: partial results, see kivi_attention.cu
+  AttnJob jobs[KIVI_MAX_LAYERS];
+};
+
 // Launchers (one per kernel family); they pick the template instance for
 // (group, bits), size the grid from the device's SM count and occupancy,
 // and return the launch's cudaError_t.
@@ -99,6 +137,16 @@ cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, bool rec
 cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, bool recon,
                                cudaStream_t stream);
 cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits, cudaStream_t stream);
+// Decode attention (head_dim 128): the main kernel, then (n_split > 1) the
+// combine kernel.
+cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits,
+                                    cudaStream_t stream);
+// Recommended number of splits for `items` (job, bh) pairs of `tiles_store`
+// store tiles each on the current device.
+int attention_splits(int64_t items, int64_t tiles_store, int group, int bits);
+// Reads and clears the device word in which kernels record a pipeline wait
+// that timed out (bit 0: decode attention).
+cudaError_t read_and_clear_fault(uint32_t *fault);
 cudaError_t launch_value_dequant(const DequantParams &p, int group, int bits,
                                  cudaStream_t stream);
 

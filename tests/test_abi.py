@@ -261,3 +261,41 @@ def test_fused_flush_validation():
     assert (c.s_q, c.res_head, c.n_res) == (32, 0, 128)
     c = _cache(bh=0, n_res=100)
     assert _flush_fq(_layers(), 2, c, hat, hat) == (0, 64)
+
+
+def _attn(cache, layers=None, n=2, batch=2, h_q=8, scale=0.1, q=None, out=None, n_split=1,
+          ws=None, ws_n=0):
+    q = q if q is not None else (C.c_void_p * n)(*[FAKE + (1 << 24) * (i + 1) for i in range(n)])
+    out = out if out is not None else (C.c_void_p * n)(*[FAKE + (1 << 28) * (i + 1)
+                                                          for i in range(n)])
+    return K.lib().kivi_decode_attention(layers if layers is not None else _layers(n), n,
+                                         C.byref(cache), batch, h_q, scale, q, out, n_split, ws,
+                                         ws_n, None)
+
+
+def test_decode_attention_validation():
+    # bh = 4: batch 2 -> h_kv 2; h_q 8 -> r = 4
+    assert _attn(_cache(d=64)) == 1                         # only head_dim 128
+    assert _attn(_cache(), batch=3) == 1                    # bh % batch
+    assert _attn(_cache(), h_q=7) == 1                      # h_q % h_kv
+    assert _attn(_cache(), h_q=18) == 1                     # r = 9 > 8
+    assert _attn(_cache(), n_split=0) == 1
+    assert _attn(_cache(), n_split=65) == 1
+    assert _attn(_cache(), n_split=2) == 1                  # no workspace
+    need = K.lib().kivi_decode_attention_workspace(C.byref(_cache()), 2, 2, 8, 2)
+    assert need == 2 * 4 * 2 * 4 * 130
+    assert _attn(_cache(), n_split=2, ws=FAKE, ws_n=need - 1) == 1
+    assert _attn(_cache(), n_split=2, ws=FAKE + 4, ws_n=need) == 2
+    assert _attn(_cache(), q=(C.c_void_p * 2)(FAKE, None)) == 1
+    assert _attn(_cache(), q=(C.c_void_p * 2)(FAKE, FAKE + 2)) == 2
+    assert _attn(_cache(), scale=float("nan")) == 1
+    assert _attn(_cache(s_q=0, n_res=0)) == 1               # nothing to attend to
+    assert _attn(_cache(bh=0), batch=1) == 1                # bh 0: no sequence to map
+    assert _attn(_cache(), layers=_layers(2, v_zero=None)) == 1
+    assert K.lib().kivi_decode_attention_workspace(C.byref(_cache()), 2, 2, 8, 1) == 0
+    assert K.lib().kivi_decode_attention_workspace(C.byref(_cache()), 2, 2, 9, 1) == -1
+    assert K.lib().kivi_decode_attention_splits(C.byref(_cache()), 2, 2) >= 1
+
+
+def test_device_fault_rejects_null():
+    assert K.lib().kivi_device_fault(None) == 1

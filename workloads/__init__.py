@@ -138,6 +138,10 @@ def _load():
             L.kivi_gen_fill.argtypes = [C.POINTER(_Spec), C.c_void_p, C.c_int64, C.c_int64,
                                         C.c_int64, C.c_int64, C.c_int64, C.c_int]
             L.kivi_gen_fill.restype = C.c_int
+            L.kivi_gen_fill_range.argtypes = [C.POINTER(_Spec), C.c_void_p, C.c_int64,
+                                              C.c_int64, C.c_int64, C.c_int64, C.c_int64,
+                                              C.c_int64, C.c_int]
+            L.kivi_gen_fill_range.restype = C.c_int
             L.kivi_gen_outliers.argtypes = [C.POINTER(_Spec), C.c_int64, C.c_int,
                                             C.POINTER(C.c_int32)]
             L.kivi_gen_outliers.restype = C.c_int
@@ -163,15 +167,16 @@ def default_threads() -> int:
 
 
 def fill(w: Workload, layer: int, kind: str, out: np.ndarray, tok0: int = 0,
-         n_threads: Optional[int] = None) -> np.ndarray:
+         n_threads: Optional[int] = None, bh0: int = 0) -> np.ndarray:
     """Fill ``out`` (uint16 [bh, n_tok, d] view, last two dims contiguous) with
-    sequence positions ``tok0 .. tok0 + n_tok`` of (layer, kind)."""
+    sequence positions ``tok0 .. tok0 + n_tok`` of (layer, kind), bh slices
+    ``bh0 .. bh0 + bh``."""
     assert out.dtype == np.uint16 and out.ndim == 3
     bh, n_tok, d = out.shape
     assert out.strides[2] == 2 and out.strides[1] == 2 * d
     spec, keep = _spec(w, layer, kind)
-    rc = _load().kivi_gen_fill(C.byref(spec), out.ctypes.data, bh, tok0, n_tok, d,
-                               out.strides[0] // 2, n_threads or default_threads())
+    rc = _load().kivi_gen_fill_range(C.byref(spec), out.ctypes.data, bh0, bh, tok0, n_tok, d,
+                                     out.strides[0] // 2, n_threads or default_threads())
     if rc != 0:
         raise ValueError("input generator rejected its arguments")
     del keep
@@ -179,12 +184,14 @@ def fill(w: Workload, layer: int, kind: str, out: np.ndarray, tok0: int = 0,
 
 
 def generate(w: Workload, layer: int, kind: str, tok0: int = 0, n_tok: Optional[int] = None,
-             bh: Optional[int] = None, n_threads: Optional[int] = None) -> np.ndarray:
-    """uint16 [bh, n_tok, d] fp16 bit patterns of (layer, kind) at positions tok0.."""
+             bh: Optional[int] = None, n_threads: Optional[int] = None,
+             bh0: int = 0) -> np.ndarray:
+    """uint16 [bh, n_tok, d] fp16 bit patterns of (layer, kind) at positions
+    tok0.., bh slices bh0 .. bh0 + bh."""
     n_tok = w.seq if n_tok is None else n_tok
-    bh = w.bh if bh is None else bh
+    bh = w.bh - bh0 if bh is None else bh
     out = np.empty((bh, n_tok, w.head_dim), np.uint16)
-    return fill(w, layer, kind, out, tok0, n_threads)
+    return fill(w, layer, kind, out, tok0, n_threads, bh0)
 
 
 def outlier_channels(w: Workload, layer: int, head: int) -> np.ndarray:

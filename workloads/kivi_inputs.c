@@ -99,6 +99,7 @@ typedef struct {
     const kivi_gen_spec *spec;
     uint16_t *out;
     int64_t r0, r1;               /* flat (bh, token) row range */
+    int64_t bh0;                  /* bh index of the first output slice */
     int64_t tok0, n_tok, d, out_bh_stride;
     const uint8_t *outlier_mask;  /* [heads][d] */
     const double *offset;         /* [heads][d] or NULL */
@@ -111,11 +112,12 @@ static void *fill_range(void *arg)
     const uint64_t key = stream_key(s, 1);
     for (int64_t r = j->r0; r < j->r1; ++r) {
         const int64_t b = r / j->n_tok, i = r % j->n_tok;
-        const int64_t head = b % s->heads;
+        const int64_t gb = j->bh0 + b;            /* bh index in the whole tensor */
+        const int64_t head = gb % s->heads;
         const uint64_t t = (uint64_t)(j->tok0 + i);
         uint16_t *row = j->out + b * j->out_bh_stride + i * j->d;
         for (int64_t c = 0; c < j->d; ++c) {
-            const uint64_t ctr = ((uint64_t)b << 40) ^ (t << 16) ^ (uint64_t)c;
+            const uint64_t ctr = ((uint64_t)gb << 40) ^ (t << 16) ^ (uint64_t)c;
             double v = s->sigma * draw(s, key, ctr);
             if (j->outlier_mask[head * j->d + c]) v *= s->outlier_mult;
             if (j->offset) v += j->offset[head * j->d + c];
@@ -126,14 +128,17 @@ static void *fill_range(void *arg)
 }
 
 /* Fill out[b * out_bh_stride + i * d + c] for b < bh, i < n_tok, c < d with
- * the value of sequence position tok0 + i.  Returns 0, or -1 on bad input. */
-int kivi_gen_fill(const kivi_gen_spec *spec, uint16_t *out, int64_t bh, int64_t tok0,
-                  int64_t n_tok, int64_t d, int64_t out_bh_stride, int n_threads)
+ * the value of bh slice bh0 + b at sequence position tok0 + i.  Returns 0, or
+ * -1 on bad input. */
+int kivi_gen_fill_range(const kivi_gen_spec *spec, uint16_t *out, int64_t bh0, int64_t bh,
+                        int64_t tok0, int64_t n_tok, int64_t d, int64_t out_bh_stride,
+                        int n_threads)
 {
-    if (!spec || !out || bh < 0 || tok0 < 0 || n_tok < 0 || d <= 0 || d >= 65536) return -1;
+    if (!spec || !out || bh0 < 0 || bh < 0 || tok0 < 0 || n_tok < 0 || d <= 0 || d >= 65536)
+        return -1;
     if (spec->heads <= 0 || spec->n_outliers < 0 || spec->n_outliers > d) return -1;
     /* the counter packs bh, token and channel into disjoint bit fields */
-    if (bh >= ((int64_t)1 << 19) || tok0 + n_tok >= ((int64_t)1 << 24)) return -1;
+    if (bh0 + bh >= ((int64_t)1 << 19) || tok0 + n_tok >= ((int64_t)1 << 24)) return -1;
     if (out_bh_stride < n_tok * d) return -1;
     if (n_threads < 1) n_threads = 1;
 
@@ -181,7 +186,7 @@ int kivi_gen_fill(const kivi_gen_spec *spec, uint16_t *out, int64_t bh, int64_t 
     if (rc == 0) {
         for (int k = 0; k < n_threads; ++k) {
             jobs[k] = (job_t){spec, out, rows * k / n_threads, rows * (k + 1) / n_threads,
-                              tok0, n_tok, d, out_bh_stride, mask, offset};
+                              bh0, tok0, n_tok, d, out_bh_stride, mask, offset};
         }
         if (n_threads == 1) {
             fill_range(&jobs[0]);
@@ -200,6 +205,13 @@ int kivi_gen_fill(const kivi_gen_spec *spec, uint16_t *out, int64_t bh, int64_t 
     }
     free(th); free(jobs); free(mask); free(offset); free(perm);
     return rc;
+}
+
+/* kivi_gen_fill_range from bh slice 0. */
+int kivi_gen_fill(const kivi_gen_spec *spec, uint16_t *out, int64_t bh, int64_t tok0,
+                  int64_t n_tok, int64_t d, int64_t out_bh_stride, int n_threads)
+{
+    return kivi_gen_fill_range(spec, out, 0, bh, tok0, n_tok, d, out_bh_stride, n_threads);
 }
 
 /* The outlier channel set of one head (for tests): writes n_outliers indices. */
