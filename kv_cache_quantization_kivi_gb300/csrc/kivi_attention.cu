@@ -10,16 +10,22 @@
 // fp16 residual tokens.  Query head h of a sequence reads KV head h / r.
 //
 // Work item (one CTA of 4 warps) = (layer, bh, split).  Its store tiles (32
-// tokens each) are dealt to the warps round-robin; each warp streams its
-// tiles' key codes, key scale/zero row, value codes and value scales/zeros
-// (six contiguous pieces) into a private shared-memory ring with bulk
-// asynchronous copies completed on per-stage mbarriers, so no CTA barrier
-// is needed until the end.  Per tile:
-//   S^T = K Q^T     m16n8k16 tensor-core MMAs: A = the dequantized key tile
-//                   (16 tokens x 16 channels), B = the query heads
+// tokens each) and, in the last split, its residual tiles are dealt to the
+// warps round-robin; each warp streams its store tiles' key codes, key
+// scale/zero row, value codes and value scales/zeros (six contiguous pieces)
+// into a private shared-memory ring with bulk asynchronous copies completed
+// on per-stage mbarriers, so no CTA barrier is needed until the end.  Per
+// tile the warp expands the codes cooperatively -- each lane one key channel
+// (four of them) or one value token, so a code word's scale is loaded once
+// and its codes are spread four to a register with one shift, one mask and
+// byte permutes -- into an fp16 tile in its own shared-memory buffer
+// (swizzled so that 16-byte stores and ldmatrix rows avoid bank conflicts),
+// then:
+//   S^T = K Q^T     m16n8k16 tensor-core MMAs: A = key tile (16 tokens x 16
+//                   channels, ldmatrix), B = the query heads
 //   online softmax  per head column, base-2 exponent with the scale folded in
-//   O^T += V^T P^T  A = the dequantized value tile (16 channels x 16 tokens),
-//                   B = P^T from the score accumulators through movmatrix
+//   O^T += V^T P^T  A = value tile (16 channels x 16 tokens, ldmatrix), B =
+//                   P^T from the score accumulators through movmatrix
 // P is scaled by 2^12 and split into fp16 high and low parts (two MMAs), so
 // the probabilities keep ~22 bits; the scale cancels against the softmax
 // denominator accumulated in fp32 from the same values.  The 4 warps' states
@@ -61,30 +67,177 @@ struct StageFmt {
   static constexpr int oKs = kKc, oKz = oKs + kKs, oVc = oKz + kKs, oVs = oVc + kVc,
                        oVz = oVs + kVs;
   static constexpr int kBytes = oVz + kVs;
-  static constexpr int NS = BITS == 2 ? 3 : 2;     // stages per warp
-  static constexpr int kSmem = kWarps * NS * kBytes + kWarps * NS * 8;
+  static constexpr int NS = 2;                     // stages per warp
+  static constexpr int kBuf = kTile * kD * 2;      // fp16 tile per warp
+  static constexpr int kRing = kWarps * NS * kBytes;
+  static constexpr int kBufs = kRing;              // [warp] fp16 tiles
+  static constexpr int kBars = kBufs + kWarps * kBuf;
+  static constexpr int kQsm = kBars + kWarps * NS * 8;   // [8][32] query fragments
+  static constexpr int kSmem = kQsm + 8 * 32 * 8;
 };
 
-// 2^23 + q as a float, from the code at bit `pos` of w.
+// ---------------------------------------------------------------------------
+// fp16 tile layouts in a warp's buffer (8 KB = 32 tokens x 128 channels)
+//   row-major [token][channel]  (values; residual keys): row 256 B, its
+//     16-byte chunk j stored at chunk j ^ (token & 7)
+//   transposed [channel][token] (store keys): row 64 B, chunk j stored at
+//     chunk j ^ ((channel >> 1) & 3)
+// so that a warp's 16-byte stores (one row per lane) and each 8-lane phase
+// of ldmatrix (8 rows, one chunk column) touch distinct bank groups.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t tok_major(int tok, int chunk) {
+  return static_cast<uint32_t>(tok * 256 + ((chunk ^ (tok & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t ch_major(int ch, int chunk) {
+  return static_cast<uint32_t>(ch * 64 + ((chunk ^ ((ch >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&a)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&a)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// 2^23 + q as floats for the codes of one word, in code order.  Codes are
+// spread four to a register (one byte each) by a shift and a mask, then a
+// byte permute puts each byte under the exponent of 2^23.
 template <int BITS>
-__device__ __forceinline__ float code_magic(uint32_t w, int pos) {
-  if (BITS == 8) return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7650u + (pos >> 3)));
-  return __uint_as_float(((w >> pos) & ((1u << BITS) - 1u)) | 0x4B000000u);
+__device__ __forceinline__ void word_magics(uint32_t w, float (&m)[32 / BITS]) {
+  constexpr int W = 32 / BITS;
+  constexpr uint32_t M = 0x4B000000u;
+  if (BITS == 8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m[k] = __uint_as_float(__byte_perm(w, M, 0x7650u + k));
+  } else {
+    constexpr int PER_BYTE = 8 / BITS;                      // codes per byte
+    constexpr uint32_t MASK = BITS == 2 ? 0x03030303u : 0x0F0F0F0Fu;
+#pragma unroll
+    for (int j = 0; j < PER_BYTE; ++j) {
+      const uint32_t y = (w >> (j * BITS)) & MASK;         // byte k: code k*PER_BYTE + j
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        m[k * PER_BYTE + j] = __uint_as_float(__byte_perm(y, M, 0x7650u + k));
+    }
+    (void)W;
+  }
 }
 
-// fp16 reconstructions of two codes (as 2^23 + q floats) with per-element
-// (scale, -2^23 scale, zero): fp16(RN(RN(q scale) + zero)) -- the product
-// formed inside an FMA with an exact addend (nothing for the compiler to
-// contract), then a separately rounded add.
-__device__ __forceinline__ uint32_t deq2(float m0, float m1, uint64_t s2, uint64_t ns2,
-                                         uint64_t z2) {
-  const uint64_t r = f2_add(f2_fma(f2_pack(m0, m1), s2, ns2), z2);
-  return h2_as_u32(__floats2half2_rn(__uint_as_float(static_cast<uint32_t>(r)),
-                                     __uint_as_float(static_cast<uint32_t>(r >> 32))));
+// fp16 reconstructions of 8 consecutive codes (as magic floats) sharing one
+// (scale, -2^23 scale, zero): fp16(RN(RN(q scale) + zero)), the product made
+// inside an FMA with an exact addend (nothing to contract), the add rounded
+// separately.
+__device__ __forceinline__ uint4 deq8(const float *m, uint64_t s2, uint64_t ns2, uint64_t z2) {
+  uint32_t h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t r = f2_add(f2_fma(f2_pack(m[2 * i], m[2 * i + 1]), s2, ns2), z2);
+    h[i] = h2_as_u32(__floats2half2_rn(__uint_as_float(static_cast<uint32_t>(r)),
+                                       __uint_as_float(static_cast<uint32_t>(r >> 32))));
+  }
+  return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-__device__ __forceinline__ uint64_t neg2p23(float s0, float s1) {
-  return f2_pack(__fmul_rn(s0, -8388608.0f), __fmul_rn(s1, -8388608.0f));
+__device__ __forceinline__ void scale_consts(float s, float z, uint64_t &s2, uint64_t &ns2,
+                                             uint64_t &z2) {
+  const float ns = __fmul_rn(s, -8388608.0f);   // -2^23 s, exact
+  s2 = f2_pack(s, s);
+  ns2 = f2_pack(ns, ns);
+  z2 = f2_pack(z, z);
+}
+
+// 2^23 + q floats of 16 consecutive codes: one word (2 bits), two (4 bits)
+// or four (8 bits), in code order.
+template <int BITS>
+__device__ __forceinline__ void magics16(const uint32_t *w, float (&m)[16]) {
+  constexpr int W = 32 / BITS;
+#pragma unroll
+  for (int i = 0; i < 16 / W; ++i) word_magics<BITS>(w[i], *reinterpret_cast<float(*)[W]>(m + i * W));
+}
+
+// Store key tile -> transposed fp16 tile.  Unit = 16 tokens of one channel
+// (tokens 16 h .. 16 h + 15); lane takes units (channel lane + 32 i, half h).
+template <int BITS>
+__device__ __forceinline__ void expand_keys(const uint32_t *kc, const float *ks, const float *kz,
+                                            uint32_t buf, int lane) {
+  constexpr int W = 32 / BITS;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = lane + 32 * i;
+    uint64_t s2, ns2, z2;
+    scale_consts(ks[c], kz[c], s2, ns2, z2);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t w[16 / W];
+#pragma unroll
+      for (int k = 0; k < 16 / W; ++k) w[k] = kc[(h * (16 / W) + k) * kD + c];
+      float m[16];
+      magics16<BITS>(w, m);
+      sts128(buf + ch_major(c, 2 * h), deq8(m, s2, ns2, z2));
+      sts128(buf + ch_major(c, 2 * h + 1), deq8(m + 8, s2, ns2, z2));
+    }
+  }
+}
+
+// Store value tile -> row-major fp16 tile.  Unit = 16 channels of one token
+// (the 16/W consecutive words of channels 16 u .. 16 u + 15); consecutive
+// lanes take consecutive units, so their word loads are consecutive too.
+template <int BITS, int G>
+__device__ __forceinline__ void expand_values(const uint32_t *vc, const float *vs, const float *vz,
+                                              uint32_t buf, int lane) {
+  constexpr int W = 32 / BITS;
+  constexpr int RW = kD / W;          // words per token
+  constexpr int NG = kD / G;
+  constexpr int WU = 16 / W;          // words per unit
+#pragma unroll 2
+  for (int k = 0; k < 8; ++k) {
+    const int u = lane + 32 * k;
+    const int tok = u >> 3, cu = u & 7;           // token, 16-channel unit
+    const int grp = (16 * cu) / G;
+    uint64_t s2, ns2, z2;
+    scale_consts(vs[tok * NG + grp], vz[tok * NG + grp], s2, ns2, z2);
+    const uint32_t *src = vc + tok * RW + cu * WU;
+    uint32_t w[WU];
+    if constexpr (WU == 4) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(src);
+      w[0] = v.x; w[1 % WU] = v.y; w[2 % WU] = v.z; w[3 % WU] = v.w;
+    } else if constexpr (WU == 2) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(src);
+      w[0] = v.x; w[1 % WU] = v.y;
+    } else {
+      w[0] = src[0];
+    }
+    float m[16];
+    magics16<BITS>(w, m);
+    sts128(buf + tok_major(tok, 2 * cu), deq8(m, s2, ns2, z2));
+    sts128(buf + tok_major(tok, 2 * cu + 1), deq8(m + 8, s2, ns2, z2));
+  }
+}
+
+// Residual tile (fp16 ring rows) -> row-major fp16 tile: lane = token; rows
+// past `valid` are zero.
+__device__ __forceinline__ void load_residual(const __half *base, int64_t r_cap, int64_t head,
+                                              int tok0, int valid, uint32_t buf, int lane) {
+  const bool ok = lane < valid;
+  const uint4 *src = nullptr;
+  if (ok) {
+    const int64_t rr = (head + tok0 + lane) % r_cap;
+    src = reinterpret_cast<const uint4 *>(base + rr * kD);
+  }
+#pragma unroll
+  for (int ch = 0; ch < 16; ++ch) {
+    const uint4 v = ok ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
+    sts128(buf + tok_major(lane, ch), v);
+  }
 }
 
 // Per-thread online-softmax state for heads 2t, 2t+1 (t = lane % 4).
@@ -94,178 +247,43 @@ struct SoftState {
   float o[8][4];  // O^T accumulators: channel block mc, (ch g, h 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
 };
 
-// Key fragments of a store tile in shared memory.
-template <int BITS, int G>
-struct StoreKeys {
-  const uint32_t *kc;
-  const float *ks, *kz;
-  int g, t;
-  uint64_t s2a, ns2a, z2a, s2b, ns2b, z2b;
-  __device__ __forceinline__ void prepare(int kk) {
-    const int c0 = 16 * kk + 2 * t;
-    const float2 sa = *reinterpret_cast<const float2 *>(ks + c0);
-    const float2 sb = *reinterpret_cast<const float2 *>(ks + c0 + 8);
-    const float2 za = *reinterpret_cast<const float2 *>(kz + c0);
-    const float2 zb = *reinterpret_cast<const float2 *>(kz + c0 + 8);
-    s2a = f2_pack(sa.x, sa.y);
-    ns2a = neg2p23(sa.x, sa.y);
-    z2a = f2_pack(za.x, za.y);
-    s2b = f2_pack(sb.x, sb.y);
-    ns2b = neg2p23(sb.x, sb.y);
-    z2b = f2_pack(zb.x, zb.y);
-  }
-  // A fragment: tokens 16 mb + {g, g+8} x channels 16 kk + {2t, 2t+1, 2t+8, 2t+9}
-  __device__ __forceinline__ void frag(int mb, int kk, uint32_t (&a)[4]) const {
-    constexpr int W = 32 / BITS;
-    const int c0 = 16 * kk + 2 * t;
-    const int tau0 = 16 * mb + g, tau1 = tau0 + 8;
-    const int r0 = tau0 / W, r1 = tau1 / W;
-    const int p0 = (tau0 % W) * BITS, p1 = (tau1 % W) * BITS;
-    const uint2 w0a = *reinterpret_cast<const uint2 *>(kc + r0 * kD + c0);
-    const uint2 w0b = *reinterpret_cast<const uint2 *>(kc + r0 * kD + c0 + 8);
-    uint2 w1a = w0a, w1b = w0b;
-    if (r1 != r0) {
-      w1a = *reinterpret_cast<const uint2 *>(kc + r1 * kD + c0);
-      w1b = *reinterpret_cast<const uint2 *>(kc + r1 * kD + c0 + 8);
-    }
-    a[0] = deq2(code_magic<BITS>(w0a.x, p0), code_magic<BITS>(w0a.y, p0), s2a, ns2a, z2a);
-    a[1] = deq2(code_magic<BITS>(w1a.x, p1), code_magic<BITS>(w1a.y, p1), s2a, ns2a, z2a);
-    a[2] = deq2(code_magic<BITS>(w0b.x, p0), code_magic<BITS>(w0b.y, p0), s2b, ns2b, z2b);
-    a[3] = deq2(code_magic<BITS>(w1b.x, p1), code_magic<BITS>(w1b.y, p1), s2b, ns2b, z2b);
-  }
-};
-
-// Value fragments of a store tile in shared memory.
-template <int BITS, int G>
-struct StoreValues {
-  const uint32_t *vc;
-  const float *vs, *vz;
-  int g, t;
-  uint64_t s2a, ns2a, z2a, s2b, ns2b, z2b;   // tokens (2t, 2t+1) and (2t+8, 2t+9)
-  int cur;                                    // (mb, group) of the loaded scales, -1: none
-  __device__ __forceinline__ void prepare(int mb, int mc) {
-    const int grp = 16 * mc / G;
-    if (mb * 16 + grp == cur) return;
-    cur = mb * 16 + grp;
-    constexpr int NG = kD / G;
-    const int ta = 16 * mb + 2 * t, tb = ta + 8;
-    const float sa0 = vs[ta * NG + grp], sa1 = vs[(ta + 1) * NG + grp];
-    const float sb0 = vs[tb * NG + grp], sb1 = vs[(tb + 1) * NG + grp];
-    const float za0 = vz[ta * NG + grp], za1 = vz[(ta + 1) * NG + grp];
-    const float zb0 = vz[tb * NG + grp], zb1 = vz[(tb + 1) * NG + grp];
-    s2a = f2_pack(sa0, sa1);
-    ns2a = neg2p23(sa0, sa1);
-    z2a = f2_pack(za0, za1);
-    s2b = f2_pack(sb0, sb1);
-    ns2b = neg2p23(sb0, sb1);
-    z2b = f2_pack(zb0, zb1);
-  }
-  // A fragment of V^T: channels 16 mc + {g, g+8} x tokens 16 mb + {2t, 2t+1, 2t+8, 2t+9}
-  __device__ __forceinline__ void frag(int mb, int mc, uint32_t (&a)[4]) const {
-    constexpr int W = 32 / BITS;
-    constexpr int RW = kD / W;                 // words per token row
-    const int c = 16 * mc + g, c8 = c + 8;
-    const int wi = c / W, wi8 = c8 / W;
-    const int pc = (c % W) * BITS, pc8 = (c8 % W) * BITS;
-    const int ta = 16 * mb + 2 * t, tb = ta + 8;
-    const uint32_t *row_a0 = vc + ta * RW, *row_a1 = row_a0 + RW;
-    const uint32_t *row_b0 = vc + tb * RW, *row_b1 = row_b0 + RW;
-    a[0] = deq2(code_magic<BITS>(row_a0[wi], pc), code_magic<BITS>(row_a1[wi], pc), s2a, ns2a, z2a);
-    a[1] = deq2(code_magic<BITS>(row_a0[wi8], pc8), code_magic<BITS>(row_a1[wi8], pc8), s2a, ns2a,
-                z2a);
-    a[2] = deq2(code_magic<BITS>(row_b0[wi], pc), code_magic<BITS>(row_b1[wi], pc), s2b, ns2b, z2b);
-    a[3] = deq2(code_magic<BITS>(row_b0[wi8], pc8), code_magic<BITS>(row_b1[wi8], pc8), s2b, ns2b,
-                z2b);
-  }
-};
-
-// Key / value fragments of a residual tile, read from the fp16 ring.
-struct ResidualKV {
-  const __half *kr, *vr;   // this bh slice of the rings
-  int64_t r_cap, head;
-  int tok0, valid;         // first logical residual token of the tile, valid tokens in it
-  int g, t;
-  __device__ __forceinline__ const __half *row(const __half *base, int tau) const {
-    int64_t rr = head + tok0 + tau;
-    rr %= r_cap;
-    return base + rr * kD;
-  }
-  __device__ __forceinline__ uint32_t ld2(const __half *base, int tau, int c) const {
-    if (tau >= valid) return 0u;
-    return *reinterpret_cast<const uint32_t *>(row(base, tau) + c);
-  }
-  __device__ __forceinline__ uint32_t pair_tok(const __half *base, int tau, int c) const {
-    // (x[tau][c], x[tau+1][c]) as a half2
-    const unsigned short lo =
-        tau < valid ? *reinterpret_cast<const unsigned short *>(row(base, tau) + c) : 0;
-    const unsigned short hi =
-        tau + 1 < valid ? *reinterpret_cast<const unsigned short *>(row(base, tau + 1) + c) : 0;
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
-  __device__ __forceinline__ void prepare(int) {}
-  __device__ __forceinline__ void prepare(int, int) {}
-  __device__ __forceinline__ void kfrag(int mb, int kk, uint32_t (&a)[4]) const {
-    const int c0 = 16 * kk + 2 * t;
-    const int tau0 = 16 * mb + g, tau1 = tau0 + 8;
-    a[0] = ld2(kr, tau0, c0);
-    a[1] = ld2(kr, tau1, c0);
-    a[2] = ld2(kr, tau0, c0 + 8);
-    a[3] = ld2(kr, tau1, c0 + 8);
-  }
-  __device__ __forceinline__ void vfrag(int mb, int mc, uint32_t (&a)[4]) const {
-    const int c = 16 * mc + g;
-    const int ta = 16 * mb + 2 * t, tb = ta + 8;
-    a[0] = pair_tok(vr, ta, c);
-    a[1] = pair_tok(vr, ta, c + 8);
-    a[2] = pair_tok(vr, tb, c);
-    a[3] = pair_tok(vr, tb, c + 8);
-  }
-};
-
-// Adapters so that attend_tile sees one interface.
-template <typename K>
-struct KeyAdapter {
-  K &k;
-  __device__ __forceinline__ void prepare(int kk) { k.prepare(kk); }
-  __device__ __forceinline__ void frag(int mb, int kk, uint32_t (&a)[4]) const { k.frag(mb, kk, a); }
-};
-template <typename V>
-struct ValueAdapter {
-  V &v;
-  __device__ __forceinline__ void prepare(int mb, int mc) { v.prepare(mb, mc); }
-  __device__ __forceinline__ void frag(int mb, int mc, uint32_t (&a)[4]) const { v.frag(mb, mc, a); }
-};
-struct ResKeyAdapter {
-  const ResidualKV &r;
-  __device__ __forceinline__ void prepare(int) {}
-  __device__ __forceinline__ void frag(int mb, int kk, uint32_t (&a)[4]) const { r.kfrag(mb, kk, a); }
-};
-struct ResValueAdapter {
-  const ResidualKV &r;
-  __device__ __forceinline__ void prepare(int, int) {}
-  __device__ __forceinline__ void frag(int mb, int mc, uint32_t (&a)[4]) const { r.vfrag(mb, mc, a); }
-};
-
-// One tile of 32 tokens (the first `valid` of them real).
-template <typename KA, typename VA>
-__device__ __forceinline__ void attend_tile(SoftState &st, const uint32_t (&qf)[8][2],
-                                            float scale_log2, int valid, KA ka, VA va, int g) {
-  float s[2][4];
+// Scores of one tile from the key tile in `buf` (transposed layout for store
+// tiles, row-major for residual tiles): s[mb] = 16 tokens x 8 heads.
+template <bool KEYS_T>
+__device__ __forceinline__ void tile_scores(uint32_t buf, const uint2 *qsm, int lane,
+                                            float (&s)[2][4]) {
+  float s2[2][4];
 #pragma unroll
   for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[mb][i] = 0.0f;
-#pragma unroll
+    for (int i = 0; i < 4; ++i) s[mb][i] = s2[mb][i] = 0.0f;
+  const int mat = lane >> 3, row = lane & 7;
+#pragma unroll 2
   for (int kk = 0; kk < 8; ++kk) {
-    ka.prepare(kk);
+    const uint2 qb = qsm[kk * 32 + lane];
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
+      // matrices (tokens tb.., channels cb..) in A order: (0,0) (8,0) (0,8) (8,8)
+      const int tb = 16 * mb + (mat & 1) * 8, cb = 16 * kk + (mat >> 1) * 8;
       uint32_t a[4];
-      ka.frag(mb, kk, a);
-      mma_16816(s[mb], a, qf[kk][0], qf[kk][1]);
+      if (KEYS_T)
+        ldsm_x4_trans(buf + ch_major(cb + row, tb >> 3), a);
+      else
+        ldsm_x4(buf + tok_major(tb + row, cb >> 3), a);
+      mma_16816((kk & 1) ? s2[mb] : s[mb], a, qb.x, qb.y);
     }
   }
-  // scale (log2 units), mask, tile maximum per head column
+#pragma unroll
+  for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[mb][i] += s2[mb][i];
+}
+
+// Online softmax update with one tile's scores; returns P^T fragments (x 2^12,
+// fp16 high and low parts) for the value products.
+__device__ __forceinline__ void tile_softmax(SoftState &st, float (&s)[2][4], float scale_log2,
+                                             int valid, int g, uint32_t (&phi)[2][2],
+                                             uint32_t (&plo)[2][2]) {
   float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
   for (int mb = 0; mb < 2; ++mb)
@@ -288,8 +306,6 @@ __device__ __forceinline__ void attend_tile(SoftState &st, const uint32_t (&qf)[
     alpha[j] = mn[j] == -INFINITY ? 1.0f : exp2f(st.m[j] - mn[j]);
     st.m[j] = mn[j];
   }
-  // probabilities (x 2^12) as fp16 high + low parts, transposed into B fragments
-  uint32_t phi[2][2], plo[2][2];
   float lsum[2] = {0.0f, 0.0f};
 #pragma unroll
   for (int mb = 0; mb < 2; ++mb) {
@@ -318,13 +334,21 @@ __device__ __forceinline__ void attend_tile(SoftState &st, const uint32_t (&qf)[
     st.o[mc][2] *= alpha[0];
     st.o[mc][3] *= alpha[1];
   }
+}
+
+// O^T += V^T P^T from the row-major value tile in `buf`.
+__device__ __forceinline__ void tile_values(SoftState &st, uint32_t buf, int lane,
+                                            const uint32_t (&phi)[2][2],
+                                            const uint32_t (&plo)[2][2]) {
+  const int mat = lane >> 3, row = lane & 7;
 #pragma unroll
   for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
     for (int mc = 0; mc < 8; ++mc) {
-      va.prepare(mb, mc);
+      // matrices (channels cb.., tokens tb..) in A order: (0,0) (8,0) (0,8) (8,8)
+      const int cb = 16 * mc + (mat & 1) * 8, tb = 16 * mb + (mat >> 1) * 8;
       uint32_t a[4];
-      va.frag(mb, mc, a);
+      ldsm_x4_trans(buf + tok_major(tb + row, cb >> 3), a);
       mma_16816(st.o[mc], a, phi[mb][0], phi[mb][1]);
       mma_16816(st.o[mc], a, plo[mb][0], plo[mb][1]);
     }
@@ -347,17 +371,6 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
   const int64_t b = bhi / p.h_kv, kvh = bhi - b * p.h_kv;
   const int64_t h_q = static_cast<int64_t>(p.h_kv) * p.r;
 
-  // query heads kvh*r .. kvh*r + r-1 as B fragments (k = channels, n = heads)
-  uint32_t qf[8][2];
-  {
-    const __half *q = static_cast<const __half *>(J.q) + (b * h_q + kvh * p.r + g) * kD;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const int c0 = 16 * kk + 2 * t;
-      qf[kk][0] = g < p.r ? *reinterpret_cast<const uint32_t *>(q + c0) : 0u;
-      qf[kk][1] = g < p.r ? *reinterpret_cast<const uint32_t *>(q + c0 + 8) : 0u;
-    }
-  }
   SoftState st;
   st.m[0] = st.m[1] = -INFINITY;
   st.l[0] = st.l[1] = 0.0f;
@@ -366,12 +379,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
 #pragma unroll
     for (int i = 0; i < 4; ++i) st.o[mc][i] = 0.0f;
 
-  // ---- store tiles through the warp's shared-memory ring
+  // ---- the block's tiles: its store range, then (last split) the residual
+  // tiles; warp w takes list positions w, w + 4, ... (store tiles first)
   const int st0 = split * p.tiles_per_split;
-  const int st1 = min(st0 + p.tiles_per_split, p.tiles_store);
-  const int n_my = st1 - st0 > warp ? (st1 - st0 - warp + kWarps - 1) / kWarps : 0;
+  const int n_store = max(0, min(st0 + p.tiles_per_split, p.tiles_store) - st0);
+  const int n_my = n_store > warp ? (n_store - warp + kWarps - 1) / kWarps : 0;
   unsigned char *ring = smem + warp * F::NS * F::kBytes;
-  const uint32_t bar0 = smem_addr(smem + kWarps * F::NS * F::kBytes) + warp * F::NS * 8;
+  const uint32_t buf = smem_addr(smem + F::kBufs + warp * F::kBuf);
+  const uint32_t bar0 = smem_addr(smem + F::kBars) + warp * F::NS * 8;
   if (lane == 0) {
 #pragma unroll
     for (int sidx = 0; sidx < F::NS; ++sidx) mbar_init(bar0 + 8 * sidx, 1);
@@ -406,6 +421,19 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
     for (; issued < min(F::NS, n_my); ++issued) issue(issued);
   issued = __shfl_sync(0xffffffffu, issued, 0);
 
+  // query heads kvh*r .. kvh*r + r-1 as B fragments (k = channels, n = heads)
+  // in shared memory, one copy per block (loaded while the first copies fly)
+  uint2 *qsm = reinterpret_cast<uint2 *>(smem + F::kQsm);
+  for (int idx = threadIdx.x; idx < 8 * 32; idx += kThreads) {
+    const int kk = idx >> 5, ql = idx & 31, qg = ql >> 2, qt = ql & 3;
+    const __half *q = static_cast<const __half *>(J.q) + (b * h_q + kvh * p.r + qg) * kD;
+    const int c0 = 16 * kk + 2 * qt;
+    qsm[idx] = qg < p.r ? make_uint2(*reinterpret_cast<const uint32_t *>(q + c0),
+                                     *reinterpret_cast<const uint32_t *>(q + c0 + 8))
+                        : make_uint2(0u, 0u);
+  }
+  __syncthreads();
+
   int done = 0;
   bool failed = false;
 #pragma unroll 1
@@ -418,20 +446,25 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
       break;
     }
     const unsigned char *stg = ring + sidx * F::kBytes;
-    StoreKeys<BITS, G> kf{reinterpret_cast<const uint32_t *>(stg),
-                          reinterpret_cast<const float *>(stg + F::oKs),
-                          reinterpret_cast<const float *>(stg + F::oKz), g, t};
-    StoreValues<BITS, G> vf{reinterpret_cast<const uint32_t *>(stg + F::oVc),
-                            reinterpret_cast<const float *>(stg + F::oVs),
-                            reinterpret_cast<const float *>(stg + F::oVz), g, t};
-    vf.cur = -1;
-    attend_tile(st, qf, p.scale_log2, kTile, KeyAdapter<StoreKeys<BITS, G>>{kf},
-                ValueAdapter<StoreValues<BITS, G>>{vf}, g);
+    float s[2][4];
+    uint32_t phi[2][2], plo[2][2];
+    expand_keys<BITS>(reinterpret_cast<const uint32_t *>(stg),
+                      reinterpret_cast<const float *>(stg + F::oKs),
+                      reinterpret_cast<const float *>(stg + F::oKz), buf, lane);
     __syncwarp();
+    tile_scores<true>(buf, qsm, lane, s);
+    tile_softmax(st, s, p.scale_log2, kTile, g, phi, plo);
+    __syncwarp();                                  // key tile read by every lane
+    expand_values<BITS, G>(reinterpret_cast<const uint32_t *>(stg + F::oVc),
+                           reinterpret_cast<const float *>(stg + F::oVs),
+                           reinterpret_cast<const float *>(stg + F::oVz), buf, lane);
+    __syncwarp();                                  // stage consumed, value tile written
     if (issued < n_my) {
       if (lane == 0) issue(issued);
       ++issued;
     }
+    tile_values(st, buf, lane, phi, plo);
+    __syncwarp();                                  // value tile read by every lane
   }
   if (failed) {
     // record the timeout and wait (bounded) for this warp's copies still in flight
@@ -445,13 +478,24 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
   if (split == p.n_split - 1 && !failed) {
     const __half *kr = static_cast<const __half *>(J.k_res) + bhi * p.r_cap * kD;
     const __half *vr = static_cast<const __half *>(J.v_res) + bhi * p.r_cap * kD;
+    // first list position >= n_store that belongs to this warp
+    const int first = n_store + ((warp - n_store) % kWarps + kWarps) % kWarps;
 #pragma unroll 1
-    for (int j = warp; j < p.tiles_res; j += kWarps) {
+    for (int j = first - n_store; j < p.tiles_res; j += kWarps) {
       const int tok0 = j * kTile;
       const int64_t left = p.n_res - tok0;
       const int valid = left < kTile ? static_cast<int>(left) : kTile;
-      ResidualKV rk{kr, vr, p.r_cap, p.res_head, tok0, valid, g, t};
-      attend_tile(st, qf, p.scale_log2, valid, ResKeyAdapter{rk}, ResValueAdapter{rk}, g);
+      float s[2][4];
+      uint32_t phi[2][2], plo[2][2];
+      load_residual(kr, p.r_cap, p.res_head, tok0, valid, buf, lane);
+      __syncwarp();
+      tile_scores<false>(buf, qsm, lane, s);
+      tile_softmax(st, s, p.scale_log2, valid, g, phi, plo);
+      __syncwarp();
+      load_residual(vr, p.r_cap, p.res_head, tok0, valid, buf, lane);
+      __syncwarp();
+      tile_values(st, buf, lane, phi, plo);
+      __syncwarp();
     }
   }
 
