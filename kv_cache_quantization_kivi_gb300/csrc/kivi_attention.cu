@@ -79,14 +79,16 @@ struct StageFmt {
 // ---------------------------------------------------------------------------
 // fp16 tile layouts in a warp's buffer (8 KB = 32 tokens x 128 channels)
 //   row-major [token][channel]  (values; residual keys): row 256 B, its
-//     16-byte chunk j stored at chunk j ^ (token & 7)
+//     16-byte chunk j stored at chunk (j ^ (j >> 3)) ^ (token & 7)
 //   transposed [channel][token] (store keys): row 64 B, chunk j stored at
 //     chunk j ^ ((channel >> 1) & 3)
-// so that a warp's 16-byte stores (one row per lane) and each 8-lane phase
-// of ldmatrix (8 rows, one chunk column) touch distinct bank groups.
+// so that every 8-lane phase of the 16-byte stores (the value expansion's 8
+// lanes write the even, then the odd chunks of one token; the others one
+// chunk of 8 rows) and of ldmatrix (8 rows, one chunk column) touches 8
+// distinct bank groups.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t tok_major(int tok, int chunk) {
-  return static_cast<uint32_t>(tok * 256 + ((chunk ^ (tok & 7)) << 4));
+  return static_cast<uint32_t>(tok * 256 + (((chunk ^ (chunk >> 3)) ^ (tok & 7)) << 4));
 }
 __device__ __forceinline__ uint32_t ch_major(int ch, int chunk) {
   return static_cast<uint32_t>(ch * 64 + ((chunk ^ ((ch >> 1) & 3)) << 4));
