@@ -592,6 +592,136 @@ class FusedDecodeFlush(DecodeFlush):
                                "dequantize of the flushed tokens, keys and values)")
 
 
+class DecodeAttention:
+    """Decode attention over the batched-decode cache: every layer's store
+    holds the first 2048 tokens of each sequence (quantized from the
+    workload's data), the residual ring the next 64 in fp16; one step = one
+    new query token per sequence and query head (32 query heads over the 8 KV
+    heads) attending to all 2112 cached tokens of every layer, reading the
+    packed codes directly."""
+
+    kernels = ("decode_attention",)
+    events_per_step = 2
+    H_Q = 32
+
+    def __init__(self, w, device):
+        import numpy as np
+        import torch
+        import kv_cache_quantization_kivi_gb300 as K
+        import workloads as W
+        self.w, self.K = w, K
+        L, bh, d, G, b = w.layers, w.bh, w.head_dim, w.group, w.bits
+        n = w.store_prefill
+        self.r_cap = 2 * w.residual
+        self.cache = K.KiviCache(L, bh, d, r_cap=self.r_cap, cap=n, group=G, bits=b,
+                                 residual=w.residual, device=device)
+        c = self.cache
+        kt, kh = pinned_u16((bh, n, d))
+        vt, vh = pinned_u16((bh, n, d))
+        for l in range(L):
+            W.fill(w, l, "k", kh)
+            W.fill(w, l, "v", vh)
+            kd, vd = kt.to(device), vt.to(device)
+            K.kivi_quantize_keys(kd, G, b, c.k_codes[l], c.k_scale[l], c.k_zero[l])
+            K.kivi_quantize_values(vd, G, b, c.v_codes[l], c.v_scale[l], c.v_zero[l])
+            c.k_res[l].copy_(torch.from_numpy(
+                W.generate(w, l, "k", tok0=n, n_tok=self.r_cap).view(np.int16)).view(
+                    torch.float16).to(device))
+            c.v_res[l].copy_(torch.from_numpy(
+                W.generate(w, l, "v", tok0=n, n_tok=self.r_cap).view(np.int16)).view(
+                    torch.float16).to(device))
+        torch.cuda.synchronize(device)
+        c.reset(s_q=n, res_head=0, n_res=self.r_cap)
+        rng = np.random.default_rng(w.seed)
+        self.q_host = torch.from_numpy(
+            rng.standard_normal((L, w.batch, self.H_Q, d)).astype(np.float16)).pin_memory()
+        self.q = self.q_host.to(device)
+        self.out = torch.empty((L, w.batch, self.H_Q, d), dtype=torch.float32, device=device)
+        self.scale = 1.0 / d ** 0.5
+        self.n_split = K.kivi_decode_attention_splits(c.state, L, w.batch)
+        need = K.kivi_decode_attention_workspace(c.state, L, w.batch, self.H_Q, self.n_split)
+        self.ws = torch.empty(max(need, 1), dtype=torch.float32, device=device)
+        self.q_ptrs = K._ptr_array(list(self.q.unbind(0)), L)
+        self.o_ptrs = K._ptr_array(list(self.out.unbind(0)), L)
+        per_tok = d * b / 8 * 2 + 8 * d / G * 2          # key + value codes, scales, zeros
+        self.tokens = n + self.r_cap
+        elems = L * bh * self.tokens * d * 2              # K and V elements attended
+        self.kernel_bytes = {"decode_attention": L * bh * (n * per_tok + self.r_cap * d * 4)
+                             + self.q.numel() * 2 + self.out.numel() * 4}
+        self.step_bytes = self.kernel_bytes["decode_attention"]
+        self.step_elems = elems
+        self.launches_per_step = 1 if self.n_split == 1 else 2
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name + "+attention", "layers": w.layers, "batch": w.batch,
+                "kv_heads": w.kv_heads, "q_heads": self.H_Q, "head_dim": w.head_dim,
+                "bits": w.bits, "group": w.group, "store_tokens": w.store_prefill,
+                "residual_tokens": self.r_cap, "n_split": self.n_split,
+                "step": "decode attention of one query token per sequence over the packed "
+                        "store + fp16 residual of every layer",
+                "bytes": "packed codes + scales/zeros + fp16 residual + queries + outputs",
+                "fp16_equivalent_bytes_per_step": self.step_elems * 2}
+
+    def step(self, stream, ev=None):
+        c = self.cache
+        if ev is not None:
+            ev[0].record(stream)
+        self.K.kivi_decode_attention(c.layers, c.n_layers, c.state, self.w.batch, self.H_Q,
+                                     self.scale, self.q_ptrs, self.o_ptrs, self.n_split,
+                                     self.ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def step_events(self, evs):
+        return evs
+
+    def kernel_times(self, e):
+        return {"decode_attention": e[0].elapsed_time(e[1])}
+
+    def e2e_setup(self):
+        import torch
+        self.out_back = torch.empty(self.out.shape, dtype=torch.float32, pin_memory=True)
+        return self.q_host.numel() * 2, self.out_back.numel() * 4
+
+    def e2e_step(self, stream):
+        self.q.copy_(self.q_host, non_blocking=True)
+        self.step(stream)
+        self.out_back.copy_(self.out, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float):
+        """The oracle's attention (binary64) over (layer, sequence) pairs of the
+        same cache until the budget is spent."""
+        import numpy as np
+        import oracle as O
+        import workloads as W
+        w, n = self.w, self.w.store_prefill
+        h_kv = w.kv_heads
+        done, t_total, pairs = 0.0, 0.0, 0
+        q = self.q_host.numpy()
+        per_pair = self.step_bytes / (w.layers * w.batch)
+        for l in range(w.layers):
+            for b in range(w.batch):
+                sl = dict(bh0=b * h_kv, bh=h_kv)
+                k_st = W.generate(w, l, "k", n_tok=n, **sl)
+                v_st = W.generate(w, l, "v", n_tok=n, **sl)
+                k_r = W.generate(w, l, "k", tok0=n, n_tok=self.r_cap, **sl)
+                v_r = W.generate(w, l, "v", tok0=n, n_tok=self.r_cap, **sl)
+                t0 = time.perf_counter()
+                kc, ks, kz = O.quantize_keys(k_st, w.group, w.bits)
+                vc, vs, vz = O.quantize_values(v_st, w.group, w.bits)
+                k = np.concatenate([O.dequantize_keys(kc, ks, kz, n, w.group, w.bits), k_r], 1)
+                v = np.concatenate([O.dequantize_values(vc, vs, vz, w.group, w.bits), v_r], 1)
+                O.decode_attention(q[l, b:b + 1].view(np.uint16), k, v, self.scale)
+                t_total += time.perf_counter() - t0
+                done += per_pair
+                pairs += 1
+                if t_total >= budget_s:
+                    return done, t_total, (f"{pairs} (layer, sequence) pairs: quantize, dequantize "
+                                           "and binary64 attention of 32 query heads")
+        return done, t_total, f"{pairs} (layer, sequence) pairs"
+
+
 class StoreSweep:
     """Full-tensor quantize of keys and values, then full dequantize, of a
     [bh, S, d] store at one (bits, group) point of the sweep."""
@@ -734,7 +864,8 @@ class FusedStoreSweep(StoreSweep):
                 (2 * bytes_per_elem(self.bits, self.group)), t, what)
 
 
-def make_workload(name, device, layers=None, bits=None, group=None, fused=False):
+def make_workload(name, device, layers=None, bits=None, group=None, fused=False,
+                  attention=False):
     import dataclasses
     import workloads as W
     w = W.CONFIGS[name]
@@ -743,6 +874,8 @@ def make_workload(name, device, layers=None, bits=None, group=None, fused=False)
     if name in ("llama3_2_3b_prefill", "qwen2_5_7b_long", "tiny_flush"):
         return FusedPrefillFlush(w, device) if fused else PrefillFlush(w, device)
     if name == "batched_decode":
+        if attention:
+            return DecodeAttention(w, device)
         return FusedDecodeFlush(w, device) if fused else DecodeFlush(w, device)
     if name == "large_store_sweep":
         return (FusedStoreSweep if fused else StoreSweep)(w, device, bits or 2, group or 32)
@@ -800,7 +933,8 @@ def run_kivi(args):
     torch.cuda.set_device(device)
     import kv_cache_quantization_kivi_gb300 as K
     K.lib()
-    wl = make_workload(args.workload, device, args.layers, args.bits, args.group, args.fused)
+    wl = make_workload(args.workload, device, args.layers, args.bits, args.group, args.fused,
+                       args.attention)
     stream = torch.cuda.current_stream(device)
 
     def new_events(n):
@@ -854,7 +988,8 @@ def run_kivi(args):
     dom = max(wl.kernels, key=lambda k: sum(k_ms[k]))
     dom_avg_s = sum(k_ms[dom]) / len(k_ms[dom]) * 1e-3
     achieved = wl.kernel_bytes[dom] / dom_avg_s / 1e9
-    traffic = ncu_traffic(args.workload + ("+fused" if args.fused else ""), dom)
+    traffic = ncu_traffic(args.workload + ("+fused" if args.fused else "")
+                          + ("+attention" if args.attention else ""), dom)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -997,6 +1132,8 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true",
                     help="time the fused fake-quant form (store and fp16 reconstruction in "
                          "one pass) instead of quantize + dequantize")
+    ap.add_argument("--attention", action="store_true",
+                    help="batched_decode: time decode attention over the packed cache")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (profiling runs only; "
                          "the reported config says so)")
