@@ -53,7 +53,8 @@ using namespace kivi_dev;
 constexpr int kD = 128;            // head_dim
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kTile = 32;          // tokens per tile
+constexpr int kTile = 32;          // tokens per tile (one pipeline stage)
+constexpr int kHalf = 16;          // tokens expanded and attended at a time
 constexpr float kPScale = 4096.0f; // P * 2^12 stays a normal fp16 down to P = 2^-26
 constexpr uint64_t kWaitLimitNs = 200000000ull;  // 0.2 s per pipeline wait
 
@@ -68,20 +69,20 @@ struct StageFmt {
                        oVz = oVs + kVs;
   static constexpr int kBytes = oVz + kVs;
   static constexpr int NS = 2;                     // stages per warp
-  static constexpr int kBuf = kTile * kD * 2;      // fp16 tile per warp
+  static constexpr int kBuf = kHalf * kD * 2;      // fp16 half tile per warp (4 KB)
   static constexpr int kRing = kWarps * NS * kBytes;
-  static constexpr int kBufs = kRing;              // [warp] fp16 tiles
+  static constexpr int kBufs = kRing;              // [warp] fp16 half tiles
   static constexpr int kBars = kBufs + kWarps * kBuf;
   static constexpr int kQsm = kBars + kWarps * NS * 8;   // [8][32] query fragments
   static constexpr int kSmem = kQsm + 8 * 32 * 8;
 };
 
 // ---------------------------------------------------------------------------
-// fp16 tile layouts in a warp's buffer (8 KB = 32 tokens x 128 channels)
+// fp16 half-tile layouts in a warp's buffer (4 KB = 16 tokens x 128 channels)
 //   row-major [token][channel]  (values; residual keys): row 256 B, its
 //     16-byte chunk j stored at chunk (j ^ (j >> 3)) ^ (token & 7)
-//   transposed [channel][token] (store keys): row 64 B, chunk j stored at
-//     chunk j ^ ((channel >> 1) & 3)
+//   transposed [channel][token] (store keys): row 32 B, chunk j stored at
+//     chunk j ^ ((channel >> 2) & 1)
 // so that every 8-lane phase of the 16-byte stores (the value expansion's 8
 // lanes write the even, then the odd chunks of one token; the others one
 // chunk of 8 rows) and of ldmatrix (8 rows, one chunk column) touches 8
@@ -91,7 +92,7 @@ __device__ __forceinline__ uint32_t tok_major(int tok, int chunk) {
   return static_cast<uint32_t>(tok * 256 + (((chunk ^ (chunk >> 3)) ^ (tok & 7)) << 4));
 }
 __device__ __forceinline__ uint32_t ch_major(int ch, int chunk) {
-  return static_cast<uint32_t>(ch * 64 + ((chunk ^ ((ch >> 1) & 3)) << 4));
+  return static_cast<uint32_t>(ch * 32 + ((chunk ^ ((ch >> 2) & 1)) << 4));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&a)[4]) {
@@ -114,8 +115,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 // spread four to a register (one byte each) by a shift and a mask, then a
 // byte permute puts each byte under the exponent of 2^23.
 template <int BITS>
-__device__ __forceinline__ void word_magics(uint32_t w, float (&m)[32 / BITS]) {
-  constexpr int W = 32 / BITS;
+__device__ __forceinline__ void word_magics(uint32_t w, float *m) {
   constexpr uint32_t M = 0x4B000000u;
   if (BITS == 8) {
 #pragma unroll
@@ -130,8 +130,16 @@ __device__ __forceinline__ void word_magics(uint32_t w, float (&m)[32 / BITS]) {
       for (int k = 0; k < 4; ++k)
         m[k * PER_BYTE + j] = __uint_as_float(__byte_perm(y, M, 0x7650u + k));
     }
-    (void)W;
   }
+}
+
+// 2^23 + q floats of 16 consecutive codes: one word (2 bits), two (4 bits)
+// or four (8 bits), in code order.
+template <int BITS>
+__device__ __forceinline__ void magics16(const uint32_t *w, float (&m)[16]) {
+  constexpr int W = 32 / BITS;
+#pragma unroll
+  for (int i = 0; i < 16 / W; ++i) word_magics<BITS>(w[i], m + i * W);
 }
 
 // fp16 reconstructions of 8 consecutive codes (as magic floats) sharing one
@@ -157,57 +165,107 @@ __device__ __forceinline__ void scale_consts(float s, float z, uint64_t &s2, uin
   z2 = f2_pack(z, z);
 }
 
-// 2^23 + q floats of 16 consecutive codes: one word (2 bits), two (4 bits)
-// or four (8 bits), in code order.
-template <int BITS>
-__device__ __forceinline__ void magics16(const uint32_t *w, float (&m)[16]) {
-  constexpr int W = 32 / BITS;
-#pragma unroll
-  for (int i = 0; i < 16 / W; ++i) word_magics<BITS>(w[i], *reinterpret_cast<float(*)[W]>(m + i * W));
+// 2-bit codes: the four possible reconstructions of a unit (one scale and
+// zero) as an fp16 table in two registers (lo = codes 0, 1; hi = codes 2, 3),
+// and the 16 codes of a word looked up with byte permutes.  A code q spread
+// into a byte becomes the byte pair selector 0x22 q + 0x10 (bytes 2q, 2q+1 of
+// the table) by one integer multiply-add over four bytes at once.  Output
+// order: half2 word i of chunk k holds codes 8k + i and 8k + i + 4, i.e.
+// position p of a chunk holds code kPerm[p] (see perm8 below).
+__device__ __forceinline__ void lut2(float s, float z, uint32_t &lo, uint32_t &hi) {
+  uint64_t s2, ns2, z2;
+  scale_consts(s, z, s2, ns2, z2);
+  const uint64_t m01 = f2_pack(__uint_as_float(0x4B000000u), __uint_as_float(0x4B000001u));
+  const uint64_t m23 = f2_pack(__uint_as_float(0x4B000002u), __uint_as_float(0x4B000003u));
+  const uint64_t r01 = f2_add(f2_fma(m01, s2, ns2), z2);
+  const uint64_t r23 = f2_add(f2_fma(m23, s2, ns2), z2);
+  lo = h2_as_u32(__floats2half2_rn(__uint_as_float(static_cast<uint32_t>(r01)),
+                                   __uint_as_float(static_cast<uint32_t>(r01 >> 32))));
+  hi = h2_as_u32(__floats2half2_rn(__uint_as_float(static_cast<uint32_t>(r23)),
+                                   __uint_as_float(static_cast<uint32_t>(r23 >> 32))));
 }
+__device__ __forceinline__ void lookup16(uint32_t w, uint32_t lo, uint32_t hi, uint4 &c0,
+                                         uint4 &c1) {
+  uint32_t h[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t y = (w >> (2 * j)) & 0x03030303u;   // byte k: code 4k + j
+    const uint32_t sel = y * 0x22u + 0x10101010u;       // byte pair selectors
+    h[j] = __byte_perm(lo, hi, sel);                    // codes j, j + 4
+    h[4 + j] = __byte_perm(lo, hi, sel >> 16);          // codes j + 8, j + 12
+  }
+  c0 = make_uint4(h[0], h[1], h[2], h[3]);
+  c1 = make_uint4(h[4], h[5], h[6], h[7]);
+}
+// Within each 8-element chunk the 2-bit path stores element perm8(p) at
+// position p: p = 2i holds i, p = 2i + 1 holds i + 4; its inverse places
+// element e at 2e (e < 4) or 2(e - 4) + 1.
+__device__ __forceinline__ int perm8(int p) { return (p >> 1) + ((p & 1) << 2); }
+__device__ __forceinline__ int perm8_inv(int e) { return ((e & 3) << 1) | (e >> 2); }
 
-// Store key tile -> transposed fp16 tile.  Unit = 16 tokens of one channel
-// (tokens 16 h .. 16 h + 15); lane takes units (channel lane + 32 i, half h).
+// Keys of tokens 16 hb .. 16 hb + 15 of a store tile -> transposed fp16 half
+// tile.  Unit = those 16 tokens of one channel; lane takes channels
+// lane + 32 i.
 template <int BITS>
 __device__ __forceinline__ void expand_keys(const uint32_t *kc, const float *ks, const float *kz,
-                                            uint32_t buf, int lane) {
+                                            int hb, uint32_t buf, int lane) {
   constexpr int W = 32 / BITS;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int c = lane + 32 * i;
-    uint64_t s2, ns2, z2;
-    scale_consts(ks[c], kz[c], s2, ns2, z2);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    if constexpr (BITS == 2) {   // tokens of each chunk in perm8 order
+      uint32_t lo, hi;
+      lut2(ks[c], kz[c], lo, hi);
+      uint4 c0, c1;
+      lookup16(kc[hb * kD + c], lo, hi, c0, c1);
+      sts128(buf + ch_major(c, 0), c0);
+      sts128(buf + ch_major(c, 1), c1);
+    } else {
+      uint64_t s2, ns2, z2;
+      scale_consts(ks[c], kz[c], s2, ns2, z2);
       uint32_t w[16 / W];
 #pragma unroll
-      for (int k = 0; k < 16 / W; ++k) w[k] = kc[(h * (16 / W) + k) * kD + c];
+      for (int k = 0; k < 16 / W; ++k) w[k] = kc[(hb * (16 / W) + k) * kD + c];
       float m[16];
       magics16<BITS>(w, m);
-      sts128(buf + ch_major(c, 2 * h), deq8(m, s2, ns2, z2));
-      sts128(buf + ch_major(c, 2 * h + 1), deq8(m + 8, s2, ns2, z2));
+      sts128(buf + ch_major(c, 0), deq8(m, s2, ns2, z2));
+      sts128(buf + ch_major(c, 1), deq8(m + 8, s2, ns2, z2));
     }
   }
 }
 
-// Store value tile -> row-major fp16 tile.  Unit = 16 channels of one token
-// (the 16/W consecutive words of channels 16 u .. 16 u + 15); consecutive
-// lanes take consecutive units, so their word loads are consecutive too.
+// Values of tokens 16 hb .. of a store tile -> row-major fp16 half tile.
+// Unit = 16 channels of one token (the 16/W consecutive words of channels
+// 16 cu ..); consecutive lanes take consecutive units, so their word loads
+// are consecutive too.
 template <int BITS, int G>
 __device__ __forceinline__ void expand_values(const uint32_t *vc, const float *vs, const float *vz,
-                                              uint32_t buf, int lane) {
+                                              int hb, uint32_t buf, int lane) {
   constexpr int W = 32 / BITS;
   constexpr int RW = kD / W;          // words per token
   constexpr int NG = kD / G;
   constexpr int WU = 16 / W;          // words per unit
 #pragma unroll 2
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < 4; ++k) {
     const int u = lane + 32 * k;
-    const int tok = u >> 3, cu = u & 7;           // token, 16-channel unit
+    const int tok = u >> 3, cu = u & 7;           // token of the half, 16-channel unit
+    const int trow = 16 * hb + tok;               // token of the tile
     const int grp = (16 * cu) / G;
+    if constexpr (BITS == 2) {
+      // the key half tile holds this half's tokens in perm8 order: so do the
+      // value rows; the channels of each chunk come out in perm8 order too
+      uint32_t lo, hi;
+      lut2(vs[trow * NG + grp], vz[trow * NG + grp], lo, hi);
+      uint4 c0, c1;
+      lookup16(vc[trow * RW + cu], lo, hi, c0, c1);
+      const int row = (tok & 8) | perm8_inv(tok & 7);
+      sts128(buf + tok_major(row, 2 * cu), c0);
+      sts128(buf + tok_major(row, 2 * cu + 1), c1);
+      continue;
+    }
     uint64_t s2, ns2, z2;
-    scale_consts(vs[tok * NG + grp], vz[tok * NG + grp], s2, ns2, z2);
-    const uint32_t *src = vc + tok * RW + cu * WU;
+    scale_consts(vs[trow * NG + grp], vz[trow * NG + grp], s2, ns2, z2);
+    const uint32_t *src = vc + trow * RW + cu * WU;
     uint32_t w[WU];
     if constexpr (WU == 4) {
       const uint4 v = *reinterpret_cast<const uint4 *>(src);
@@ -225,20 +283,27 @@ __device__ __forceinline__ void expand_values(const uint32_t *vc, const float *v
   }
 }
 
-// Residual tile (fp16 ring rows) -> row-major fp16 tile: lane = token; rows
-// past `valid` are zero.
+// Residual half tile (fp16 ring rows tok0 .. tok0 + 15) -> row-major fp16
+// half tile; rows past `valid` (counted from tok0) are zero.  Two lanes per
+// token (lanes l and l + 16), eight chunks each.
+template <bool PERM>
 __device__ __forceinline__ void load_residual(const __half *base, int64_t r_cap, int64_t head,
                                               int tok0, int valid, uint32_t buf, int lane) {
-  const bool ok = lane < valid;
+  const int tok = lane & 15, c0 = (lane >> 4) * 8;
+  const bool ok = tok < valid;
   const uint4 *src = nullptr;
   if (ok) {
-    const int64_t rr = (head + tok0 + lane) % r_cap;
+    const int64_t rr = (head + tok0 + tok) % r_cap;
     src = reinterpret_cast<const uint4 *>(base + rr * kD);
   }
 #pragma unroll
-  for (int ch = 0; ch < 16; ++ch) {
-    const uint4 v = ok ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-    sts128(buf + tok_major(lane, ch), v);
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4 v = ok ? src[c0 + ch] : make_uint4(0u, 0u, 0u, 0u);
+    if (PERM) {   // channels of the chunk in perm8 order: (0,4) (1,5) (2,6) (3,7)
+      v = make_uint4(__byte_perm(v.x, v.z, 0x5410u), __byte_perm(v.x, v.z, 0x7632u),
+                     __byte_perm(v.y, v.w, 0x5410u), __byte_perm(v.y, v.w, 0x7632u));
+    }
+    sts128(buf + tok_major(tok, c0 + ch), v);
   }
 }
 
@@ -249,53 +314,44 @@ struct SoftState {
   float o[8][4];  // O^T accumulators: channel block mc, (ch g, h 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)
 };
 
-// Scores of one tile from the key tile in `buf` (transposed layout for store
-// tiles, row-major for residual tiles): s[mb] = 16 tokens x 8 heads.
+// Scores of 16 tokens x 8 heads from the key half tile in `buf` (transposed
+// layout for store tiles, row-major for residual tiles).
 template <bool KEYS_T>
-__device__ __forceinline__ void tile_scores(uint32_t buf, const uint2 *qsm, int lane,
-                                            float (&s)[2][4]) {
-  float s2[2][4];
+__device__ __forceinline__ void half_scores(uint32_t buf, const uint2 *qsm, int lane,
+                                            float (&s)[4]) {
+  float s2[4];
 #pragma unroll
-  for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[mb][i] = s2[mb][i] = 0.0f;
+  for (int i = 0; i < 4; ++i) s[i] = s2[i] = 0.0f;
   const int mat = lane >> 3, row = lane & 7;
-#pragma unroll 2
+#pragma unroll 4
   for (int kk = 0; kk < 8; ++kk) {
     const uint2 qb = qsm[kk * 32 + lane];
-#pragma unroll
-    for (int mb = 0; mb < 2; ++mb) {
-      // matrices (tokens tb.., channels cb..) in A order: (0,0) (8,0) (0,8) (8,8)
-      const int tb = 16 * mb + (mat & 1) * 8, cb = 16 * kk + (mat >> 1) * 8;
-      uint32_t a[4];
-      if (KEYS_T)
-        ldsm_x4_trans(buf + ch_major(cb + row, tb >> 3), a);
-      else
-        ldsm_x4(buf + tok_major(tb + row, cb >> 3), a);
-      mma_16816((kk & 1) ? s2[mb] : s[mb], a, qb.x, qb.y);
-    }
+    // matrices (tokens tb.., channels cb..) in A order: (0,0) (8,0) (0,8) (8,8)
+    const int tb = (mat & 1) * 8, cb = 16 * kk + (mat >> 1) * 8;
+    uint32_t a[4];
+    if (KEYS_T)
+      ldsm_x4_trans(buf + ch_major(cb + row, tb >> 3), a);
+    else
+      ldsm_x4(buf + tok_major(tb + row, cb >> 3), a);
+    mma_16816((kk & 1) ? s2 : s, a, qb.x, qb.y);
   }
 #pragma unroll
-  for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) s[mb][i] += s2[mb][i];
+  for (int i = 0; i < 4; ++i) s[i] += s2[i];
 }
 
-// Online softmax update with one tile's scores; returns P^T fragments (x 2^12,
-// fp16 high and low parts) for the value products.
-__device__ __forceinline__ void tile_softmax(SoftState &st, float (&s)[2][4], float scale_log2,
-                                             int valid, int g, uint32_t (&phi)[2][2],
-                                             uint32_t (&plo)[2][2]) {
+// Online softmax update with 16 tokens' scores (the first `valid` real);
+// returns the P^T fragments (x 2^12, fp16 high and low parts).
+__device__ __forceinline__ void half_softmax(SoftState &st, float (&s)[4], float scale_log2,
+                                             int valid, int g, uint32_t (&phi)[2],
+                                             uint32_t (&plo)[2]) {
   float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-  for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int tok = 16 * mb + g + (i >= 2 ? 8 : 0);
-      const float v = tok < valid ? s[mb][i] * scale_log2 : -INFINITY;
-      s[mb][i] = v;
-      mt[i & 1] = fmaxf(mt[i & 1], v);
-    }
+  for (int i = 0; i < 4; ++i) {
+    const int tok = g + (i >= 2 ? 8 : 0);
+    const float v = tok < valid ? s[i] * scale_log2 : -INFINITY;
+    s[i] = v;
+    mt[i & 1] = fmaxf(mt[i & 1], v);
+  }
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     mt[0] = fmaxf(mt[0], __shfl_xor_sync(0xffffffffu, mt[0], off));
@@ -308,27 +364,22 @@ __device__ __forceinline__ void tile_softmax(SoftState &st, float (&s)[2][4], fl
     alpha[j] = mn[j] == -INFINITY ? 1.0f : exp2f(st.m[j] - mn[j]);
     st.m[j] = mn[j];
   }
-  float lsum[2] = {0.0f, 0.0f};
+  float p[4];
 #pragma unroll
-  for (int mb = 0; mb < 2; ++mb) {
-    float p[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float m = mn[i & 1];
-      p[i] = m == -INFINITY ? 0.0f : exp2f(s[mb][i] - m) * kPScale;
-      lsum[i & 1] += p[i];
-    }
-    const __half2 h0 = __floats2half2_rn(p[0], p[1]);   // token g: heads 2t, 2t+1
-    const __half2 h1 = __floats2half2_rn(p[2], p[3]);   // token g+8
-    const __half2 l0 = __floats2half2_rn(p[0] - __low2float(h0), p[1] - __high2float(h0));
-    const __half2 l1 = __floats2half2_rn(p[2] - __low2float(h1), p[3] - __high2float(h1));
-    phi[mb][0] = movmatrix_trans(h2_as_u32(h0));
-    phi[mb][1] = movmatrix_trans(h2_as_u32(h1));
-    plo[mb][0] = movmatrix_trans(h2_as_u32(l0));
-    plo[mb][1] = movmatrix_trans(h2_as_u32(l1));
+  for (int i = 0; i < 4; ++i) {
+    const float m = mn[i & 1];
+    p[i] = m == -INFINITY ? 0.0f : exp2f(s[i] - m) * kPScale;
   }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) st.l[j] = st.l[j] * alpha[j] + lsum[j];
+  const __half2 h0 = __floats2half2_rn(p[0], p[1]);   // token g: heads 2t, 2t+1
+  const __half2 h1 = __floats2half2_rn(p[2], p[3]);   // token g+8
+  const __half2 l0 = __floats2half2_rn(p[0] - __low2float(h0), p[1] - __high2float(h0));
+  const __half2 l1 = __floats2half2_rn(p[2] - __low2float(h1), p[3] - __high2float(h1));
+  phi[0] = movmatrix_trans(h2_as_u32(h0));
+  phi[1] = movmatrix_trans(h2_as_u32(h1));
+  plo[0] = movmatrix_trans(h2_as_u32(l0));
+  plo[1] = movmatrix_trans(h2_as_u32(l1));
+  st.l[0] = st.l[0] * alpha[0] + (p[0] + p[2]);
+  st.l[1] = st.l[1] * alpha[1] + (p[1] + p[3]);
 #pragma unroll
   for (int mc = 0; mc < 8; ++mc) {
     st.o[mc][0] *= alpha[0];
@@ -338,22 +389,19 @@ __device__ __forceinline__ void tile_softmax(SoftState &st, float (&s)[2][4], fl
   }
 }
 
-// O^T += V^T P^T from the row-major value tile in `buf`.
-__device__ __forceinline__ void tile_values(SoftState &st, uint32_t buf, int lane,
-                                            const uint32_t (&phi)[2][2],
-                                            const uint32_t (&plo)[2][2]) {
+// O^T += V^T P^T from the row-major value half tile in `buf`.
+__device__ __forceinline__ void half_values(SoftState &st, uint32_t buf, int lane,
+                                            const uint32_t (&phi)[2], const uint32_t (&plo)[2]) {
   const int mat = lane >> 3, row = lane & 7;
 #pragma unroll
-  for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-    for (int mc = 0; mc < 8; ++mc) {
-      // matrices (channels cb.., tokens tb..) in A order: (0,0) (8,0) (0,8) (8,8)
-      const int cb = 16 * mc + (mat & 1) * 8, tb = 16 * mb + (mat >> 1) * 8;
-      uint32_t a[4];
-      ldsm_x4_trans(buf + tok_major(tb + row, cb >> 3), a);
-      mma_16816(st.o[mc], a, phi[mb][0], phi[mb][1]);
-      mma_16816(st.o[mc], a, plo[mb][0], plo[mb][1]);
-    }
+  for (int mc = 0; mc < 8; ++mc) {
+    // matrices (channels cb.., tokens tb..) in A order: (0,0) (8,0) (0,8) (8,8)
+    const int cb = 16 * mc + (mat & 1) * 8, tb = (mat >> 1) * 8;
+    uint32_t a[4];
+    ldsm_x4_trans(buf + tok_major(tb + row, cb >> 3), a);
+    mma_16816(st.o[mc], a, phi[0], phi[1]);
+    mma_16816(st.o[mc], a, plo[0], plo[1]);
+  }
 }
 
 template <int BITS, int G>
@@ -448,25 +496,28 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
       break;
     }
     const unsigned char *stg = ring + sidx * F::kBytes;
-    float s[2][4];
-    uint32_t phi[2][2], plo[2][2];
-    expand_keys<BITS>(reinterpret_cast<const uint32_t *>(stg),
-                      reinterpret_cast<const float *>(stg + F::oKs),
-                      reinterpret_cast<const float *>(stg + F::oKz), buf, lane);
-    __syncwarp();
-    tile_scores<true>(buf, qsm, lane, s);
-    tile_softmax(st, s, p.scale_log2, kTile, g, phi, plo);
-    __syncwarp();                                  // key tile read by every lane
-    expand_values<BITS, G>(reinterpret_cast<const uint32_t *>(stg + F::oVc),
-                           reinterpret_cast<const float *>(stg + F::oVs),
-                           reinterpret_cast<const float *>(stg + F::oVz), buf, lane);
-    __syncwarp();                                  // stage consumed, value tile written
-    if (issued < n_my) {
-      if (lane == 0) issue(issued);
-      ++issued;
+#pragma unroll 1
+    for (int hb = 0; hb < 2; ++hb) {
+      float s[4];
+      uint32_t phi[2], plo[2];
+      expand_keys<BITS>(reinterpret_cast<const uint32_t *>(stg),
+                        reinterpret_cast<const float *>(stg + F::oKs),
+                        reinterpret_cast<const float *>(stg + F::oKz), hb, buf, lane);
+      __syncwarp();
+      half_scores<true>(buf, qsm, lane, s);
+      half_softmax(st, s, p.scale_log2, kHalf, g, phi, plo);
+      __syncwarp();                                // key half tile read by every lane
+      expand_values<BITS, G>(reinterpret_cast<const uint32_t *>(stg + F::oVc),
+                             reinterpret_cast<const float *>(stg + F::oVs),
+                             reinterpret_cast<const float *>(stg + F::oVz), hb, buf, lane);
+      __syncwarp();                                // value half tile written
+      if (hb == 1 && issued < n_my) {              // stage consumed: refill it
+        if (lane == 0) issue(issued);
+        ++issued;
+      }
+      half_values(st, buf, lane, phi, plo);
+      __syncwarp();                                // value half tile read by every lane
     }
-    tile_values(st, buf, lane, phi, plo);
-    __syncwarp();                                  // value tile read by every lane
   }
   if (failed) {
     // record the timeout and wait (bounded) for this warp's copies still in flight
@@ -476,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
       mbar_wait_bounded(bar0 + 8 * (i % F::NS), (i / F::NS) & 1, kWaitLimitNs);
   }
 
-  // ---- residual tiles (last split): fp16 rows read directly
+  // ---- residual tiles (last split): fp16 rows read directly, 16 tokens at a time
   if (split == p.n_split - 1 && !failed) {
     const __half *kr = static_cast<const __half *>(J.k_res) + bhi * p.r_cap * kD;
     const __half *vr = static_cast<const __half *>(J.v_res) + bhi * p.r_cap * kD;
@@ -484,20 +535,24 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
     const int first = n_store + ((warp - n_store) % kWarps + kWarps) % kWarps;
 #pragma unroll 1
     for (int j = first - n_store; j < p.tiles_res; j += kWarps) {
-      const int tok0 = j * kTile;
-      const int64_t left = p.n_res - tok0;
-      const int valid = left < kTile ? static_cast<int>(left) : kTile;
-      float s[2][4];
-      uint32_t phi[2][2], plo[2][2];
-      load_residual(kr, p.r_cap, p.res_head, tok0, valid, buf, lane);
-      __syncwarp();
-      tile_scores<false>(buf, qsm, lane, s);
-      tile_softmax(st, s, p.scale_log2, valid, g, phi, plo);
-      __syncwarp();
-      load_residual(vr, p.r_cap, p.res_head, tok0, valid, buf, lane);
-      __syncwarp();
-      tile_values(st, buf, lane, phi, plo);
-      __syncwarp();
+#pragma unroll 1
+      for (int hb = 0; hb < 2; ++hb) {
+        const int tok0 = j * kTile + hb * kHalf;
+        const int64_t left = p.n_res - tok0;
+        if (left <= 0) break;
+        const int valid = left < kHalf ? static_cast<int>(left) : kHalf;
+        float s[4];
+        uint32_t phi[2], plo[2];
+        load_residual<false>(kr, p.r_cap, p.res_head, tok0, valid, buf, lane);
+        __syncwarp();
+        half_scores<false>(buf, qsm, lane, s);
+        half_softmax(st, s, p.scale_log2, valid, g, phi, plo);
+        __syncwarp();
+        load_residual<BITS == 2>(vr, p.r_cap, p.res_head, tok0, valid, buf, lane);
+        __syncwarp();
+        half_values(st, buf, lane, phi, plo);
+        __syncwarp();
+      }
     }
   }
 
@@ -516,9 +571,12 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
     red_l[warp * 8 + 2 * t] = st.l[0];
     red_l[warp * 8 + 2 * t + 1] = st.l[1];
   }
+  // accumulator row g of channel block mc is channel 16 mc + g, or with the
+  // 2-bit path's chunk order 16 mc + perm8(g) (rows g + 8: + 8)
+  const int cg = BITS == 2 ? perm8(g) : g;
 #pragma unroll
   for (int mc = 0; mc < 8; ++mc) {
-    float *o0 = red_o + (warp * 8 + 2 * t) * kD + 16 * mc + g;
+    float *o0 = red_o + (warp * 8 + 2 * t) * kD + 16 * mc + cg;
     float *o1 = o0 + kD;
     o0[0] = st.o[mc][0];
     o1[0] = st.o[mc][1];
