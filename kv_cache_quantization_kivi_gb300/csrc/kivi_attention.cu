@@ -245,7 +245,7 @@ __device__ __forceinline__ void expand_values(const uint32_t *vc, const float *v
   constexpr int RW = kD / W;          // words per token
   constexpr int NG = kD / G;
   constexpr int WU = 16 / W;          // words per unit
-#pragma unroll 2
+#pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int u = lane + 32 * k;
     const int tok = u >> 3, cu = u & 7;           // token of the half, 16-channel unit
@@ -380,12 +380,15 @@ __device__ __forceinline__ void half_softmax(SoftState &st, float (&s)[4], float
   plo[1] = movmatrix_trans(h2_as_u32(l1));
   st.l[0] = st.l[0] * alpha[0] + (p[0] + p[2]);
   st.l[1] = st.l[1] * alpha[1] + (p[1] + p[3]);
+  // once the running maximum settles most steps leave it unchanged (alpha 1)
+  if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll
-  for (int mc = 0; mc < 8; ++mc) {
-    st.o[mc][0] *= alpha[0];
-    st.o[mc][1] *= alpha[1];
-    st.o[mc][2] *= alpha[0];
-    st.o[mc][3] *= alpha[1];
+    for (int mc = 0; mc < 8; ++mc) {
+      st.o[mc][0] *= alpha[0];
+      st.o[mc][1] *= alpha[1];
+      st.o[mc][2] *= alpha[0];
+      st.o[mc][3] *= alpha[1];
+    }
   }
 }
 
@@ -393,12 +396,16 @@ __device__ __forceinline__ void half_softmax(SoftState &st, float (&s)[4], float
 __device__ __forceinline__ void half_values(SoftState &st, uint32_t buf, int lane,
                                             const uint32_t (&phi)[2], const uint32_t (&plo)[2]) {
   const int mat = lane >> 3, row = lane & 7;
+  // matrices (channels cb.., tokens tb..) in A order: (0,0) (8,0) (0,8) (8,8);
+  // chunk 2 mc + (mat & 1) of row tb + row, stored at chunk
+  // (2 mc ^ (mc >> 2)) ^ ((mat & 1) ^ row)   (tok_major with tok & 7 = row)
+  const int tok = (mat >> 1) * 8 + row;
+  const uint32_t rbase = buf + tok * 256;
+  const int lb = (mat & 1) ^ row;
 #pragma unroll
   for (int mc = 0; mc < 8; ++mc) {
-    // matrices (channels cb.., tokens tb..) in A order: (0,0) (8,0) (0,8) (8,8)
-    const int cb = 16 * mc + (mat & 1) * 8, tb = (mat >> 1) * 8;
     uint32_t a[4];
-    ldsm_x4_trans(buf + tok_major(tb + row, cb >> 3), a);
+    ldsm_x4_trans(rbase + ((((2 * mc) ^ (mc >> 2)) ^ lb) << 4), a);
     mma_16816(st.o[mc], a, phi[0], phi[1]);
     mma_16816(st.o[mc], a, plo[0], plo[1]);
   }
