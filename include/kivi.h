@@ -316,6 +316,24 @@ KIVI_API int32_t kivi_decode_attention_splits(const kivi_cache *cache, int n_lay
 KIVI_API int64_t kivi_decode_attention_workspace(const kivi_cache *cache, int n_layers,
                                                  int64_t batch, int32_t h_q, int32_t n_split);
 
+/* kivi_decode_attention without a caller workspace and without allocating:
+ * with n_split > 1 the partial results go to a fixed device array inside
+ * the library (2^24 floats, 64 MiB, one per device; its address is looked
+ * up once per device).  A call whose kivi_decode_attention_workspace size
+ * exceeds it returns KIVI_ERR_CAPACITY before any CUDA call.  Every partial
+ * a call reads is written earlier in the same call, so the array is never
+ * cleared.  Calls that overlap on the device (different streams, or
+ * different host threads without ordering) share the array and race: order
+ * them on one stream.  Otherwise identical to kivi_decode_attention,
+ * including its results.
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN, KIVI_ERR_CAPACITY or
+ * KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_decode_attention_noalloc(const kivi_layer *layers, int n_layers,
+                                                   const kivi_cache *cache, int64_t batch,
+                                                   int32_t h_q, float sm_scale,
+                                                   const void *const *q, float *const *out,
+                                                   int32_t n_split, kivi_stream_t stream);
+
 /* The device word in which kernels record that a pipeline wait (a bulk copy
  * that never arrived) gave up after its time limit (bit 0: decode
  * attention); read and cleared by this call (synchronous).  Results of a

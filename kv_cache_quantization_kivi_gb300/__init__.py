@@ -27,7 +27,7 @@ __all__ = [
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
     "kivi_fakequant_keys", "kivi_fakequant_values", "kivi_flush_fakequant",
     "kivi_decode_attention", "kivi_decode_attention_splits", "kivi_decode_attention_workspace",
-    "kivi_device_fault",
+    "kivi_decode_attention_noalloc", "kivi_device_fault",
     "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
     "KIVI_MAX_LAYERS", "event_handles",
 ]
@@ -119,6 +119,11 @@ def lib():
             L.kivi_decode_attention_workspace.argtypes = [C.POINTER(kivi_cache), _int, _i64,
                                                           C.c_int32, C.c_int32]
             L.kivi_decode_attention_workspace.restype = _i64
+            L.kivi_decode_attention_noalloc.argtypes = [C.POINTER(kivi_layer), _int,
+                                                        C.POINTER(kivi_cache), _i64, C.c_int32,
+                                                        C.c_float, C.POINTER(_vp),
+                                                        C.POINTER(_vp), C.c_int32, _vp]
+            L.kivi_decode_attention_noalloc.restype = _int
             L.kivi_device_fault.argtypes = [C.POINTER(C.c_uint32)]
             L.kivi_device_fault.restype = _int
             L.kivi_flush_size.argtypes = [_i64, _int, _int]
@@ -386,6 +391,19 @@ def kivi_decode_attention(layers, n_layers: int, cache: kivi_cache, batch: int, 
                                        _ptr_array(out, n_layers), n_split, wp, wn,
                                        _stream_handle(stream)),
            "kivi_decode_attention")
+
+
+def kivi_decode_attention_noalloc(layers, n_layers: int, cache: kivi_cache, batch: int,
+                                  h_q: int, sm_scale: float, q, out, n_split: int = 1,
+                                  stream=None) -> None:
+    """As :func:`kivi_decode_attention`, the split workspace being the library's
+    fixed device array (no workspace argument, nothing allocated; calls that
+    overlap on the device race)."""
+    _check(lib().kivi_decode_attention_noalloc(layers, n_layers, C.byref(cache), batch, h_q,
+                                               float(sm_scale), _ptr_array(q, n_layers),
+                                               _ptr_array(out, n_layers), n_split,
+                                               _stream_handle(stream)),
+           "kivi_decode_attention_noalloc")
 
 
 def kivi_device_fault() -> int:

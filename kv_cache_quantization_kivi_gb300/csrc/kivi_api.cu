@@ -512,11 +512,11 @@ int64_t kivi_decode_attention_workspace(const kivi_cache *cache, int n_layers, i
   return sat_mul(sat_mul(sat_mul(n_layers, cache->bh), n_split), g.r * (kAttnD + 2));
 }
 
-kivi_status kivi_decode_attention(const kivi_layer *layers, int n_layers, const kivi_cache *cache,
-                                  int64_t batch, int32_t h_q, float sm_scale,
-                                  const void *const *q, float *const *out, int32_t n_split,
-                                  float *workspace, int64_t workspace_floats,
-                                  kivi_stream_t stream) {
+// Validation and parameter block of a decode-attention call; the workspace
+// (n_split > 1) is checked by the caller of this function.
+static kivi_status attn_prepare(const kivi_layer *layers, int n_layers, const kivi_cache *cache,
+                                int64_t batch, int32_t h_q, float sm_scale, const void *const *q,
+                                float *const *out, int32_t n_split, kivi_impl::AttnParams *p) {
   const kivi_status st = check_cache(layers, n_layers, cache);
   if (st != KIVI_OK) return st;
   AttnGeom g;
@@ -529,34 +529,67 @@ kivi_status kivi_decode_attention(const kivi_layer *layers, int n_layers, const 
     if (!q[l] || !out[l]) return KIVI_ERR_INVAL;
     if (!aligned16(q[l]) || !aligned16(out[l])) return KIVI_ERR_ALIGN;
   }
-  const int64_t need = kivi_decode_attention_workspace(cache, n_layers, batch, h_q, n_split);
-  if (n_split > 1) {
-    if (!workspace || workspace_floats < need) return KIVI_ERR_INVAL;
-    if (!aligned16(workspace)) return KIVI_ERR_ALIGN;
-  }
   if (sat_mul(sat_mul(n_layers, cache->bh), n_split) > kMaxUnits) return KIVI_ERR_INVAL;
-  if (cache->bh == 0) return KIVI_OK;
 
-  kivi_impl::AttnParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.n_jobs = n_layers;
-  p.r = static_cast<int32_t>(g.r);
-  p.h_kv = static_cast<int32_t>(g.h_kv);
-  p.n_split = n_split;
-  p.tiles_store = static_cast<int32_t>(g.tiles_store);
-  p.tiles_res = static_cast<int32_t>(g.tiles_res);
-  p.tiles_per_split = static_cast<int32_t>((g.tiles_store + n_split - 1) / n_split);
-  p.bh = cache->bh;
-  p.cap = cache->cap;
-  p.r_cap = cache->r_cap;
-  p.res_head = cache->res_head;
-  p.n_res = cache->n_res;
-  p.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
-  p.ws = n_split > 1 ? workspace : nullptr;
+  std::memset(p, 0, sizeof(*p));
+  p->n_jobs = n_layers;
+  p->r = static_cast<int32_t>(g.r);
+  p->h_kv = static_cast<int32_t>(g.h_kv);
+  p->n_split = n_split;
+  p->tiles_store = static_cast<int32_t>(g.tiles_store);
+  p->tiles_res = static_cast<int32_t>(g.tiles_res);
+  p->tiles_per_split = static_cast<int32_t>((g.tiles_store + n_split - 1) / n_split);
+  p->bh = cache->bh;
+  p->cap = cache->cap;
+  p->r_cap = cache->r_cap;
+  p->res_head = cache->res_head;
+  p->n_res = cache->n_res;
+  p->scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
   for (int l = 0; l < n_layers; ++l) {
     const kivi_layer &L = layers[l];
-    p.jobs[l] = {L.k_codes, L.k_scale, L.k_zero, L.v_codes, L.v_scale, L.v_zero,
-                 L.k_res, L.v_res, q[l], out[l]};
+    p->jobs[l] = {L.k_codes, L.k_scale, L.k_zero, L.v_codes, L.v_scale, L.v_zero,
+                  L.k_res, L.v_res, q[l], out[l]};
+  }
+  return KIVI_OK;
+}
+
+kivi_status kivi_decode_attention(const kivi_layer *layers, int n_layers, const kivi_cache *cache,
+                                  int64_t batch, int32_t h_q, float sm_scale,
+                                  const void *const *q, float *const *out, int32_t n_split,
+                                  float *workspace, int64_t workspace_floats,
+                                  kivi_stream_t stream) {
+  kivi_impl::AttnParams p;
+  const kivi_status st =
+      attn_prepare(layers, n_layers, cache, batch, h_q, sm_scale, q, out, n_split, &p);
+  if (st != KIVI_OK) return st;
+  if (n_split > 1) {
+    const int64_t need = kivi_decode_attention_workspace(cache, n_layers, batch, h_q, n_split);
+    if (!workspace || workspace_floats < need) return KIVI_ERR_INVAL;
+    if (!aligned16(workspace)) return KIVI_ERR_ALIGN;
+    p.ws = workspace;
+  }
+  if (cache->bh == 0) return KIVI_OK;
+  return cuda_status(kivi_impl::launch_decode_attention(p, cache->group, cache->bits, stream));
+}
+
+kivi_status kivi_decode_attention_noalloc(const kivi_layer *layers, int n_layers,
+                                          const kivi_cache *cache, int64_t batch, int32_t h_q,
+                                          float sm_scale, const void *const *q,
+                                          float *const *out, int32_t n_split,
+                                          kivi_stream_t stream) {
+  kivi_impl::AttnParams p;
+  const kivi_status st =
+      attn_prepare(layers, n_layers, cache, batch, h_q, sm_scale, q, out, n_split, &p);
+  if (st != KIVI_OK) return st;
+  if (n_split > 1) {
+    const int64_t need = kivi_decode_attention_workspace(cache, n_layers, batch, h_q, n_split);
+    if (need > kivi_impl::attention_scratch_floats()) return KIVI_ERR_CAPACITY;
+  }
+  if (cache->bh == 0) return KIVI_OK;
+  if (n_split > 1) {   // every check is done: the first CUDA call
+    int64_t max_floats = 0;
+    const kivi_status s2 = cuda_status(kivi_impl::attention_scratch(&p.ws, &max_floats));
+    if (s2 != KIVI_OK) return s2;
   }
   return cuda_status(kivi_impl::launch_decode_attention(p, cache->group, cache->bits, stream));
 }

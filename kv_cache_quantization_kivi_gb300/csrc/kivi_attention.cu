@@ -46,6 +46,14 @@ namespace kivi_impl {
 // bit 0: a pipeline wait of the decode-attention kernel timed out
 __device__ unsigned int g_fault_word;
 
+// Split-K workspace of the allocation-free decode-attention entry point: a
+// fixed file-scope device array (kAttnScratchFloats floats), so that call
+// needs no caller workspace and allocates nothing.  Every partial a call
+// reads was written earlier in the same call, so nothing in it needs
+// clearing; two calls that overlap on the device share it and race.
+constexpr int64_t kAttnScratchFloats = int64_t{1} << 24;   // 64 MiB
+static __device__ __align__(256) float g_attn_scratch[kAttnScratchFloats];
+
 namespace {
 
 using namespace kivi_dev;
@@ -704,6 +712,27 @@ int attention_splits(int64_t items, int64_t tiles_store, int group, int bits) {
   const int64_t most = std::max<int64_t>(1, std::min<int64_t>(64, tiles_store / (2 * kWarps)));
   return static_cast<int>(std::max<int64_t>(1, std::min(want, most)));
 }
+
+cudaError_t attention_scratch(float **ptr, int64_t *max_floats) {
+  // the symbol's address, looked up once per device
+  constexpr int kMaxDevices = 64;
+  static float *addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!addr[dev]) {
+    void *a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_attn_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<float *>(a);
+  }
+  *ptr = addr[dev];
+  *max_floats = kAttnScratchFloats;
+  return cudaSuccess;
+}
+
+int64_t attention_scratch_floats() { return kAttnScratchFloats; }
 
 cudaError_t read_and_clear_fault(uint32_t *fault) {
   unsigned int v = 0;

@@ -144,6 +144,10 @@ cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits,
 // Recommended number of splits for `items` (job, bh) pairs of `tiles_store`
 // store tiles each on the current device.
 int attention_splits(int64_t items, int64_t tiles_store, int group, int bits);
+// The file-scope device workspace of the allocation-free decode attention:
+// its address on the current device (looked up once per device) and size.
+cudaError_t attention_scratch(float **ptr, int64_t *max_floats);
+int64_t attention_scratch_floats();
 // Reads and clears the device word in which kernels record a pipeline wait
 // that timed out (bit 0: decode attention).
 cudaError_t read_and_clear_fault(uint32_t *fault);

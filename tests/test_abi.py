@@ -299,3 +299,20 @@ def test_decode_attention_validation():
 
 def test_device_fault_rejects_null():
     assert K.lib().kivi_device_fault(None) == 1
+
+
+def test_decode_attention_noalloc_validation():
+    L = K.lib()
+    q = (C.c_void_p * 2)(FAKE + (1 << 24), FAKE + (2 << 24))
+    out = (C.c_void_p * 2)(FAKE + (1 << 28), FAKE + (2 << 28))
+    # workspace need 2 * 4096 * 64 * 8 * 130 floats > the fixed 2^24: refused before any CUDA call
+    big = _cache(bh=4096, n_res=40)
+    assert L.kivi_decode_attention_noalloc(_layers(2), 2, C.byref(big), 512, 64, 0.1, q, out, 64,
+                                           None) == 3
+    # argument errors keep their own status
+    assert L.kivi_decode_attention_noalloc(_layers(2), 2, C.byref(_cache()), 3, 8, 0.1, q, out,
+                                           2, None) == 1
+    assert L.kivi_decode_attention_noalloc(_layers(2), 2, C.byref(_cache()), 2, 8, 0.1, q, out,
+                                           0, None) == 1
+    assert L.kivi_decode_attention_noalloc(_layers(2), 2, C.byref(_cache(bh=0)), 1, 8, 0.1, q,
+                                           out, 2, None) == 1
