@@ -44,8 +44,8 @@ if ROOT not in sys.path:
 METRIC = "quantize+dequant HBM GB/s (bytes in+out) and % of GB300 HBM peak"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-CSRC_FILES = ("kivi_api.cu", "kivi_keys.cu", "kivi_values.cu", "kivi_device.cuh", "kivi_launch.h",
-              "kivi_dispatch.h")
+CSRC_FILES = ("kivi_api.cu", "kivi_keys.cu", "kivi_values.cu", "kivi_attention.cu",
+              "kivi_device.cuh", "kivi_launch.h", "kivi_dispatch.h")
 
 
 def bytes_per_elem(bits: int, group: int) -> float:
@@ -913,9 +913,10 @@ def ncu_traffic(workload: str, kernel: str):
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("csrc_hash") != csrc_hash():
+    wl = d.get("workloads", {}).get(workload, {})
+    if wl.get("csrc_hash", d.get("csrc_hash")) != csrc_hash():
         return None
-    entry = d.get("workloads", {}).get(workload, {}).get(kernel)
+    entry = wl.get(kernel)
     return None if entry is None else float(entry.get("dram_bytes_per_launch"))
 
 
