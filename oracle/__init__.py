@@ -94,6 +94,20 @@ def lib():
             L.kivi_oracle_attention.argtypes = [_u16p, _i64, _u16p, _u16p, _i64, _i64,
                                                 C.c_double, _f64p]
             L.kivi_oracle_attention.restype = C.c_int
+            _i64a = np.ctypeslib.ndpointer(np.int64, flags="C_CONTIGUOUS")
+            L.kivi_oracle_sink_scores.argtypes = [_u16p, _i64, _i64, _i64, _i64, _i64, _f32p]
+            L.kivi_oracle_sink_scores.restype = C.c_int
+            L.kivi_oracle_sink_topk.argtypes = [_i64, _i64a, _f32p, _i64p, _f32p, _i64, _i64]
+            L.kivi_oracle_sink_topk.restype = C.c_int
+            L.kivi_oracle_flush_sink.argtypes = [_u16p, _u16p, _i64, _i64, _i64, _i64, _i64,
+                                                 C.c_int, C.c_int, C.c_int, _u32p, _f32p, _f32p,
+                                                 _u32p, _f32p, _f32p, _i64p, _i64p, _i64p,
+                                                 _i64, _i64a, _i64a, _i64, _i64a, _i64a,
+                                                 _u16p, _u16p]
+            L.kivi_oracle_flush_sink.restype = _i64
+            L.kivi_oracle_sink_restore.argtypes = [_u16p, _u16p, _i64, _i64, _i64, _i64, _i64,
+                                                   _i64a, _i64a, _u16p, _u16p]
+            L.kivi_oracle_sink_restore.restype = C.c_int
             _lib = L
     return _lib
 
@@ -309,3 +323,71 @@ def cache_kv(store: Store, s_q: int, k_ring: np.ndarray, v_ring: np.ndarray, res
         parts_v.append(v_ring[:, rows])
     return (np.ascontiguousarray(np.concatenate(parts_k, axis=1)),
             np.ascontiguousarray(np.concatenate(parts_v, axis=1)))
+
+
+# ---------------------------------------------------------------------------
+# KIVI-Sink
+# ---------------------------------------------------------------------------
+
+def sink_scores(k: np.ndarray, heads: int) -> np.ndarray:
+    """Key-norm scores of k [batch*heads, n, d] (fp16 bits) -> float32 [batch, n]:
+    the mean over the KV heads of each token's key L2 norm."""
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    bh, n, d = k.shape
+    batch = bh // heads
+    out = np.zeros((batch, n), np.float32)
+    _check(lib().kivi_oracle_sink_scores(k, batch, heads, n, d, n * d, out), "sink_scores")
+    return out
+
+
+class SinkState:
+    """Running top-k positions of every sequence and the sink store of one layer."""
+
+    def __init__(self, batch: int, heads: int, d: int, k_top: int, sink_cap: int):
+        self.batch, self.heads, self.d, self.k_top, self.sink_cap = batch, heads, d, k_top, sink_cap
+        self.top_pos = np.zeros((batch, max(k_top, 1)), np.int64)
+        self.top_score = np.zeros((batch, max(k_top, 1)), np.float32)
+        self.top_count = np.zeros(batch, np.int64)
+        self.sink_pos = np.zeros((batch, max(sink_cap, 1)), np.int64)
+        self.sink_count = np.zeros(batch, np.int64)
+        self.sink_k = np.zeros((batch * heads, max(sink_cap, 1), d), np.uint16)
+        self.sink_v = np.zeros((batch * heads, max(sink_cap, 1), d), np.uint16)
+
+    def update(self, scores: np.ndarray, p0: int) -> None:
+        """Merge the scores [batch, n] of positions p0 .. p0+n-1 into the top-k."""
+        scores = np.ascontiguousarray(scores, dtype=np.float32)
+        for b in range(self.batch):
+            pos = np.ascontiguousarray(self.top_pos[b])
+            sc = np.ascontiguousarray(self.top_score[b])
+            cnt = C.c_int64(int(self.top_count[b]))
+            _check(lib().kivi_oracle_sink_topk(self.k_top, pos, sc, C.byref(cnt),
+                                               np.ascontiguousarray(scores[b]), p0,
+                                               scores.shape[1]), "sink_topk")
+            self.top_pos[b], self.top_score[b], self.top_count[b] = pos, sc, cnt.value
+
+
+def flush_sink(k_res: np.ndarray, v_res: np.ndarray, store: "Store", residual: int, s_q: int,
+               res_head: int, n_res: int, state: SinkState):
+    """Flush with sink protection; returns ``(n_flushed, s_q, res_head, n_res)``."""
+    k_res = np.ascontiguousarray(k_res, dtype=np.uint16)
+    v_res = np.ascontiguousarray(v_res, dtype=np.uint16)
+    bh, r_cap, d = k_res.shape
+    a, b, c = C.c_int64(s_q), C.c_int64(res_head), C.c_int64(n_res)
+    n = lib().kivi_oracle_flush_sink(
+        k_res, v_res, state.batch, state.heads, d, r_cap, store.cap, store.group, store.bits,
+        residual, store.k_codes, store.k_scale, store.k_zero, store.v_codes, store.v_scale,
+        store.v_zero, C.byref(a), C.byref(b), C.byref(c), state.top_pos.shape[1],
+        state.top_pos, state.top_count, state.sink_pos.shape[1], state.sink_pos,
+        state.sink_count, state.sink_k, state.sink_v)
+    if n < 0:
+        raise ValueError(f"oracle sink flush rejected its arguments (rc={n})")
+    return int(n), a.value, b.value, c.value
+
+
+def sink_restore(k: np.ndarray, v: np.ndarray, state: SinkState) -> None:
+    """Put the sink rows back into dequantized k, v [bh, s, d] (in place)."""
+    bh, s, d = k.shape
+    _check(lib().kivi_oracle_sink_restore(k, v, state.batch, state.heads, s, d,
+                                          state.sink_pos.shape[1], state.sink_pos,
+                                          state.sink_count, state.sink_k, state.sink_v),
+           "sink_restore")

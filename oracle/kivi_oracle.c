@@ -390,3 +390,193 @@ int kivi_oracle_attention(const uint16_t *q, int64_t r, const uint16_t *k,
     free(s);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* KIVI-Sink: high key-norm tokens kept fp16 and out of the calibration     */
+/* (VeloxQuant-MLX project description, "KVSink-adapted sink protection")   */
+/* ------------------------------------------------------------------------ */
+
+int kivi_oracle_sink_scores(const uint16_t *k, int64_t batch, int64_t heads, int64_t n,
+                            int64_t d, int64_t bh_stride, float *score)
+{
+    if (batch < 0 || heads <= 0 || n < 0 || d <= 0 || bh_stride < n * d) return -1;
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t t = 0; t < n; ++t) {
+            float sum = 0.0f;
+            for (int64_t h = 0; h < heads; ++h) {
+                const uint16_t *row = k + (b * heads + h) * bh_stride + t * d;
+                float acc = 0.0f;                      /* squared L2 norm, in channel order */
+                for (int64_t c = 0; c < d; ++c) {
+                    const float x = kivi_oracle_half_to_float(row[c]);
+                    acc = fmaf(x, x, acc);
+                }
+                sum = sum + sqrtf(acc);                /* norms summed in head order */
+            }
+            score[b * n + t] = sum / (float)heads;    /* mean over the KV heads */
+        }
+    return 0;
+}
+
+/* a before b in the ranking: larger score, then smaller position */
+static int ranks_before(float sa, int64_t pa, float sb, int64_t pb)
+{
+    return sa > sb || (sa == sb && pa < pb);
+}
+
+int kivi_oracle_sink_topk(int64_t k, int64_t *pos, float *score, int64_t *count,
+                          const float *cand, int64_t p0, int64_t n)
+{
+    if (k < 0 || n < 0 || *count < 0 || *count > k) return -1;
+    const int64_t total = *count + n;
+    int64_t *ap = (int64_t *)malloc(sizeof(int64_t) * (size_t)(total > 0 ? total : 1));
+    float *as = (float *)malloc(sizeof(float) * (size_t)(total > 0 ? total : 1));
+    char *used = (char *)calloc((size_t)(total > 0 ? total : 1), 1);
+    if (!ap || !as || !used) { free(ap); free(as); free(used); return -1; }
+    for (int64_t i = 0; i < *count; ++i) { ap[i] = pos[i]; as[i] = score[i]; }
+    for (int64_t i = 0; i < n; ++i) {
+        if (!isfinite(cand[i])) { free(ap); free(as); free(used); return -1; }
+        ap[*count + i] = p0 + i;
+        as[*count + i] = cand[i];
+    }
+    /* selection: k times the best entry not yet taken */
+    const int64_t keep = total < k ? total : k;
+    for (int64_t j = 0; j < keep; ++j) {
+        int64_t best = -1;
+        for (int64_t i = 0; i < total; ++i) {
+            if (used[i]) continue;
+            if (best < 0 || ranks_before(as[i], ap[i], as[best], ap[best])) best = i;
+        }
+        used[best] = 1;
+        pos[j] = ap[best];
+        score[j] = as[best];
+    }
+    *count = keep;
+    free(ap); free(as); free(used);
+    return 0;
+}
+
+static int is_sink(const int64_t *top, int64_t n_top, int64_t p)
+{
+    for (int64_t i = 0; i < n_top; ++i)
+        if (top[i] == p) return 1;
+    return 0;
+}
+
+int64_t kivi_oracle_flush_sink(const uint16_t *k_res, const uint16_t *v_res,
+                               int64_t batch, int64_t heads, int64_t d, int64_t r_cap,
+                               int64_t cap, int group, int bits, int residual,
+                               uint32_t *k_codes, float *k_scale, float *k_zero,
+                               uint32_t *v_codes, float *v_scale, float *v_zero,
+                               int64_t *s_q, int64_t *res_head, int64_t *n_res,
+                               int64_t k_top, const int64_t *top_pos, const int64_t *top_count,
+                               int64_t sink_cap, int64_t *sink_pos, int64_t *sink_count,
+                               uint16_t *sink_k, uint16_t *sink_v)
+{
+    if (!valid_bits(bits) || !valid_group(group) || batch < 0 || heads <= 0 || d <= 0) return -1;
+    if (r_cap <= 0 || r_cap % group || cap % group || *s_q % group || *res_head % group) return -1;
+    if (d % group != 0 || d % codes_per_word(bits) != 0 || k_top < 0 || sink_cap < 0) return -1;
+    const int64_t n = kivi_oracle_flush_size(*n_res, residual, group);
+    if (n <= 0) return n < 0 ? -1 : 0;
+    if (*s_q + n > cap) return -3;
+    const int64_t bh = batch * heads;
+    const int w = codes_per_word(bits);
+    const int64_t head = *res_head;
+    /* sinks among the flushed tokens: every one must fit into the sink store */
+    for (int64_t b = 0; b < batch; ++b) {
+        int64_t add = 0;
+        for (int64_t i = 0; i < n; ++i)
+            add += is_sink(top_pos + b * k_top, top_count[b], *s_q + i);
+        if (sink_count[b] + add > sink_cap) return -3;
+    }
+    float vals[KIVI_ORACLE_MAX_GROUP];
+    int keep_idx[KIVI_ORACLE_MAX_GROUP];
+    for (int64_t bb = 0; bb < bh; ++bb) {
+        const int64_t b = bb / heads;
+        const int64_t *top = top_pos + b * k_top;
+        /* keys: per channel and group, the non-sink tokens set the parameters */
+        for (int64_t j = 0; j < n / group; ++j) {
+            for (int64_t c = 0; c < d; ++c) {
+                int kept = 0;
+                for (int i = 0; i < group; ++i) {
+                    const int64_t li = j * group + i;                 /* logical residual token */
+                    if (is_sink(top, top_count[b], *s_q + li)) continue;
+                    const int64_t row = (head + li) % r_cap;
+                    vals[kept] = kivi_oracle_half_to_float(k_res[(bb * r_cap + row) * d + c]);
+                    keep_idx[kept] = i;
+                    ++kept;
+                }
+                float sc = 0.0f, ze = 0.0f;           /* a group of sinks only: both 0 */
+                if (kept > 0 && kivi_oracle_group_params(vals, kept, bits, &sc, &ze) != 0) return -1;
+                const int64_t gq = *s_q / group + j;
+                k_scale[(bb * (cap / group) + gq) * d + c] = sc;
+                k_zero[(bb * (cap / group) + gq) * d + c] = ze;
+                uint32_t q[KIVI_ORACLE_MAX_GROUP];
+                for (int i = 0; i < group; ++i) q[i] = 0u;            /* sink tokens: code 0 */
+                for (int e = 0; e < kept; ++e) q[keep_idx[e]] = kivi_oracle_code(vals[e], sc, ze, bits);
+                for (int i = 0; i < group; ++i) {
+                    const int64_t t = gq * group + i;
+                    uint32_t *word = &k_codes[(bb * (cap / w) + t / w) * d + c];
+                    if (i % w == 0) *word = 0u;
+                    *word |= q[i] << ((t % w) * bits);
+                }
+            }
+        }
+        /* values: a sink token's row is not quantized (codes, scales, zeros 0) */
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t row = (head + i) % r_cap;
+            const int64_t t = *s_q + i;
+            uint32_t *vw = v_codes + (bb * cap + t) * (d / w);
+            float *vs = v_scale + (bb * cap + t) * (d / group);
+            float *vz = v_zero + (bb * cap + t) * (d / group);
+            if (is_sink(top, top_count[b], t)) {
+                for (int64_t j2 = 0; j2 < d / w; ++j2) vw[j2] = 0u;
+                for (int64_t g2 = 0; g2 < d / group; ++g2) { vs[g2] = 0.0f; vz[g2] = 0.0f; }
+                continue;
+            }
+            if (kivi_oracle_value_row(v_res + (bb * r_cap + row) * d, d, group, bits, vw, vs, vz) != 0)
+                return -1;
+        }
+    }
+    /* the sink tokens' fp16 rows, in position order, for every head */
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t i = 0; i < n; ++i) {
+            const int64_t t = *s_q + i;
+            if (!is_sink(top_pos + b * k_top, top_count[b], t)) continue;
+            const int64_t slot = sink_count[b]++;
+            sink_pos[b * sink_cap + slot] = t;
+            const int64_t row = (head + i) % r_cap;
+            for (int64_t h = 0; h < heads; ++h) {
+                const int64_t bb = b * heads + h;
+                memcpy(sink_k + (bb * sink_cap + slot) * d, k_res + (bb * r_cap + row) * d,
+                       sizeof(uint16_t) * (size_t)d);
+                memcpy(sink_v + (bb * sink_cap + slot) * d, v_res + (bb * r_cap + row) * d,
+                       sizeof(uint16_t) * (size_t)d);
+            }
+        }
+    }
+    *s_q += n;
+    *res_head = (head + n) % r_cap;
+    *n_res -= n;
+    return n;
+}
+
+int kivi_oracle_sink_restore(uint16_t *k, uint16_t *v, int64_t batch, int64_t heads, int64_t s,
+                             int64_t d, int64_t sink_cap, const int64_t *sink_pos,
+                             const int64_t *sink_count, const uint16_t *sink_k,
+                             const uint16_t *sink_v)
+{
+    if (batch < 0 || heads <= 0 || s < 0 || d <= 0 || sink_cap < 0) return -1;
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t j = 0; j < sink_count[b]; ++j) {
+            const int64_t t = sink_pos[b * sink_cap + j];
+            if (t < 0 || t >= s) continue;              /* not in the dequantized range */
+            for (int64_t h = 0; h < heads; ++h) {
+                const int64_t bb = b * heads + h;
+                memcpy(k + (bb * s + t) * d, sink_k + (bb * sink_cap + j) * d,
+                       sizeof(uint16_t) * (size_t)d);
+                memcpy(v + (bb * s + t) * d, sink_v + (bb * sink_cap + j) * d,
+                       sizeof(uint16_t) * (size_t)d);
+            }
+        }
+    return 0;
+}

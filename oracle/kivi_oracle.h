@@ -134,6 +134,55 @@ int kivi_oracle_attention(const uint16_t *q, int64_t r, const uint16_t *k,
                           const uint16_t *v, int64_t n, int64_t d, double scale,
                           double *out);
 
+/* KIVI-Sink (VeloxQuant-MLX project description, section "KVSink-adapted
+ * sink protection"): tokens with anomalously high key L2-norm (mean over the
+ * KV heads; a running top-k of token positions) are kept fp16 and excluded
+ * from the quantization-parameter calibration.
+ *
+ * Score of token t of sequence b (keys k: [batch*heads] slices, bh stride
+ * bh_stride elements, n rows of d):
+ *     score = (sum_h sqrt(sum_c k_c^2)) / heads
+ * in binary32: the squared norm accumulated with fmaf in channel order,
+ * sqrtf, the norms summed in head order, one division.  score[b*n + t]. */
+int kivi_oracle_sink_scores(const uint16_t *k, int64_t batch, int64_t heads, int64_t n,
+                            int64_t d, int64_t bh_stride, float *score);
+
+/* Running top-k of one sequence: merges candidates (position p0 + i, score
+ * cand[i]) into (pos, score)[0 .. *count), keeping the k best ranked by
+ * larger score, then smaller position; the result is sorted in that order.
+ * Returns -1 for bad sizes or a non-finite score. */
+int kivi_oracle_sink_topk(int64_t k, int64_t *pos, float *score, int64_t *count,
+                          const float *cand, int64_t p0, int64_t n);
+
+/* kivi_oracle_flush with sink protection (bh = batch * heads; flushed
+ * logical residual token i of sequence b has position *s_q + i).  A flushed
+ * token whose position is in its sequence's top set (top_pos[b][0 ..
+ * top_count[b])) is a sink:
+ *   keys    excluded from its groups' min/max (a group of sinks only gets
+ *           scale 0 and zero 0); its code slots hold 0
+ *   values  its row gets codes 0, scales 0, zeros 0
+ *   store   its position and its fp16 key and value rows (every head) are
+ *           appended to the sink store: sink_pos [batch][sink_cap],
+ *           sink_count [batch], sink_k / sink_v [bh][sink_cap][d]
+ * With no top positions it equals kivi_oracle_flush.  Returns the tokens
+ * flushed, -1 (bad arguments) or -3 (store or sink store capacity). */
+int64_t kivi_oracle_flush_sink(const uint16_t *k_res, const uint16_t *v_res,
+                               int64_t batch, int64_t heads, int64_t d, int64_t r_cap,
+                               int64_t cap, int group, int bits, int residual,
+                               uint32_t *k_codes, float *k_scale, float *k_zero,
+                               uint32_t *v_codes, float *v_scale, float *v_zero,
+                               int64_t *s_q, int64_t *res_head, int64_t *n_res,
+                               int64_t k_top, const int64_t *top_pos, const int64_t *top_count,
+                               int64_t sink_cap, int64_t *sink_pos, int64_t *sink_count,
+                               uint16_t *sink_k, uint16_t *sink_v);
+
+/* Puts the sink tokens' fp16 rows back into dequantized keys and values
+ * [bh][s][d] (positions >= s are skipped). */
+int kivi_oracle_sink_restore(uint16_t *k, uint16_t *v, int64_t batch, int64_t heads, int64_t s,
+                             int64_t d, int64_t sink_cap, const int64_t *sink_pos,
+                             const int64_t *sink_count, const uint16_t *sink_k,
+                             const uint16_t *sink_v);
+
 #ifdef __cplusplus
 }
 #endif
