@@ -45,7 +45,7 @@ METRIC = "quantize+dequant HBM GB/s (bytes in+out) and % of GB300 HBM peak"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 CSRC_FILES = ("kivi_api.cu", "kivi_keys.cu", "kivi_values.cu", "kivi_attention.cu",
-              "kivi_device.cuh", "kivi_launch.h", "kivi_dispatch.h")
+              "kivi_sink.cu", "kivi_device.cuh", "kivi_launch.h", "kivi_dispatch.h")
 
 
 def bytes_per_elem(bits: int, group: int) -> float:

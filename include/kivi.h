@@ -269,6 +269,81 @@ KIVI_API kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n
                                                  void *const events[3]);
 
 /* ------------------------------------------------------------------------ */
+/* KIVI-Sink: high key-norm tokens kept fp16                                */
+/* ------------------------------------------------------------------------ */
+
+/* KIVI-Sink (VeloxQuant-MLX project description, section "KVSink-adapted
+ * sink protection"): every token is scored by its key L2 norm averaged over
+ * the KV heads, a running top-k of token positions is kept per sequence, and
+ * a flushed token that is in it is kept fp16 in a sink store and left out of
+ * its groups' quantization parameters.  With k_top == 0 the flush is plain
+ * KIVI, bit for bit.  Scores are binary32: squared norm by fused
+ * multiply-adds in channel order, correctly rounded square root, norms added
+ * in head order, one division; ranking by larger score, then smaller
+ * position.  A token's position is its index in the sequence: residual token
+ * i (0 = oldest) has position s_q + i. */
+
+/* One layer's KIVI-Sink state, all device memory owned by the caller:
+ *   top_pos    int64 [batch][k_top]  running top-k positions, ranked
+ *   top_score  f32   [batch][k_top]  their scores
+ *   top_count  int32 [batch]         entries in use (start at 0)
+ *   sink_pos   int64 [batch][sink_cap]  positions of the stored sinks, in
+ *                                       flush order (ascending)
+ *   sink_count int32 [batch]         sinks stored (start at 0)
+ *   sink_k,    fp16  [bh][sink_cap][d]  the sinks' key / value rows
+ *   sink_v
+ *   mask       u32   [batch][r_cap/32]  scratch of the flush */
+typedef struct {
+    int64_t *top_pos;
+    float *top_score;
+    int32_t *top_count;
+    int64_t *sink_pos;
+    int32_t *sink_count;
+    void *sink_k;
+    void *sink_v;
+    uint32_t *mask;
+} kivi_sink_layer;
+
+/* batch: sequences (cache->bh / batch KV heads each); k_top: 0..64;
+ * sink_cap: sink store capacity per sequence; reserved must be 0. */
+typedef struct {
+    int64_t batch;
+    int32_t k_top;
+    int32_t sink_cap;
+    int32_t reserved;
+    int32_t reserved2;
+} kivi_sink_cfg;
+
+/* Scores residual tokens i0 .. i0+n-1 (already in the rings) of every layer
+ * and merges them into the layers' running top-k.  Call once per token, in
+ * order (after appending, before flushing).  KIVI_ERR_INVAL if the range is
+ * not inside the residual. */
+KIVI_API kivi_status kivi_sink_update(const kivi_layer *layers, const kivi_sink_layer *sinks,
+                                      int n_layers, const kivi_cache *cache,
+                                      const kivi_sink_cfg *cfg, int64_t i0, int64_t n,
+                                      kivi_stream_t stream);
+
+/* kivi_flush with sink protection: flushed tokens in their sequence's top-k
+ * are left out of the key groups' min/max (a group of sinks only gets scale
+ * and zero 0) with code 0, their value rows get codes, scales and zeros 0,
+ * and their positions and fp16 key / value rows (every head) are appended
+ * to the sink store.  A sink store that would overflow keeps what fits and
+ * sets bit 1 of the device fault word (kivi_device_fault).
+ * Returns as kivi_flush. */
+KIVI_API kivi_status kivi_flush_sink(const kivi_layer *layers, const kivi_sink_layer *sinks,
+                                     int n_layers, kivi_cache *cache,
+                                     const kivi_sink_cfg *cfg, int64_t *n_flushed,
+                                     kivi_stream_t stream);
+
+/* Puts the stored sinks' fp16 rows back into dequantized store tensors
+ * k_out[l], v_out[l] (fp16 [bh][s_q][d], as kivi_dequantize_cache writes
+ * them), at their positions. */
+KIVI_API kivi_status kivi_sink_restore(const kivi_sink_layer *sinks, int n_layers,
+                                       const kivi_cache *cache, const kivi_sink_cfg *cfg,
+                                       void *const *k_out, void *const *v_out,
+                                       kivi_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Decode attention over the packed cache                                    */
 /* ------------------------------------------------------------------------ */
 

@@ -27,7 +27,8 @@ __all__ = [
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
     "kivi_fakequant_keys", "kivi_fakequant_values", "kivi_flush_fakequant",
     "kivi_decode_attention", "kivi_decode_attention_splits", "kivi_decode_attention_workspace",
-    "kivi_decode_attention_noalloc", "kivi_device_fault",
+    "kivi_decode_attention_noalloc", "kivi_device_fault", "kivi_sink_update", "kivi_flush_sink",
+    "kivi_sink_restore", "kivi_sink_layer", "kivi_sink_cfg", "KiviSinks",
     "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
     "KIVI_MAX_LAYERS", "event_handles",
 ]
@@ -60,6 +61,17 @@ class kivi_cache(C.Structure):
                 ("group", C.c_int32), ("bits", C.c_int32), ("residual", C.c_int32),
                 ("reserved", C.c_int32), ("s_q", C.c_int64), ("res_head", C.c_int64),
                 ("n_res", C.c_int64)]
+
+
+class kivi_sink_layer(C.Structure):
+    _fields_ = [("top_pos", C.c_void_p), ("top_score", C.c_void_p), ("top_count", C.c_void_p),
+                ("sink_pos", C.c_void_p), ("sink_count", C.c_void_p), ("sink_k", C.c_void_p),
+                ("sink_v", C.c_void_p), ("mask", C.c_void_p)]
+
+
+class kivi_sink_cfg(C.Structure):
+    _fields_ = [("batch", C.c_int64), ("k_top", C.c_int32), ("sink_cap", C.c_int32),
+                ("reserved", C.c_int32), ("reserved2", C.c_int32)]
 
 
 _lock = threading.Lock()
@@ -124,6 +136,18 @@ def lib():
                                                         C.c_float, C.POINTER(_vp),
                                                         C.POINTER(_vp), C.c_int32, _vp]
             L.kivi_decode_attention_noalloc.restype = _int
+            L.kivi_sink_update.argtypes = [C.POINTER(kivi_layer), C.POINTER(kivi_sink_layer),
+                                           _int, C.POINTER(kivi_cache), C.POINTER(kivi_sink_cfg),
+                                           _i64, _i64, _vp]
+            L.kivi_sink_update.restype = _int
+            L.kivi_flush_sink.argtypes = [C.POINTER(kivi_layer), C.POINTER(kivi_sink_layer), _int,
+                                          C.POINTER(kivi_cache), C.POINTER(kivi_sink_cfg),
+                                          C.POINTER(_i64), _vp]
+            L.kivi_flush_sink.restype = _int
+            L.kivi_sink_restore.argtypes = [C.POINTER(kivi_sink_layer), _int, C.POINTER(kivi_cache),
+                                            C.POINTER(kivi_sink_cfg), C.POINTER(_vp),
+                                            C.POINTER(_vp), _vp]
+            L.kivi_sink_restore.restype = _int
             L.kivi_device_fault.argtypes = [C.POINTER(C.c_uint32)]
             L.kivi_device_fault.restype = _int
             L.kivi_flush_size.argtypes = [_i64, _int, _int]
@@ -555,3 +579,71 @@ class KiviCache:
         kivi_dequantize_cache(self.layers, self.n_layers, self.state, k_out, v_out, stream,
                               events)
         return k_out, v_out
+
+
+# ---------------------------------------------------------------------------
+# KIVI-Sink
+# ---------------------------------------------------------------------------
+
+def kivi_sink_update(layers, sinks, n_layers: int, cache: kivi_cache, cfg: kivi_sink_cfg,
+                     i0: int, n: int, stream=None) -> None:
+    _check(lib().kivi_sink_update(layers, sinks, n_layers, C.byref(cache), C.byref(cfg), i0, n,
+                                  _stream_handle(stream)), "kivi_sink_update")
+
+
+def kivi_flush_sink(layers, sinks, n_layers: int, cache: kivi_cache, cfg: kivi_sink_cfg,
+                    stream=None) -> int:
+    n = C.c_int64(0)
+    _check(lib().kivi_flush_sink(layers, sinks, n_layers, C.byref(cache), C.byref(cfg),
+                                 C.byref(n), _stream_handle(stream)), "kivi_flush_sink")
+    return int(n.value)
+
+
+def kivi_sink_restore(sinks, n_layers: int, cache: kivi_cache, cfg: kivi_sink_cfg, k_out, v_out,
+                      stream=None) -> None:
+    _check(lib().kivi_sink_restore(sinks, n_layers, C.byref(cache), C.byref(cfg),
+                                   _ptr_array(k_out, n_layers), _ptr_array(v_out, n_layers),
+                                   _stream_handle(stream)), "kivi_sink_restore")
+
+
+class KiviSinks:
+    """KIVI-Sink state of every layer of a :class:`KiviCache` (device tensors):
+    running top-k positions and scores, the sink store (positions and fp16
+    key / value rows) and the flush's mask scratch."""
+
+    def __init__(self, cache: "KiviCache", batch: int, k_top: int, sink_cap: int):
+        import torch
+        st = cache.state
+        L, bh, d, r_cap = cache.n_layers, int(st.bh), int(st.d), int(st.r_cap)
+        dev = cache.k_res[0].device
+        self.cache, self.batch, self.k_top, self.sink_cap = cache, batch, k_top, sink_cap
+        z = lambda shape, dt: torch.zeros((L,) + shape, dtype=dt, device=dev)  # noqa: E731
+        kt, sc = max(k_top, 1), max(sink_cap, 1)
+        self.top_pos = z((batch, kt), torch.int64)
+        self.top_score = z((batch, kt), torch.float32)
+        self.top_count = z((batch,), torch.int32)
+        self.sink_pos = z((batch, sc), torch.int64)
+        self.sink_count = z((batch,), torch.int32)
+        self.sink_k = z((bh, sc, d), torch.float16)
+        self.sink_v = z((bh, sc, d), torch.float16)
+        self.mask = z((batch, max(r_cap // 32, 1)), torch.int32)
+        self.layers = (kivi_sink_layer * L)(*[
+            kivi_sink_layer(self.top_pos[i].data_ptr(), self.top_score[i].data_ptr(),
+                            self.top_count[i].data_ptr(), self.sink_pos[i].data_ptr(),
+                            self.sink_count[i].data_ptr(), self.sink_k[i].data_ptr(),
+                            self.sink_v[i].data_ptr(), self.mask[i].data_ptr())
+            for i in range(L)])
+        self.cfg = kivi_sink_cfg(batch, k_top, sink_cap, 0, 0)
+
+    def update(self, i0: int, n: int, stream=None) -> None:
+        """Score residual tokens i0 .. i0+n-1 and merge them into the top-k."""
+        c = self.cache
+        kivi_sink_update(c.layers, self.layers, c.n_layers, c.state, self.cfg, i0, n, stream)
+
+    def flush(self, stream=None) -> int:
+        c = self.cache
+        return kivi_flush_sink(c.layers, self.layers, c.n_layers, c.state, self.cfg, stream)
+
+    def restore(self, k_out, v_out, stream=None) -> None:
+        c = self.cache
+        kivi_sink_restore(self.layers, c.n_layers, c.state, self.cfg, k_out, v_out, stream)

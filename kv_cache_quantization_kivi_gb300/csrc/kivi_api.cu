@@ -594,6 +594,167 @@ kivi_status kivi_decode_attention_noalloc(const kivi_layer *layers, int n_layers
   return cuda_status(kivi_impl::launch_decode_attention(p, cache->group, cache->bits, stream));
 }
 
+// ---------------------------------------------------------------------------
+// KIVI-Sink
+// ---------------------------------------------------------------------------
+
+static kivi_status check_sinks(const kivi_sink_layer *sinks, int n_layers, const kivi_cache *c,
+                               const kivi_sink_cfg *cfg) {
+  if (!sinks || !cfg) return KIVI_ERR_INVAL;
+  if (cfg->batch < 1 || c->bh % cfg->batch != 0 || cfg->k_top < 0 ||
+      cfg->k_top > kivi_impl::kMaxSinkTop || cfg->sink_cap < 0 || cfg->reserved != 0)
+    return KIVI_ERR_INVAL;
+  for (int l = 0; l < n_layers; ++l) {
+    const kivi_sink_layer &S = sinks[l];
+    const void *ptrs[8] = {S.top_pos, S.top_score, S.top_count, S.sink_pos,
+                           S.sink_count, S.sink_k, S.sink_v, S.mask};
+    for (const void *q : ptrs)
+      if (!q) return KIVI_ERR_INVAL;
+    if (!aligned16(S.sink_k) || !aligned16(S.sink_v)) return KIVI_ERR_ALIGN;
+  }
+  return KIVI_OK;
+}
+
+static void sink_params(const kivi_layer *layers, const kivi_sink_layer *sinks, int n_layers,
+                        const kivi_cache *c, const kivi_sink_cfg *cfg,
+                        kivi_impl::SinkParams *p) {
+  std::memset(p, 0, sizeof(*p));
+  p->n_jobs = n_layers;
+  p->k_top = cfg->k_top;
+  p->sink_cap = cfg->sink_cap;
+  p->batch = cfg->batch;
+  p->heads = c->bh / cfg->batch;
+  p->d = c->d;
+  p->r_cap = c->r_cap;
+  p->res_head = c->res_head;
+  p->s_q = c->s_q;
+  p->mask_words = c->r_cap / 32;
+  for (int l = 0; l < n_layers; ++l) {
+    const kivi_sink_layer &S = sinks[l];
+    kivi_impl::SinkJob &J = p->jobs[l];
+    J.k_res = layers ? layers[l].k_res : nullptr;
+    J.v_res = layers ? layers[l].v_res : nullptr;
+    J.top_pos = S.top_pos;
+    J.top_score = S.top_score;
+    J.top_count = S.top_count;
+    J.sink_pos = S.sink_pos;
+    J.sink_count = S.sink_count;
+    J.sink_k = S.sink_k;
+    J.sink_v = S.sink_v;
+    J.mask = S.mask;
+  }
+}
+
+kivi_status kivi_sink_update(const kivi_layer *layers, const kivi_sink_layer *sinks, int n_layers,
+                             const kivi_cache *cache, const kivi_sink_cfg *cfg, int64_t i0,
+                             int64_t n, kivi_stream_t stream) {
+  kivi_status st = check_cache(layers, n_layers, cache);
+  if (st != KIVI_OK) return st;
+  st = check_sinks(sinks, n_layers, cache, cfg);
+  if (st != KIVI_OK) return st;
+  if (i0 < 0 || n < 0 || i0 + n > cache->n_res) return KIVI_ERR_INVAL;
+  if (n == 0 || cache->bh == 0 || cfg->k_top == 0) return KIVI_OK;
+  kivi_impl::SinkParams p;
+  sink_params(layers, sinks, n_layers, cache, cfg, &p);
+  p.i0 = i0;
+  p.n = n;
+  return cuda_status(kivi_impl::launch_sink_update(p, stream));
+}
+
+kivi_status kivi_flush_sink(const kivi_layer *layers, const kivi_sink_layer *sinks, int n_layers,
+                            kivi_cache *cache, const kivi_sink_cfg *cfg, int64_t *n_flushed,
+                            kivi_stream_t stream) {
+  kivi_status st = check_cache(layers, n_layers, cache);
+  if (st != KIVI_OK) return st;
+  st = check_sinks(sinks, n_layers, cache, cfg);
+  if (st != KIVI_OK) return st;
+  const int64_t G = cache->group;
+  const int W = 32 / cache->bits;
+  const int64_t n = kivi_flush_size(cache->n_res, cache->residual, cache->group);
+  if (n > 0 && cache->s_q + n > cache->cap) return KIVI_ERR_CAPACITY;
+  if (n == 0 || cache->bh == 0) {
+    if (n_flushed) *n_flushed = 0;
+    if (n > 0) {
+      cache->s_q += n;
+      cache->res_head = (cache->res_head + n) % cache->r_cap;
+      cache->n_res -= n;
+      if (n_flushed) *n_flushed = n;
+    }
+    return KIVI_OK;
+  }
+  kivi_impl::SinkParams sp;
+  sink_params(layers, sinks, n_layers, cache, cfg, &sp);
+  sp.n = n;
+
+  const int64_t d = cache->d;
+  kivi_impl::QuantParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.n_jobs = n_layers;
+  kp.d = static_cast<int32_t>(d);
+  kp.bh = cache->bh;
+  kp.rows = n;
+  kp.x_bh_stride = cache->r_cap * d;
+  kp.ring = cache->r_cap;
+  kp.head = cache->res_head;
+  kp.heads = cache->bh / cfg->batch;
+  kp.mask_words = cache->r_cap / 32;
+  kivi_impl::QuantParams vp = kp;
+  kp.codes_bh_stride = cache->cap / W * d;
+  kp.sz_bh_stride = cache->cap / G * d;
+  kp.out0 = cache->s_q / G;
+  vp.codes_bh_stride = cache->cap * (d / W);
+  vp.sz_bh_stride = cache->cap * (d / G);
+  vp.out0 = cache->s_q;
+  for (int l = 0; l < n_layers; ++l) {
+    const kivi_layer &L = layers[l];
+    kp.jobs[l] = {L.k_res, L.k_codes, L.k_scale, L.k_zero, nullptr, sinks[l].mask};
+    vp.jobs[l] = {L.v_res, L.v_codes, L.v_scale, L.v_zero, nullptr, sinks[l].mask};
+  }
+  cudaStream_t s = stream;
+  const int mode = cfg->k_top > 0 ? kivi_impl::kQuantSink : kivi_impl::kQuantPlain;
+  kivi_status r = KIVI_OK;
+  if (cfg->k_top > 0) r = cuda_status(kivi_impl::launch_sink_mask(sp, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(kivi_impl::launch_key_quant(kp, cache->group, cache->bits, mode, s));
+  if (r != KIVI_OK) return r;
+  r = cuda_status(kivi_impl::launch_value_quant(vp, cache->group, cache->bits, mode, s));
+  if (r != KIVI_OK) return r;
+  if (cfg->k_top > 0) {
+    r = cuda_status(kivi_impl::fault_word_address(&sp.fault));
+    if (r != KIVI_OK) return r;
+    r = cuda_status(kivi_impl::launch_sink_copy(sp, s));
+  }
+  if (r != KIVI_OK) return r;
+  cache->s_q += n;
+  cache->res_head = (cache->res_head + n) % cache->r_cap;
+  cache->n_res -= n;
+  if (n_flushed) *n_flushed = n;
+  return KIVI_OK;
+}
+
+kivi_status kivi_sink_restore(const kivi_sink_layer *sinks, int n_layers, const kivi_cache *cache,
+                              const kivi_sink_cfg *cfg, void *const *k_out, void *const *v_out,
+                              kivi_stream_t stream) {
+  if (!cache || n_layers < 1 || n_layers > KIVI_MAX_LAYERS) return KIVI_ERR_INVAL;
+  if (!valid_key_dim(cache->d) || cache->bh < 0 || cache->s_q < 0) return KIVI_ERR_INVAL;
+  const kivi_status st = check_sinks(sinks, n_layers, cache, cfg);
+  if (st != KIVI_OK) return st;
+  if (!k_out || !v_out) return KIVI_ERR_INVAL;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!k_out[l] || !v_out[l]) return KIVI_ERR_INVAL;
+    if (!aligned16(k_out[l]) || !aligned16(v_out[l])) return KIVI_ERR_ALIGN;
+  }
+  if (cache->bh == 0 || cache->s_q == 0 || cfg->sink_cap == 0) return KIVI_OK;
+  kivi_impl::SinkParams p;
+  sink_params(nullptr, sinks, n_layers, cache, cfg, &p);
+  p.out_rows = cache->s_q;
+  for (int l = 0; l < n_layers; ++l) {
+    p.jobs[l].k_out = k_out[l];
+    p.jobs[l].v_out = v_out[l];
+  }
+  return cuda_status(kivi_impl::launch_sink_restore(p, stream));
+}
+
 kivi_status kivi_device_fault(uint32_t *fault) {
   if (!fault) return KIVI_ERR_INVAL;
   return cuda_status(kivi_impl::read_and_clear_fault(fault));

@@ -43,7 +43,8 @@
 
 namespace kivi_impl {
 
-// bit 0: a pipeline wait of the decode-attention kernel timed out
+// bit 0: a pipeline wait of the decode-attention kernel timed out; bit 1: a
+// sink store overflowed (kivi_sink.cu, through fault_word_address)
 __device__ unsigned int g_fault_word;
 
 // Split-K workspace of the allocation-free decode-attention entry point: a
@@ -733,6 +734,23 @@ cudaError_t attention_scratch(float **ptr, int64_t *max_floats) {
 }
 
 int64_t attention_scratch_floats() { return kAttnScratchFloats; }
+
+cudaError_t fault_word_address(unsigned int **ptr) {
+  constexpr int kMaxDevices = 64;
+  static unsigned int *addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!addr[dev]) {
+    void *a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_fault_word);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<unsigned int *>(a);
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 cudaError_t read_and_clear_fault(uint32_t *fault) {
   unsigned int v = 0;

@@ -23,36 +23,30 @@
     }                                                                 \
   } while (0)
 
-// The same for kernels with a compile-time reconstruction flag R.
-#define KIVI_DISPATCH_DR(FN, B, G, R, P, STREAM) \
-  return (P).d == 128 ? FN<B, G, 128, R>(P, STREAM) : FN<B, G, 0, R>(P, STREAM)
+// The same for kernels with a compile-time mode M (see kivi_launch.h).
+#define KIVI_DISPATCH_DM(FN, B, G, M, P, STREAM) \
+  return (P).d == 128 ? FN<B, G, 128, M>(P, STREAM) : FN<B, G, 0, M>(P, STREAM)
 
-#define KIVI_DISPATCH_R(FN, P, GROUP, BITS, RECON, STREAM)                              \
+#define KIVI_DISPATCH_BG(FN, P, GROUP, BITS, M, STREAM)                                  \
+  switch ((BITS) * 1000 + (GROUP)) {                                                    \
+    case 2032: KIVI_DISPATCH_DM(FN, 2, 32, M, P, STREAM);                               \
+    case 2064: KIVI_DISPATCH_DM(FN, 2, 64, M, P, STREAM);                               \
+    case 2128: KIVI_DISPATCH_DM(FN, 2, 128, M, P, STREAM);                              \
+    case 4032: KIVI_DISPATCH_DM(FN, 4, 32, M, P, STREAM);                               \
+    case 4064: KIVI_DISPATCH_DM(FN, 4, 64, M, P, STREAM);                               \
+    case 4128: KIVI_DISPATCH_DM(FN, 4, 128, M, P, STREAM);                              \
+    case 8032: KIVI_DISPATCH_DM(FN, 8, 32, M, P, STREAM);                               \
+    case 8064: KIVI_DISPATCH_DM(FN, 8, 64, M, P, STREAM);                               \
+    case 8128: KIVI_DISPATCH_DM(FN, 8, 128, M, P, STREAM);                              \
+    default: return cudaErrorInvalidValue;                                              \
+  }
+
+#define KIVI_DISPATCH_MODE(FN, P, GROUP, BITS, MODE, STREAM)                            \
   do {                                                                                  \
-    if (RECON) {                                                                        \
-      switch ((BITS) * 1000 + (GROUP)) {                                                \
-        case 2032: KIVI_DISPATCH_DR(FN, 2, 32, true, P, STREAM);                        \
-        case 2064: KIVI_DISPATCH_DR(FN, 2, 64, true, P, STREAM);                        \
-        case 2128: KIVI_DISPATCH_DR(FN, 2, 128, true, P, STREAM);                       \
-        case 4032: KIVI_DISPATCH_DR(FN, 4, 32, true, P, STREAM);                        \
-        case 4064: KIVI_DISPATCH_DR(FN, 4, 64, true, P, STREAM);                        \
-        case 4128: KIVI_DISPATCH_DR(FN, 4, 128, true, P, STREAM);                       \
-        case 8032: KIVI_DISPATCH_DR(FN, 8, 32, true, P, STREAM);                        \
-        case 8064: KIVI_DISPATCH_DR(FN, 8, 64, true, P, STREAM);                        \
-        case 8128: KIVI_DISPATCH_DR(FN, 8, 128, true, P, STREAM);                       \
-        default: return cudaErrorInvalidValue;                                          \
-      }                                                                                 \
-    }                                                                                   \
-    switch ((BITS) * 1000 + (GROUP)) {                                                  \
-      case 2032: KIVI_DISPATCH_DR(FN, 2, 32, false, P, STREAM);                         \
-      case 2064: KIVI_DISPATCH_DR(FN, 2, 64, false, P, STREAM);                         \
-      case 2128: KIVI_DISPATCH_DR(FN, 2, 128, false, P, STREAM);                        \
-      case 4032: KIVI_DISPATCH_DR(FN, 4, 32, false, P, STREAM);                         \
-      case 4064: KIVI_DISPATCH_DR(FN, 4, 64, false, P, STREAM);                         \
-      case 4128: KIVI_DISPATCH_DR(FN, 4, 128, false, P, STREAM);                        \
-      case 8032: KIVI_DISPATCH_DR(FN, 8, 32, false, P, STREAM);                         \
-      case 8064: KIVI_DISPATCH_DR(FN, 8, 64, false, P, STREAM);                         \
-      case 8128: KIVI_DISPATCH_DR(FN, 8, 128, false, P, STREAM);                        \
+    switch (MODE) {                                                                     \
+      case 0: KIVI_DISPATCH_BG(FN, P, GROUP, BITS, 0, STREAM)                           \
+      case 1: KIVI_DISPATCH_BG(FN, P, GROUP, BITS, 1, STREAM)                           \
+      case 2: KIVI_DISPATCH_BG(FN, P, GROUP, BITS, 2, STREAM)                           \
       default: return cudaErrorInvalidValue;                                            \
     }                                                                                   \
   } while (0)

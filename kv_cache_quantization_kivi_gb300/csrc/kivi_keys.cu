@@ -144,8 +144,10 @@ __device__ __forceinline__ KeyUnit decode_key_unit_xch(uint32_t u, const QuantPa
   return k;
 }
 
-template <int BITS, int G, int DC, bool RECON>
+template <int BITS, int G, int DC, int MODE>
 __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_constant__ QuantParams p) {
+  constexpr bool RECON = MODE == kQuantRecon;
+  constexpr bool SINK = MODE == kQuantSink;
   constexpr int T = G / 32;                  // token splits per group
   constexpr int W = CodeFmt<BITS>::W;        // codes per word
   constexpr int WPT = 32 / W;                // words per channel per thread (= BITS)
@@ -186,21 +188,41 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
                          k.col + static_cast<int64_t>(k.split) * 32 * (D / 2);
     const bool full = active && rows_here >= 32;
 
+    // sink mode: bit t = token t of this split is a sink (left out of the
+    // group's min / max, code 0); the flush only moves whole groups
+    uint32_t sink_bits = 0u;
+    if (SINK && full)
+      sink_bits = job.mask[static_cast<int64_t>(k.b / p.heads) * p.mask_words + k.g * T + k.split];
+
     // 32 tokens of this thread's channel pair; min / max in four chains
     __half2 h[32];
     __half2 gmn, gmx;
     if (full) {
 #pragma unroll
       for (int t = 0; t < 32; ++t) h[t] = __ldcs(src + t * (D / 2));
-      __half2 mn[4] = {h[0], h[1], h[2], h[3]};
-      __half2 mx[4] = {h[0], h[1], h[2], h[3]};
+      if (SINK) {
+        const __half2 pinf = u32_as_h2(0x7C007C00u), ninf = u32_as_h2(0xFC00FC00u);
+        __half2 mn[4] = {pinf, pinf, pinf, pinf};
+        __half2 mx[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll
-      for (int t = 4; t < 32; ++t) {
-        mn[t & 3] = __hmin2(mn[t & 3], h[t]);
-        mx[t & 3] = __hmax2(mx[t & 3], h[t]);
+        for (int t = 0; t < 32; ++t) {
+          const bool sk = (sink_bits >> t) & 1u;
+          mn[t & 3] = __hmin2(mn[t & 3], sk ? pinf : h[t]);
+          mx[t & 3] = __hmax2(mx[t & 3], sk ? ninf : h[t]);
+        }
+        gmn = __hmin2(__hmin2(mn[0], mn[1]), __hmin2(mn[2], mn[3]));
+        gmx = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
+      } else {
+        __half2 mn[4] = {h[0], h[1], h[2], h[3]};
+        __half2 mx[4] = {h[0], h[1], h[2], h[3]};
+#pragma unroll
+        for (int t = 4; t < 32; ++t) {
+          mn[t & 3] = __hmin2(mn[t & 3], h[t]);
+          mx[t & 3] = __hmax2(mx[t & 3], h[t]);
+        }
+        gmn = __hmin2(__hmin2(mn[0], mn[1]), __hmin2(mn[2], mn[3]));
+        gmx = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
       }
-      gmn = __hmin2(__hmin2(mn[0], mn[1]), __hmin2(mn[2], mn[3]));
-      gmx = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
     } else if (active) {  // ragged last group: padded by repeating the last row
       const uint2 e = key_partial_ragged(src, rows_here, D);
       gmn = u32_as_h2(e.x);
@@ -227,6 +249,13 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
         gmn = __hmin2(gmn, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(gmn), off)));
         gmx = __hmax2(gmx, u32_as_h2(__shfl_xor_sync(0xffffffffu, h2_as_u32(gmx), off)));
       }
+    }
+
+    if (SINK) {
+      // a group of sinks only (no finite extreme) gets scale 0 and zero 0
+      const float2 a = __half22float2(gmn), bx = __half22float2(gmx);
+      gmn = __floats2half2_rn(a.x > bx.x ? 0.0f : a.x, a.y > bx.y ? 0.0f : a.y);
+      gmx = __floats2half2_rn(a.x > bx.x ? 0.0f : bx.x, a.y > bx.y ? 0.0f : bx.y);
     }
 
     if (active) {
@@ -283,8 +312,9 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
             const int t0 = wi * W + hh * H;
 #pragma unroll
             for (int j = 0; j < H; ++j) {
-              const uint64_t n = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x,
-                                                    mnf.y, mxf.y);
+              uint64_t n = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x,
+                                              mnf.y, mxf.y);
+              if (SINK && ((sink_bits >> (t0 + j)) & 1u)) n = 0ull;   // +0.0f, +0.0f
               half[hh] = j == 0 ? n
                                 : f2_fma(n, f2_const(static_cast<float>(1u << (BITS * j))),
                                          half[hh]);
@@ -375,10 +405,10 @@ int num_sms() {
   return g_num_sms;
 }
 
-template <int BITS, int G, int DC, bool RECON>
+template <int BITS, int G, int DC, int MODE>
 cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
   const int threads = kKeyThreads;
-  auto kern = key_quant_kernel<BITS, G, DC, RECON>;
+  auto kern = key_quant_kernel<BITS, G, DC, MODE>;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
   if (err != cudaSuccess) return err;
@@ -419,9 +449,9 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
 
 #include "kivi_dispatch.h"
 
-cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, bool recon,
+cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, int mode,
                              cudaStream_t stream) {
-  KIVI_DISPATCH_R(key_quant_launch, p, group, bits, recon, stream);
+  KIVI_DISPATCH_MODE(key_quant_launch, p, group, bits, mode, stream);
 }
 
 cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits,

@@ -43,6 +43,7 @@ struct QuantJob {
   float *scale;
   float *zero;
   void *y;
+  const uint32_t *mask;  // sink mode: [batch][mask_words] bit r = logical row r is a sink
 };
 
 // Quantization of n_jobs tensors [bh][*][d].
@@ -64,6 +65,8 @@ struct QuantParams {
   int64_t out0;
   int64_t y_bh_stride;      // fp16 elements (reconstruction)
   int64_t y_row0;           // row of the reconstruction of logical row 0
+  int64_t heads;            // sink mode: bh slices per sequence (sequence = bh / heads)
+  int64_t mask_words;       // sink mode: mask words per sequence
   // filled by the launchers: divisors of the kernels' unit index
   FastDiv div_chunks, div_rows, div_bh;
   QuantJob jobs[KIVI_MAX_LAYERS];
@@ -127,14 +130,55 @@ struct AttnParams {
   AttnJob jobs[KIVI_MAX_LAYERS];
 };
 
+// KIVI-Sink state of one layer (device arrays) and the call's parameters.
+constexpr int kMaxSinkTop = 64;   // largest running top-k
+struct SinkJob {
+  const void *k_res;      // fp16 rings [bh][r_cap][d]
+  const void *v_res;
+  int64_t *top_pos;       // [batch][k_top] running top-k positions, ranked
+  float *top_score;       // [batch][k_top]
+  int32_t *top_count;     // [batch]
+  int64_t *sink_pos;      // [batch][sink_cap] positions of the stored sinks
+  int32_t *sink_count;    // [batch]
+  void *sink_k;           // fp16 [bh][sink_cap][d]
+  void *sink_v;
+  uint32_t *mask;         // [batch][mask_words] flush scratch
+  void *k_out;            // restore: fp16 [bh][out_rows][d]
+  void *v_out;
+};
+struct SinkParams {
+  int32_t n_jobs;
+  int32_t k_top;
+  int32_t sink_cap;
+  int32_t pad;
+  int64_t batch;
+  int64_t heads;
+  int64_t d;
+  int64_t r_cap;
+  int64_t res_head;
+  int64_t s_q;            // store tokens before the call (positions of residual token i: s_q + i)
+  int64_t i0, n;          // update: residual tokens i0 .. i0+n-1; flush: n tokens flushed
+  int64_t mask_words;
+  int64_t out_rows;       // restore: rows of k_out / v_out
+  unsigned int *fault;    // the device fault word (bit 1: sink store overflow)
+  SinkJob jobs[KIVI_MAX_LAYERS];
+};
+cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream);
+cudaError_t launch_sink_mask(const SinkParams &p, cudaStream_t stream);
+cudaError_t launch_sink_copy(const SinkParams &p, cudaStream_t stream);
+cudaError_t launch_sink_restore(const SinkParams &p, cudaStream_t stream);
+
 // Launchers (one per kernel family); they pick the template instance for
 // (group, bits), size the grid from the device's SM count and occupancy,
 // and return the launch's cudaError_t.
-// recon: also write the fp16 reconstruction of every quantized element
-// (jobs[i].y, p.y_bh_stride, p.y_row0).
-cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, bool recon,
+// mode kQuantPlain: codes, scales, zeros; kQuantRecon: also the fp16
+// reconstruction of every quantized element (jobs[i].y, p.y_bh_stride,
+// p.y_row0); kQuantSink: rows flagged in jobs[i].mask are left out of the
+// key groups' min/max and get code 0 (value rows: codes, scales, zeros 0).
+enum { kQuantPlain = 0, kQuantRecon = 1, kQuantSink = 2 };
+cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, int mode,
                              cudaStream_t stream);
-cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, bool recon,
+cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, int mode,
                                cudaStream_t stream);
 cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits, cudaStream_t stream);
 // Decode attention (head_dim 128): the main kernel, then (n_split > 1) the
@@ -148,6 +192,9 @@ int attention_splits(int64_t items, int64_t tiles_store, int group, int bits);
 // its address on the current device (looked up once per device) and size.
 cudaError_t attention_scratch(float **ptr, int64_t *max_floats);
 int64_t attention_scratch_floats();
+// Address of the device fault word on the current device (looked up once
+// per device), for kernels of other translation units.
+cudaError_t fault_word_address(unsigned int **ptr);
 // Reads and clears the device word in which kernels record a pipeline wait
 // that timed out (bit 0: decode attention).
 cudaError_t read_and_clear_fault(uint32_t *fault);

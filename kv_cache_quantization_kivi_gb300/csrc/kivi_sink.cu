@@ -1,0 +1,281 @@
+// kivi_sink.cu -- KIVI-Sink: tokens with anomalously high key L2-norm kept
+// fp16 and left out of the quantization-parameter calibration (VeloxQuant-MLX
+// project description, section "KVSink-adapted sink protection": the mean of
+// the key norms over the KV heads ranks the token positions, a running top-k
+// is kept, and a flushed token in it is stored fp16 instead of quantized).
+//
+//   sink_update_kernel   block per (layer, sequence): scores of new residual
+//                        tokens merged into the running top-k
+//   sink_mask_kernel     per (layer, sequence, 32 flushed tokens): which of
+//                        the tokens being flushed are in the top-k (one bit
+//                        each), read by the quantize kernels' sink mode
+//   sink_copy_kernel     block per (layer, sequence): the flushed sinks'
+//                        positions and fp16 key / value rows into the sink
+//                        store, in position order
+//   sink_restore_kernel  the sink rows put back into dequantized tensors
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kivi_device.cuh"
+#include "kivi_launch.h"
+
+namespace kivi_impl {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// a ranks before b: larger score, then smaller position
+__device__ __forceinline__ bool ranks_before(float sa, int64_t pa, float sb, int64_t pb) {
+  return sa > sb || (sa == sb && pa < pb);
+}
+
+// Score of one token: (sum over heads of the key row's L2 norm) / heads, in
+// binary32 -- squared norm by fused multiply-adds in channel order, correctly
+// rounded square root, norms added in head order, one correctly rounded
+// division.
+__device__ float token_score(const __half *k_seq, int64_t head_stride, int heads, int64_t d) {
+  float sum = 0.0f;
+  for (int h = 0; h < heads; ++h) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(k_seq + h * head_stride);
+    float acc = 0.0f;
+    for (int64_t c8 = 0; c8 < d / 8; ++c8) {
+      const uint4 v = row[c8];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(kivi_dev::u32_as_h2(w[i]));
+        acc = __fmaf_rn(f.x, f.x, acc);
+        acc = __fmaf_rn(f.y, f.y, acc);
+      }
+    }
+    sum = __fadd_rn(sum, __fsqrt_rn(acc));
+  }
+  return __fdiv_rn(sum, static_cast<float>(heads));
+}
+
+__global__ void __launch_bounds__(kThreads) sink_update_kernel(const __grid_constant__ SinkParams p) {
+  const int job = static_cast<int>(blockIdx.x / p.batch);
+  const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
+  const SinkJob &J = p.jobs[job];
+  __shared__ float top_s[kMaxSinkTop];
+  __shared__ int64_t top_p[kMaxSinkTop];
+  __shared__ float new_s[kMaxSinkTop];
+  __shared__ int64_t new_p[kMaxSinkTop];
+  __shared__ float red_s[kWarps];
+  __shared__ int64_t red_p[kWarps];
+  __shared__ int red_i[kWarps];
+  __shared__ int top_n;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) top_n = J.top_count[seq];
+  __syncthreads();
+  if (tid < top_n) {
+    top_s[tid] = J.top_score[seq * p.k_top + tid];
+    top_p[tid] = J.top_pos[seq * p.k_top + tid];
+  }
+  __syncthreads();
+  const __half *k_seq = static_cast<const __half *>(J.k_res) + seq * p.heads * p.r_cap * p.d;
+  for (int64_t start = 0; start < p.n; start += kThreads) {
+    // this thread's candidates: one new token and (tid < top_n) one kept entry
+    float cs = 0.0f;
+    int64_t cp = 0;
+    bool c_ok = start + tid < p.n;
+    if (c_ok) {
+      const int64_t li = p.i0 + start + tid;                      // logical residual token
+      const int64_t row = (p.res_head + li) % p.r_cap;
+      cs = token_score(k_seq + row * p.d, p.r_cap * p.d, static_cast<int>(p.heads), p.d);
+      cp = p.s_q + li;
+    }
+    const int tn = top_n;
+    bool t_ok = tid < tn;
+    const float ts = t_ok ? top_s[tid] : 0.0f;
+    const int64_t tp = t_ok ? top_p[tid] : 0;
+    const int64_t left = p.n - start;
+    const int avail = static_cast<int>(left < kThreads ? left : kThreads) + tn;
+    const int keep = min(p.k_top, avail);
+    for (int j = 0; j < keep; ++j) {
+      // best remaining candidate of this thread
+      bool have = c_ok || t_ok;
+      float bs = 0.0f;
+      int64_t bp = 0;
+      int which = -1;
+      if (t_ok && (!c_ok || ranks_before(ts, tp, cs, cp))) {
+        bs = ts; bp = tp; which = 1;
+      } else if (c_ok) {
+        bs = cs; bp = cp; which = 0;
+      }
+      // warp reduction of (have, score, position, owner)
+      int owner = have ? tid : -1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+        const int64_t op = __shfl_xor_sync(0xffffffffu, bp, off);
+        const int oo = __shfl_xor_sync(0xffffffffu, owner, off);
+        if (oo >= 0 && (owner < 0 || ranks_before(os, op, bs, bp))) {
+          bs = os; bp = op; owner = oo;
+        }
+      }
+      if (lane == 0) {
+        red_s[warp] = bs;
+        red_p[warp] = bp;
+        red_i[warp] = owner;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float ws = red_s[0];
+        int64_t wp = red_p[0];
+        int wo = red_i[0];
+        for (int w = 1; w < kWarps; ++w) {
+          if (red_i[w] >= 0 && (wo < 0 || ranks_before(red_s[w], red_p[w], ws, wp))) {
+            ws = red_s[w]; wp = red_p[w]; wo = red_i[w];
+          }
+        }
+        new_s[j] = ws;
+        new_p[j] = wp;
+        red_i[0] = wo;
+      }
+      __syncthreads();
+      if (red_i[0] == tid) {   // the winner's candidate is used up
+        if (which == 1) t_ok = false; else c_ok = false;
+      }
+      __syncthreads();
+    }
+    if (tid < keep) {
+      top_s[tid] = new_s[tid];
+      top_p[tid] = new_p[tid];
+    }
+    if (tid == 0) top_n = keep;
+    __syncthreads();
+  }
+  if (tid < top_n) {
+    J.top_score[seq * p.k_top + tid] = top_s[tid];
+    J.top_pos[seq * p.k_top + tid] = top_p[tid];
+  }
+  if (tid == 0) J.top_count[seq] = top_n;
+}
+
+// thread = (job, sequence, word of 32 flushed tokens)
+__global__ void __launch_bounds__(kThreads) sink_mask_kernel(const __grid_constant__ SinkParams p) {
+  const int64_t words = p.n / 32;
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (u >= static_cast<int64_t>(p.n_jobs) * p.batch * words) return;
+  const int64_t w = u % words;
+  const int64_t js = u / words;
+  const int job = static_cast<int>(js / p.batch);
+  const int64_t seq = js - static_cast<int64_t>(job) * p.batch;
+  const SinkJob &J = p.jobs[job];
+  const int64_t lo = p.s_q + 32 * w;
+  uint32_t bits = 0u;
+  const int tn = J.top_count[seq];
+  for (int e = 0; e < tn; ++e) {
+    const int64_t pos = J.top_pos[seq * p.k_top + e];
+    if (pos >= lo && pos < lo + 32) bits |= 1u << (pos - lo);
+  }
+  J.mask[seq * p.mask_words + w] = bits;
+}
+
+// block = (job, sequence)
+__global__ void __launch_bounds__(kThreads) sink_copy_kernel(const __grid_constant__ SinkParams p) {
+  const int job = static_cast<int>(blockIdx.x / p.batch);
+  const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
+  const SinkJob &J = p.jobs[job];
+  __shared__ int64_t pos[kMaxSinkTop];
+  __shared__ int slot0, m;
+  if (threadIdx.x == 0) {
+    // flushed top positions, ascending
+    int cnt = 0;
+    const int tn = J.top_count[seq];
+    for (int e = 0; e < tn; ++e) {
+      const int64_t q = J.top_pos[seq * p.k_top + e];
+      if (q < p.s_q || q >= p.s_q + p.n) continue;
+      int i = cnt++;
+      while (i > 0 && pos[i - 1] > q) {
+        pos[i] = pos[i - 1];
+        --i;
+      }
+      pos[i] = q;
+    }
+    const int have = J.sink_count[seq];
+    if (have + cnt > p.sink_cap) {   // the store is full: record it, keep what fits
+      atomicOr(p.fault, 2u);
+      cnt = max(0, p.sink_cap - have);
+    }
+    for (int i = 0; i < cnt; ++i) J.sink_pos[seq * p.sink_cap + have + i] = pos[i];
+    J.sink_count[seq] = have + cnt;
+    slot0 = have;
+    m = cnt;
+  }
+  __syncthreads();
+  const int64_t chunks = p.d / 8;                       // 16-byte pieces per row
+  const int64_t total = static_cast<int64_t>(m) * p.heads * chunks;
+  for (int64_t idx = threadIdx.x; idx < total; idx += kThreads) {
+    const int64_t c = idx % chunks;
+    const int64_t hj = idx / chunks;
+    const int64_t h = hj % p.heads, j = hj / p.heads;
+    const int64_t bb = seq * p.heads + h;
+    const int64_t row = (p.res_head + (pos[j] - p.s_q)) % p.r_cap;
+    const int64_t dst = (bb * p.sink_cap + slot0 + j) * p.d + 8 * c;
+    const int64_t src = (bb * p.r_cap + row) * p.d + 8 * c;
+    *reinterpret_cast<uint4 *>(static_cast<__half *>(J.sink_k) + dst) =
+        *reinterpret_cast<const uint4 *>(static_cast<const __half *>(J.k_res) + src);
+    *reinterpret_cast<uint4 *>(static_cast<__half *>(J.sink_v) + dst) =
+        *reinterpret_cast<const uint4 *>(static_cast<const __half *>(J.v_res) + src);
+  }
+}
+
+// thread = (job, sequence, sink slot, head, 16-byte piece)
+__global__ void __launch_bounds__(kThreads) sink_restore_kernel(const __grid_constant__ SinkParams p) {
+  const int64_t chunks = p.d / 8;
+  const int64_t per_seq = static_cast<int64_t>(p.sink_cap) * p.heads * chunks;
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (u >= static_cast<int64_t>(p.n_jobs) * p.batch * per_seq) return;
+  const int64_t js = u / per_seq, r = u % per_seq;
+  const int job = static_cast<int>(js / p.batch);
+  const int64_t seq = js - static_cast<int64_t>(job) * p.batch;
+  const SinkJob &J = p.jobs[job];
+  const int64_t c = r % chunks, hj = r / chunks;
+  const int64_t h = hj % p.heads, j = hj / p.heads;
+  if (j >= J.sink_count[seq]) return;
+  const int64_t t = J.sink_pos[seq * p.sink_cap + j];
+  if (t < 0 || t >= p.out_rows) return;
+  const int64_t bb = seq * p.heads + h;
+  const int64_t src = (bb * p.sink_cap + j) * p.d + 8 * c;
+  const int64_t dst = (bb * p.out_rows + t) * p.d + 8 * c;
+  *reinterpret_cast<uint4 *>(static_cast<__half *>(J.k_out) + dst) =
+      *reinterpret_cast<const uint4 *>(static_cast<const __half *>(J.sink_k) + src);
+  *reinterpret_cast<uint4 *>(static_cast<__half *>(J.v_out) + dst) =
+      *reinterpret_cast<const uint4 *>(static_cast<const __half *>(J.sink_v) + src);
+}
+
+unsigned blocks_for(int64_t threads) {
+  return static_cast<unsigned>((threads + kThreads - 1) / kThreads);
+}
+
+}  // namespace
+
+cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream) {
+  sink_update_kernel<<<static_cast<unsigned>(p.n_jobs * p.batch), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sink_mask(const SinkParams &p, cudaStream_t stream) {
+  const int64_t threads = static_cast<int64_t>(p.n_jobs) * p.batch * (p.n / 32);
+  if (threads == 0) return cudaSuccess;
+  sink_mask_kernel<<<blocks_for(threads), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sink_copy(const SinkParams &p, cudaStream_t stream) {
+  sink_copy_kernel<<<static_cast<unsigned>(p.n_jobs * p.batch), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sink_restore(const SinkParams &p, cudaStream_t stream) {
+  const int64_t threads =
+      static_cast<int64_t>(p.n_jobs) * p.batch * p.sink_cap * p.heads * (p.d / 8);
+  if (threads == 0) return cudaSuccess;
+  sink_restore_kernel<<<blocks_for(threads), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kivi_impl

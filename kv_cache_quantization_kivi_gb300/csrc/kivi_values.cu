@@ -81,9 +81,11 @@ __device__ __forceinline__ void warp_store_units(uint32_t *blk, uint32_t lane, b
   __syncwarp();
 }
 
-template <int BITS, int G, int DC, bool RECON>
+template <int BITS, int G, int DC, int MODE>
 __global__ void __launch_bounds__(kBlockThreads, 4)
     value_quant_kernel(const __grid_constant__ QuantParams p) {
+  constexpr bool RECON = MODE == kQuantRecon;
+  constexpr bool SINK = MODE == kQuantSink;
   constexpr int L = G / 32;               // lanes per group
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
@@ -162,6 +164,23 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
       const float gmn = __low2float(ext), gmx = -__high2float(ext);
       const int64_t out_row = p.out0 + t.r;
       const bool codes_out = !RECON || job.codes != nullptr;
+      // sink mode: a sink token's row is not quantized (codes, scales, zeros 0)
+      if (SINK && ((job.mask[static_cast<int64_t>(t.b / p.heads) * p.mask_words + (t.r >> 5)] >>
+                    (t.r & 31)) & 1u)) {
+        if (t.k % L == 0) {
+          const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k / L;
+          __stcs(job.scale + so, 0.0f);
+          __stcs(job.zero + so, 0.0f);
+        }
+        uint32_t *dst = job.codes + t.b * p.codes_bh_stride + out_row * (D / W) + t.k * BITS;
+        if (BITS == 2) {
+          st_stream(dst, make_uint2(0u, 0u));
+        } else {
+#pragma unroll
+          for (int i = 0; i < BITS; i += 4) st_stream(dst + i, make_uint4(0u, 0u, 0u, 0u));
+        }
+        continue;
+      }
       GroupQ2 gq;
       uint64_t sc2 = 0, nsc2 = 0, ze2 = 0;
       {
@@ -329,10 +348,10 @@ P with_dividers(const P &p) {
   return q;
 }
 
-template <int BITS, int G, int DC, bool RECON>
+template <int BITS, int G, int DC, int MODE>
 cudaError_t value_quant_launch(const QuantParams &p, cudaStream_t stream) {
   const int threads = kBlockThreads;
-  auto kern = value_quant_kernel<BITS, G, DC, RECON>;
+  auto kern = value_quant_kernel<BITS, G, DC, MODE>;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
   int64_t grid = 0;
   cudaError_t err = persistent_grid(kern, threads, units, &grid);
@@ -357,9 +376,9 @@ cudaError_t value_dequant_launch(const DequantParams &p, cudaStream_t stream) {
 
 #include "kivi_dispatch.h"
 
-cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, bool recon,
+cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, int mode,
                                cudaStream_t stream) {
-  KIVI_DISPATCH_R(value_quant_launch, p, group, bits, recon, stream);
+  KIVI_DISPATCH_MODE(value_quant_launch, p, group, bits, mode, stream);
 }
 
 cudaError_t launch_value_dequant(const DequantParams &p, int group, int bits,

@@ -1,0 +1,174 @@
+"""KIVI-Sink on the GPU (``kivi_sink_update``, ``kivi_flush_sink``,
+``kivi_sink_restore``) against the oracle, bit for bit: the binary32 scores
+and the ranked top-k, the sink-protected store, the sink store and the
+restored reconstruction, over prefill and decode sequences with ring
+wrap-around, planted high-norm tokens, every code width and two head dims."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from gpu_util import assert_same, bits32, host_f32_bits, host_u16, host_u32, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import kv_cache_quantization_kivi_gb300 as K  # noqa: E402
+
+
+class SinkPair:
+    """A GPU cache + sinks and the oracle's mirror, fed the same tokens."""
+
+    def __init__(self, layers, batch, heads, d, bits, group, residual, r_cap, cap, k_top,
+                 sink_cap, seed, plant_every=0):
+        self.layers, self.batch, self.heads, self.d = layers, batch, heads, d
+        self.bh = batch * heads
+        self.group, self.bits, self.residual, self.r_cap, self.cap = group, bits, residual, r_cap, cap
+        self.cache = K.KiviCache(layers, self.bh, d, r_cap=r_cap, cap=cap, group=group, bits=bits,
+                                 residual=residual)
+        self.sinks = K.KiviSinks(self.cache, batch, k_top, sink_cap)
+        self.w = W.custom(seed=seed, batch=batch, kv_heads=heads, seq=cap + r_cap, head_dim=d)
+        self.plant_every = plant_every
+        self.ring_k = [np.zeros((self.bh, r_cap, d), np.uint16) for _ in range(layers)]
+        self.ring_v = [np.zeros((self.bh, r_cap, d), np.uint16) for _ in range(layers)]
+        self.stores = [O.Store(self.bh, d, cap, group, bits) for _ in range(layers)]
+        self.states = [O.SinkState(batch, heads, d, k_top, sink_cap) for _ in range(layers)]
+        self.s_q = self.head = self.n_res = self.pos = 0
+
+    def tokens(self, l, kind, n):
+        x = W.generate(self.w, l, kind, tok0=self.pos, n_tok=n)
+        if self.plant_every:
+            f = x.view(np.float16).astype(np.float32)
+            rng = np.random.default_rng(self.pos * 7 + l)
+            for b in range(self.batch):
+                for i in range(n):
+                    if rng.integers(self.plant_every) == 0:   # a high-norm token
+                        f[b * self.heads:(b + 1) * self.heads, i] *= (30.0 if kind == "k" else 8.0)
+            x = f.astype(np.float16).view(np.uint16)
+        return np.ascontiguousarray(x)
+
+    def append(self, n_new, flush=True):
+        rows = (self.head + self.n_res + np.arange(n_new)) % self.r_cap
+        i0 = self.n_res
+        for l in range(self.layers):
+            k, v = self.tokens(l, "k", n_new), self.tokens(l, "v", n_new)
+            self.ring_k[l][:, rows] = k
+            self.ring_v[l][:, rows] = v
+            self.cache.append(l, to_dev(k), to_dev(v))
+            self.states[l].update(O.sink_scores(k, self.heads), self.s_q + i0)
+        self.cache.advance(n_new)
+        self.sinks.update(i0, n_new)
+        self.n_res += n_new
+        self.pos += n_new
+        if flush:
+            n_gpu = self.sinks.flush()
+            for l in range(self.layers):
+                n, s_q, head, n_res = O.flush_sink(self.ring_k[l], self.ring_v[l], self.stores[l],
+                                                   self.residual, self.s_q, self.head, self.n_res,
+                                                   self.states[l])
+            assert n_gpu == n
+            self.s_q, self.head, self.n_res = s_q, head, n_res
+            assert (self.cache.s_q, self.cache.res_head, self.cache.n_res) == (s_q, head, n_res)
+
+    def check(self):
+        torch.cuda.synchronize()
+        assert K.kivi_device_fault() == 0
+        sk = self.sinks
+        for l in range(self.layers):
+            st, o = self.stores[l], self.states[l]
+            kt = self.sinks.k_top
+            cnt = sk.top_count[l].cpu().numpy()
+            assert np.array_equal(cnt, o.top_count), (l, cnt, o.top_count)
+            tp = sk.top_pos[l].cpu().numpy()
+            ts = host_f32_bits(sk.top_score[l])
+            for b in range(self.batch):
+                c = int(cnt[b])
+                assert np.array_equal(tp[b, :c], o.top_pos[b, :c]), (l, b)
+                assert np.array_equal(ts[b, :c], bits32(o.top_score[b, :c])), (l, b)
+            assert_same("key codes", host_u32(self.cache.k_codes[l]), st.k_codes)
+            assert_same("key scale", host_f32_bits(self.cache.k_scale[l]), bits32(st.k_scale))
+            assert_same("key zero", host_f32_bits(self.cache.k_zero[l]), bits32(st.k_zero))
+            assert_same("value codes", host_u32(self.cache.v_codes[l]), st.v_codes)
+            assert_same("value scale", host_f32_bits(self.cache.v_scale[l]), bits32(st.v_scale))
+            assert_same("value zero", host_f32_bits(self.cache.v_zero[l]), bits32(st.v_zero))
+            scnt = sk.sink_count[l].cpu().numpy()
+            assert np.array_equal(scnt, o.sink_count), (l, scnt, o.sink_count)
+            spos = sk.sink_pos[l].cpu().numpy()
+            for b in range(self.batch):
+                c = int(scnt[b])
+                assert np.array_equal(spos[b, :c], o.sink_pos[b, :c])
+                for h in range(self.heads):
+                    bb = b * self.heads + h
+                    assert np.array_equal(host_u16(sk.sink_k[l][bb, :c]), o.sink_k[bb, :c])
+                    assert np.array_equal(host_u16(sk.sink_v[l][bb, :c]), o.sink_v[bb, :c])
+        # dequantized store with the sinks restored
+        ky, vy = self.cache.dequantize()
+        sk.restore(ky, vy)
+        torch.cuda.synchronize()
+        for l in range(self.layers):
+            kref, vref = O.cache_kv(self.stores[l], self.s_q, self.ring_k[l], self.ring_v[l],
+                                    self.head, 0)
+            O.sink_restore(kref, vref, self.states[l])
+            assert_same("restored keys", host_u16(ky[l]), kref)
+            assert_same("restored values", host_u16(vy[l]), vref)
+
+
+@pytest.mark.parametrize("bits,group,d", [(2, 32, 128), (4, 64, 128), (8, 128, 128),
+                                          (2, 64, 64), (4, 32, 64)])
+def test_sink_prefill_flush(bits, group, d):
+    batch, heads, S = 2, 2, 8 * group
+    pair = SinkPair(2, batch, heads, d, bits, group, group, r_cap=S, cap=S, k_top=5,
+                    sink_cap=8, seed=40 + bits + group + d, plant_every=60)
+    pair.append(S, flush=True)
+    assert pair.s_q == S - group
+    assert (pair.sinks.sink_count.cpu().numpy() > 0).all()
+    pair.check()
+
+
+@pytest.mark.parametrize("bits,group", [(2, 32), (4, 64)])
+def test_sink_decode_sequence_with_ring_wrap(bits, group):
+    batch, heads, d = 3, 2, 128
+    pair = SinkPair(2, batch, heads, d, bits, group, group, r_cap=4 * group, cap=16 * group,
+                    k_top=6, sink_cap=40, seed=70 + bits, plant_every=90)
+    pair.append(3 * group)                      # a prefill
+    rng = np.random.default_rng(bits)
+    while pair.s_q + pair.n_res < 14 * group:
+        n = int(min(rng.integers(1, group), pair.r_cap - pair.n_res))
+        pair.append(n)
+    assert pair.head > 0
+    pair.check()
+
+
+def test_no_top_k_is_plain_kivi():
+    batch, heads, d, group, bits = 2, 2, 128, 32, 2
+    pair = SinkPair(1, batch, heads, d, bits, group, group, r_cap=256, cap=256, k_top=0,
+                    sink_cap=0, seed=5, plant_every=40)
+    pair.append(256)
+    pair.check()
+    st = O.Store(pair.bh, d, 256, group, bits)
+    O.flush(pair.ring_k[0], pair.ring_v[0], st, group, 0, 0, 256)
+    assert_same("plain key codes", host_u32(pair.cache.k_codes[0]), st.k_codes)
+    assert_same("plain value codes", host_u32(pair.cache.v_codes[0]), st.v_codes)
+
+
+def test_sink_store_overflow_is_recorded():
+    batch, heads, d, group, bits = 1, 2, 128, 32, 4
+    pair = SinkPair(1, batch, heads, d, bits, group, group, r_cap=256, cap=256, k_top=8,
+                    sink_cap=3, seed=9, plant_every=20)
+    pair.sinks.update(0, 0)
+    rows = np.arange(256)
+    k = pair.tokens(0, "k", 256)
+    v = pair.tokens(0, "v", 256)
+    pair.cache.append(0, to_dev(k), to_dev(v))
+    pair.cache.advance(256)
+    pair.sinks.update(0, 256)
+    pair.sinks.flush()
+    torch.cuda.synchronize()
+    assert K.kivi_device_fault() == 2
+    assert int(pair.sinks.sink_count[0, 0]) == 3
+    del rows
