@@ -287,6 +287,95 @@ class PrefillFlush:
         return done_bytes, t_total, f"{layers} of {w.layers} layers (flush + dequantize, keys and values)"
 
 
+class SinkPrefillFlush(PrefillFlush):
+    """The prefill flush with KIVI-Sink protection: every prompt token's key
+    norm is scored and ranked (top 5 per sequence), the flush keeps the
+    flushed top-5 tokens fp16 in the sink store and out of the groups'
+    min/max, and the dequantized store gets the sinks' rows back."""
+
+    kernels = ("sink_update", "flush_sink", "dequantize", "sink_restore")
+    events_per_step = 5
+    K_TOP = 5
+
+    def __init__(self, w, device):
+        super().__init__(w, device)
+        K = self.K
+        self.sinks = K.KiviSinks(self.cache, w.batch, self.K_TOP, 2 * self.K_TOP)
+        elems = w.layers * w.bh * self.n * w.head_dim
+        score_bytes = w.layers * w.bh * w.seq * w.head_dim * 2        # the prompt's keys read
+        bpe = bytes_per_elem(w.bits, w.group)
+        self.kernel_bytes = {"sink_update": score_bytes, "flush_sink": 2 * elems * bpe,
+                             "dequantize": 2 * elems * bpe, "sink_restore": 0.0}
+        self.step_bytes = score_bytes + 4 * elems * bpe
+        self.launches_per_step = 8
+        self.k_list = list(self.k_out.unbind(0))
+        self.v_list = list(self.v_out.unbind(0))
+
+    def config(self):
+        c = super().config()
+        c["step"] = ("KIVI-Sink: key-norm scores and top-5 of every prompt token, sink-protected "
+                     "flush (mask, quantize, sink store), dequantize of the store, sinks restored")
+        c["k_top"] = self.K_TOP
+        return c
+
+    def step(self, stream, ev=None):
+        c, sk = self.cache, self.sinks
+        sk.top_count.zero_()
+        sk.sink_count.zero_()
+        c.reset(s_q=0, res_head=0, n_res=self.w.seq)
+        if ev is not None:
+            ev[0].record(stream)
+        sk.update(0, self.w.seq, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        n = sk.flush(stream)
+        assert n == self.n
+        if ev is not None:
+            ev[2].record(stream)
+        self.K.kivi_dequantize_cache(c.layers, c.n_layers, c.state, self.k_ptrs, self.v_ptrs,
+                                     stream)
+        if ev is not None:
+            ev[3].record(stream)
+        sk.restore(self.k_list, self.v_list, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    def step_events(self, evs):
+        return evs
+
+    def kernel_times(self, e):
+        return {"sink_update": e[0].elapsed_time(e[1]), "flush_sink": e[1].elapsed_time(e[2]),
+                "dequantize": e[2].elapsed_time(e[3]), "sink_restore": e[3].elapsed_time(e[4])}
+
+    def cpu_sample(self, budget_s: float):
+        import oracle as O
+        w = self.w
+        done, t_total, layers = 0.0, 0.0, 0
+        W_ = 32 // w.bits
+        per_layer = self.step_bytes / w.layers
+        for l in range(w.layers):
+            st = O.Store(w.bh, w.head_dim, w.seq, w.group, w.bits)
+            ss = O.SinkState(w.batch, w.kv_heads, w.head_dim, self.K_TOP, 2 * self.K_TOP)
+            k, v = self.k_host[l], self.v_host[l]
+            t0 = time.perf_counter()
+            ss.update(O.sink_scores(k, w.kv_heads), 0)
+            n, _, _, _ = O.flush_sink(k, v, st, w.residual, 0, 0, w.seq, ss)
+            ky = O.dequantize_keys(st.k_codes[:, :n // W_], st.k_scale[:, :n // w.group],
+                                   st.k_zero[:, :n // w.group], n, w.group, w.bits)
+            vy = O.dequantize_values(st.v_codes[:, :n], st.v_scale[:, :n], st.v_zero[:, :n],
+                                     w.group, w.bits)
+            O.sink_restore(ky, vy, ss)
+            t_total += time.perf_counter() - t0
+            done += per_layer
+            layers += 1
+            if t_total >= budget_s:
+                break
+        return done, t_total, f"{layers} of {w.layers} layers (KIVI-Sink score, flush, dequantize, restore)"
+
+    def e2e_setup(self):
+        return super().e2e_setup()
+
+
 class FusedPrefillFlush(PrefillFlush):
     """The prefill flush in its fused fake-quant form: one launch per tensor
     kind over all layers quantizes the flushed tokens into the store and
@@ -865,13 +954,15 @@ class FusedStoreSweep(StoreSweep):
 
 
 def make_workload(name, device, layers=None, bits=None, group=None, fused=False,
-                  attention=False):
+                  attention=False, sink=False):
     import dataclasses
     import workloads as W
     w = W.CONFIGS[name]
     if layers:
         w = dataclasses.replace(w, layers=int(layers))
     if name in ("llama3_2_3b_prefill", "qwen2_5_7b_long", "tiny_flush"):
+        if sink:
+            return SinkPrefillFlush(w, device)
         return FusedPrefillFlush(w, device) if fused else PrefillFlush(w, device)
     if name == "batched_decode":
         if attention:
@@ -935,7 +1026,7 @@ def run_kivi(args):
     import kv_cache_quantization_kivi_gb300 as K
     K.lib()
     wl = make_workload(args.workload, device, args.layers, args.bits, args.group, args.fused,
-                       args.attention)
+                       args.attention, args.sink)
     stream = torch.cuda.current_stream(device)
 
     def new_events(n):
@@ -990,7 +1081,8 @@ def run_kivi(args):
     dom_avg_s = sum(k_ms[dom]) / len(k_ms[dom]) * 1e-3
     achieved = wl.kernel_bytes[dom] / dom_avg_s / 1e9
     traffic = ncu_traffic(args.workload + ("+fused" if args.fused else "")
-                          + ("+attention" if args.attention else ""), dom)
+                          + ("+attention" if args.attention else "")
+                          + ("+sink" if args.sink else ""), dom)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -1133,6 +1225,9 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true",
                     help="time the fused fake-quant form (store and fp16 reconstruction in "
                          "one pass) instead of quantize + dequantize")
+    ap.add_argument("--sink", action="store_true",
+                    help="prefill workloads: the KIVI-Sink flush (scores, top-5, protected "
+                         "flush, dequantize, restore)")
     ap.add_argument("--attention", action="store_true",
                     help="batched_decode: time decode attention over the packed cache")
     ap.add_argument("--layers", type=int, default=None,

@@ -316,3 +316,44 @@ def test_decode_attention_noalloc_validation():
                                            0, None) == 1
     assert L.kivi_decode_attention_noalloc(_layers(2), 2, C.byref(_cache(bh=0)), 1, 8, 0.1, q,
                                            out, 2, None) == 1
+
+
+def _sinks(n=2, **kw):
+    arr = (K.kivi_sink_layer * n)()
+    for i in range(n):
+        for f, _ in K.kivi_sink_layer._fields_:
+            setattr(arr[i], f, FAKE + (1 << 20) * (i + 1))
+        for f, v in kw.items():
+            setattr(arr[i], f, v)
+    return arr
+
+
+def test_sink_validation():
+    L = K.lib()
+    c = _cache(n_res=40)
+    cfg = lambda **kw: K.kivi_sink_cfg(**{**dict(batch=2, k_top=5, sink_cap=8, reserved=0,  # noqa
+                                                   reserved2=0), **kw})
+    upd = lambda cc, s, cf, i0, n: L.kivi_sink_update(_layers(2), s, 2, C.byref(cc),  # noqa
+                                                      C.byref(cf), i0, n, None)
+    assert upd(c, _sinks(), cfg(batch=3), 0, 8) == 1            # bh % batch
+    assert upd(c, _sinks(), cfg(k_top=65), 0, 8) == 1           # top-k beyond 64
+    assert upd(c, _sinks(), cfg(k_top=-1), 0, 8) == 1
+    assert upd(c, _sinks(), cfg(reserved=1), 0, 8) == 1
+    assert upd(c, _sinks(mask=None), cfg(), 0, 8) == 1
+    assert upd(c, _sinks(sink_k=FAKE + 4), cfg(), 0, 8) == 2
+    assert upd(c, _sinks(), cfg(), 30, 11) == 1                 # past the residual
+    assert upd(c, _sinks(), cfg(), 0, 0) == 0                   # nothing to score
+    assert upd(c, _sinks(), cfg(k_top=0), 0, 8) == 0            # no top-k kept
+    out = C.c_int64(-1)
+    c2 = _cache(n_res=63)                                       # nothing to flush
+    assert L.kivi_flush_sink(_layers(2), _sinks(), 2, C.byref(c2), C.byref(cfg()),
+                             C.byref(out), None) == 0 and out.value == 0
+    c3 = _cache(cap=64, s_q=32, n_res=128)
+    assert L.kivi_flush_sink(_layers(2), _sinks(), 2, C.byref(c3), C.byref(cfg()),
+                             C.byref(out), None) == 3
+    assert (c3.s_q, c3.n_res) == (32, 128)
+    ptrs = (C.c_void_p * 2)(FAKE, FAKE)
+    assert L.kivi_sink_restore(_sinks(), 2, C.byref(_cache(s_q=0)), C.byref(cfg()), ptrs, ptrs,
+                               None) == 0
+    assert L.kivi_sink_restore(_sinks(), 2, C.byref(_cache(s_q=32)), C.byref(cfg()),
+                               (C.c_void_p * 2)(FAKE, None), ptrs, None) == 1
