@@ -292,7 +292,8 @@ KIVI_API kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n
  *   sink_count int32 [batch]         sinks stored (start at 0)
  *   sink_k,    fp16  [bh][sink_cap][d]  the sinks' key / value rows
  *   sink_v
- *   mask       u32   [batch][r_cap/32]  scratch of the flush */
+ *   mask       u32   [batch][r_cap/32]  scratch of the flush
+ *   scores     f32   [batch][r_cap]     scratch of the update */
 typedef struct {
     int64_t *top_pos;
     float *top_score;
@@ -302,6 +303,7 @@ typedef struct {
     void *sink_k;
     void *sink_v;
     uint32_t *mask;
+    float *scores;
 } kivi_sink_layer;
 
 /* batch: sequences (cache->bh / batch KV heads each); k_top: 0..64;

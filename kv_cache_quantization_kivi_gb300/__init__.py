@@ -66,7 +66,7 @@ class kivi_cache(C.Structure):
 class kivi_sink_layer(C.Structure):
     _fields_ = [("top_pos", C.c_void_p), ("top_score", C.c_void_p), ("top_count", C.c_void_p),
                 ("sink_pos", C.c_void_p), ("sink_count", C.c_void_p), ("sink_k", C.c_void_p),
-                ("sink_v", C.c_void_p), ("mask", C.c_void_p)]
+                ("sink_v", C.c_void_p), ("mask", C.c_void_p), ("scores", C.c_void_p)]
 
 
 class kivi_sink_cfg(C.Structure):
@@ -627,11 +627,13 @@ class KiviSinks:
         self.sink_k = z((bh, sc, d), torch.float16)
         self.sink_v = z((bh, sc, d), torch.float16)
         self.mask = z((batch, max(r_cap // 32, 1)), torch.int32)
+        self.scores = z((batch, r_cap), torch.float32)
         self.layers = (kivi_sink_layer * L)(*[
             kivi_sink_layer(self.top_pos[i].data_ptr(), self.top_score[i].data_ptr(),
                             self.top_count[i].data_ptr(), self.sink_pos[i].data_ptr(),
                             self.sink_count[i].data_ptr(), self.sink_k[i].data_ptr(),
-                            self.sink_v[i].data_ptr(), self.mask[i].data_ptr())
+                            self.sink_v[i].data_ptr(), self.mask[i].data_ptr(),
+                            self.scores[i].data_ptr())
             for i in range(L)])
         self.cfg = kivi_sink_cfg(batch, k_top, sink_cap, 0, 0)
 

@@ -606,8 +606,8 @@ static kivi_status check_sinks(const kivi_sink_layer *sinks, int n_layers, const
     return KIVI_ERR_INVAL;
   for (int l = 0; l < n_layers; ++l) {
     const kivi_sink_layer &S = sinks[l];
-    const void *ptrs[8] = {S.top_pos, S.top_score, S.top_count, S.sink_pos,
-                           S.sink_count, S.sink_k, S.sink_v, S.mask};
+    const void *ptrs[9] = {S.top_pos, S.top_score, S.top_count, S.sink_pos,
+                           S.sink_count, S.sink_k, S.sink_v, S.mask, S.scores};
     for (const void *q : ptrs)
       if (!q) return KIVI_ERR_INVAL;
     if (!aligned16(S.sink_k) || !aligned16(S.sink_v)) return KIVI_ERR_ALIGN;
@@ -642,6 +642,7 @@ static void sink_params(const kivi_layer *layers, const kivi_sink_layer *sinks, 
     J.sink_k = S.sink_k;
     J.sink_v = S.sink_v;
     J.mask = S.mask;
+    J.scores = S.scores;
   }
 }
 

@@ -143,6 +143,7 @@ struct SinkJob {
   void *sink_k;           // fp16 [bh][sink_cap][d]
   void *sink_v;
   uint32_t *mask;         // [batch][mask_words] flush scratch
+  float *scores;          // [batch][r_cap] update scratch
   void *k_out;            // restore: fp16 [bh][out_rows][d]
   void *v_out;
 };

@@ -4,8 +4,9 @@
 // the key norms over the KV heads ranks the token positions, a running top-k
 // is kept, and a flushed token in it is stored fp16 instead of quantized).
 //
-//   sink_update_kernel   block per (layer, sequence): scores of new residual
-//                        tokens merged into the running top-k
+//   sink_score_kernel    thread per new token: its score
+//   sink_select_kernel   block per (layer, sequence): the new scores merged
+//                        into the running top-k
 //   sink_mask_kernel     per (layer, sequence, 32 flushed tokens): which of
 //                        the tokens being flushed are in the top-k (one bit
 //                        each), read by the quantize kernels' sink mode
@@ -54,104 +55,110 @@ __device__ float token_score(const __half *k_seq, int64_t head_stride, int heads
   return __fdiv_rn(sum, static_cast<float>(heads));
 }
 
-__global__ void __launch_bounds__(kThreads) sink_update_kernel(const __grid_constant__ SinkParams p) {
+// thread = (job, sequence, new token): its score into the scores scratch
+__global__ void __launch_bounds__(kThreads) sink_score_kernel(const __grid_constant__ SinkParams p) {
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (u >= static_cast<int64_t>(p.n_jobs) * p.batch * p.n) return;
+  const int64_t i = u % p.n, js = u / p.n;
+  const int job = static_cast<int>(js / p.batch);
+  const int64_t seq = js - static_cast<int64_t>(job) * p.batch;
+  const SinkJob &J = p.jobs[job];
+  const int64_t li = p.i0 + i;                                   // logical residual token
+  const int64_t row = (p.res_head + li) % p.r_cap;
+  const __half *k_seq = static_cast<const __half *>(J.k_res) + seq * p.heads * p.r_cap * p.d;
+  J.scores[seq * p.r_cap + i] =
+      token_score(k_seq + row * p.d, p.r_cap * p.d, static_cast<int>(p.heads), p.d);
+}
+
+// Sorted (best first) list of up to LK candidates kept by one thread.
+template <int LK>
+struct LocalTop {
+  float s[LK];
+  int64_t q[LK];
+  int n;
+  __device__ __forceinline__ void init() { n = 0; }
+  __device__ __forceinline__ void offer(float sc, int64_t pos, int k) {
+    if (n == k && !ranks_before(sc, pos, s[n - 1], q[n - 1])) return;
+    int i = n < k ? n++ : n - 1;                  // slot freed at the end
+#pragma unroll 1
+    while (i > 0 && ranks_before(sc, pos, s[i - 1], q[i - 1])) {
+      s[i] = s[i - 1];
+      q[i] = q[i - 1];
+      --i;
+    }
+    s[i] = sc;
+    q[i] = pos;
+  }
+};
+
+// block = (job, sequence): the new scores and the kept top-k merged.  Each
+// thread keeps the best k of its strided share; k rounds of a block-wide
+// argmax over the threads' list heads then give the k best overall.
+template <int LK>
+__global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_constant__ SinkParams p) {
   const int job = static_cast<int>(blockIdx.x / p.batch);
   const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
   const SinkJob &J = p.jobs[job];
-  __shared__ float top_s[kMaxSinkTop];
-  __shared__ int64_t top_p[kMaxSinkTop];
   __shared__ float new_s[kMaxSinkTop];
   __shared__ int64_t new_p[kMaxSinkTop];
   __shared__ float red_s[kWarps];
   __shared__ int64_t red_p[kWarps];
   __shared__ int red_i[kWarps];
-  __shared__ int top_n;
+  __shared__ int winner;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) top_n = J.top_count[seq];
-  __syncthreads();
-  if (tid < top_n) {
-    top_s[tid] = J.top_score[seq * p.k_top + tid];
-    top_p[tid] = J.top_pos[seq * p.k_top + tid];
-  }
-  __syncthreads();
-  const __half *k_seq = static_cast<const __half *>(J.k_res) + seq * p.heads * p.r_cap * p.d;
-  for (int64_t start = 0; start < p.n; start += kThreads) {
-    // this thread's candidates: one new token and (tid < top_n) one kept entry
-    float cs = 0.0f;
-    int64_t cp = 0;
-    bool c_ok = start + tid < p.n;
-    if (c_ok) {
-      const int64_t li = p.i0 + start + tid;                      // logical residual token
-      const int64_t row = (p.res_head + li) % p.r_cap;
-      cs = token_score(k_seq + row * p.d, p.r_cap * p.d, static_cast<int>(p.heads), p.d);
-      cp = p.s_q + li;
-    }
-    const int tn = top_n;
-    bool t_ok = tid < tn;
-    const float ts = t_ok ? top_s[tid] : 0.0f;
-    const int64_t tp = t_ok ? top_p[tid] : 0;
-    const int64_t left = p.n - start;
-    const int avail = static_cast<int>(left < kThreads ? left : kThreads) + tn;
-    const int keep = min(p.k_top, avail);
-    for (int j = 0; j < keep; ++j) {
-      // best remaining candidate of this thread
-      bool have = c_ok || t_ok;
-      float bs = 0.0f;
-      int64_t bp = 0;
-      int which = -1;
-      if (t_ok && (!c_ok || ranks_before(ts, tp, cs, cp))) {
-        bs = ts; bp = tp; which = 1;
-      } else if (c_ok) {
-        bs = cs; bp = cp; which = 0;
-      }
-      // warp reduction of (have, score, position, owner)
-      int owner = have ? tid : -1;
+  const int k = p.k_top;
+  LocalTop<LK> lt;
+  lt.init();
+  const int tn = J.top_count[seq];
+  for (int e = tid; e < tn; e += kThreads)
+    lt.offer(J.top_score[seq * p.k_top + e], J.top_pos[seq * p.k_top + e], k);
+  for (int64_t i = tid; i < p.n; i += kThreads)
+    lt.offer(J.scores[seq * p.r_cap + i], p.s_q + p.i0 + i, k);
+  const int64_t avail = tn + p.n;
+  const int keep = avail < k ? static_cast<int>(avail) : k;
+  int head = 0;
+  for (int j = 0; j < keep; ++j) {
+    bool have = head < lt.n;
+    float bs = have ? lt.s[head] : 0.0f;
+    int64_t bp = have ? lt.q[head] : 0;
+    int owner = have ? tid : -1;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-        const int64_t op = __shfl_xor_sync(0xffffffffu, bp, off);
-        const int oo = __shfl_xor_sync(0xffffffffu, owner, off);
-        if (oo >= 0 && (owner < 0 || ranks_before(os, op, bs, bp))) {
-          bs = os; bp = op; owner = oo;
+    for (int off = 16; off > 0; off >>= 1) {
+      const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+      const int64_t op = __shfl_xor_sync(0xffffffffu, bp, off);
+      const int oo = __shfl_xor_sync(0xffffffffu, owner, off);
+      if (oo >= 0 && (owner < 0 || ranks_before(os, op, bs, bp))) {
+        bs = os; bp = op; owner = oo;
+      }
+    }
+    if (lane == 0) {
+      red_s[warp] = bs;
+      red_p[warp] = bp;
+      red_i[warp] = owner;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float ws = red_s[0];
+      int64_t wp = red_p[0];
+      int wo = red_i[0];
+      for (int w = 1; w < kWarps; ++w) {
+        if (red_i[w] >= 0 && (wo < 0 || ranks_before(red_s[w], red_p[w], ws, wp))) {
+          ws = red_s[w]; wp = red_p[w]; wo = red_i[w];
         }
       }
-      if (lane == 0) {
-        red_s[warp] = bs;
-        red_p[warp] = bp;
-        red_i[warp] = owner;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        float ws = red_s[0];
-        int64_t wp = red_p[0];
-        int wo = red_i[0];
-        for (int w = 1; w < kWarps; ++w) {
-          if (red_i[w] >= 0 && (wo < 0 || ranks_before(red_s[w], red_p[w], ws, wp))) {
-            ws = red_s[w]; wp = red_p[w]; wo = red_i[w];
-          }
-        }
-        new_s[j] = ws;
-        new_p[j] = wp;
-        red_i[0] = wo;
-      }
-      __syncthreads();
-      if (red_i[0] == tid) {   // the winner's candidate is used up
-        if (which == 1) t_ok = false; else c_ok = false;
-      }
-      __syncthreads();
+      new_s[j] = ws;
+      new_p[j] = wp;
+      winner = wo;
     }
-    if (tid < keep) {
-      top_s[tid] = new_s[tid];
-      top_p[tid] = new_p[tid];
-    }
-    if (tid == 0) top_n = keep;
+    __syncthreads();
+    if (winner == tid) ++head;
     __syncthreads();
   }
-  if (tid < top_n) {
-    J.top_score[seq * p.k_top + tid] = top_s[tid];
-    J.top_pos[seq * p.k_top + tid] = top_p[tid];
+  if (tid < keep) {
+    J.top_score[seq * p.k_top + tid] = new_s[tid];
+    J.top_pos[seq * p.k_top + tid] = new_p[tid];
   }
-  if (tid == 0) J.top_count[seq] = top_n;
+  if (tid == 0) J.top_count[seq] = keep;
 }
 
 // thread = (job, sequence, word of 32 flushed tokens)
@@ -254,7 +261,15 @@ unsigned blocks_for(int64_t threads) {
 }  // namespace
 
 cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream) {
-  sink_update_kernel<<<static_cast<unsigned>(p.n_jobs * p.batch), kThreads, 0, stream>>>(p);
+  const int64_t threads = static_cast<int64_t>(p.n_jobs) * p.batch * p.n;
+  sink_score_kernel<<<blocks_for(threads), kThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = static_cast<unsigned>(p.n_jobs * p.batch);
+  if (p.k_top <= 8)
+    sink_select_kernel<8><<<blocks, kThreads, 0, stream>>>(p);
+  else
+    sink_select_kernel<kMaxSinkTop><<<blocks, kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
