@@ -43,8 +43,8 @@
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream);
  *     outputs are complete when the stream reaches that point.  Calls that
  *     overlap on the GPU with writes to their inputs or outputs race.
- *   - Supported: bits in {2, 4, 8}; group in {32, 64, 128}; 8 <= d <= 256
- *     with d % 8 == 0 for keys and d % group == 0 for values.
+ *   - Supported: bits in {2, 4, 8}; group in {16, 32, 64, 128}; 8 <= d <= 256
+ *     with d % 8 == 0 for keys and d % group == 0, d % 32 == 0 for values.
  *   - Alignment (KIVI_ERR_ALIGN otherwise): every base pointer 16-byte
  *     aligned; bh strides of fp16 tensors and of key codes multiples of 16
  *     bytes; key scale/zero bh strides multiples of 8 bytes (16 for
@@ -292,7 +292,7 @@ KIVI_API kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n
  *   sink_count int32 [batch]         sinks stored (start at 0)
  *   sink_k,    fp16  [bh][sink_cap][d]  the sinks' key / value rows
  *   sink_v
- *   mask       u32   [batch][r_cap/32]  scratch of the flush
+ *   mask       u32   [batch][ceil(r_cap/32)]  scratch of the flush
  *   scores     f32   [batch][r_cap]     scratch of the update */
 typedef struct {
     int64_t *top_pos;

@@ -626,7 +626,7 @@ class KiviSinks:
         self.sink_count = z((batch,), torch.int32)
         self.sink_k = z((bh, sc, d), torch.float16)
         self.sink_v = z((bh, sc, d), torch.float16)
-        self.mask = z((batch, max(r_cap // 32, 1)), torch.int32)
+        self.mask = z((batch, (r_cap + 31) // 32), torch.int32)
         self.scores = z((batch, r_cap), torch.float32)
         self.layers = (kivi_sink_layer * L)(*[
             kivi_sink_layer(self.top_pos[i].data_ptr(), self.top_score[i].data_ptr(),

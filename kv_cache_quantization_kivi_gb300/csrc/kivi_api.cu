@@ -17,7 +17,7 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 
 bool valid_bits(int bits) { return bits == 2 || bits == 4 || bits == 8; }
-bool valid_group(int g) { return g == 32 || g == 64 || g == 128; }
+bool valid_group(int g) { return g == 16 || g == 32 || g == 64 || g == 128; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool bytes16(int64_t n_elems, int64_t elem_bytes) { return (n_elems * elem_bytes) % 16 == 0; }
 bool bytes_mult(int64_t n_elems, int64_t elem_bytes, int64_t m) {
@@ -30,7 +30,10 @@ int64_t value_code_align(int bits) { return bits == 2 ? 8 : 16; }
 constexpr int64_t kMaxUnits = (int64_t{1} << 31) - 1;
 
 bool valid_key_dim(int64_t d) { return d >= 8 && d <= 256 && d % 8 == 0; }
-bool valid_value_dim(int64_t d, int group) { return d >= 32 && d <= 256 && d % group == 0; }
+// values are processed in 32-channel pieces (two 16-channel groups at G = 16)
+bool valid_value_dim(int64_t d, int group) {
+  return d >= 32 && d <= 256 && d % group == 0 && d % 32 == 0;
+}
 
 int64_t groups_of(int64_t s, int group) { return s / group + (s % group != 0); }
 
@@ -57,10 +60,10 @@ KeyGeom key_geom(int64_t s, int64_t d, int group, int bits) {
 }
 
 // Threads of the key quantize kernel: one per (bh, group, channel pair,
-// 32-token split); of the value kernels and the key dequantize kernel: one
-// per 32 (values) or 8 (keys) channels of a row or group.
+// min(G, 32)-token split); of the value kernels and the key dequantize
+// kernel: one per 32 (values) or 8 (keys) channels of a row or group.
 int64_t key_quant_units(int64_t bh, int64_t s, int64_t d, int group) {
-  return sat_mul(sat_mul(bh, groups_of(s, group)), (d / 2) * (group / 32));
+  return sat_mul(sat_mul(bh, groups_of(s, group)), (d / 2) * (group < 32 ? 1 : group / 32));
 }
 int64_t key_dequant_units(int64_t bh, int64_t s, int64_t d, int group) {
   return sat_mul(sat_mul(bh, groups_of(s, group)), d / 8);
@@ -491,7 +494,7 @@ static kivi_status attn_geom(const kivi_cache *c, int64_t batch, int32_t h_q, At
   if (g->h_kv < 1 || h_q < 1 || h_q % g->h_kv != 0) return KIVI_ERR_INVAL;
   g->r = h_q / g->h_kv;
   if (g->r > 8) return KIVI_ERR_INVAL;
-  g->tiles_store = c->s_q / kAttnTile;
+  g->tiles_store = (c->s_q + kAttnTile - 1) / kAttnTile;   // the last one half at G = 16
   g->tiles_res = (c->n_res + kAttnTile - 1) / kAttnTile;
   return KIVI_OK;
 }
@@ -499,7 +502,7 @@ static kivi_status attn_geom(const kivi_cache *c, int64_t batch, int32_t h_q, At
 int32_t kivi_decode_attention_splits(const kivi_cache *cache, int n_layers, int64_t batch) {
   if (!cache || n_layers < 1 || batch < 1 || cache->bh < 0) return 1;
   const int64_t items = sat_mul(n_layers, cache->bh);
-  const int64_t tiles = cache->s_q > 0 ? cache->s_q / kAttnTile : 0;
+  const int64_t tiles = cache->s_q > 0 ? (cache->s_q + kAttnTile - 1) / kAttnTile : 0;
   return kivi_impl::attention_splits(items, tiles, cache->group, cache->bits);
 }
 
@@ -539,6 +542,7 @@ static kivi_status attn_prepare(const kivi_layer *layers, int n_layers, const ki
   p->tiles_store = static_cast<int32_t>(g.tiles_store);
   p->tiles_res = static_cast<int32_t>(g.tiles_res);
   p->tiles_per_split = static_cast<int32_t>((g.tiles_store + n_split - 1) / n_split);
+  p->tail_half = cache->s_q % kAttnTile != 0;
   p->bh = cache->bh;
   p->cap = cache->cap;
   p->r_cap = cache->r_cap;
@@ -628,7 +632,7 @@ static void sink_params(const kivi_layer *layers, const kivi_sink_layer *sinks, 
   p->r_cap = c->r_cap;
   p->res_head = c->res_head;
   p->s_q = c->s_q;
-  p->mask_words = c->r_cap / 32;
+  p->mask_words = (c->r_cap + 31) / 32;
   for (int l = 0; l < n_layers; ++l) {
     const kivi_sink_layer &S = sinks[l];
     kivi_impl::SinkJob &J = p->jobs[l];
@@ -698,7 +702,7 @@ kivi_status kivi_flush_sink(const kivi_layer *layers, const kivi_sink_layer *sin
   kp.ring = cache->r_cap;
   kp.head = cache->res_head;
   kp.heads = cache->bh / cfg->batch;
-  kp.mask_words = cache->r_cap / 32;
+  kp.mask_words = (cache->r_cap + 31) / 32;
   kivi_impl::QuantParams vp = kp;
   kp.codes_bh_stride = cache->cap / W * d;
   kp.sz_bh_stride = cache->cap / G * d;

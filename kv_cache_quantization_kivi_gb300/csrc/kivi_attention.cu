@@ -10,9 +10,10 @@
 // fp16 residual tokens.  Query head h of a sequence reads KV head h / r.
 //
 // Work item (one CTA of 4 warps) = (layer, bh, split).  Its store tiles (32
-// tokens each) and, in the last split, its residual tiles are dealt to the
+// tokens each; at G = 16 the last may hold 16) and, in the last split, its
+// residual tiles are dealt to the
 // warps round-robin; each warp streams its store tiles' key codes, key
-// scale/zero row, value codes and value scales/zeros (six contiguous pieces)
+// scale/zero rows, value codes and value scales/zeros (six contiguous pieces)
 // into a private shared-memory ring with bulk asynchronous copies completed
 // on per-stage mbarriers, so no CTA barrier is needed until the end.  Per
 // tile the warp expands the codes cooperatively -- each lane one key channel
@@ -70,8 +71,9 @@ constexpr uint64_t kWaitLimitNs = 200000000ull;  // 0.2 s per pipeline wait
 // Shared-memory stage of one store tile (byte offsets).
 template <int BITS, int G>
 struct StageFmt {
+  static constexpr int KR = G < 32 ? kTile / G : 1; // key groups per tile
   static constexpr int kKc = BITS * kD * 4;        // key codes: 32/W rows x D words
-  static constexpr int kKs = kD * 4;               // key scale (or zero) row of the group
+  static constexpr int kKs = KR * kD * 4;          // key scale (or zero) rows of the groups
   static constexpr int kVc = BITS * kD * 4;        // value codes: 32 rows x D/W words
   static constexpr int kVs = kTile * (kD / G) * 4; // value scales (or zeros) of 32 tokens
   static constexpr int oKs = kKc, oKz = oKs + kKs, oVc = oKz + kKs, oVs = oVc + kVc,
@@ -473,14 +475,17 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
     const uint32_t dst = smem_addr(ring + sidx * F::kBytes);
     const uint32_t bar = bar0 + 8 * sidx;
     const int64_t tok = tile * kTile;
+    // a store that ends half way through its last tile (G = 16): that tile's
+    // first 16 tokens only, the first half of each piece
+    const int sh = G < 32 && p.tail_half && tile == p.tiles_store - 1 ? 1 : 0;
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, F::kBytes);
-    bulk_load(dst, kc_bh + (tok / W) * kD, F::kKc, bar, pol);
-    bulk_load(dst + F::oKs, ks_bh + (tok / G) * kD, F::kKs, bar, pol);
-    bulk_load(dst + F::oKz, kz_bh + (tok / G) * kD, F::kKs, bar, pol);
-    bulk_load(dst + F::oVc, vc_bh + tok * (kD / W), F::kVc, bar, pol);
-    bulk_load(dst + F::oVs, vs_bh + tok * (kD / G), F::kVs, bar, pol);
-    bulk_load(dst + F::oVz, vz_bh + tok * (kD / G), F::kVs, bar, pol);
+    mbar_arrive_expect_tx(bar, F::kBytes >> sh);
+    bulk_load(dst, kc_bh + (tok / W) * kD, F::kKc >> sh, bar, pol);
+    bulk_load(dst + F::oKs, ks_bh + (tok / G) * kD, F::kKs >> sh, bar, pol);
+    bulk_load(dst + F::oKz, kz_bh + (tok / G) * kD, F::kKs >> sh, bar, pol);
+    bulk_load(dst + F::oVc, vc_bh + tok * (kD / W), F::kVc >> sh, bar, pol);
+    bulk_load(dst + F::oVs, vs_bh + tok * (kD / G), F::kVs >> sh, bar, pol);
+    bulk_load(dst + F::oVz, vz_bh + tok * (kD / G), F::kVs >> sh, bar, pol);
   };
   int issued = 0;
   if (lane == 0)
@@ -512,13 +517,17 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
       break;
     }
     const unsigned char *stg = ring + sidx * F::kBytes;
+    const int n_hb = G < 32 && p.tail_half && st0 + warp + kWarps * done == p.tiles_store - 1
+                         ? 1 : 2;                  // halves of this tile
 #pragma unroll 1
-    for (int hb = 0; hb < 2; ++hb) {
+    for (int hb = 0; hb < n_hb; ++hb) {
       float s[4];
       uint32_t phi[2], plo[2];
+      // key scale / zero row of the half's group
+      const int krow = G < 32 ? hb * kD : 0;
       expand_keys<BITS>(reinterpret_cast<const uint32_t *>(stg),
-                        reinterpret_cast<const float *>(stg + F::oKs),
-                        reinterpret_cast<const float *>(stg + F::oKz), hb, buf, lane);
+                        reinterpret_cast<const float *>(stg + F::oKs) + krow,
+                        reinterpret_cast<const float *>(stg + F::oKz) + krow, hb, buf, lane);
       __syncwarp();
       half_scores<true>(buf, qsm, lane, s);
       half_softmax(st, s, p.scale_log2, kHalf, g, phi, plo);
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
                              reinterpret_cast<const float *>(stg + F::oVs),
                              reinterpret_cast<const float *>(stg + F::oVz), hb, buf, lane);
       __syncwarp();                                // value half tile written
-      if (hb == 1 && issued < n_my) {              // stage consumed: refill it
+      if (hb == n_hb - 1 && issued < n_my) {       // stage consumed: refill it
         if (lane == 0) issue(issued);
         ++issued;
       }
@@ -691,6 +700,9 @@ cudaError_t attention_launch(const AttnParams &p, cudaStream_t stream) {
 
 cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits, cudaStream_t stream) {
   switch (bits * 1000 + group) {
+    case 2016: return attention_launch<2, 16>(p, stream);
+    case 4016: return attention_launch<4, 16>(p, stream);
+    case 8016: return attention_launch<8, 16>(p, stream);
     case 2032: return attention_launch<2, 32>(p, stream);
     case 2064: return attention_launch<2, 64>(p, stream);
     case 2128: return attention_launch<2, 128>(p, stream);

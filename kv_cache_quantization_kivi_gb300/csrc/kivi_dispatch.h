@@ -10,6 +10,9 @@
 #define KIVI_DISPATCH(FN, P, GROUP, BITS, STREAM)                     \
   do {                                                                \
     switch ((BITS) * 1000 + (GROUP)) {                                \
+      case 2016: KIVI_DISPATCH_D(FN, 2, 16, P, STREAM);               \
+      case 4016: KIVI_DISPATCH_D(FN, 4, 16, P, STREAM);               \
+      case 8016: KIVI_DISPATCH_D(FN, 8, 16, P, STREAM);               \
       case 2032: KIVI_DISPATCH_D(FN, 2, 32, P, STREAM);               \
       case 2064: KIVI_DISPATCH_D(FN, 2, 64, P, STREAM);               \
       case 2128: KIVI_DISPATCH_D(FN, 2, 128, P, STREAM);              \
@@ -29,6 +32,9 @@
 
 #define KIVI_DISPATCH_BG(FN, P, GROUP, BITS, M, STREAM)                                  \
   switch ((BITS) * 1000 + (GROUP)) {                                                    \
+    case 2016: KIVI_DISPATCH_DM(FN, 2, 16, M, P, STREAM);                               \
+    case 4016: KIVI_DISPATCH_DM(FN, 4, 16, M, P, STREAM);                               \
+    case 8016: KIVI_DISPATCH_DM(FN, 8, 16, M, P, STREAM);                               \
     case 2032: KIVI_DISPATCH_DM(FN, 2, 32, M, P, STREAM);                               \
     case 2064: KIVI_DISPATCH_DM(FN, 2, 64, M, P, STREAM);                               \
     case 2128: KIVI_DISPATCH_DM(FN, 2, 128, M, P, STREAM);                              \

@@ -8,9 +8,10 @@
 // Quantize: as in the post's "Kernel A", a thread owns whole columns of a
 // group, so the reduction over tokens happens in registers and a warp's loads
 // are coalesced along d; no transpose is materialised and no shared memory or
-// barrier is needed.  Here a thread owns a channel pair (half2) and 32 tokens;
-// for G = 64 and 128 the G/32 threads of a column are adjacent lanes that
-// combine their extremes with two-step shuffles.  The arithmetic is the
+// barrier is needed.  Here a thread owns a channel pair (half2) and
+// min(G, 32) tokens (a whole group at G = 16); for G = 64 and 128 the G/32
+// threads of a column are adjacent lanes that combine their extremes with
+// two-step shuffles.  The arithmetic is the
 // packed binary32 fast path of kivi_device.cuh with the exact-division
 // fallback; codes are packed along tokens in registers and stored as 8-byte
 // words pairs.  (A variant that staged each G x d tile into shared memory with
@@ -33,9 +34,9 @@ namespace {
 using namespace kivi_dev;
 
 // Work unit of the quantize kernel: u = ((job * bh + b) * ng + g) * (C * T)
-// + col * T + split, with C = d/2 channel pairs and T = G/32 token splits.
-// Thread u owns channels (2 col, 2 col + 1) and tokens [32 split, 32 split +
-// 32) of group g.  Consecutive lanes take consecutive splits, then columns,
+// + col * T + split, with C = d/2 channel pairs, TPT = min(G, 32) tokens per
+// thread and T = G/TPT token splits.  Thread u owns channels (2 col, 2 col +
+// 1) and tokens [TPT split, TPT split + TPT) of group g.  Consecutive lanes take consecutive splits, then columns,
 // so every warp load reads T rows x (32/T) columns x 4 bytes: whole 32-byte
 // sectors, and the T threads of one column are adjacent lanes that combine
 // their partial extremes with __shfl_xor_sync.
@@ -63,19 +64,20 @@ __device__ __forceinline__ KeyUnit decode_key_unit(uint32_t u, const QuantParams
 // Rare paths, kept out of line so that they do not weigh on the register
 // allocation of the main loop.
 
-// Token t (0..31) of a split with `rows_here` valid rows, padded by repeating
+// Token t (0 .. TPT-1) of a split with `rows_here` valid rows, padded by repeating
 // the group's last row (which is row rows_here - 1 of the split, or lies in
 // an earlier split when rows_here <= 0).
 __device__ __forceinline__ int padded_row(int t, int rows_here) {
   return t < rows_here ? t : rows_here - 1;
 }
 
-// Partial (min, max) of a split of a ragged group.
+// Partial (min, max) of a split of TPT tokens of a ragged group.
+template <int TPT>
 __device__ __noinline__ uint2 key_partial_ragged(const __half2 *src, int rows_here, int D) {
   __half2 mn = __ldcs(src + static_cast<int64_t>(padded_row(0, rows_here)) * (D / 2));
   __half2 mx = mn;
 #pragma unroll 1
-  for (int t = 1; t < 32; ++t) {
+  for (int t = 1; t < TPT; ++t) {
     const __half2 h = __ldcs(src + static_cast<int64_t>(padded_row(t, rows_here)) * (D / 2));
     mn = __hmin2(mn, h);
     mx = __hmax2(mx, h);
@@ -83,9 +85,9 @@ __device__ __noinline__ uint2 key_partial_ragged(const __half2 *src, int rows_he
   return make_uint2(h2_as_u32(mn), h2_as_u32(mx));
 }
 
-// Exact codes of one thread's 32 tokens x 2 channels (rows padded as above),
+// Exact codes of one thread's TPT tokens x 2 channels (rows padded as above),
 // computed from global memory with the literal division, and stored.
-template <int BITS>
+template <int BITS, int TPT>
 __device__ __noinline__ void key_exact_store(const __half2 *src, int rows_here, int D,
                                              uint32_t ext_mn, uint32_t ext_mx, uint32_t *cdst,
                                              __half *ycol) {
@@ -96,7 +98,7 @@ __device__ __noinline__ void key_exact_store(const __half2 *src, int rows_here, 
   const GroupQ g0 = make_group(mnf.x, mxf.x, qf);
   const GroupQ g1 = make_group(mnf.y, mxf.y, qf);
 #pragma unroll 1
-  for (int wr = 0; wr < 32 / W; ++wr) {
+  for (int wr = 0; wr < TPT / W; ++wr) {
     uint32_t a0 = 0u, a1 = 0u;
 #pragma unroll 1
     for (int k = 0; k < W; ++k) {
@@ -148,9 +150,10 @@ template <int BITS, int G, int DC, int MODE>
 __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr bool RECON = MODE == kQuantRecon;
   constexpr bool SINK = MODE == kQuantSink;
-  constexpr int T = G / 32;                  // token splits per group
+  constexpr int TPT = G < 32 ? G : 32;      // tokens per thread
+  constexpr int T = G / TPT;                 // token splits per group
   constexpr int W = CodeFmt<BITS>::W;        // codes per word
-  constexpr int WPT = 32 / W;                // words per channel per thread (= BITS)
+  constexpr int WPT = TPT / W;               // words per channel per thread
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
   // split-major units with the shared-memory exchange: with the fused
   // reconstruction (whose row pieces would otherwise be 128 / T bytes); the
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
     const KeyUnit k = XCH ? decode_key_unit_xch<T>(ud, p) : decode_key_unit<T>(ud, p);
     const QuantJob &job = p.jobs[k.job];
     int64_t row0 = static_cast<int64_t>(k.g) * G;  // first stored row of the group
-    const int rows_here = static_cast<int>(p.rows - row0) - k.split * 32;  // valid rows of the split
+    const int rows_here = static_cast<int>(p.rows - row0) - k.split * TPT;  // valid rows of the split
     if (p.ring > 0) {
       row0 += p.head;
       if (row0 >= p.ring) row0 -= p.ring;    // head < ring and g*G < ring
@@ -185,27 +188,31 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
     const __half2 *src = reinterpret_cast<const __half2 *>(
                              static_cast<const __half *>(job.x) +
                              static_cast<int64_t>(k.b) * p.x_bh_stride + row0 * D) +
-                         k.col + static_cast<int64_t>(k.split) * 32 * (D / 2);
-    const bool full = active && rows_here >= 32;
+                         k.col + static_cast<int64_t>(k.split) * TPT * (D / 2);
+    const bool full = active && rows_here >= TPT;
 
     // sink mode: bit t = token t of this split is a sink (left out of the
-    // group's min / max, code 0); the flush only moves whole groups
+    // group's min / max, code 0); the flush only moves whole groups.  Mask
+    // bit r of a sequence is logical row r.
     uint32_t sink_bits = 0u;
-    if (SINK && full)
-      sink_bits = job.mask[static_cast<int64_t>(k.b / p.heads) * p.mask_words + k.g * T + k.split];
+    if (SINK && full) {
+      const int64_t lr = static_cast<int64_t>(k.g) * G + k.split * TPT;   // first logical row
+      sink_bits = job.mask[static_cast<int64_t>(k.b / p.heads) * p.mask_words + (lr >> 5)] >>
+                  (lr & 31);
+    }
 
-    // 32 tokens of this thread's channel pair; min / max in four chains
-    __half2 h[32];
+    // TPT tokens of this thread's channel pair; min / max in four chains
+    __half2 h[TPT];
     __half2 gmn, gmx;
     if (full) {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) h[t] = __ldcs(src + t * (D / 2));
+      for (int t = 0; t < TPT; ++t) h[t] = __ldcs(src + t * (D / 2));
       if (SINK) {
         const __half2 pinf = u32_as_h2(0x7C007C00u), ninf = u32_as_h2(0xFC00FC00u);
         __half2 mn[4] = {pinf, pinf, pinf, pinf};
         __half2 mx[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
+        for (int t = 0; t < TPT; ++t) {
           const bool sk = (sink_bits >> t) & 1u;
           mn[t & 3] = __hmin2(mn[t & 3], sk ? pinf : h[t]);
           mx[t & 3] = __hmax2(mx[t & 3], sk ? ninf : h[t]);
@@ -216,7 +223,7 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
         __half2 mn[4] = {h[0], h[1], h[2], h[3]};
         __half2 mx[4] = {h[0], h[1], h[2], h[3]};
 #pragma unroll
-        for (int t = 4; t < 32; ++t) {
+        for (int t = 4; t < TPT; ++t) {
           mn[t & 3] = __hmin2(mn[t & 3], h[t]);
           mx[t & 3] = __hmax2(mx[t & 3], h[t]);
         }
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
         gmx = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
       }
     } else if (active) {  // ragged last group: padded by repeating the last row
-      const uint2 e = key_partial_ragged(src, rows_here, D);
+      const uint2 e = key_partial_ragged<TPT>(src, rows_here, D);
       gmn = u32_as_h2(e.x);
       gmx = u32_as_h2(e.y);
     } else {
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
       // reconstruction: column (2 col, 2 col + 1) of the first token of the split
       __half *ycol = RECON ? static_cast<__half *>(job.y) +
                                  static_cast<int64_t>(k.b) * p.y_bh_stride +
-                                 (p.y_row0 + static_cast<int64_t>(k.g) * G + k.split * 32) * D +
+                                 (p.y_row0 + static_cast<int64_t>(k.g) * G + k.split * TPT) * D +
                                  2 * k.col
                            : nullptr;
       GroupQ2 gq;
@@ -291,10 +298,10 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
       }
       if (!full) {
         // ragged group: literal division, rows read again from memory
-        key_exact_store<BITS>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst, ycol);
+        key_exact_store<BITS, TPT>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst, ycol);
       } else {
         // Quantize and pack along tokens: WPT words per channel, word wi holds
-        // tokens [wi*W, wi*W + W) of this thread's 32 (token wi*W + j at bits
+        // tokens [wi*W, wi*W + W) of this thread's TPT (token wi*W + j at bits
         // [j*BITS, (j+1)*BITS)).  Each half-word (H = 16/BITS tokens)
         // accumulates the code pairs of both channels with packed FMAs by
         // powers of two.
@@ -414,7 +421,7 @@ cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const int64_t ng = (p.rows + G - 1) / G;
-  const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 2) * (G / 32);
+  const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 2) * (G < 32 ? 1 : G / 32);
   const int64_t blocks = (units + threads - 1) / threads;
   const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(num_sms()) * per_sm);
   QuantParams q = p;

@@ -109,7 +109,8 @@ struct AttnJob {
 };
 
 // Work item = (job, bh, split): split s covers store tiles [s*tps, (s+1)*tps)
-// (tiles of 32 tokens) and the last split also the residual tiles.
+// (tiles of 32 tokens; with G = 16 the last one may hold 16) and the last
+// split also the residual tiles.
 struct AttnParams {
   int32_t n_jobs;
   int32_t r;          // query heads per KV head
@@ -118,7 +119,7 @@ struct AttnParams {
   int32_t tiles_store;
   int32_t tiles_res;
   int32_t tiles_per_split;
-  int32_t pad0;
+  int32_t tail_half;  // 1: the last store tile holds 16 tokens (G = 16, s_q = 16 mod 32)
   int64_t bh;
   int64_t cap;        // store capacity (tokens)
   int64_t r_cap;      // ring capacity (tokens)

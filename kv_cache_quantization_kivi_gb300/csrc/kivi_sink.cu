@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_cons
 
 // thread = (job, sequence, word of 32 flushed tokens)
 __global__ void __launch_bounds__(kThreads) sink_mask_kernel(const __grid_constant__ SinkParams p) {
-  const int64_t words = p.n / 32;
+  const int64_t words = (p.n + 31) / 32;
   const int64_t u = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   if (u >= static_cast<int64_t>(p.n_jobs) * p.batch * words) return;
   const int64_t w = u % words;
@@ -274,7 +274,7 @@ cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream) {
 }
 
 cudaError_t launch_sink_mask(const SinkParams &p, cudaStream_t stream) {
-  const int64_t threads = static_cast<int64_t>(p.n_jobs) * p.batch * (p.n / 32);
+  const int64_t threads = static_cast<int64_t>(p.n_jobs) * p.batch * ((p.n + 31) / 32);
   if (threads == 0) return cudaSuccess;
   sink_mask_kernel<<<blocks_for(threads), kThreads, 0, stream>>>(p);
   return cudaGetLastError();

@@ -3,9 +3,10 @@
 // Values are grouped along the contiguous head_dim axis: one (scale, zero)
 // per token per group of G channels (VeloxQuant-MLX KIVI fused-kernel post,
 // "The layout problem that shapes everything").  One thread owns 32
-// consecutive channels of one token (four 16-byte loads); a group of G
+// consecutive channels of one token (four 16-byte loads); a group of G >= 32
 // channels is a sub-warp of G/32 lanes, reduced with __shfl_xor_sync on the
-// packed half2 {min, -max} (one shuffle per step carries both extremes).
+// packed half2 {min, -max} (one shuffle per step carries both extremes), and
+// at G = 16 a thread holds two whole groups.
 // Codes are packed along channels in registers and written with one 8- or
 // 16-byte store per word group.
 //
@@ -86,7 +87,8 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
     value_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr bool RECON = MODE == kQuantRecon;
   constexpr bool SINK = MODE == kQuantSink;
-  constexpr int L = G / 32;               // lanes per group
+  constexpr int L = G < 32 ? 1 : G / 32;  // lanes per group
+  constexpr int SUB = G < 32 ? 32 / G : 1; // groups per thread
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
   const float qf = static_cast<float>(Q);
@@ -129,30 +131,36 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
       h[4 * i + 3] = u32_as_h2(v[i].w);
     }
 
-    // min / max of the 32 channels (tree in half2, then the two halves)
+    // min / max of each group's channels (tree in half2 over the group's
+    // 8 / SUB slots of four channels, then the two halves)
     __half2 mn2[8], mx2[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       mn2[i] = __hmin2(h[2 * i], h[2 * i + 1]);
       mx2[i] = __hmax2(h[2 * i], h[2 * i + 1]);
     }
-#pragma unroll
-    for (int w = 4; w >= 1; w >>= 1) {
-#pragma unroll
-      for (int i = 0; i < w; ++i) {
-        mn2[i] = __hmin2(mn2[i], mn2[i + w]);
-        mx2[i] = __hmax2(mx2[i], mx2[i + w]);
-      }
-    }
-    const __half mn = __hmin(__low2half(mn2[0]), __high2half(mn2[0]));
-    const __half mx = __hmax(__low2half(mx2[0]), __high2half(mx2[0]));
     // {min, -max}: a single element-wise min combines both extremes
-    __half2 ext = __halves2half2(mn, __hneg(mx));
+    __half2 ext[SUB];
+#pragma unroll
+    for (int sg = 0; sg < SUB; ++sg) {
+      const int i0 = sg * (8 / SUB);
+#pragma unroll
+      for (int w = 4 / SUB; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+          mn2[i0 + i] = __hmin2(mn2[i0 + i], mn2[i0 + i + w]);
+          mx2[i0 + i] = __hmax2(mx2[i0 + i], mx2[i0 + i + w]);
+        }
+      }
+      const __half mn = __hmin(__low2half(mn2[i0]), __high2half(mn2[i0]));
+      const __half mx = __hmax(__low2half(mx2[i0]), __high2half(mx2[i0]));
+      ext[sg] = __halves2half2(mn, __hneg(mx));
+    }
     if (L > 1) {
 #pragma unroll
       for (int off = 1; off < L; off <<= 1) {
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, h2_as_u32(ext), off);
-        ext = __hmin2(ext, u32_as_h2(other));
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, h2_as_u32(ext[0]), off);
+        ext[0] = __hmin2(ext[0], u32_as_h2(other));
       }
     }
     __half *ydst = RECON ? static_cast<__half *>(job.y) + t.b * p.y_bh_stride +
@@ -161,16 +169,25 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
     if (!RECON && !active) continue;
     uint32_t out[16];  // reconstruction of the 32 channels (RECON)
     if (active) {
-      const float gmn = __low2float(ext), gmx = -__high2float(ext);
+      float gmn[SUB], gmx[SUB];
+#pragma unroll
+      for (int sg = 0; sg < SUB; ++sg) {
+        gmn[sg] = __low2float(ext[sg]);
+        gmx[sg] = -__high2float(ext[sg]);
+      }
       const int64_t out_row = p.out0 + t.r;
       const bool codes_out = !RECON || job.codes != nullptr;
+      // (scale, zero) of this thread's first group: row out_row, entry k SUB / L
+      const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k * SUB / L;
       // sink mode: a sink token's row is not quantized (codes, scales, zeros 0)
       if (SINK && ((job.mask[static_cast<int64_t>(t.b / p.heads) * p.mask_words + (t.r >> 5)] >>
                     (t.r & 31)) & 1u)) {
         if (t.k % L == 0) {
-          const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k / L;
-          __stcs(job.scale + so, 0.0f);
-          __stcs(job.zero + so, 0.0f);
+#pragma unroll
+          for (int sg = 0; sg < SUB; ++sg) {
+            __stcs(job.scale + so + sg, 0.0f);
+            __stcs(job.zero + so + sg, 0.0f);
+          }
         }
         uint32_t *dst = job.codes + t.b * p.codes_bh_stride + out_row * (D / W) + t.k * BITS;
         if (BITS == 2) {
@@ -181,32 +198,35 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
         }
         continue;
       }
-      GroupQ2 gq;
-      uint64_t sc2 = 0, nsc2 = 0, ze2 = 0;
-      {
-        const GroupQ g = make_group(gmn, gmx, qf);
-        gq = make_group2(g, g);
+      GroupQ2 gq[SUB];
+      uint64_t sc2[SUB], nsc2[SUB], ze2[SUB];
+#pragma unroll
+      for (int sg = 0; sg < SUB; ++sg) {
+        const GroupQ g = make_group(gmn[sg], gmx[sg], qf);
+        gq[sg] = make_group2(g, g);
+        sc2[sg] = nsc2[sg] = ze2[sg] = 0;
         if (RECON) {
-          sc2 = f2_pack(g.scale, g.scale);
-          nsc2 = neg_scale_2p23_pair(g.scale, g.scale);
-          ze2 = f2_pack(g.zero, g.zero);
+          sc2[sg] = f2_pack(g.scale, g.scale);
+          nsc2[sg] = neg_scale_2p23_pair(g.scale, g.scale);
+          ze2[sg] = f2_pack(g.zero, g.zero);
         }
         if (t.k % L == 0 && codes_out) {
-          const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k / L;
-          __stcs(job.scale + so, g.scale);
-          __stcs(job.zero + so, g.zero);
+          __stcs(job.scale + so + sg, g.scale);
+          __stcs(job.zero + so + sg, g.zero);
         }
       }
 
       // Pack along channels: word wi holds channels [wi*W, wi*W + W) of this
-      // thread's 32.  A half-word (H = 16/BITS channels) accumulates its H/2
-      // channel pairs with packed FMAs by powers of two, which leaves even
-      // channels in the low and odd channels in the high element; one more FMA
-      // interleaves them.
+      // thread's 32 (all in group sg = wi W / G when SUB = 2, as W <= 16).  A
+      // half-word (H = 16/BITS channels) accumulates its H/2 channel pairs
+      // with packed FMAs by powers of two, which leaves even channels in the
+      // low and odd channels in the high element; one more FMA interleaves
+      // them.
       constexpr int H = 16 / BITS;
       uint32_t w[BITS];
 #pragma unroll
       for (int wi = 0; wi < BITS; ++wi) {
+        const int sg = SUB == 1 ? 0 : (wi * W) / G;
         uint64_t acc[2];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -214,11 +234,13 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
           uint32_t neg_acc = 0xFFFFFFFFu;
           uint64_t n[H / 2];
 #pragma unroll
-          for (int j = 0; j < H / 2; ++j) n[j] = codes2_nobranch(h2_to_f2(h[p0 + j]), gq, neg_acc);
+          for (int j = 0; j < H / 2; ++j)
+            n[j] = codes2_nobranch(h2_to_f2(h[p0 + j]), gq[sg], neg_acc);
           if (!(neg_acc >> 31)) {  // rare: redo this half pair by pair, exactly where needed
 #pragma unroll
             for (int j = 0; j < H / 2; ++j)
-              n[j] = codes2<BITS, false>(h2_to_f2(h[p0 + j]), gq, gmn, gmx, gmn, gmx);
+              n[j] = codes2<BITS, false>(h2_to_f2(h[p0 + j]), gq[sg], gmn[sg], gmx[sg], gmn[sg],
+                                         gmx[sg]);
           }
           acc[hh] = n[0];
 #pragma unroll
@@ -226,7 +248,8 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
             acc[hh] = f2_fma(n[j], f2_const(static_cast<float>(1u << (2 * BITS * j))), acc[hh]);
           if (RECON) {
 #pragma unroll
-            for (int j = 0; j < H / 2; ++j) out[p0 + j] = recon_pair(n[j], sc2, nsc2, ze2);
+            for (int j = 0; j < H / 2; ++j)
+              out[p0 + j] = recon_pair(n[j], sc2[sg], nsc2[sg], ze2[sg]);
           }
         }
         // even channels (low) + odd channels (high) shifted by one code
@@ -260,7 +283,8 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
 template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(kBlockThreads)
     value_dequant_kernel(const __grid_constant__ DequantParams p) {
-  constexpr int L = G / 32;
+  constexpr int L = G < 32 ? 1 : G / 32;  // lanes per group
+  constexpr int SUB = G < 32 ? 32 / G : 1; // groups per thread
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
   const int D = DC > 0 ? DC : p.d;
@@ -299,16 +323,22 @@ __global__ void __launch_bounds__(kBlockThreads)
           w[(i + 3) % BITS] = a.w;
         }
       }
-      const int64_t so = t.b * p.sz_bh_stride + static_cast<int64_t>(t.r) * (D / G) + t.k / L;
-      const float sc = __ldcs(J.scale + so);
-      const float ze = __ldcs(J.zero + so);
-      const float nsc = __fmul_rn(sc, -8388608.0f);  // -2^23 * scale, exact
+      const int64_t so =
+          t.b * p.sz_bh_stride + static_cast<int64_t>(t.r) * (D / G) + t.k * SUB / L;
+      float sc[SUB], ze[SUB], nsc[SUB];
+#pragma unroll
+      for (int sg = 0; sg < SUB; ++sg) {
+        sc[sg] = __ldcs(J.scale + so + sg);
+        ze[sg] = __ldcs(J.zero + so + sg);
+        nsc[sg] = __fmul_rn(sc[sg], -8388608.0f);  // -2^23 * scale, exact
+      }
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
+        const int sg = SUB == 1 ? 0 : e / G;       // channels e, e + 1 share a group
         const uint32_t q0 = (w[e / W] >> ((e % W) * BITS)) & Q;
         const uint32_t q1 = (w[(e + 1) / W] >> (((e + 1) % W) * BITS)) & Q;
-        const float r0 = recon_f32(q0, sc, nsc, ze);
-        const float r1 = recon_f32(q1, sc, nsc, ze);
+        const float r0 = recon_f32(q0, sc[sg], nsc[sg], ze[sg]);
+        const float r1 = recon_f32(q1, sc[sg], nsc[sg], ze[sg]);
         out[e >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
       }
     }

@@ -25,7 +25,7 @@
 #define KIVI_ORACLE_MAX_GROUP 128
 
 static int valid_bits(int bits) { return bits == 2 || bits == 4 || bits == 8; }
-static int valid_group(int g) { return g == 32 || g == 64 || g == 128; }
+static int valid_group(int g) { return g == 16 || g == 32 || g == 64 || g == 128; }
 static uint32_t qmax_of(int bits) { return (1u << bits) - 1u; }
 static int codes_per_word(int bits) { return 32 / bits; }
 

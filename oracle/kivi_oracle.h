@@ -32,7 +32,7 @@
  * with W = 32/b codes per word and ng = ceil(s/G).
  *
  * Return values: 0 on success, -1 on an argument the operation does not
- * define (bits not in {2,4,8}, G not in {32,64,128}, d not divisible as
+ * define (bits not in {2,4,8}, G not in {16,32,64,128}, d not divisible as
  * required, non-finite input).  Functions never allocate caller memory.
  */
 #ifndef KIVI_ORACLE_H

@@ -84,7 +84,8 @@ def _qv(**kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(bits=3), 1), (dict(bits=16), 1), (dict(group=48), 1), (dict(group=16), 1),
+    (dict(bits=3), 1), (dict(bits=16), 1), (dict(group=48), 1), (dict(group=8), 1),
+    (dict(group=256), 1),
     (dict(d=100), 1), (dict(d=264), 1), (dict(d=0), 1), (dict(bh=-1), 1), (dict(s=-3), 1),
     (dict(x=None), 1), (dict(codes=None), 1), (dict(zero=None), 1),
     (dict(xs=64 * 128 - 8), 1), (dict(cs=100), 1), (dict(ss=128), 1),
@@ -98,6 +99,7 @@ def test_quantize_keys_validation(kw, status):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(bits=5), 1), (dict(group=64, d=96), 1), (dict(d=16), 1), (dict(d=48), 1),
+    (dict(group=16, d=48), 1), (dict(group=16, d=16), 1), (dict(group=8, d=64), 1),
     (dict(scale=None), 1), (dict(cs=10 * 8 - 1), 1), (dict(ss=10 * 4 - 1), 1),
     (dict(xs=10 * 128 + 4), 2), (dict(bits=4, cs=10 * 16 + 2), 2), (dict(zero=FAKE + 4), 2),
     (dict(bh=0), 0), (dict(s=0), 0),
@@ -152,7 +154,7 @@ def test_flush_nothing_to_move_launches_nothing():
 
 
 @pytest.mark.parametrize("kw", [
-    dict(bits=3), dict(group=16), dict(residual=-1), dict(reserved=1), dict(d=80),
+    dict(bits=3), dict(group=8), dict(residual=-1), dict(reserved=1), dict(d=80),
     dict(r_cap=100), dict(cap=250), dict(s_q=16), dict(s_q=288), dict(res_head=16),
     dict(res_head=128), dict(n_res=129), dict(n_res=-1), dict(bh=-2),
 ])
@@ -203,7 +205,7 @@ def _fq(fn, **kw):
 
 @pytest.mark.parametrize("fn", ["kivi_fakequant_keys", "kivi_fakequant_values"])
 @pytest.mark.parametrize("kw,status", [
-    (dict(y=None), 1), (dict(x=None), 1), (dict(bits=3), 1), (dict(group=16), 1),
+    (dict(y=None), 1), (dict(x=None), 1), (dict(bits=3), 1), (dict(group=8), 1),
     (dict(codes=None), 1), (dict(scale=None), 1), (dict(codes=None, zero=None), 1),
     (dict(ys=64 * 128 - 8), 1), (dict(xs=64 * 128 - 8), 1),
     (dict(y=FAKE + 2), 2), (dict(ys=64 * 128 + 4), 2), (dict(codes=FAKE + 4), 2),

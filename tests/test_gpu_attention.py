@@ -125,7 +125,7 @@ def check(pair, q16, batch, got, sm_scale):
     return worst
 
 
-COMBOS = [(b, g) for b in (2, 4, 8) for g in (32, 64, 128)]
+COMBOS = [(b, g) for b in (2, 4, 8) for g in (16, 32, 64, 128)]
 
 
 @pytest.mark.parametrize("bits,group", COMBOS)
@@ -140,6 +140,28 @@ def test_attention_store_and_residual(bits, group):
     sc = 1.0 / math.sqrt(D)
     for n_split in (1, 2, 3):
         check(pair, q, batch, run_gpu(pair, q, batch, n_split=n_split, sm_scale=sc), sc)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+def test_attention_g16_store_ending_mid_tile(bits):
+    """G = 16 lets the store end half way through a 32-token tile (here at
+    240 tokens, 16 short of the capacity, after flushes of 16 to 48 tokens
+    through an 80-row ring): that tile's first 16 tokens are attended and the
+    rest of the tile is not read.  Uniform weights (q = 0) make a dropped or
+    an extra (zero) token visible."""
+    batch, h_kv, r = 2, 2, 2
+    pair = Pair(2, batch * h_kv, bits, 16, residual=16, r_cap=80, cap=256, seed=80 + bits)
+    for n in (50, 30, 17, 40, 29, 45, 21, 33):
+        pair.append(n)
+    assert (pair.s_q, pair.n_res, pair.head) == (240, 25, 0)
+    sc = 1.0 / math.sqrt(D)
+    q = queries(2, batch, h_kv * r, 31 + bits)
+    for n_split in (1, 2, 5):
+        check(pair, q, batch, run_gpu(pair, q, batch, n_split=n_split, sm_scale=sc), sc)
+    q0 = np.zeros_like(q)
+    assert check(pair, q0, batch, run_gpu(pair, q0, batch, n_split=3, sm_scale=1.0), 1.0) < 1.0
+    pair.set_state(pair.s_q, pair.head, 0)            # store only, ending mid-tile
+    check(pair, q, batch, run_gpu(pair, q, batch, n_split=4, sm_scale=sc), sc)
 
 
 @pytest.mark.parametrize("r", [1, 2, 8])

@@ -26,7 +26,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 
 import kv_cache_quantization_kivi_gb300 as K  # noqa: E402
 
-COMBOS = [(b, g) for b in (2, 4, 8) for g in (32, 64, 128)]
+COMBOS = [(b, g) for b in (2, 4, 8) for g in (16, 32, 64, 128)]
 
 
 def _x(bh, s, d, seed, kind):

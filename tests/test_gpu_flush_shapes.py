@@ -23,6 +23,7 @@ import kv_cache_quantization_kivi_gb300 as K  # noqa: E402
 @pytest.mark.parametrize("d,bits,group,fused", [
     (64, 2, 32, False), (64, 4, 64, True), (256, 8, 32, False), (256, 2, 128, True),
     (96, 4, 32, True), (192, 2, 64, False), (256, 4, 64, False), (64, 8, 64, True),
+    (64, 4, 16, True), (256, 2, 16, False), (96, 8, 16, True), (32, 2, 16, False),
 ])
 def test_flush_sequence_other_head_dims(d, bits, group, fused):
     layers, bh, residual = 2, 3, group

@@ -26,7 +26,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 
 import kv_cache_quantization_kivi_gb300 as K  # noqa: E402
 
-COMBOS = [(b, g) for b in (2, 4, 8) for g in (32, 64, 128)]
+COMBOS = [(b, g) for b in (2, 4, 8) for g in (16, 32, 64, 128)]
 
 
 # ---------------------------------------------------------------------------
@@ -88,6 +88,7 @@ def test_values_several_rows(bits, group):
 @pytest.mark.parametrize("shape", [
     (1, 1, 128, 32, 2), (2, 5, 64, 64, 4), (1, 200, 8, 32, 2), (2, 100, 40, 64, 8),
     (1, 129, 256, 128, 2), (4, 64, 256, 32, 4), (2, 300, 16, 128, 8), (5, 31, 128, 32, 2),
+    (2, 37, 64, 16, 2), (1, 17, 8, 16, 8), (3, 100, 40, 16, 4), (1, 1, 256, 16, 2),
 ], ids=str)
 def test_keys_odd_shapes(shape):
     bh, s, d, g, b = shape
@@ -97,6 +98,7 @@ def test_keys_odd_shapes(shape):
 @pytest.mark.parametrize("shape", [
     (1, 1, 32, 32, 2), (2, 50, 96, 32, 4), (1, 33, 256, 128, 8), (2, 64, 192, 64, 2),
     (1, 40, 64, 64, 8), (7, 3, 128, 128, 4),
+    (2, 19, 96, 16, 2), (1, 5, 256, 16, 8), (3, 33, 32, 16, 4),
 ], ids=str)
 def test_values_odd_shapes(shape):
     bh, s, d, g, b = shape
@@ -199,7 +201,8 @@ def compare_store(cache, layer: int, st) -> None:
     assert_same("store value zero", host_f32_bits(cache.v_zero[layer]), bits32(st.v_zero))
 
 
-@pytest.mark.parametrize("bits,group,residual", [(4, 32, 32), (8, 64, 64), (2, 128, 32)])
+@pytest.mark.parametrize("bits,group,residual", [(4, 32, 32), (8, 64, 64), (2, 128, 32),
+                                                  (2, 16, 16), (8, 16, 32)])
 def test_multi_layer_flush_sequence_with_ring_wrap(bits, group, residual):
     layers, bh, d = 3, 4, 128
     r_cap = 3 * group + (residual // group + 1) * group

@@ -119,7 +119,7 @@ class SinkPair:
 
 
 @pytest.mark.parametrize("bits,group,d", [(2, 32, 128), (4, 64, 128), (8, 128, 128),
-                                          (2, 64, 64), (4, 32, 64)])
+                                          (2, 64, 64), (4, 32, 64), (2, 16, 128), (8, 16, 64)])
 def test_sink_prefill_flush(bits, group, d):
     batch, heads, S = 2, 2, 8 * group
     pair = SinkPair(2, batch, heads, d, bits, group, group, r_cap=S, cap=S, k_top=5,
@@ -130,10 +130,10 @@ def test_sink_prefill_flush(bits, group, d):
     pair.check()
 
 
-@pytest.mark.parametrize("bits,group", [(2, 32), (4, 64)])
-def test_sink_decode_sequence_with_ring_wrap(bits, group):
+@pytest.mark.parametrize("bits,group,r_groups", [(2, 32, 4), (4, 64, 4), (4, 16, 5)])
+def test_sink_decode_sequence_with_ring_wrap(bits, group, r_groups):
     batch, heads, d = 3, 2, 128
-    pair = SinkPair(2, batch, heads, d, bits, group, group, r_cap=4 * group, cap=16 * group,
+    pair = SinkPair(2, batch, heads, d, bits, group, group, r_cap=r_groups * group, cap=16 * group,
                     k_top=6, sink_cap=40, seed=70 + bits, plant_every=90)
     pair.append(3 * group)                      # a prefill
     rng = np.random.default_rng(bits)

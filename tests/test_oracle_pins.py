@@ -124,7 +124,7 @@ def test_rounding_ties_worked_examples(row):
 
 
 @pytest.mark.parametrize("row", list(_parse_ties()), ids=lambda r: f"b{r[0]}-{r[1][:3]}")
-@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("group", [16, 32, 64])
 def test_rounding_ties_through_tensor_paths(row, group):
     """The same worked examples, placed in a key group (token axis) and in a
     value group (channel axis) and padded by repeating their last value
@@ -245,6 +245,7 @@ def test_constant_groups_reconstruct_exactly(bits):
 SHAPES = [  # (bh, s, d, group, bits)
     (3, 96, 128, 32, 2), (2, 100, 64, 32, 4), (2, 77, 128, 64, 8),
     (1, 130, 128, 128, 2), (2, 64, 256, 64, 4), (1, 5, 32, 32, 8),
+    (2, 50, 64, 16, 2), (1, 40, 96, 16, 4), (2, 37, 32, 16, 8),
 ]
 
 
@@ -451,9 +452,14 @@ def _np_pack(q: np.ndarray, bits: int, axis: int) -> np.ndarray:
     return np.moveaxis(words, -1, axis)
 
 
-@pytest.mark.parametrize("name", ["tiny_flush"])
+REDERIVE = {"tiny_flush": W.CONFIGS["tiny_flush"],
+            "g16_b4": W.custom(seed=12, kv_heads=3, seq=80, head_dim=64, bits=4, group=16),
+            "g16_b2": W.custom(seed=13, kv_heads=2, seq=48, head_dim=128, bits=2, group=16)}
+
+
+@pytest.mark.parametrize("name", sorted(REDERIVE))
 def test_numpy_rederivation_matches_oracle_bit_for_bit(name):
-    w = W.CONFIGS[name]
+    w = REDERIVE[name]
     g, bits = w.group, w.bits
     for kind in ("k", "v"):
         x = W.generate(w, 0, kind)
@@ -529,6 +535,40 @@ def test_flush_sequence_with_ring_wrap_equals_full_quantization():
     # the residual holds the newest tokens, oldest first, starting at head
     rows = (head + np.arange(n_res)) % r_cap
     assert np.array_equal(k_res[:, rows], K[:, s_q:total])
+
+
+def test_flush_sequence_g16_odd_ring_equals_full_quantization():
+    """The same at G = 16 with a ring of 80 rows (not a multiple of 32), so
+    groups start at every multiple of 16 and the ring wraps mid-way."""
+    G, R, bits, bh, d = 16, 16, 4, 2, 32
+    total = 64 + 9 * 16
+    w = W.custom(seed=19, batch=1, kv_heads=bh, seq=total, head_dim=d)
+    K = W.generate(w, 0, "k")
+    V = W.generate(w, 0, "v")
+    r_cap, cap = 80, 256
+    k_res = np.zeros((bh, r_cap, d), np.uint16)
+    v_res = np.zeros((bh, r_cap, d), np.uint16)
+    st = O.Store(bh, d, cap, G, bits)
+    s_q, head, n_res, pos = 0, 0, 0, 0
+    flushed = []
+    for n_new in [64] + [16] * 9:
+        for _ in range(n_new):
+            row = (head + n_res) % r_cap
+            k_res[:, row] = K[:, pos]
+            v_res[:, row] = V[:, pos]
+            n_res += 1
+            pos += 1
+        n, s_q, head, n_res = O.flush(k_res, v_res, st, R, s_q, head, n_res)
+        flushed.append(n)
+    assert flushed == [48] + [16] * 9
+    assert s_q == total - 16 and n_res == 16 and head == s_q % r_cap
+    ck, sk, zk = O.quantize_keys(np.ascontiguousarray(K[:, :s_q]), G, bits)
+    cv, sv, zv = O.quantize_values(np.ascontiguousarray(V[:, :s_q]), G, bits)
+    w_ = 32 // bits
+    assert np.array_equal(st.k_codes[:, :s_q // w_], ck)
+    assert np.array_equal(st.k_scale[:, :s_q // G], sk) and np.array_equal(st.k_zero[:, :s_q // G], zk)
+    assert np.array_equal(st.v_codes[:, :s_q], cv)
+    assert np.array_equal(st.v_scale[:, :s_q], sv) and np.array_equal(st.v_zero[:, :s_q], zv)
 
 
 def test_flush_rejects_overflowing_store_and_bad_state():
