@@ -44,8 +44,14 @@ if ROOT not in sys.path:
 METRIC = "quantize+dequant HBM GB/s (bytes in+out) and % of GB300 HBM peak"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-CSRC_FILES = ("kivi_api.cu", "kivi_keys.cu", "kivi_values.cu", "kivi_attention.cu",
-              "kivi_sink.cu", "kivi_device.cuh", "kivi_launch.h", "kivi_dispatch.h")
+# Kernel sources behind each kind of workload: a committed ncu traffic figure
+# stays valid while these files hash to the value stored with it.
+_COMMON_FILES = ("kivi_api.cu", "kivi_device.cuh", "kivi_launch.h", "kivi_dispatch.h")
+CSRC_FILES = {
+    "flush": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu"),
+    "attention": _COMMON_FILES + ("kivi_attention.cu",),
+    "sink": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu", "kivi_sink.cu"),
+}
 
 
 def bytes_per_elem(bits: int, group: int) -> float:
@@ -987,9 +993,10 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def csrc_hash() -> str:
+def csrc_hash(kind: str = "flush") -> str:
+    """First 16 hex digits of the sha256 of the kernel sources of `kind`."""
     h = hashlib.sha256()
-    for f in CSRC_FILES:
+    for f in CSRC_FILES[kind]:
         with open(os.path.join(ROOT, "kv_cache_quantization_kivi_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -1005,7 +1012,8 @@ def ncu_traffic(workload: str, kernel: str):
     except (OSError, ValueError):
         return None
     wl = d.get("workloads", {}).get(workload, {})
-    if wl.get("csrc_hash", d.get("csrc_hash")) != csrc_hash():
+    kind = "attention" if "+attention" in workload else "sink" if "+sink" in workload else "flush"
+    if wl.get("csrc_hash") != csrc_hash(kind):
         return None
     entry = wl.get(kernel)
     return None if entry is None else float(entry.get("dram_bytes_per_launch"))
