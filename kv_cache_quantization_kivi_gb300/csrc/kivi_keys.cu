@@ -207,15 +207,16 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
     if (full) {
 #pragma unroll
       for (int t = 0; t < TPT; ++t) h[t] = __ldcs(src + t * (D / 2));
-      if (SINK) {
+      if (SINK && sink_bits != 0u) {   // a group holding sinks (rare)
         const __half2 pinf = u32_as_h2(0x7C007C00u), ninf = u32_as_h2(0xFC00FC00u);
         __half2 mn[4] = {pinf, pinf, pinf, pinf};
         __half2 mx[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll
         for (int t = 0; t < TPT; ++t) {
-          const bool sk = (sink_bits >> t) & 1u;
-          mn[t & 3] = __hmin2(mn[t & 3], sk ? pinf : h[t]);
-          mx[t & 3] = __hmax2(mx[t & 3], sk ? ninf : h[t]);
+          const uint32_t m = 0u - ((sink_bits >> t) & 1u);   // all ones for a sink
+          const uint32_t x = h2_as_u32(h[t]);
+          mn[t & 3] = __hmin2(mn[t & 3], u32_as_h2((x & ~m) | (0x7C007C00u & m)));
+          mx[t & 3] = __hmax2(mx[t & 3], u32_as_h2((x & ~m) | (0xFC00FC00u & m)));
         }
         gmn = __hmin2(__hmin2(mn[0], mn[1]), __hmin2(mn[2], mn[3]));
         gmx = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
@@ -258,11 +259,19 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
       }
     }
 
-    if (SINK) {
+    if (SINK && sink_bits != 0u) {
       // a group of sinks only (no finite extreme) gets scale 0 and zero 0
       const float2 a = __half22float2(gmn), bx = __half22float2(gmx);
       gmn = __floats2half2_rn(a.x > bx.x ? 0.0f : a.x, a.y > bx.y ? 0.0f : a.y);
       gmx = __floats2half2_rn(a.x > bx.x ? 0.0f : bx.x, a.y > bx.y ? 0.0f : bx.y);
+      // a sink takes the group minimum's place, whose code is 0 by the
+      // definition (x - zero = 0), and the fast path yields exactly 0 for it
+      const uint32_t gm = h2_as_u32(gmn);
+#pragma unroll
+      for (int t = 0; t < TPT; ++t) {
+        const uint32_t m = 0u - ((sink_bits >> t) & 1u);   // all ones for a sink
+        h[t] = u32_as_h2((h2_as_u32(h[t]) & ~m) | (gm & m));
+      }
     }
 
     if (active) {
@@ -319,9 +328,8 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
             const int t0 = wi * W + hh * H;
 #pragma unroll
             for (int j = 0; j < H; ++j) {
-              uint64_t n = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x,
-                                              mnf.y, mxf.y);
-              if (SINK && ((sink_bits >> (t0 + j)) & 1u)) n = 0ull;   // +0.0f, +0.0f
+              const uint64_t n = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x,
+                                                    mnf.y, mxf.y);
               half[hh] = j == 0 ? n
                                 : f2_fma(n, f2_const(static_cast<float>(1u << (BITS * j))),
                                          half[hh]);

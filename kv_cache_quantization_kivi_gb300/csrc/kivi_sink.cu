@@ -35,19 +35,29 @@ __device__ __forceinline__ bool ranks_before(float sa, int64_t pa, float sb, int
 // binary32 -- squared norm by fused multiply-adds in channel order, correctly
 // rounded square root, norms added in head order, one correctly rounded
 // division.
+// The row is read 8 sixteen-byte pieces at a time (the loads of a batch are
+// in flight together; the accumulation order stays the channel order).
 __device__ float token_score(const __half *k_seq, int64_t head_stride, int heads, int64_t d) {
+  constexpr int kBatch = 8;
   float sum = 0.0f;
   for (int h = 0; h < heads; ++h) {
     const uint4 *row = reinterpret_cast<const uint4 *>(k_seq + h * head_stride);
     float acc = 0.0f;
-    for (int64_t c8 = 0; c8 < d / 8; ++c8) {
-      const uint4 v = row[c8];
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int64_t c0 = 0; c0 < d / 8; c0 += kBatch) {
+      uint4 v[kBatch];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(kivi_dev::u32_as_h2(w[i]));
-        acc = __fmaf_rn(f.x, f.x, acc);
-        acc = __fmaf_rn(f.y, f.y, acc);
+      for (int b = 0; b < kBatch; ++b)
+        v[b] = c0 + b < d / 8 ? row[c0 + b] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (c0 + b >= d / 8) break;
+        const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(kivi_dev::u32_as_h2(w[i]));
+          acc = __fmaf_rn(f.x, f.x, acc);
+          acc = __fmaf_rn(f.y, f.y, acc);
+        }
       }
     }
     sum = __fadd_rn(sum, __fsqrt_rn(acc));
@@ -112,8 +122,23 @@ __global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_cons
   const int tn = J.top_count[seq];
   for (int e = tid; e < tn; e += kThreads)
     lt.offer(J.top_score[seq * p.k_top + e], J.top_pos[seq * p.k_top + e], k);
-  for (int64_t i = tid; i < p.n; i += kThreads)
-    lt.offer(J.scores[seq * p.r_cap + i], p.s_q + p.i0 + i, k);
+  // the thread's strided share of the new scores, loaded kBatch at a time
+  // (independent loads in flight together) and then offered in order
+  constexpr int kBatch = 8;
+  const float *sc = J.scores + seq * p.r_cap;
+  for (int64_t i0 = tid; i0 < p.n; i0 += kBatch * kThreads) {
+    float v[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t i = i0 + static_cast<int64_t>(b) * kThreads;
+      v[b] = i < p.n ? sc[i] : 0.0f;
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t i = i0 + static_cast<int64_t>(b) * kThreads;
+      if (i < p.n) lt.offer(v[b], p.s_q + p.i0 + i, k);
+    }
+  }
   const int64_t avail = tn + p.n;
   const int keep = avail < k ? static_cast<int>(avail) : k;
   int head = 0;
@@ -151,8 +176,9 @@ __global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_cons
       winner = wo;
     }
     __syncthreads();
+    // every thread reads `winner` here, before it reaches the next round's
+    // first barrier, after which alone thread 0 writes it again
     if (winner == tid) ++head;
-    __syncthreads();
   }
   if (tid < keep) {
     J.top_score[seq * p.k_top + tid] = new_s[tid];
