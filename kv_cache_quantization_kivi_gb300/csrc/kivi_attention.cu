@@ -245,6 +245,21 @@ __device__ __forceinline__ void expand_keys(const uint32_t *kc, const float *ks,
   }
 }
 
+// 2-bit keys with tables built once per tile (G >= 32: one scale and zero per
+// channel for the whole tile): lo/hi of channels lane + 32 i.
+__device__ __forceinline__ void expand_keys2_lut(const uint32_t *kc, const uint32_t (&lo)[4],
+                                                 const uint32_t (&hi)[4], int hb, uint32_t buf,
+                                                 int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = lane + 32 * i;
+    uint4 c0, c1;
+    lookup16(kc[hb * kD + c], lo[i], hi[i], c0, c1);
+    sts128(buf + ch_major(c, 0), c0);
+    sts128(buf + ch_major(c, 1), c1);
+  }
+}
+
 // Values of tokens 16 hb .. of a store tile -> row-major fp16 half tile.
 // Unit = 16 channels of one token (the 16/W consecutive words of channels
 // 16 cu ..); consecutive lanes take consecutive units, so their word loads
@@ -291,6 +306,37 @@ __device__ __forceinline__ void expand_values(const uint32_t *vc, const float *v
     magics16<BITS>(w, m);
     sts128(buf + tok_major(tok, 2 * cu), deq8(m, s2, ns2, z2));
     sts128(buf + tok_major(tok, 2 * cu + 1), deq8(m + 8, s2, ns2, z2));
+  }
+}
+
+// 2-bit values with G >= 32: unit = 32 channels of one token (one group, so
+// one table, and two code words); lane takes units lane and lane + 32 (token
+// u / 4, channels 32 (u % 4) ..).  Rows and channel chunks in perm8 order as
+// in expand_values; each 8-lane phase of a 16-byte store covers two token
+// rows whose permuted indices differ by 2, whose chunk sets are
+// complementary under the swizzle, so the stores are conflict-free.
+template <int G>
+__device__ __forceinline__ void expand_values2_32(const uint32_t *vc, const float *vs,
+                                                  const float *vz, int hb, uint32_t buf, int lane) {
+  constexpr int RW = kD / 16;         // words per token
+  constexpr int NG = kD / G;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int u = lane + 32 * k;
+    const int tok = u >> 2, cq = u & 3;
+    const int trow = 16 * hb + tok;
+    const int grp = (32 * cq) / G;
+    uint32_t lo, hi;
+    lut2(vs[trow * NG + grp], vz[trow * NG + grp], lo, hi);
+    const uint2 w = *reinterpret_cast<const uint2 *>(vc + trow * RW + 2 * cq);
+    const int row = (tok & 8) | perm8_inv(tok & 7);
+    uint4 c0, c1;
+    lookup16(w.x, lo, hi, c0, c1);
+    sts128(buf + tok_major(row, 4 * cq), c0);
+    sts128(buf + tok_major(row, 4 * cq + 1), c1);
+    lookup16(w.y, lo, hi, c0, c1);
+    sts128(buf + tok_major(row, 4 * cq + 2), c0);
+    sts128(buf + tok_major(row, 4 * cq + 3), c1);
   }
 }
 
@@ -519,22 +565,38 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
     const unsigned char *stg = ring + sidx * F::kBytes;
     const int n_hb = G < 32 && p.tail_half && st0 + warp + kWarps * done == p.tiles_store - 1
                          ? 1 : 2;                  // halves of this tile
+    constexpr bool KLUT = BITS == 2 && G >= 32;    // key tables shared by both halves
+    uint32_t klo[4], khi[4];
+    if (KLUT) {
+      const float *ks = reinterpret_cast<const float *>(stg + F::oKs);
+      const float *kz = reinterpret_cast<const float *>(stg + F::oKz);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) lut2(ks[lane + 32 * i], kz[lane + 32 * i], klo[i], khi[i]);
+    }
 #pragma unroll 1
     for (int hb = 0; hb < n_hb; ++hb) {
       float s[4];
       uint32_t phi[2], plo[2];
       // key scale / zero row of the half's group
       const int krow = G < 32 ? hb * kD : 0;
-      expand_keys<BITS>(reinterpret_cast<const uint32_t *>(stg),
-                        reinterpret_cast<const float *>(stg + F::oKs) + krow,
-                        reinterpret_cast<const float *>(stg + F::oKz) + krow, hb, buf, lane);
+      if (KLUT)
+        expand_keys2_lut(reinterpret_cast<const uint32_t *>(stg), klo, khi, hb, buf, lane);
+      else
+        expand_keys<BITS>(reinterpret_cast<const uint32_t *>(stg),
+                          reinterpret_cast<const float *>(stg + F::oKs) + krow,
+                          reinterpret_cast<const float *>(stg + F::oKz) + krow, hb, buf, lane);
       __syncwarp();
       half_scores<true>(buf, qsm, lane, s);
       half_softmax(st, s, p.scale_log2, kHalf, g, phi, plo);
       __syncwarp();                                // key half tile read by every lane
-      expand_values<BITS, G>(reinterpret_cast<const uint32_t *>(stg + F::oVc),
+      if constexpr (BITS == 2 && G >= 32)
+        expand_values2_32<G>(reinterpret_cast<const uint32_t *>(stg + F::oVc),
                              reinterpret_cast<const float *>(stg + F::oVs),
                              reinterpret_cast<const float *>(stg + F::oVz), hb, buf, lane);
+      else
+        expand_values<BITS, G>(reinterpret_cast<const uint32_t *>(stg + F::oVc),
+                               reinterpret_cast<const float *>(stg + F::oVs),
+                               reinterpret_cast<const float *>(stg + F::oVz), hb, buf, lane);
       __syncwarp();                                // value half tile written
       if (hb == n_hb - 1 && issued < n_my) {       // stage consumed: refill it
         if (lane == 0) issue(issued);
