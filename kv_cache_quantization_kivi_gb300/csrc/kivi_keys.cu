@@ -146,8 +146,13 @@ __device__ __forceinline__ KeyUnit decode_key_unit_xch(uint32_t u, const QuantPa
   return k;
 }
 
+// Register budget: 64 per thread (4 blocks per SM) at 2 bits; 85 (3 blocks)
+// at 4 and 8 bits, whose branch-free halves (below) keep more values live.
+template <int BITS>
+__host__ __device__ constexpr int key_min_blocks() { return BITS >= 4 ? 3 : 4; }
+
 template <int BITS, int G, int DC, int MODE>
-__global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_constant__ QuantParams p) {
+__global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant_kernel(const __grid_constant__ QuantParams p) {
   constexpr bool RECON = MODE == kQuantRecon;
   constexpr bool SINK = MODE == kQuantSink;
   constexpr int TPT = G < 32 ? G : 32;      // tokens per thread
@@ -317,25 +322,38 @@ __global__ void __launch_bounds__(kKeyThreads, 4) key_quant_kernel(const __grid_
         constexpr int H = 16 / BITS;
 #pragma unroll
         for (int wi = 0; wi < WPT; ++wi) {
-          // (a pair the fast path declines is recomputed on the spot.  Measured
-          // alternatives -- a branch-free check per half with a redo of the
-          // half from registers or from global memory -- were slower here: the
-          // 32 tokens a thread holds leave no registers for the longer live
-          // ranges.)
+          // 2 bits: a pair the fast path declines is recomputed on the spot (a
+          // branch per pair, almost never taken).  4 and 8 bits: the H <= 4
+          // pairs of a half run without branches, their acceptance tests AND-ed,
+          // and the half is redone from registers when a pair is declined; with
+          // the larger register budget this was 3-4% faster there and slower
+          // at 2 bits (measured).
+          constexpr bool BF = BITS >= 4;
           uint64_t half[2];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int t0 = wi * W + hh * H;
+            uint64_t n[H];
+            if constexpr (BF) {
+              uint32_t ok = 0xFFFFFFFFu;
+#pragma unroll
+              for (int j = 0; j < H; ++j) n[j] = codes2_nobranch(h2_to_f2(h[t0 + j]), gq, ok);
+              if (!(ok >> 31)) {   // rare: redo this half pair by pair from registers
+#pragma unroll
+                for (int j = 0; j < H; ++j)
+                  n[j] = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
+              }
+            }
 #pragma unroll
             for (int j = 0; j < H; ++j) {
-              const uint64_t n = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x,
-                                                    mnf.y, mxf.y);
-              half[hh] = j == 0 ? n
-                                : f2_fma(n, f2_const(static_cast<float>(1u << (BITS * j))),
+              if constexpr (!BF)
+                n[j] = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
+              half[hh] = j == 0 ? n[j]
+                                : f2_fma(n[j], f2_const(static_cast<float>(1u << (BITS * j))),
                                          half[hh]);
               if (RECON)
                 __stcs(reinterpret_cast<unsigned int *>(ycol + static_cast<int64_t>(t0 + j) * D),
-                       recon_pair(n, sc2, nsc2, ze2));
+                       recon_pair(n[j], sc2, nsc2, ze2));
             }
           }
           if (codes_out)
