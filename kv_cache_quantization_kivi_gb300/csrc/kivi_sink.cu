@@ -80,13 +80,14 @@ __global__ void __launch_bounds__(kThreads) sink_score_kernel(const __grid_const
       token_score(k_seq + row * p.d, p.r_cap * p.d, static_cast<int>(p.heads), p.d);
 }
 
-// Sorted (best first) list of up to LK candidates kept by one thread.
+// Sorted (best first) list of up to LK candidates kept by one thread;
+// has() / hs() / hq(): the best candidate not yet taken; pop() takes it.
 template <int LK>
 struct LocalTop {
   float s[LK];
   int64_t q[LK];
-  int n;
-  __device__ __forceinline__ void init() { n = 0; }
+  int n, head;
+  __device__ __forceinline__ void init() { n = head = 0; }
   __device__ __forceinline__ void offer(float sc, int64_t pos, int k) {
     if (n == k && !ranks_before(sc, pos, s[n - 1], q[n - 1])) return;
     int i = n < k ? n++ : n - 1;                  // slot freed at the end
@@ -99,12 +100,60 @@ struct LocalTop {
     s[i] = sc;
     q[i] = pos;
   }
+  __device__ __forceinline__ bool has() const { return head < n; }
+  __device__ __forceinline__ float hs() const { return s[head]; }
+  __device__ __forceinline__ int64_t hq() const { return q[head]; }
+  __device__ __forceinline__ void pop() { ++head; }
+};
+
+// The same for k <= 8, held in registers: every index is static (an unrolled
+// insertion network), empty slots are sentinels that every real candidate
+// ranks before (scores are finite and non-negative), and the list keeps its
+// best 8 (a superset of the best k).
+struct RegTop8 {
+  static constexpr int LK = 8;
+  static constexpr int64_t kNone = INT64_MAX;
+  float s[LK];
+  int64_t q[LK];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int i = 0; i < LK; ++i) {
+      s[i] = -INFINITY;
+      q[i] = kNone;
+    }
+  }
+  __device__ __forceinline__ void offer(float sc, int64_t pos, int) {
+    if (!ranks_before(sc, pos, s[LK - 1], q[LK - 1])) return;
+#pragma unroll
+    for (int i = LK - 1; i > 0; --i) {   // slot i from the old slots i-1 and i
+      const bool here = ranks_before(sc, pos, s[i], q[i]);
+      const bool above = ranks_before(sc, pos, s[i - 1], q[i - 1]);
+      s[i] = here ? (above ? s[i - 1] : sc) : s[i];
+      q[i] = here ? (above ? q[i - 1] : pos) : q[i];
+    }
+    if (ranks_before(sc, pos, s[0], q[0])) {
+      s[0] = sc;
+      q[0] = pos;
+    }
+  }
+  __device__ __forceinline__ bool has() const { return q[0] != kNone; }
+  __device__ __forceinline__ float hs() const { return s[0]; }
+  __device__ __forceinline__ int64_t hq() const { return q[0]; }
+  __device__ __forceinline__ void pop() {
+#pragma unroll
+    for (int i = 0; i < LK - 1; ++i) {
+      s[i] = s[i + 1];
+      q[i] = q[i + 1];
+    }
+    s[LK - 1] = -INFINITY;
+    q[LK - 1] = kNone;
+  }
 };
 
 // block = (job, sequence): the new scores and the kept top-k merged.  Each
 // thread keeps the best k of its strided share; k rounds of a block-wide
 // argmax over the threads' list heads then give the k best overall.
-template <int LK>
+template <typename List>
 __global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_constant__ SinkParams p) {
   const int job = static_cast<int>(blockIdx.x / p.batch);
   const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
@@ -117,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_cons
   __shared__ int winner;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = p.k_top;
-  LocalTop<LK> lt;
+  List lt;
   lt.init();
   const int tn = J.top_count[seq];
   for (int e = tid; e < tn; e += kThreads)
@@ -141,11 +190,10 @@ __global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_cons
   }
   const int64_t avail = tn + p.n;
   const int keep = avail < k ? static_cast<int>(avail) : k;
-  int head = 0;
   for (int j = 0; j < keep; ++j) {
-    bool have = head < lt.n;
-    float bs = have ? lt.s[head] : 0.0f;
-    int64_t bp = have ? lt.q[head] : 0;
+    bool have = lt.has();
+    float bs = have ? lt.hs() : 0.0f;
+    int64_t bp = have ? lt.hq() : 0;
     int owner = have ? tid : -1;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -178,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_cons
     __syncthreads();
     // every thread reads `winner` here, before it reaches the next round's
     // first barrier, after which alone thread 0 writes it again
-    if (winner == tid) ++head;
+    if (winner == tid) lt.pop();
   }
   if (tid < keep) {
     J.top_score[seq * p.k_top + tid] = new_s[tid];
@@ -293,9 +341,9 @@ cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const unsigned blocks = static_cast<unsigned>(p.n_jobs * p.batch);
   if (p.k_top <= 8)
-    sink_select_kernel<8><<<blocks, kThreads, 0, stream>>>(p);
+    sink_select_kernel<RegTop8><<<blocks, kThreads, 0, stream>>>(p);
   else
-    sink_select_kernel<kMaxSinkTop><<<blocks, kThreads, 0, stream>>>(p);
+    sink_select_kernel<LocalTop<kMaxSinkTop>><<<blocks, kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
