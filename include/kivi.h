@@ -413,9 +413,18 @@ KIVI_API kivi_status kivi_decode_attention_noalloc(const kivi_layer *layers, int
 
 /* The device word in which kernels record that a pipeline wait (a bulk copy
  * that never arrived) gave up after its time limit (bit 0: decode
- * attention); read and cleared by this call (synchronous).  Results of a
- * call that set it are unspecified. */
+ * attention; bit 1: a sink store overflow, see kivi_flush_sink; bit 2: the
+ * self-test below); read and cleared by this call (synchronous).  Results
+ * of a call that set bit 0 are unspecified. */
 KIVI_API kivi_status kivi_device_fault(uint32_t *fault);
+
+/* Self-test of the bounded-wait path: one warp waits, with the same bounded
+ * mbarrier wait as the decode-attention pipeline, on a barrier phase that
+ * nothing completes; after limit_us microseconds (1 .. 1000000) the wait
+ * gives up and bit 2 of the device fault word is set.  Asynchronous on the
+ * stream; touches no other memory.  KIVI_ERR_INVAL for a limit out of
+ * range. */
+KIVI_API kivi_status kivi_selftest_wait_timeout(uint32_t limit_us, kivi_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Sizes and diagnostics                                                    */

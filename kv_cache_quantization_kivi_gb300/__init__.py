@@ -27,7 +27,8 @@ __all__ = [
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
     "kivi_fakequant_keys", "kivi_fakequant_values", "kivi_flush_fakequant",
     "kivi_decode_attention", "kivi_decode_attention_splits", "kivi_decode_attention_workspace",
-    "kivi_decode_attention_noalloc", "kivi_device_fault", "kivi_sink_update", "kivi_flush_sink",
+    "kivi_decode_attention_noalloc", "kivi_device_fault", "kivi_selftest_wait_timeout",
+    "kivi_sink_update", "kivi_flush_sink",
     "kivi_sink_restore", "kivi_sink_layer", "kivi_sink_cfg", "KiviSinks",
     "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
     "KIVI_MAX_LAYERS", "event_handles",
@@ -150,6 +151,8 @@ def lib():
             L.kivi_sink_restore.restype = _int
             L.kivi_device_fault.argtypes = [C.POINTER(C.c_uint32)]
             L.kivi_device_fault.restype = _int
+            L.kivi_selftest_wait_timeout.argtypes = [C.c_uint32, _vp]
+            L.kivi_selftest_wait_timeout.restype = _int
             L.kivi_flush_size.argtypes = [_i64, _int, _int]
             L.kivi_flush_size.restype = _i64
             L.kivi_key_code_words.argtypes = [_i64, _i64, _int, _int]
@@ -428,6 +431,13 @@ def kivi_decode_attention_noalloc(layers, n_layers: int, cache: kivi_cache, batc
                                                _ptr_array(out, n_layers), n_split,
                                                _stream_handle(stream)),
            "kivi_decode_attention_noalloc")
+
+
+def kivi_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Raw C call: one warp's bounded wait on a phase nothing completes; bit 2
+    of the device fault word is set once it gives up (asynchronous)."""
+    _check(lib().kivi_selftest_wait_timeout(limit_us, _stream_handle(stream)),
+           "kivi_selftest_wait_timeout")
 
 
 def kivi_device_fault() -> int:

@@ -760,6 +760,12 @@ kivi_status kivi_sink_restore(const kivi_sink_layer *sinks, int n_layers, const 
   return cuda_status(kivi_impl::launch_sink_restore(p, stream));
 }
 
+kivi_status kivi_selftest_wait_timeout(uint32_t limit_us, kivi_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return KIVI_ERR_INVAL;
+  return cuda_status(
+      kivi_impl::launch_wait_timeout_selftest(uint64_t{limit_us} * 1000u, stream));
+}
+
 kivi_status kivi_device_fault(uint32_t *fault) {
   if (!fault) return KIVI_ERR_INVAL;
   return cuda_status(kivi_impl::read_and_clear_fault(fault));

@@ -826,6 +826,25 @@ cudaError_t fault_word_address(unsigned int **ptr) {
   return cudaSuccess;
 }
 
+// One warp waits (bounded) on a phase that nothing completes: the wait gives
+// up after limit_ns and the timeout is recorded as bit 2 of the fault word.
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);      // one arrival expected; none ever happens
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(b, 0, limit_ns));
+  if (!done && threadIdx.x == 0) atomicOr(&g_fault_word, 4u);
+}
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_fault(uint32_t *fault) {
   unsigned int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_fault_word, sizeof(v));

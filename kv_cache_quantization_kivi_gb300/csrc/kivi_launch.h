@@ -200,6 +200,9 @@ cudaError_t fault_word_address(unsigned int **ptr);
 // Reads and clears the device word in which kernels record a pipeline wait
 // that timed out (bit 0: decode attention).
 cudaError_t read_and_clear_fault(uint32_t *fault);
+// One warp's bounded wait on a phase that nothing completes (bit 2 of the
+// fault word once it gives up).
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_value_dequant(const DequantParams &p, int group, int bits,
                                  cudaStream_t stream);
 

@@ -299,6 +299,11 @@ def test_decode_attention_validation():
     assert K.lib().kivi_decode_attention_splits(C.byref(_cache()), 2, 2) >= 1
 
 
+def test_selftest_wait_limits():
+    assert K.lib().kivi_selftest_wait_timeout(0, None) == 1
+    assert K.lib().kivi_selftest_wait_timeout(1_000_001, None) == 1
+
+
 def test_device_fault_rejects_null():
     assert K.lib().kivi_device_fault(None) == 1
 
