@@ -46,7 +46,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 # Kernel sources behind each kind of workload: a committed ncu traffic figure
 # stays valid while these files hash to the value stored with it.
-_COMMON_FILES = ("kivi_api.cu", "kivi_device.cuh", "kivi_launch.h", "kivi_dispatch.h")
+_COMMON_FILES = ("kivi_api.cu", "kivi_device.cuh", "kivi_arith.cuh", "kivi_launch.h",
+                 "kivi_dispatch.h")
 CSRC_FILES = {
     "flush": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu"),
     "attention": _COMMON_FILES + ("kivi_attention.cu",),

@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "kivi_arith.cuh"
+
 namespace kivi_dev {
 
 // ---------------------------------------------------------------------------
@@ -57,20 +59,6 @@ struct GroupQ {
   float thr;    // fast-path acceptance threshold on |v - rint(v)|
 };
 
-// RN(x / Q) for x >= 0 and Q = 2^b - 1 (b = 2, 4, 8) without a division:
-// q0 = RN(x * RN(1/Q)), the residual x - q0*Q is exact in one fused
-// multiply-add, and one more corrects q0 (the correction step of P. W.
-// Markstein, "Computation of elementary functions on the IBM RISC
-// System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  That the result is
-// the correctly rounded quotient was checked exhaustively, for each of the
-// three Q, over every finite binary32 x >= 0 (tests/native/divq_check.c).
-__device__ __forceinline__ float div_by_q(float x, float qf) {
-  const float inv = qf == 3.0f ? 0x1.555556p-2f : qf == 15.0f ? 0x1.111112p-4f : 0x1.010102p-8f;
-  const float q0 = __fmul_rn(x, inv);
-  const float r = __fmaf_rn(-q0, qf, x);
-  return __fmaf_rn(r, inv, q0);
-}
-
 __device__ __forceinline__ GroupQ make_group(float mn, float mx, float qf) {
   GroupQ g;
   // A zero extreme may arrive as -0 or +0; adding +0 gives +0 either way.
@@ -79,7 +67,7 @@ __device__ __forceinline__ GroupQ make_group(float mn, float mx, float qf) {
   g.zero = mn;
   g.scale = div_by_q(__fsub_rn(mx, mn), qf);   // = RN((mx - mn) / Q)
   if (g.scale > 0.0f) {
-    g.r = __frcp_rn(g.scale);
+    g.r = rcp_rn(g.scale);                      // = RN(1 / scale)
     g.c = __fmul_rn(-mn, g.r);
     // 2E = 2^-23 (4.01 Q + 1.01 |c|)
     const float two_e = __fmul_rn(__fmaf_rn(1.01f, fabsf(g.c), __fmul_rn(4.01f, qf)), 0x1p-23f);
