@@ -1,7 +1,10 @@
-"""GPU check of the reciprocal the quantize kernels use for a group's fast
-path (kivi_arith.cuh): bit-identical to the correctly rounded reciprocal
-for every normal float in [2^-126, 2^126), the whole range a group scale can
-take and more.  The checker includes the kernels' own header."""
+"""GPU checks of the quantize kernels' arithmetic, each compiled against the
+kernels' own headers: the group reciprocal (kivi_arith.cuh) is bit-identical
+to the correctly rounded reciprocal for every normal float in [2^-126,
+2^126), the whole range a group scale can take and more; the per-element
+code (kivi_device.cuh, codes2: the error-bounded fast path and its exact
+fallback) equals the literal definition with the IEEE division on random
+binary16 groups and on elements next to a rounding midpoint."""
 from __future__ import annotations
 
 import os
@@ -19,11 +22,22 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def test_reciprocal_equals_correctly_rounded_everywhere(tmp_path):
+def build_and_run(tmp_path, name):
     nvcc = os.environ.get("NVCC") or shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
-    exe = str(tmp_path / "rcp_check")
+    exe = str(tmp_path / name)
     subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
-                    os.path.join(HERE, "native", "rcp_check.cu"), "-o", exe], check=True)
-    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+                    os.path.join(HERE, "native", name + ".cu"), "-o", exe], check=True)
+    return subprocess.run([exe], capture_output=True, text=True, timeout=300)
+
+
+def test_reciprocal_equals_correctly_rounded_everywhere(tmp_path):
+    r = build_and_run(tmp_path, "rcp_check")
     assert r.returncode == 0, r.stdout + r.stderr
     assert "checked=2113929216 mismatches=0" in r.stdout
+
+
+def test_codes_equal_the_literal_definition(tmp_path):
+    r = build_and_run(tmp_path, "quot_check")
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = r.stdout.strip().splitlines()
+    assert len(lines) == 2 and all("mismatches=0" in l for l in lines), r.stdout
