@@ -411,6 +411,22 @@ KIVI_API kivi_status kivi_decode_attention_noalloc(const kivi_layer *layers, int
                                                    const void *const *q, float *const *out,
                                                    int32_t n_split, kivi_stream_t stream);
 
+/* kivi_decode_attention over a cache whose flushes were sink-protected
+ * (kivi_flush_sink): the store slots of each sequence's stored sinks (code 0)
+ * are replaced by the sinks' exact fp16 key and value rows from the sink
+ * store, so the keys and values attended are those of the restored cache
+ * (kivi_dequantize_cache then kivi_sink_restore).  sinks, cfg as for
+ * kivi_flush_sink; cfg->batch must equal batch; the sink stores are only
+ * read.  Other arguments, results and errors as kivi_decode_attention. */
+KIVI_API kivi_status kivi_decode_attention_sinks(const kivi_layer *layers,
+                                                 const kivi_sink_layer *sinks, int n_layers,
+                                                 const kivi_cache *cache,
+                                                 const kivi_sink_cfg *cfg, int64_t batch,
+                                                 int32_t h_q, float sm_scale,
+                                                 const void *const *q, float *const *out,
+                                                 int32_t n_split, float *workspace,
+                                                 int64_t workspace_floats, kivi_stream_t stream);
+
 /* The device word in which kernels record that a pipeline wait (a bulk copy
  * that never arrived) gave up after its time limit (bit 0: decode
  * attention; bit 1: a sink store overflow, see kivi_flush_sink; bit 2: the

@@ -27,7 +27,8 @@ __all__ = [
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
     "kivi_fakequant_keys", "kivi_fakequant_values", "kivi_flush_fakequant",
     "kivi_decode_attention", "kivi_decode_attention_splits", "kivi_decode_attention_workspace",
-    "kivi_decode_attention_noalloc", "kivi_device_fault", "kivi_selftest_wait_timeout",
+    "kivi_decode_attention_noalloc", "kivi_decode_attention_sinks", "kivi_device_fault",
+    "kivi_selftest_wait_timeout",
     "kivi_sink_update", "kivi_flush_sink",
     "kivi_sink_restore", "kivi_sink_layer", "kivi_sink_cfg", "KiviSinks",
     "KiviCache", "kivi_layer", "kivi_cache", "STATUS",
@@ -127,6 +128,13 @@ def lib():
                                                 C.c_float, C.POINTER(_vp), C.POINTER(_vp),
                                                 C.c_int32, _vp, _i64, _vp]
             L.kivi_decode_attention.restype = _int
+            L.kivi_decode_attention_sinks.argtypes = [C.POINTER(kivi_layer),
+                                                      C.POINTER(kivi_sink_layer), _int,
+                                                      C.POINTER(kivi_cache),
+                                                      C.POINTER(kivi_sink_cfg), _i64, C.c_int32,
+                                                      C.c_float, C.POINTER(_vp), C.POINTER(_vp),
+                                                      C.c_int32, _vp, _i64, _vp]
+            L.kivi_decode_attention_sinks.restype = _int
             L.kivi_decode_attention_splits.argtypes = [C.POINTER(kivi_cache), _int, _i64]
             L.kivi_decode_attention_splits.restype = C.c_int32
             L.kivi_decode_attention_workspace.argtypes = [C.POINTER(kivi_cache), _int, _i64,
@@ -420,6 +428,20 @@ def kivi_decode_attention(layers, n_layers: int, cache: kivi_cache, batch: int, 
            "kivi_decode_attention")
 
 
+def kivi_decode_attention_sinks(layers, sinks, n_layers: int, cache: kivi_cache,
+                                cfg: "kivi_sink_cfg", batch: int, h_q: int, sm_scale: float, q,
+                                out, n_split: int = 1, workspace=None, stream=None) -> None:
+    """As :func:`kivi_decode_attention`, over a sink-protected cache: the stored
+    sinks' exact fp16 rows replace their store slots."""
+    wp = workspace.data_ptr() if workspace is not None else None
+    wn = workspace.numel() if workspace is not None else 0
+    _check(lib().kivi_decode_attention_sinks(layers, sinks, n_layers, C.byref(cache),
+                                             C.byref(cfg), batch, h_q, float(sm_scale),
+                                             _ptr_array(q, n_layers), _ptr_array(out, n_layers),
+                                             n_split, wp, wn, _stream_handle(stream)),
+           "kivi_decode_attention_sinks")
+
+
 def kivi_decode_attention_noalloc(layers, n_layers: int, cache: kivi_cache, batch: int,
                                   h_q: int, sm_scale: float, q, out, n_split: int = 1,
                                   stream=None) -> None:
@@ -550,10 +572,12 @@ class KiviCache:
                                     self._v_hat_ptrs, stream, events)
 
     def decode_attention(self, q, batch: int, sm_scale: Optional[float] = None, out=None,
-                         n_split: Optional[int] = None, workspace=None, stream=None):
+                         n_split: Optional[int] = None, workspace=None, stream=None,
+                         sinks: Optional["KiviSinks"] = None):
         """Attention of the new query tokens over everything the cache holds
-        (packed store + fp16 residual).  ``q``: fp16 [n_layers, batch, h_q, d]
-        (or a per-layer list); returns fp32 [n_layers, batch, h_q, d]."""
+        (packed store + fp16 residual; with ``sinks``, the stored sinks' fp16
+        rows in place of their store slots).  ``q``: fp16 [n_layers, batch,
+        h_q, d] (or a per-layer list); returns fp32 [n_layers, batch, h_q, d]."""
         import math
         import torch
         qs = list(q.unbind(0)) if hasattr(q, "unbind") else list(q)
@@ -569,8 +593,13 @@ class KiviCache:
         if n_split > 1 and workspace is None:
             need = kivi_decode_attention_workspace(self.state, self.n_layers, batch, h_q, n_split)
             workspace = torch.empty(max(need, 1), dtype=torch.float32, device=qs[0].device)
-        kivi_decode_attention(self.layers, self.n_layers, self.state, batch, h_q, sm_scale, qs,
-                              outs, n_split, workspace, stream)
+        if sinks is None:
+            kivi_decode_attention(self.layers, self.n_layers, self.state, batch, h_q, sm_scale,
+                                  qs, outs, n_split, workspace, stream)
+        else:
+            kivi_decode_attention_sinks(self.layers, sinks.layers, self.n_layers, self.state,
+                                        sinks.cfg, batch, h_q, sm_scale, qs, outs, n_split,
+                                        workspace, stream)
         return out
 
     def dequantize(self, k_out=None, v_out=None, stream=None, events=None):

@@ -766,6 +766,38 @@ kivi_status kivi_selftest_wait_timeout(uint32_t limit_us, kivi_stream_t stream) 
       kivi_impl::launch_wait_timeout_selftest(uint64_t{limit_us} * 1000u, stream));
 }
 
+kivi_status kivi_decode_attention_sinks(const kivi_layer *layers, const kivi_sink_layer *sinks,
+                                        int n_layers, const kivi_cache *cache,
+                                        const kivi_sink_cfg *cfg, int64_t batch, int32_t h_q,
+                                        float sm_scale, const void *const *q, float *const *out,
+                                        int32_t n_split, float *workspace,
+                                        int64_t workspace_floats, kivi_stream_t stream) {
+  kivi_impl::AttnParams p;
+  kivi_status st =
+      attn_prepare(layers, n_layers, cache, batch, h_q, sm_scale, q, out, n_split, &p);
+  if (st != KIVI_OK) return st;
+  st = check_sinks(sinks, n_layers, cache, cfg);
+  if (st != KIVI_OK) return st;
+  if (cfg->batch != batch) return KIVI_ERR_INVAL;
+  if (n_split > 1) {
+    const int64_t need = kivi_decode_attention_workspace(cache, n_layers, batch, h_q, n_split);
+    if (!workspace || workspace_floats < need) return KIVI_ERR_INVAL;
+    if (!aligned16(workspace)) return KIVI_ERR_ALIGN;
+    p.ws = workspace;
+  }
+  if (cache->bh == 0) return KIVI_OK;
+  if (cfg->sink_cap > 0) {
+    p.sink_cap = cfg->sink_cap;
+    for (int l = 0; l < n_layers; ++l) {
+      p.jobs[l].sink_pos = sinks[l].sink_pos;
+      p.jobs[l].sink_count = sinks[l].sink_count;
+      p.jobs[l].sink_k = sinks[l].sink_k;
+      p.jobs[l].sink_v = sinks[l].sink_v;
+    }
+  }
+  return cuda_status(kivi_impl::launch_decode_attention(p, cache->group, cache->bits, stream));
+}
+
 kivi_status kivi_device_fault(uint32_t *fault) {
   if (!fault) return KIVI_ERR_INVAL;
   return cuda_status(kivi_impl::read_and_clear_fault(fault));

@@ -309,6 +309,40 @@ __device__ __forceinline__ void expand_values(const uint32_t *vc, const float *v
   }
 }
 
+// KIVI-Sink: the store slots of sink tokens hold code 0; their exact fp16
+// rows, kept in the sink store, replace them in the expanded half tiles
+// before the tensor cores read the tiles.  Token tt (0..15) of a half is, in
+// the transposed key tile, element perm(tt & 7) of chunk tt >> 3 of every
+// channel row, and in the value tile row (tt & 8) | perm(tt & 7) with the
+// channels of each chunk in perm8 order (2 bits: the order the table lookups
+// produce; other widths: natural order).
+__device__ __forceinline__ void sts16(uint32_t addr, unsigned short v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+template <int BITS>
+__device__ __forceinline__ void sink_key_column(uint32_t buf, const __half *row, int tt, int lane) {
+  const int chunk = tt >> 3;
+  const int pos = BITS == 2 ? perm8_inv(tt & 7) : (tt & 7);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = lane + 32 * i;
+    sts16(buf + ch_major(c, chunk) + 2 * pos, __half_as_ushort(row[c]));
+  }
+}
+template <int BITS>
+__device__ __forceinline__ void sink_value_row(uint32_t buf, const __half *row, int tt, int lane) {
+  if (lane < kD / 8) {
+    uint4 v = *reinterpret_cast<const uint4 *>(row + 8 * lane);
+    int r = tt;
+    if (BITS == 2) {   // rows and chunk channels in perm8 order: (0,4) (1,5) (2,6) (3,7)
+      r = (tt & 8) | perm8_inv(tt & 7);
+      v = make_uint4(__byte_perm(v.x, v.z, 0x5410u), __byte_perm(v.x, v.z, 0x7632u),
+                     __byte_perm(v.y, v.w, 0x5410u), __byte_perm(v.y, v.w, 0x7632u));
+    }
+    sts128(buf + tok_major(r, lane), v);
+  }
+}
+
 // 2-bit values with G >= 32: unit = 32 channels of one token (one group, so
 // one table, and two code words); lane takes units lane and lane + 32 (token
 // u / 4, channels 32 (u % 4) ..).  Rows and channel chunks in perm8 order as
@@ -468,7 +502,7 @@ __device__ __forceinline__ void half_values(SoftState &st, uint32_t buf, int lan
   }
 }
 
-template <int BITS, int G>
+template <int BITS, int G, bool SINKS>
 __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __grid_constant__ AttnParams p) {
   using F = StageFmt<BITS, G>;
   constexpr int W = 32 / BITS;
@@ -551,6 +585,18 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
   }
   __syncthreads();
 
+  // KIVI-Sink: this sequence's sink positions (ascending) and this bh's rows;
+  // `sc` is the warp's cursor into the list (its tiles come in order)
+  const int64_t *spos = nullptr;
+  const __half *srow_k = nullptr, *srow_v = nullptr;
+  int scnt = 0, sc = 0;
+  if (SINKS) {
+    spos = J.sink_pos + b * p.sink_cap;
+    scnt = min(J.sink_count[b], p.sink_cap);
+    srow_k = static_cast<const __half *>(J.sink_k) + bhi * p.sink_cap * kD;
+    srow_v = static_cast<const __half *>(J.sink_v) + bhi * p.sink_cap * kD;
+  }
+
   int done = 0;
   bool failed = false;
 #pragma unroll 1
@@ -579,6 +625,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
       uint32_t phi[2], plo[2];
       // key scale / zero row of the half's group
       const int krow = G < 32 ? hb * kD : 0;
+      // sinks of this half: list entries [sc, se)
+      const int64_t tok0 = static_cast<int64_t>(st0 + warp + kWarps * done) * kTile + kHalf * hb;
+      int se = sc;
+      if (SINKS) {
+        while (sc < scnt && spos[sc] < tok0) ++sc;   // other warps' tiles
+        se = sc;
+        while (se < scnt && spos[se] < tok0 + kHalf) ++se;
+      }
       if (KLUT)
         expand_keys2_lut(reinterpret_cast<const uint32_t *>(stg), klo, khi, hb, buf, lane);
       else
@@ -586,6 +640,12 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
                           reinterpret_cast<const float *>(stg + F::oKs) + krow,
                           reinterpret_cast<const float *>(stg + F::oKz) + krow, hb, buf, lane);
       __syncwarp();
+      if (SINKS && se > sc) {                      // the sinks' exact key columns
+        for (int j = sc; j < se; ++j)
+          sink_key_column<BITS>(buf, srow_k + static_cast<int64_t>(j) * kD,
+                                static_cast<int>(spos[j] - tok0), lane);
+        __syncwarp();
+      }
       half_scores<true>(buf, qsm, lane, s);
       half_softmax(st, s, p.scale_log2, kHalf, g, phi, plo);
       __syncwarp();                                // key half tile read by every lane
@@ -598,6 +658,13 @@ __global__ void __launch_bounds__(kThreads, 4) decode_attention_kernel(const __g
                                reinterpret_cast<const float *>(stg + F::oVs),
                                reinterpret_cast<const float *>(stg + F::oVz), hb, buf, lane);
       __syncwarp();                                // value half tile written
+      if (SINKS && se > sc) {                      // the sinks' exact value rows
+        for (int j = sc; j < se; ++j)
+          sink_value_row<BITS>(buf, srow_v + static_cast<int64_t>(j) * kD,
+                               static_cast<int>(spos[j] - tok0), lane);
+        __syncwarp();
+      }
+      sc = se;
       if (hb == n_hb - 1 && issued < n_my) {       // stage consumed: refill it
         if (lane == 0) issue(issued);
         ++issued;
@@ -739,10 +806,10 @@ int num_sms() {
   return g_num_sms;
 }
 
-template <int BITS, int G>
-cudaError_t attention_launch(const AttnParams &p, cudaStream_t stream) {
+template <int BITS, int G, bool SINKS>
+cudaError_t attention_launch_k(const AttnParams &p, cudaStream_t stream) {
   using F = StageFmt<BITS, G>;
-  auto kern = decode_attention_kernel<BITS, G>;
+  auto kern = decode_attention_kernel<BITS, G, SINKS>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F::kSmem);
@@ -758,6 +825,11 @@ cudaError_t attention_launch(const AttnParams &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int BITS, int G>
+cudaError_t attention_launch(const AttnParams &p, cudaStream_t stream) {
+  return p.sink_cap > 0 ? attention_launch_k<BITS, G, true>(p, stream)
+                        : attention_launch_k<BITS, G, false>(p, stream);
+}
 }  // namespace
 
 cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits, cudaStream_t stream) {

@@ -106,6 +106,12 @@ struct AttnJob {
   const void *v_res;
   const void *q;
   float *out;
+  // KIVI-Sink store of the layer (all null without sinks): per sequence the
+  // positions (ascending) and count, per bh the fp16 key / value rows
+  const int64_t *sink_pos;    // [batch][sink_cap]
+  const int32_t *sink_count;  // [batch]
+  const void *sink_k;         // fp16 [bh][sink_cap][d]
+  const void *sink_v;
 };
 
 // Work item = (job, bh, split): split s covers store tiles [s*tps, (s+1)*tps)
@@ -126,7 +132,7 @@ struct AttnParams {
   int64_t res_head;
   int64_t n_res;
   float scale_log2;   // softmax scale * log2(e)
-  float pad1;
+  int32_t sink_cap;   // > 0: the jobs' sink stores are read (see AttnJob)
   float *ws;          // n_split > 1: partial results, see kivi_attention.cu
   AttnJob jobs[KIVI_MAX_LAYERS];
 };

@@ -364,3 +364,21 @@ def test_sink_validation():
                                None) == 0
     assert L.kivi_sink_restore(_sinks(), 2, C.byref(_cache(s_q=32)), C.byref(cfg()),
                                (C.c_void_p * 2)(FAKE, None), ptrs, None) == 1
+
+
+def test_decode_attention_sinks_validation():
+    L = K.lib()
+    q = (C.c_void_p * 2)(FAKE + (1 << 24), FAKE + (2 << 24))
+    out = (C.c_void_p * 2)(FAKE + (1 << 28), FAKE + (2 << 28))
+    cfg = lambda **kw: K.kivi_sink_cfg(**{**dict(batch=2, k_top=5, sink_cap=8, reserved=0,  # noqa
+                                                   reserved2=0), **kw})
+    call = lambda c, s, cf, batch=2, n_split=1: L.kivi_decode_attention_sinks(  # noqa
+        _layers(2), s, 2, C.byref(c), C.byref(cf), batch, 8, 0.1, q, out, n_split, None, 0, None)
+    assert call(_cache(), _sinks(), cfg(batch=1)) == 1          # cfg batch != batch
+    assert call(_cache(), _sinks(sink_pos=None), cfg()) == 1
+    assert call(_cache(), _sinks(sink_k=FAKE + 4), cfg()) == 2
+    assert call(_cache(), _sinks(), cfg(reserved=1)) == 1
+    assert call(_cache(d=64), _sinks(), cfg()) == 1             # attention needs head_dim 128
+    assert call(_cache(), _sinks(), cfg(), n_split=2) == 1      # no workspace
+    assert L.kivi_decode_attention_sinks(_layers(2), None, 2, C.byref(_cache()), C.byref(cfg()),
+                                         2, 8, 0.1, q, out, 1, None, 0, None) == 1

@@ -172,3 +172,61 @@ def test_sink_store_overflow_is_recorded():
     assert K.kivi_device_fault() == 2
     assert int(pair.sinks.sink_count[0, 0]) == 3
     del rows
+
+
+def attention_bound_check(q16, k, v, got, sm_scale, batch):
+    """Every output element within (2^-16 + 2^-16 A) B of the oracle's
+    attention (the bound of tests/test_gpu_attention.py)."""
+    ref = O.decode_attention(q16.view(np.uint16), k, v, sm_scale)
+    kf = k.view(np.float16).astype(np.float64)
+    vf = v.view(np.float16).astype(np.float64)
+    qf = q16.astype(np.float64)
+    h_q = q16.shape[1]
+    h_kv = k.shape[0] // batch
+    r = h_q // h_kv
+    for b in range(batch):
+        for h in range(h_q):
+            j = b * h_kv + h // r
+            sc = sm_scale * (kf[j] @ qf[b, h])
+            p = np.exp(sc - sc.max())
+            p /= p.sum()
+            A = sm_scale * np.max(np.abs(kf[j]) @ np.abs(qf[b, h]))
+            B = p @ np.abs(vf[j])
+            tol = (2.0 ** -16) * (1.0 + A) * B + 1e-30
+            assert (np.abs(got[b, h] - ref[b, h]) <= tol).all(), (b, h)
+    return ref
+
+
+@pytest.mark.parametrize("bits,group", [(2, 32), (4, 64), (8, 16)])
+def test_attention_over_sink_protected_cache(bits, group):
+    """Decode attention over a sink-protected cache equals the oracle's
+    attention over the restored cache (store dequantized, sinks' fp16 rows
+    put back, residual appended), within the attention bound; without the
+    sink store the stored sinks' zeroed slots would be attended instead."""
+    batch, heads, d = 2, 2, 128
+    pair = SinkPair(2, batch, heads, d, bits, group, group, r_cap=4 * group, cap=16 * group,
+                    k_top=6, sink_cap=40, seed=90 + bits + group, plant_every=50)
+    pair.append(3 * group)
+    rng = np.random.default_rng(bits + group)
+    while pair.s_q + pair.n_res < 11 * group:
+        pair.append(int(min(rng.integers(1, group), pair.r_cap - pair.n_res)))
+    assert (pair.sinks.sink_count.cpu().numpy() > 0).all() and pair.n_res > 0
+    h_q = 4 * heads
+    q16 = (rng.standard_normal((2, batch, h_q, d)) * 0.5).astype(np.float16)
+    qd = torch.from_numpy(q16.view(np.int16)).view(torch.float16).cuda()
+    sc = 1.0 / np.sqrt(d)
+    differs = False
+    for n_split in (1, 3):
+        got = pair.cache.decode_attention(qd, batch, sm_scale=sc, n_split=n_split,
+                                          sinks=pair.sinks).cpu().numpy().astype(np.float64)
+        plain = pair.cache.decode_attention(qd, batch, sm_scale=sc,
+                                            n_split=n_split).cpu().numpy().astype(np.float64)
+        torch.cuda.synchronize()
+        assert K.kivi_device_fault() == 0
+        for l in range(2):
+            k, v = O.cache_kv(pair.stores[l], pair.s_q, pair.ring_k[l], pair.ring_v[l],
+                              pair.head, pair.n_res)
+            O.sink_restore(k, v, pair.states[l])
+            ref = attention_bound_check(q16[l], k, v, got[l], sc, batch)
+            differs |= bool(np.abs(plain[l] - ref).max() > 1e-3)
+    assert differs
