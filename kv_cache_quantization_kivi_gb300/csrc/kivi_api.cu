@@ -6,11 +6,30 @@
 // KIVI_ERR_CUDA with the cudaError_t kept per host thread.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
 #include "../../include/kivi.h"
 #include "kivi_launch.h"
+
+namespace kivi_impl {
+
+int current_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> count[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  int n = count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 1;
+    count[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+}  // namespace kivi_impl
 
 namespace {
 

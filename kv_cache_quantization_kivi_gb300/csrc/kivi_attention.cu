@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "kivi_device.cuh"
@@ -794,27 +795,22 @@ __global__ void __launch_bounds__(kD) attention_combine_kernel(const __grid_cons
   p.jobs[job].out[(b * h_q + kvh * p.r + h) * kD + c] = O / L;
 }
 
-int g_num_sms = 0;
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    g_num_sms = n > 0 ? n : 1;
-  }
-  return g_num_sms;
-}
 
 template <int BITS, int G, bool SINKS>
 cudaError_t attention_launch_k(const AttnParams &p, cudaStream_t stream) {
   using F = StageFmt<BITS, G>;
   auto kern = decode_attention_kernel<BITS, G, SINKS>;
-  static bool configured = false;
-  if (!configured) {
+  // the shared-memory opt-in is a per-device function attribute: set once per device
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> configured[kMaxDevices];
+  int dev = 0;
+  cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 != cudaSuccess) return e0;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, F::kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   const int64_t items = static_cast<int64_t>(p.n_jobs) * p.bh * p.n_split;
   kern<<<static_cast<unsigned>(items), kThreads, F::kSmem, stream>>>(p);
@@ -854,7 +850,7 @@ int attention_splits(int64_t items, int64_t tiles_store, int group, int bits) {
   (void)group;
   (void)bits;
   if (items <= 0) return 1;
-  const int64_t target = static_cast<int64_t>(num_sms()) * 4 * 2;   // two waves of 4 CTAs per SM
+  const int64_t target = static_cast<int64_t>(current_sm_count()) * 4 * 2;   // two waves of 4 CTAs per SM
   const int64_t want = (target + items - 1) / items;
   const int64_t most = std::max<int64_t>(1, std::min<int64_t>(64, tiles_store / (2 * kWarps)));
   return static_cast<int>(std::max<int64_t>(1, std::min(want, most)));

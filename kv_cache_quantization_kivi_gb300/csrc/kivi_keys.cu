@@ -426,17 +426,6 @@ __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant_
   }
 }
 
-int g_num_sms = 0;
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    g_num_sms = n > 0 ? n : 1;
-  }
-  return g_num_sms;
-}
 
 template <int BITS, int G, int DC, int MODE>
 cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
@@ -449,7 +438,7 @@ cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
   const int64_t ng = (p.rows + G - 1) / G;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 2) * (G < 32 ? 1 : G / 32);
   const int64_t blocks = (units + threads - 1) / threads;
-  const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(num_sms()) * per_sm);
+  const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(current_sm_count()) * per_sm);
   QuantParams q = p;
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 2));
   q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));
@@ -469,7 +458,7 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   const int64_t ng = (p.rows + G - 1) / G;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 8);
   const int64_t blocks = (units + threads - 1) / threads;
-  const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(num_sms()) * per_sm);
+  const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(current_sm_count()) * per_sm);
   DequantParams q = p;
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 8));
   q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));

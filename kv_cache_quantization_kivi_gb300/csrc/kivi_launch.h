@@ -200,6 +200,8 @@ int attention_splits(int64_t items, int64_t tiles_store, int group, int bits);
 // its address on the current device (looked up once per device) and size.
 cudaError_t attention_scratch(float **ptr, int64_t *max_floats);
 int64_t attention_scratch_floats();
+// SM count of the current device (looked up once per device).
+int current_sm_count();
 // Address of the device fault word on the current device (looked up once
 // per device), for kernels of other translation units.
 cudaError_t fault_word_address(unsigned int **ptr);

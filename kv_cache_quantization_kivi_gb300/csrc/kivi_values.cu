@@ -346,17 +346,6 @@ __global__ void __launch_bounds__(kBlockThreads)
   }
 }
 
-int g_num_sms = 0;
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    g_num_sms = n > 0 ? n : 1;
-  }
-  return g_num_sms;
-}
 
 template <typename K>
 cudaError_t persistent_grid(K kern, int threads, int64_t units, int64_t *grid) {
@@ -365,7 +354,7 @@ cudaError_t persistent_grid(K kern, int threads, int64_t units, int64_t *grid) {
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   const int64_t blocks = (units + threads - 1) / threads;
-  *grid = std::max<int64_t>(1, std::min<int64_t>(blocks, static_cast<int64_t>(num_sms()) * per_sm));
+  *grid = std::max<int64_t>(1, std::min<int64_t>(blocks, static_cast<int64_t>(current_sm_count()) * per_sm));
   return cudaSuccess;
 }
 
