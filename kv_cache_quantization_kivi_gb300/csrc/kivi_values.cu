@@ -49,14 +49,21 @@ __device__ __forceinline__ RowRef decode_unit(uint32_t u, const P &p) {
 }
 
 // Coalesced store of a warp's 32 units of 64 bytes (32 fp16 each): each lane
-// parks its unit in a per-warp shared-memory block (16 bytes of padding per
-// unit against bank conflicts), and each 16-byte store instruction of the
-// warp then writes 512 consecutive bytes: lane l stores chunk l + 32 i of the
-// block, whose destination is that of unit (l + 32 i) / 4, taken from the
-// owning lane by a shuffle.  All 32 lanes must call it; `valid` marks lanes
-// whose unit exists (their `out` and `dst` are used).
-constexpr int kUnitWords = 20;   // 64 bytes of data + 16 bytes of padding
+// parks its unit in a per-warp shared-memory block, and each 16-byte store
+// instruction of the warp then writes 512 consecutive bytes: lane l stores
+// chunk l + 32 i of the block, whose destination is that of unit (l + 32 i)
+// / 4, taken from the owning lane by a shuffle.  Chunk c of unit u sits at
+// slot 4 u + (c ^ ((u >> 1) & 3)): in every 8-lane phase the writes (8 units,
+// one chunk each) and the reads (2 units, 4 chunks each) then touch 8
+// distinct 16-byte bank groups (a padded stride serves only one of the two
+// patterns).  All 32 lanes must call it; `valid` marks lanes whose unit
+// exists (their `out` and `dst` are used).
+constexpr int kUnitWords = 16;   // 64 bytes per unit, no padding
 constexpr int kBlockThreads = 256;
+
+__device__ __forceinline__ uint32_t unit_slot(uint32_t u, uint32_t c) {
+  return u * kUnitWords + 4u * (c ^ ((u >> 1) & 3u));
+}
 
 __device__ __forceinline__ void warp_store_units(uint32_t *blk, uint32_t lane, bool valid,
                                                  const uint32_t (&out)[16], __half *dst,
@@ -64,7 +71,7 @@ __device__ __forceinline__ void warp_store_units(uint32_t *blk, uint32_t lane, b
   if (valid) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      *reinterpret_cast<uint4 *>(blk + lane * kUnitWords + 4 * i) =
+      *reinterpret_cast<uint4 *>(blk + unit_slot(lane, i)) =
           make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
   }
   __syncwarp();
@@ -75,7 +82,7 @@ __device__ __forceinline__ void warp_store_units(uint32_t *blk, uint32_t lane, b
     const uint32_t owner = j >> 2;          // unit (lane) that produced it
     const unsigned long long d = __shfl_sync(0xffffffffu, dbits, owner);
     if (base + owner < total) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(blk + owner * kUnitWords + 4 * (j & 3));
+      const uint4 v = *reinterpret_cast<const uint4 *>(blk + unit_slot(owner, j & 3u));
       st_stream(reinterpret_cast<__half *>(d) + 8 * (j & 3), v);
     }
   }
