@@ -230,3 +230,52 @@ def test_attention_over_sink_protected_cache(bits, group):
             ref = attention_bound_check(q16[l], k, v, got[l], sc, batch)
             differs |= bool(np.abs(plain[l] - ref).max() > 1e-3)
     assert differs
+
+
+@pytest.mark.slow
+def test_sink_prefill_full_size_as_benchmarked():
+    """The benchmark's KIVI-Sink step (llama3_2_3b_prefill: 28 layers x 8 KV
+    heads x 4096 tokens, top 5 per sequence) in its own launch configuration;
+    two layers are compared with the oracle in full: the ranked top-k, the
+    sink-protected store, the sink store and the restored reconstruction."""
+    import importlib.util
+    import os
+    spec = importlib.util.spec_from_file_location(
+        "bench_mod", os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                                  "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    dev = torch.device("cuda", 0)
+    wl = bench.make_workload("llama3_2_3b_prefill", dev, sink=True)
+    stream = torch.cuda.current_stream(dev)
+    wl.step(stream)
+    wl.step(stream)                       # a second step from the reset state
+    torch.cuda.synchronize()
+    assert K.kivi_device_fault() == 0
+    w, c, sk = wl.w, wl.cache, wl.sinks
+    heads = w.bh // w.batch
+    for l in (0, w.layers - 1):
+        k = np.ascontiguousarray(wl.k_host[l])
+        v = np.ascontiguousarray(wl.v_host[l])
+        st = O.SinkState(w.batch, heads, w.head_dim, wl.K_TOP, 2 * wl.K_TOP)
+        st.update(O.sink_scores(k, heads), 0)
+        store = O.Store(w.bh, w.head_dim, w.seq, w.group, w.bits)
+        n, s_q, _, _ = O.flush_sink(k, v, store, w.residual, 0, 0, w.seq, st)
+        assert n == s_q == wl.n
+        cnt = sk.top_count[l].cpu().numpy()
+        assert np.array_equal(cnt, st.top_count)
+        assert np.array_equal(sk.top_pos[l].cpu().numpy()[:, :wl.K_TOP], st.top_pos[:, :wl.K_TOP])
+        assert_same("key codes", host_u32(c.k_codes[l]), store.k_codes)
+        assert_same("key scale", host_f32_bits(c.k_scale[l]), bits32(store.k_scale))
+        assert_same("key zero", host_f32_bits(c.k_zero[l]), bits32(store.k_zero))
+        assert_same("value codes", host_u32(c.v_codes[l]), store.v_codes)
+        assert_same("value scale", host_f32_bits(c.v_scale[l]), bits32(store.v_scale))
+        assert np.array_equal(sk.sink_count[l].cpu().numpy(), st.sink_count)
+        for b in range(w.batch):
+            m = int(st.sink_count[b])
+            assert m > 0
+            assert np.array_equal(sk.sink_pos[l].cpu().numpy()[b, :m], st.sink_pos[b, :m])
+        kref, vref = O.cache_kv(store, n, k, v, 0, 0)
+        O.sink_restore(kref, vref, st)
+        assert_same("restored keys", host_u16(wl.k_out[l]), kref)
+        assert_same("restored values", host_u16(wl.v_out[l]), vref)
