@@ -431,14 +431,22 @@ template <int BITS, int G, int DC, int MODE>
 cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
   const int threads = kKeyThreads;
   auto kern = key_quant_kernel<BITS, G, DC, MODE>;
-  int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) per_sm = 1;
   const int64_t ng = (p.rows + G - 1) / G;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 2) * (G < 32 ? 1 : G / 32);
-  const int64_t blocks = (units + threads - 1) / threads;
-  const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(current_sm_count()) * per_sm);
+  // Grid shape by measurement over bits x G on stores larger than L2: one
+  // block per 256 units (flat) is 6-17% faster for the fused reconstruction
+  // and ~3.5% faster for 2-bit codes with G <= 64; a persistent grid (SMs x
+  // resident blocks) is 3-11% faster for the plain 4- and 8-bit quantize,
+  // whose kernels hold more registers and fit fewer blocks per SM.
+  constexpr bool kFlat = MODE == kQuantRecon || (BITS == 2 && G <= 64);
+  int64_t grid = flat_grid(units, threads);
+  if (!kFlat) {
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    grid = std::min<int64_t>(grid, static_cast<int64_t>(current_sm_count()) * per_sm);
+  }
   QuantParams q = p;
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 2));
   q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));
@@ -451,14 +459,10 @@ template <int BITS, int G, int DC>
 cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   const int threads = 256;
   auto kern = key_dequant_kernel<BITS, G, DC>;
-  int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) per_sm = 1;
   const int64_t ng = (p.rows + G - 1) / G;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 8);
-  const int64_t blocks = (units + threads - 1) / threads;
-  const int64_t grid = std::min<int64_t>(blocks, static_cast<int64_t>(current_sm_count()) * per_sm);
+  // one block per 256 units, not a persistent grid (see flat_grid)
+  const int64_t grid = flat_grid(units, threads);
   DequantParams q = p;
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 8));
   q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));

@@ -202,6 +202,12 @@ cudaError_t attention_scratch(float **ptr, int64_t *max_floats);
 int64_t attention_scratch_floats();
 // SM count of the current device (looked up once per device).
 int current_sm_count();
+// Grid of one block per `threads` units for a grid-stride kernel, clamped to
+// the launch limit of 2^31 - 1 blocks in x (at least one block).
+inline int64_t flat_grid(int64_t units, int threads) {
+  const int64_t blocks = (units + threads - 1) / threads;
+  return blocks < 1 ? 1 : (blocks > 2147483647 ? 2147483647 : blocks);
+}
 // Address of the device fault word on the current device (looked up once
 // per device), for kernels of other translation units.
 cudaError_t fault_word_address(unsigned int **ptr);
