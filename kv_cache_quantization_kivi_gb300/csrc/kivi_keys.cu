@@ -435,9 +435,10 @@ cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 2) * (G < 32 ? 1 : G / 32);
   // Grid shape by measurement over bits x G on stores larger than L2: one
   // block per 256 units (flat) is 6-17% faster for the fused reconstruction
-  // and ~3.5% faster for 2-bit codes with G <= 64; a persistent grid (SMs x
-  // resident blocks) is 3-11% faster for the plain 4- and 8-bit quantize,
-  // whose kernels hold more registers and fit fewer blocks per SM.
+  // and ~3.5% faster for 2-bit codes with G <= 64; two waves of resident
+  // blocks are 3-11% faster for the plain 4- and 8-bit quantize, whose
+  // kernels hold more registers and fit fewer blocks per SM (one wave is
+  // ~1% slower, three or more waves lose again at 8 bits).
   constexpr bool kFlat = MODE == kQuantRecon || (BITS == 2 && G <= 64);
   int64_t grid = flat_grid(units, threads);
   if (!kFlat) {
@@ -445,7 +446,7 @@ cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) per_sm = 1;
-    grid = std::min<int64_t>(grid, static_cast<int64_t>(current_sm_count()) * per_sm);
+    grid = std::min<int64_t>(grid, 2 * static_cast<int64_t>(current_sm_count()) * per_sm);
   }
   QuantParams q = p;
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 2));

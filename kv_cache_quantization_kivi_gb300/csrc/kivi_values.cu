@@ -382,6 +382,12 @@ cudaError_t value_quant_launch(const QuantParams &p, cudaStream_t stream) {
   int64_t grid = 0;
   cudaError_t err = persistent_grid(kern, threads, units, &grid);
   if (err != cudaSuccess) return err;
+  // Three waves of resident blocks, by measurement over bits x G and the
+  // model-shaped stores: 1-3% faster than one wave (which leaves each block
+  // a long fixed stride) and than one block per 256 units, except for the
+  // fused reconstruction at G = 16, where the flat grid is 12% faster.
+  const int64_t flat = flat_grid(units, threads);
+  grid = (MODE == kQuantRecon && G == 16) ? flat : std::min<int64_t>(flat, 3 * grid);
   kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(with_dividers(p));
   return cudaGetLastError();
 }
