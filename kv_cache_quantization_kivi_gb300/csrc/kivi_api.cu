@@ -78,14 +78,14 @@ KeyGeom key_geom(int64_t s, int64_t d, int group, int bits) {
   return {ng * group / (32 / bits) * d, ng * d};
 }
 
-// Threads of the key quantize kernel: one per (bh, group, channel pair,
-// min(G, 32)-token split); of the value kernels and the key dequantize
-// kernel: one per 32 (values) or 8 (keys) channels of a row or group.
+// Threads of the key kernels: one per (bh, group, min(G, 32)-token split)
+// and channel pair (quantize) or 8 channels (dequantize); of the value
+// kernels: one per 32 channels of a row.
 int64_t key_quant_units(int64_t bh, int64_t s, int64_t d, int group) {
   return sat_mul(sat_mul(bh, groups_of(s, group)), (d / 2) * (group < 32 ? 1 : group / 32));
 }
 int64_t key_dequant_units(int64_t bh, int64_t s, int64_t d, int group) {
-  return sat_mul(sat_mul(bh, groups_of(s, group)), d / 8);
+  return sat_mul(sat_mul(bh, groups_of(s, group)), (d / 8) * (group < 32 ? 1 : group / 32));
 }
 int64_t value_units(int64_t bh, int64_t s, int64_t d) { return sat_mul(sat_mul(bh, s), d / 32); }
 

@@ -373,13 +373,20 @@ __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant_
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
   const int D = DC > 0 ? DC : p.d;
-  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * p.div_bh.d * p.div_rows.d *
+  // a unit is 8 channels x one TPU-token split of a group: groups above 32
+  // tokens are split so that every G gives a thread the work of G = 32 (the
+  // group's scale and zero are read once per split, the repeats from cache)
+  constexpr int TPU = G < 32 ? G : 32;
+  constexpr int S = G / TPU;                  // splits per group
+  const uint32_t total = static_cast<uint32_t>(p.n_jobs) * p.div_bh.d * p.div_rows.d * S *
                          p.div_chunks.d;
   const uint32_t stride = gridDim.x * blockDim.x;
 #pragma unroll 1
   for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
-    const uint32_t bg_all = p.div_chunks.div(u);
-    const int ch = static_cast<int>(u - bg_all * p.div_chunks.d);
+    const uint32_t gs_all = p.div_chunks.div(u);
+    const int ch = static_cast<int>(u - gs_all * p.div_chunks.d);
+    const int split = static_cast<int>(gs_all % S);
+    const uint32_t bg_all = gs_all / S;
     const uint32_t jb = p.div_rows.div(bg_all);
     const int64_t g = bg_all - jb * p.div_rows.d;
     const uint32_t job = p.div_bh.div(jb);
@@ -399,11 +406,12 @@ __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant_
 #pragma unroll
     for (int c = 0; c < 8; ++c) nsc[c] = __fmul_rn(sc[c], -8388608.0f);  // -2^23 * scale, exact
 
-    const uint32_t *cw = J.codes + b * p.codes_bh_stride + g * (G / W) * D + ch * 8;
+    const uint32_t *cw =
+        J.codes + b * p.codes_bh_stride + (g * (G / W) + split * (TPU / W)) * D + ch * 8;
     __half *y = static_cast<__half *>(J.y) + b * p.y_bh_stride + ch * 8;
-    const int64_t t0 = g * G;
+    const int64_t t0 = g * G + split * TPU;
 #pragma unroll 1
-    for (int wr = 0; wr < G / W; ++wr) {
+    for (int wr = 0; wr < TPU / W; ++wr) {
       const uint4 ca = ld_stream(cw + static_cast<int64_t>(wr) * D);
       const uint4 cb = ld_stream(cw + static_cast<int64_t>(wr) * D + 4);
       const uint32_t words[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
@@ -461,7 +469,7 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   const int threads = 256;
   auto kern = key_dequant_kernel<BITS, G, DC>;
   const int64_t ng = (p.rows + G - 1) / G;
-  const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (p.d / 8);
+  const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * ng * (G < 32 ? 1 : G / 32) * (p.d / 8);
   // one block per 256 units, not a persistent grid (see flat_grid)
   const int64_t grid = flat_grid(units, threads);
   DequantParams q = p;
