@@ -4,7 +4,9 @@
 // the key norms over the KV heads ranks the token positions, a running top-k
 // is kept, and a flushed token in it is stored fp16 instead of quantized).
 //
-//   sink_score_kernel    thread per new token: its score
+//   sink_score_tile_kernel  block per 32 new tokens of a (layer, sequence):
+//                        rows staged in shared memory, the scores
+//                        (sink_score_kernel, thread per token: > 64 heads)
 //   sink_select_kernel   block per (layer, sequence): the new scores merged
 //                        into the running top-k
 //   sink_mask_kernel     per (layer, sequence, 32 flushed tokens): which of
@@ -65,7 +67,103 @@ __device__ float token_score(const __half *k_seq, int64_t head_stride, int heads
   return __fdiv_rn(sum, static_cast<float>(heads));
 }
 
+// Scores of 32 consecutive new tokens of one (layer, sequence) per block.
+// A warp stages 32 rows of one head through shared memory, 64 channels at a
+// time, with coalesced loads (8 lanes per 128-byte row segment), and each
+// lane then runs its own row's fused multiply-adds in channel order from
+// shared memory; the roots of the heads' squared norms are added in head
+// order and divided by the head count -- the arithmetic of token_score.
+// (Reading a whole row per lane straight from global memory touches 32
+// lines per warp load for 16 bytes each and caps the read near 4.5 TB/s.)
+constexpr int kScoreTile = 32;                    // tokens per block
+constexpr int kScoreChunk = 64;                   // channels staged per pass
+constexpr int kScoreRow = kScoreChunk * 2 + 16;   // padded row: conflict-free 16-byte reads
+constexpr int kScoreMaxHeads = 64;
+
+__global__ void __launch_bounds__(kThreads, 3) sink_score_tile_kernel(const __grid_constant__ SinkParams p) {
+  __shared__ __align__(16) unsigned char stage[kWarps][kScoreTile * kScoreRow];
+  __shared__ float norm[kScoreMaxHeads * kScoreTile];
+  // grid = layers x sequences x tiles (< 2^31 blocks, host-checked)
+  const uint32_t tiles = static_cast<uint32_t>((p.n + kScoreTile - 1) / kScoreTile);
+  const uint32_t js = blockIdx.x / tiles;
+  const int64_t tile = blockIdx.x - js * tiles;
+  const int job = static_cast<int>(js / static_cast<uint32_t>(p.batch));
+  const int64_t seq = js - static_cast<uint32_t>(job) * static_cast<uint32_t>(p.batch);
+  const SinkJob &J = p.jobs[job];
+  const int64_t i_base = tile * kScoreTile;
+  const int ntok = static_cast<int>(p.n - i_base < kScoreTile ? p.n - i_base : kScoreTile);
+  const int heads = static_cast<int>(p.heads);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char *st = stage[warp];
+  const int pc = lane & 7;                        // this lane's 16-byte piece when loading
+  // the ring row of the tile's first token; this lane loads rows (lane >> 3) + 4 m
+  const int64_t row0 = (p.res_head + p.i0 + i_base) % p.r_cap;
+  const int64_t r_lane = row0 + (lane >> 3);
+  // The warp's work is the sequence of items (head h = warp + 8 k, chunk c);
+  // the loads of item i + 1 are issued before item i is accumulated.
+  const int chunks = static_cast<int>((p.d + kScoreChunk - 1) / kScoreChunk);
+  const int my_heads = heads > warp ? (heads - warp + kWarps - 1) / kWarps : 0;
+  const int items = my_heads * chunks;
+  uint4 v[kScoreTile / 4];
+  auto load = [&](int item) {
+    const int h = warp + kWarps * (item / chunks);
+    const int64_t c0 = static_cast<int64_t>(item % chunks) * kScoreChunk;
+    const int pieces = static_cast<int>(p.d - c0 < kScoreChunk ? p.d - c0 : kScoreChunk) / 8;
+    const __half *kc = static_cast<const __half *>(J.k_res) +
+                       (seq * p.heads + h) * p.r_cap * p.d + c0 + 8 * pc;
+#pragma unroll
+    for (int m = 0; m < kScoreTile / 4; ++m) {
+      const int r = (lane >> 3) + 4 * m;
+      if (r < ntok && pc < pieces) {
+        int64_t row = r_lane + 4 * m;
+        if (row >= p.r_cap) row -= p.r_cap;       // r < n <= r_cap: one wrap at most
+        v[m] = *reinterpret_cast<const uint4 *>(kc + row * p.d);
+      }
+    }
+  };
+  if (items > 0) load(0);
+  float acc = 0.0f;
+  for (int it = 0; it < items; ++it) {
+    const int c = it % chunks;
+    const int64_t c0 = static_cast<int64_t>(c) * kScoreChunk;
+    const int pieces = static_cast<int>(p.d - c0 < kScoreChunk ? p.d - c0 : kScoreChunk) / 8;
+#pragma unroll
+    for (int m = 0; m < kScoreTile / 4; ++m) {
+      const int r = (lane >> 3) + 4 * m;
+      if (r < ntok && pc < pieces)
+        *reinterpret_cast<uint4 *>(st + r * kScoreRow + 16 * pc) = v[m];
+    }
+    __syncwarp();
+    if (it + 1 < items) load(it + 1);             // in flight during the accumulation
+    if (lane < ntok) {
+      for (int q = 0; q < pieces; ++q) {
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(st + lane * kScoreRow + 16 * q);
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __half22float2(kivi_dev::u32_as_h2(w[i]));
+          acc = __fmaf_rn(f.x, f.x, acc);
+          acc = __fmaf_rn(f.y, f.y, acc);
+        }
+      }
+    }
+    __syncwarp();
+    if (c == chunks - 1) {                        // the head's last chunk
+      const int h = warp + kWarps * (it / chunks);
+      if (lane < ntok) norm[h * kScoreTile + lane] = __fsqrt_rn(acc);
+      acc = 0.0f;
+    }
+  }
+  __syncthreads();
+  if (static_cast<int>(threadIdx.x) < ntok) {
+    float sum = 0.0f;
+    for (int h = 0; h < heads; ++h) sum = __fadd_rn(sum, norm[h * kScoreTile + threadIdx.x]);
+    J.scores[seq * p.r_cap + i_base + threadIdx.x] = __fdiv_rn(sum, static_cast<float>(heads));
+  }
+}
+
 // thread = (job, sequence, new token): its score into the scores scratch
+// (more than 64 heads per sequence)
 __global__ void __launch_bounds__(kThreads) sink_score_kernel(const __grid_constant__ SinkParams p) {
   const int64_t u = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   if (u >= static_cast<int64_t>(p.n_jobs) * p.batch * p.n) return;
@@ -151,50 +249,47 @@ struct RegTop8 {
 };
 
 // block = (job, sequence): the new scores and the kept top-k merged.  Each
-// thread keeps the best k of its strided share; k rounds of a block-wide
-// argmax over the threads' list heads then give the k best overall.
-template <typename List>
-__global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_constant__ SinkParams p) {
+// of the NT threads keeps the best k of its strided share; k rounds of a
+// block-wide argmax over the threads' list heads (shuffles within each warp,
+// then across the warps' winners in warp 0) give the k best overall.
+template <typename List, int NT>
+__global__ void __launch_bounds__(NT) sink_select_kernel(const __grid_constant__ SinkParams p) {
+  constexpr int NW = NT / 32;
   const int job = static_cast<int>(blockIdx.x / p.batch);
   const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
   const SinkJob &J = p.jobs[job];
   __shared__ float new_s[kMaxSinkTop];
   __shared__ int64_t new_p[kMaxSinkTop];
-  __shared__ float red_s[kWarps];
-  __shared__ int64_t red_p[kWarps];
-  __shared__ int red_i[kWarps];
+  __shared__ float red_s[NW];
+  __shared__ int64_t red_p[NW];
+  __shared__ int red_i[NW];
   __shared__ int winner;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = p.k_top;
   List lt;
   lt.init();
   const int tn = J.top_count[seq];
-  for (int e = tid; e < tn; e += kThreads)
+  for (int e = tid; e < tn; e += NT)
     lt.offer(J.top_score[seq * p.k_top + e], J.top_pos[seq * p.k_top + e], k);
   // the thread's strided share of the new scores, loaded kBatch at a time
   // (independent loads in flight together) and then offered in order
   constexpr int kBatch = 8;
   const float *sc = J.scores + seq * p.r_cap;
-  for (int64_t i0 = tid; i0 < p.n; i0 += kBatch * kThreads) {
+  for (int64_t i0 = tid; i0 < p.n; i0 += kBatch * NT) {
     float v[kBatch];
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      const int64_t i = i0 + static_cast<int64_t>(b) * kThreads;
+      const int64_t i = i0 + static_cast<int64_t>(b) * NT;
       v[b] = i < p.n ? sc[i] : 0.0f;
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      const int64_t i = i0 + static_cast<int64_t>(b) * kThreads;
+      const int64_t i = i0 + static_cast<int64_t>(b) * NT;
       if (i < p.n) lt.offer(v[b], p.s_q + p.i0 + i, k);
     }
   }
-  const int64_t avail = tn + p.n;
-  const int keep = avail < k ? static_cast<int>(avail) : k;
-  for (int j = 0; j < keep; ++j) {
-    bool have = lt.has();
-    float bs = have ? lt.hs() : 0.0f;
-    int64_t bp = have ? lt.hq() : 0;
-    int owner = have ? tid : -1;
+  // best of (bs, bp, owner) over the 32 lanes of a warp; owner < 0: none
+  auto warp_best = [](float &bs, int64_t &bp, int &owner) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float os = __shfl_xor_sync(0xffffffffu, bs, off);
@@ -204,28 +299,35 @@ __global__ void __launch_bounds__(kThreads) sink_select_kernel(const __grid_cons
         bs = os; bp = op; owner = oo;
       }
     }
+  };
+  const int64_t avail = tn + p.n;
+  const int keep = avail < k ? static_cast<int>(avail) : k;
+  for (int j = 0; j < keep; ++j) {
+    const bool have = lt.has();
+    float bs = have ? lt.hs() : 0.0f;
+    int64_t bp = have ? lt.hq() : 0;
+    int owner = have ? tid : -1;
+    warp_best(bs, bp, owner);
     if (lane == 0) {
       red_s[warp] = bs;
       red_p[warp] = bp;
       red_i[warp] = owner;
     }
     __syncthreads();
-    if (tid == 0) {
-      float ws = red_s[0];
-      int64_t wp = red_p[0];
-      int wo = red_i[0];
-      for (int w = 1; w < kWarps; ++w) {
-        if (red_i[w] >= 0 && (wo < 0 || ranks_before(red_s[w], red_p[w], ws, wp))) {
-          ws = red_s[w]; wp = red_p[w]; wo = red_i[w];
-        }
+    if (warp == 0) {
+      float ws = lane < NW ? red_s[lane] : 0.0f;
+      int64_t wp = lane < NW ? red_p[lane] : 0;
+      int wo = lane < NW ? red_i[lane] : -1;
+      warp_best(ws, wp, wo);
+      if (lane == 0) {
+        new_s[j] = ws;
+        new_p[j] = wp;
+        winner = wo;
       }
-      new_s[j] = ws;
-      new_p[j] = wp;
-      winner = wo;
     }
     __syncthreads();
     // every thread reads `winner` here, before it reaches the next round's
-    // first barrier, after which alone thread 0 writes it again
+    // first barrier, after which alone warp 0 writes it again
     if (winner == tid) lt.pop();
   }
   if (tid < keep) {
@@ -335,15 +437,24 @@ unsigned blocks_for(int64_t threads) {
 }  // namespace
 
 cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream) {
-  const int64_t threads = static_cast<int64_t>(p.n_jobs) * p.batch * p.n;
-  sink_score_kernel<<<blocks_for(threads), kThreads, 0, stream>>>(p);
+  if (p.heads <= kScoreMaxHeads) {
+    const int64_t tiles = (p.n + kScoreTile - 1) / kScoreTile;
+    sink_score_tile_kernel<<<static_cast<unsigned>(p.n_jobs * p.batch * tiles), kThreads, 0,
+                             stream>>>(p);
+  } else {
+    sink_score_kernel<<<blocks_for(static_cast<int64_t>(p.n_jobs) * p.batch * p.n), kThreads, 0,
+                        stream>>>(p);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned blocks = static_cast<unsigned>(p.n_jobs * p.batch);
+  // 1024 threads: a short share of the scores per thread (the offers are the
+  // serial part); the list heads meet in two shuffle stages per round
+  constexpr int kSelectThreads = 1024;
   if (p.k_top <= 8)
-    sink_select_kernel<RegTop8><<<blocks, kThreads, 0, stream>>>(p);
+    sink_select_kernel<RegTop8, kSelectThreads><<<blocks, kSelectThreads, 0, stream>>>(p);
   else
-    sink_select_kernel<LocalTop<kMaxSinkTop>><<<blocks, kThreads, 0, stream>>>(p);
+    sink_select_kernel<LocalTop<kMaxSinkTop>, kSelectThreads><<<blocks, kSelectThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -232,6 +232,30 @@ def test_attention_over_sink_protected_cache(bits, group):
     assert differs
 
 
+@pytest.mark.parametrize("batch,heads,d", [(2, 1, 128), (1, 3, 128), (3, 5, 64), (2, 8, 128),
+                                           (1, 11, 96), (2, 9, 256), (1, 64, 64), (1, 65, 32),
+                                           (1, 300, 32)])
+def test_sink_scores_every_head_count(batch, heads, d):
+    """The scores scratch equals the oracle's scores bit for bit for head
+    counts below, at and above the eight warps of a score block (each warp
+    takes heads w, w + 8, ...), head dims that stage in one, one and a half
+    (96) and four 64-channel passes, a token count with a ragged last tile,
+    and more than 64 heads (the thread-per-token kernel); then the whole
+    sink pipeline on those tokens."""
+    group = 32
+    pair = SinkPair(2, batch, heads, d, 2, group, group, r_cap=4 * group, cap=8 * group,
+                    k_top=5, sink_cap=12, seed=heads * 10 + batch, plant_every=9)
+    n = 3 * group + 7
+    pair.append(n, flush=False)
+    torch.cuda.synchronize()
+    for l in range(pair.layers):
+        want = O.sink_scores(pair.ring_k[l][:, :n], heads)
+        got = host_f32_bits(pair.sinks.scores[l])[:, :n]
+        assert np.array_equal(got, bits32(want)), (l, heads)
+    pair.append(group - 10)     # 125 of 128 ring rows, then a flush of 64
+    pair.check()
+
+
 @pytest.mark.slow
 def test_sink_prefill_full_size_as_benchmarked():
     """The benchmark's KIVI-Sink step (llama3_2_3b_prefill: 28 layers x 8 KV
