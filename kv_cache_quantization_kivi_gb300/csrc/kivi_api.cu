@@ -737,17 +737,15 @@ kivi_status kivi_flush_sink(const kivi_layer *layers, const kivi_sink_layer *sin
   cudaStream_t s = stream;
   const int mode = cfg->k_top > 0 ? kivi_impl::kQuantSink : kivi_impl::kQuantPlain;
   kivi_status r = KIVI_OK;
-  if (cfg->k_top > 0) r = cuda_status(kivi_impl::launch_sink_mask(sp, s));
-  if (r != KIVI_OK) return r;
+  if (cfg->k_top > 0) {   // mask and sink store first: the quantizers read the mask only
+    r = cuda_status(kivi_impl::fault_word_address(&sp.fault));
+    if (r != KIVI_OK) return r;
+    r = cuda_status(kivi_impl::launch_sink_prepare(sp, s));
+    if (r != KIVI_OK) return r;
+  }
   r = cuda_status(kivi_impl::launch_key_quant(kp, cache->group, cache->bits, mode, s));
   if (r != KIVI_OK) return r;
   r = cuda_status(kivi_impl::launch_value_quant(vp, cache->group, cache->bits, mode, s));
-  if (r != KIVI_OK) return r;
-  if (cfg->k_top > 0) {
-    r = cuda_status(kivi_impl::fault_word_address(&sp.fault));
-    if (r != KIVI_OK) return r;
-    r = cuda_status(kivi_impl::launch_sink_copy(sp, s));
-  }
   if (r != KIVI_OK) return r;
   cache->s_q += n;
   cache->res_head = (cache->res_head + n) % cache->r_cap;

@@ -172,8 +172,7 @@ struct SinkParams {
   SinkJob jobs[KIVI_MAX_LAYERS];
 };
 cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream);
-cudaError_t launch_sink_mask(const SinkParams &p, cudaStream_t stream);
-cudaError_t launch_sink_copy(const SinkParams &p, cudaStream_t stream);
+cudaError_t launch_sink_prepare(const SinkParams &p, cudaStream_t stream);
 cudaError_t launch_sink_restore(const SinkParams &p, cudaStream_t stream);
 
 // Launchers (one per kernel family); they pick the template instance for

@@ -9,12 +9,12 @@
 //                        (sink_score_kernel, thread per token: > 64 heads)
 //   sink_select_kernel   block per (layer, sequence): the new scores merged
 //                        into the running top-k
-//   sink_mask_kernel     per (layer, sequence, 32 flushed tokens): which of
-//                        the tokens being flushed are in the top-k (one bit
-//                        each), read by the quantize kernels' sink mode
-//   sink_copy_kernel     block per (layer, sequence): the flushed sinks'
-//                        positions and fp16 key / value rows into the sink
-//                        store, in position order
+//   sink_prepare_kernel  block per (layer, sequence), before the flush's
+//                        quantize kernels: which of the tokens being flushed
+//                        are in the top-k (one bit each, read by their sink
+//                        mode), and the flushed sinks' positions and fp16
+//                        key / value rows into the sink store, in position
+//                        order
 //   sink_restore_kernel  the sink rows put back into dequantized tensors
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -337,35 +337,20 @@ __global__ void __launch_bounds__(NT) sink_select_kernel(const __grid_constant__
   if (tid == 0) J.top_count[seq] = keep;
 }
 
-// thread = (job, sequence, word of 32 flushed tokens)
-__global__ void __launch_bounds__(kThreads) sink_mask_kernel(const __grid_constant__ SinkParams p) {
-  const int64_t words = (p.n + 31) / 32;
-  const int64_t u = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  if (u >= static_cast<int64_t>(p.n_jobs) * p.batch * words) return;
-  const int64_t w = u % words;
-  const int64_t js = u / words;
-  const int job = static_cast<int>(js / p.batch);
-  const int64_t seq = js - static_cast<int64_t>(job) * p.batch;
-  const SinkJob &J = p.jobs[job];
-  const int64_t lo = p.s_q + 32 * w;
-  uint32_t bits = 0u;
-  const int tn = J.top_count[seq];
-  for (int e = 0; e < tn; ++e) {
-    const int64_t pos = J.top_pos[seq * p.k_top + e];
-    if (pos >= lo && pos < lo + 32) bits |= 1u << (pos - lo);
-  }
-  J.mask[seq * p.mask_words + w] = bits;
-}
-
-// block = (job, sequence)
-__global__ void __launch_bounds__(kThreads) sink_copy_kernel(const __grid_constant__ SinkParams p) {
+// block = (job, sequence), before the flush's quantize kernels: the
+// flushed top-k positions in ascending order; one mask bit per flushed token
+// (in the top-k or not), read by the quantize kernels' sink mode; the sinks'
+// positions and fp16 key / value rows of every head appended to the sink
+// store (the quantize kernels read neither the store nor its count).  An
+// overflowing store keeps what fits and sets bit 1 of the device fault
+// word; the mask still flags every flushed top-k token.
+__global__ void __launch_bounds__(kThreads) sink_prepare_kernel(const __grid_constant__ SinkParams p) {
   const int job = static_cast<int>(blockIdx.x / p.batch);
   const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
   const SinkJob &J = p.jobs[job];
   __shared__ int64_t pos[kMaxSinkTop];
-  __shared__ int slot0, m;
+  __shared__ int slot0, m, cnt_all;
   if (threadIdx.x == 0) {
-    // flushed top positions, ascending
     int cnt = 0;
     const int tn = J.top_count[seq];
     for (int e = 0; e < tn; ++e) {
@@ -378,6 +363,7 @@ __global__ void __launch_bounds__(kThreads) sink_copy_kernel(const __grid_consta
       }
       pos[i] = q;
     }
+    cnt_all = cnt;
     const int have = J.sink_count[seq];
     if (have + cnt > p.sink_cap) {   // the store is full: record it, keep what fits
       atomicOr(p.fault, 2u);
@@ -389,6 +375,14 @@ __global__ void __launch_bounds__(kThreads) sink_copy_kernel(const __grid_consta
     m = cnt;
   }
   __syncthreads();
+  const int64_t words = (p.n + 31) / 32;
+  for (int64_t w = threadIdx.x; w < words; w += kThreads) {
+    const int64_t lo = p.s_q + 32 * w;
+    uint32_t bits = 0u;
+    for (int e = 0; e < cnt_all; ++e)
+      if (pos[e] >= lo && pos[e] < lo + 32) bits |= 1u << (pos[e] - lo);
+    J.mask[seq * p.mask_words + w] = bits;
+  }
   const int64_t chunks = p.d / 8;                       // 16-byte pieces per row
   const int64_t total = static_cast<int64_t>(m) * p.heads * chunks;
   for (int64_t idx = threadIdx.x; idx < total; idx += kThreads) {
@@ -458,15 +452,8 @@ cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_sink_mask(const SinkParams &p, cudaStream_t stream) {
-  const int64_t threads = static_cast<int64_t>(p.n_jobs) * p.batch * ((p.n + 31) / 32);
-  if (threads == 0) return cudaSuccess;
-  sink_mask_kernel<<<blocks_for(threads), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_sink_copy(const SinkParams &p, cudaStream_t stream) {
-  sink_copy_kernel<<<static_cast<unsigned>(p.n_jobs * p.batch), kThreads, 0, stream>>>(p);
+cudaError_t launch_sink_prepare(const SinkParams &p, cudaStream_t stream) {
+  sink_prepare_kernel<<<static_cast<unsigned>(p.n_jobs * p.batch), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
