@@ -1,0 +1,42 @@
+"""Host logic of bench.py that needs no GPU: the layer chunks of the
+end-to-end pipeline."""
+from __future__ import annotations
+
+import importlib.util
+import os
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def load_bench():
+    spec = importlib.util.spec_from_file_location("bench_host", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.mark.parametrize("layers", [1, 2, 3, 4, 5, 7, 9, 16, 28, 32, 36, 80, 128])
+@pytest.mark.parametrize("chunks,ramp", [(5, (1, 1, 2, 2)), (7, (1, 1, 2)), (7, ()), (14, (1, 1))])
+def test_e2e_bounds_cover_every_layer_once(layers, chunks, ramp):
+    b = load_bench().e2e_bounds(layers, chunks, ramp)
+    assert b[0] == 0 and b[-1] == layers
+    assert all(x < y for x, y in zip(b, b[1:]))          # non-empty chunks, in order
+    sizes = [y - x for x, y in zip(b, b[1:])]
+    base = -(-layers // chunks)
+    # the ramp's sizes lead, each below the base chunk; no later chunk is
+    # far above the base size
+    lead = [r for r in ramp if r < base]
+    k = 0
+    while k < len(lead) and sum(lead[:k + 1]) <= layers:
+        k += 1
+    assert sizes[:k] == lead[:k]
+    assert max(sizes) <= 2 * base
+
+
+def test_e2e_bounds_of_the_benchmarked_prefill():
+    bench = load_bench()
+    b = bench.e2e_bounds(28, bench.PrefillFlush.E2E_CHUNKS, bench.PrefillFlush.E2E_RAMP)
+    assert b[:5] == [0, 1, 2, 4, 6]
+    assert b[-1] == 28 and len(b) - 1 == 8
