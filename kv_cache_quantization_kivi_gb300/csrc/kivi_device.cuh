@@ -304,6 +304,18 @@ __device__ __forceinline__ void st_stream(void *p, uint2 v) {
 // non-tensor form of the tensor memory accelerator), written as inline PTX.
 // ---------------------------------------------------------------------------
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may be scheduled while the previous grid in its stream
+// drains; griddepcontrol.wait (a no-op without such a dependency) holds it
+// until that grid has completed and its memory operations are visible, and
+// launch_dependents lets the next grid be scheduled early in turn.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -153,6 +153,8 @@ __host__ __device__ constexpr int key_min_blocks() { return BITS >= 4 ? 3 : 4; }
 
 template <int BITS, int G, int DC, int MODE>
 __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant_kernel(const __grid_constant__ QuantParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   constexpr bool RECON = MODE == kQuantRecon;
   constexpr bool SINK = MODE == kQuantSink;
   constexpr int TPT = G < 32 ? G : 32;      // tokens per thread
@@ -370,6 +372,8 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
 // p.div_chunks, p.div_rows and p.div_bh divide by d/8, ng and bh.
 template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant__ DequantParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
   const int D = DC > 0 ? DC : p.d;
@@ -460,8 +464,7 @@ cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 2));
   q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));
   q.div_bh = FastDiv::make(static_cast<uint32_t>(p.bh));
-  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(q);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, threads, stream, q);
 }
 
 template <int BITS, int G, int DC>
@@ -476,8 +479,7 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 8));
   q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));
   q.div_bh = FastDiv::make(static_cast<uint32_t>(p.bh));
-  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(q);
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, threads, stream, q);
 }
 
 }  // namespace

@@ -201,6 +201,25 @@ cudaError_t attention_scratch(float **ptr, int64_t *max_floats);
 int64_t attention_scratch_floats();
 // SM count of the current device (looked up once per device).
 int current_sm_count();
+// Launch of a grid-stride kernel that starts with grid_dependency_wait():
+// with programmatic stream serialization, so that its blocks are scheduled
+// while the previous kernel in the stream drains and start their work the
+// moment it completes (the ordering is that of a plain launch).
+template <typename P>
+cudaError_t launch_dependent(void (*kern)(P), int64_t grid, int threads, cudaStream_t stream,
+                             const P &params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, params);
+}
 // Grid of one block per `threads` units for a grid-stride kernel, clamped to
 // the launch limit of 2^31 - 1 blocks in x (at least one block).
 inline int64_t flat_grid(int64_t units, int threads) {

@@ -81,6 +81,8 @@ constexpr int kScoreRow = kScoreChunk * 2 + 16;   // padded row: conflict-free 1
 constexpr int kScoreMaxHeads = 64;
 
 __global__ void __launch_bounds__(kThreads, 3) sink_score_tile_kernel(const __grid_constant__ SinkParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   __shared__ __align__(16) unsigned char stage[kWarps][kScoreTile * kScoreRow];
   __shared__ float norm[kScoreMaxHeads * kScoreTile];
   // grid = layers x sequences x tiles (< 2^31 blocks, host-checked)
@@ -165,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 3) sink_score_tile_kernel(const __gr
 // thread = (job, sequence, new token): its score into the scores scratch
 // (more than 64 heads per sequence)
 __global__ void __launch_bounds__(kThreads) sink_score_kernel(const __grid_constant__ SinkParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   const int64_t u = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   if (u >= static_cast<int64_t>(p.n_jobs) * p.batch * p.n) return;
   const int64_t i = u % p.n, js = u / p.n;
@@ -254,6 +258,8 @@ struct RegTop8 {
 // then across the warps' winners in warp 0) give the k best overall.
 template <typename List, int NT>
 __global__ void __launch_bounds__(NT) sink_select_kernel(const __grid_constant__ SinkParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   constexpr int NW = NT / 32;
   const int job = static_cast<int>(blockIdx.x / p.batch);
   const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
@@ -345,6 +351,8 @@ __global__ void __launch_bounds__(NT) sink_select_kernel(const __grid_constant__
 // overflowing store keeps what fits and sets bit 1 of the device fault
 // word; the mask still flags every flushed top-k token.
 __global__ void __launch_bounds__(kThreads) sink_prepare_kernel(const __grid_constant__ SinkParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   const int job = static_cast<int>(blockIdx.x / p.batch);
   const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
   const SinkJob &J = p.jobs[job];
@@ -402,6 +410,8 @@ __global__ void __launch_bounds__(kThreads) sink_prepare_kernel(const __grid_con
 
 // thread = (job, sequence, sink slot, head, 16-byte piece)
 __global__ void __launch_bounds__(kThreads) sink_restore_kernel(const __grid_constant__ SinkParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   const int64_t chunks = p.d / 8;
   const int64_t per_seq = static_cast<int64_t>(p.sink_cap) * p.heads * chunks;
   const int64_t u = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
@@ -431,38 +441,38 @@ unsigned blocks_for(int64_t threads) {
 }  // namespace
 
 cudaError_t launch_sink_update(const SinkParams &p, cudaStream_t stream) {
+  cudaError_t e;
   if (p.heads <= kScoreMaxHeads) {
     const int64_t tiles = (p.n + kScoreTile - 1) / kScoreTile;
-    sink_score_tile_kernel<<<static_cast<unsigned>(p.n_jobs * p.batch * tiles), kThreads, 0,
-                             stream>>>(p);
+    e = launch_dependent(sink_score_tile_kernel, p.n_jobs * p.batch * tiles, kThreads, stream, p);
   } else {
-    sink_score_kernel<<<blocks_for(static_cast<int64_t>(p.n_jobs) * p.batch * p.n), kThreads, 0,
-                        stream>>>(p);
+    e = launch_dependent(sink_score_kernel,
+                         static_cast<int64_t>(blocks_for(static_cast<int64_t>(p.n_jobs) * p.batch * p.n)),
+                         kThreads, stream, p);
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const unsigned blocks = static_cast<unsigned>(p.n_jobs * p.batch);
+  const int64_t blocks = static_cast<int64_t>(p.n_jobs) * p.batch;
   // 1024 threads: a short share of the scores per thread (the offers are the
   // serial part); the list heads meet in two shuffle stages per round
   constexpr int kSelectThreads = 1024;
   if (p.k_top <= 8)
-    sink_select_kernel<RegTop8, kSelectThreads><<<blocks, kSelectThreads, 0, stream>>>(p);
-  else
-    sink_select_kernel<LocalTop<kMaxSinkTop>, kSelectThreads><<<blocks, kSelectThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+    return launch_dependent(sink_select_kernel<RegTop8, kSelectThreads>, blocks, kSelectThreads,
+                            stream, p);
+  return launch_dependent(sink_select_kernel<LocalTop<kMaxSinkTop>, kSelectThreads>, blocks,
+                          kSelectThreads, stream, p);
 }
 
 cudaError_t launch_sink_prepare(const SinkParams &p, cudaStream_t stream) {
-  sink_prepare_kernel<<<static_cast<unsigned>(p.n_jobs * p.batch), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(sink_prepare_kernel, static_cast<int64_t>(p.n_jobs) * p.batch, kThreads,
+                          stream, p);
 }
 
 cudaError_t launch_sink_restore(const SinkParams &p, cudaStream_t stream) {
   const int64_t threads =
       static_cast<int64_t>(p.n_jobs) * p.batch * p.sink_cap * p.heads * (p.d / 8);
   if (threads == 0) return cudaSuccess;
-  sink_restore_kernel<<<blocks_for(threads), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(sink_restore_kernel, static_cast<int64_t>(blocks_for(threads)), kThreads,
+                          stream, p);
 }
 
 }  // namespace kivi_impl

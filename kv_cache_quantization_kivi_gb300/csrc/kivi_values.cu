@@ -92,6 +92,8 @@ __device__ __forceinline__ void warp_store_units(uint32_t *blk, uint32_t lane, b
 template <int BITS, int G, int DC, int MODE>
 __global__ void __launch_bounds__(kBlockThreads, 4)
     value_quant_kernel(const __grid_constant__ QuantParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   constexpr bool RECON = MODE == kQuantRecon;
   constexpr bool SINK = MODE == kQuantSink;
   constexpr int L = G < 32 ? 1 : G / 32;  // lanes per group
@@ -290,6 +292,8 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
 template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(kBlockThreads)
     value_dequant_kernel(const __grid_constant__ DequantParams p) {
+  kivi_dev::grid_dependency_wait();
+  kivi_dev::grid_launch_dependents();
   constexpr int L = G < 32 ? 1 : G / 32;  // lanes per group
   constexpr int SUB = G < 32 ? 32 / G : 1; // groups per thread
   constexpr int W = CodeFmt<BITS>::W;
@@ -388,8 +392,7 @@ cudaError_t value_quant_launch(const QuantParams &p, cudaStream_t stream) {
   // fused reconstruction at G = 16, where the flat grid is 12% faster.
   const int64_t flat = flat_grid(units, threads);
   grid = (MODE == kQuantRecon && G == 16) ? flat : std::min<int64_t>(flat, 3 * grid);
-  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(with_dividers(p));
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, threads, stream, with_dividers(p));
 }
 
 // The dequantize kernels take one block per kBlockThreads units rather than a
@@ -404,8 +407,7 @@ cudaError_t value_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   auto kern = value_dequant_kernel<BITS, G, DC>;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
   const int64_t grid = flat_grid(units, threads);
-  kern<<<static_cast<unsigned>(grid), threads, 0, stream>>>(with_dividers(p));
-  return cudaGetLastError();
+  return launch_dependent(kern, grid, threads, stream, with_dividers(p));
 }
 
 }  // namespace
