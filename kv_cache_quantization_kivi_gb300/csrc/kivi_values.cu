@@ -343,14 +343,45 @@ __global__ void __launch_bounds__(kBlockThreads)
         ze[sg] = __ldcs(J.zero + so + sg);
         nsc[sg] = __fmul_rn(sc[sg], -8388608.0f);  // -2^23 * scale, exact
       }
+      if constexpr (BITS == 2) {
+        // The four possible fp16 reconstructions of a group (codes 0..3, the
+        // same arithmetic as below) as an 8-byte table in two registers;
+        // code q is bytes 2q, 2q + 1, and a byte permute picks two codes'
+        // values at once.  Four codes (one byte of a word) are spread one to
+        // a byte, and q * 0x22 + 0x10 gives the nibble pair (2q, 2q + 1):
+        // the permute selectors of channels (4k, 4k + 1) in the low half and
+        // (4k + 2, 4k + 3) in the high half.
+        uint32_t lo[SUB], hi[SUB];
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const int sg = SUB == 1 ? 0 : e / G;       // channels e, e + 1 share a group
-        const uint32_t q0 = (w[e / W] >> ((e % W) * BITS)) & Q;
-        const uint32_t q1 = (w[(e + 1) / W] >> (((e + 1) % W) * BITS)) & Q;
-        const float r0 = recon_f32(q0, sc[sg], nsc[sg], ze[sg]);
-        const float r1 = recon_f32(q1, sc[sg], nsc[sg], ze[sg]);
-        out[e >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
+        for (int sg = 0; sg < SUB; ++sg) {
+          lo[sg] = h2_as_u32(__floats2half2_rn(recon_f32(0u, sc[sg], nsc[sg], ze[sg]),
+                                               recon_f32(1u, sc[sg], nsc[sg], ze[sg])));
+          hi[sg] = h2_as_u32(__floats2half2_rn(recon_f32(2u, sc[sg], nsc[sg], ze[sg]),
+                                               recon_f32(3u, sc[sg], nsc[sg], ze[sg])));
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {              // word i: channels 16 i .. 16 i + 15
+          const int sg = SUB == 1 ? 0 : i;         // at G = 16 a word is one group
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t bt = (w[i] >> (8 * k)) & 0xFFu;
+            uint32_t x = (bt | (bt << 12)) & 0x000F000Fu;
+            x = (x | (x << 6)) & 0x03030303u;      // code 4k + j in byte j
+            const uint32_t sel = x * 0x22u + 0x10101010u;
+            out[8 * i + 2 * k] = __byte_perm(lo[sg], hi[sg], sel);
+            out[8 * i + 2 * k + 1] = __byte_perm(lo[sg], hi[sg], sel >> 16);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int sg = SUB == 1 ? 0 : e / G;     // channels e, e + 1 share a group
+          const uint32_t q0 = (w[e / W] >> ((e % W) * BITS)) & Q;
+          const uint32_t q1 = (w[(e + 1) / W] >> (((e + 1) % W) * BITS)) & Q;
+          const float r0 = recon_f32(q0, sc[sg], nsc[sg], ze[sg]);
+          const float r1 = recon_f32(q1, sc[sg], nsc[sg], ze[sg]);
+          out[e >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
+        }
       }
     }
     warp_store_units(blk, lane, active, out, y, base, total);
