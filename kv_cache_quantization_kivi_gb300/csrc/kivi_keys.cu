@@ -414,6 +414,54 @@ __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant_
         J.codes + b * p.codes_bh_stride + (g * (G / W) + split * (TPU / W)) * D + ch * 8;
     __half *y = static_cast<__half *>(J.y) + b * p.y_bh_stride + ch * 8;
     const int64_t t0 = g * G + split * TPU;
+    if constexpr (BITS == 2) {
+      // Each channel's four fp16 reconstructions (codes 0..3, the same
+      // arithmetic as below) as an 8-byte table in two registers; one byte
+      // permute fetches a channel's values for two consecutive tokens (its
+      // selector from the two codes, q * 0x22 + 0x10 per byte after spreading
+      // four codes one to a byte), and a 2 x 2 transpose of halves (two more
+      // permutes) turns channel pairs of tokens into token rows of channel
+      // pairs.
+      uint32_t lo[8], hi[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        lo[c] = h2_as_u32(__floats2half2_rn(recon_f32(0u, sc[c], nsc[c], ze[c]),
+                                            recon_f32(1u, sc[c], nsc[c], ze[c])));
+        hi[c] = h2_as_u32(__floats2half2_rn(recon_f32(2u, sc[c], nsc[c], ze[c]),
+                                            recon_f32(3u, sc[c], nsc[c], ze[c])));
+      }
+#pragma unroll 1
+      for (int wr = 0; wr < TPU / W; ++wr) {
+        const uint4 ca = ld_stream(cw + static_cast<int64_t>(wr) * D);
+        const uint4 cb = ld_stream(cw + static_cast<int64_t>(wr) * D + 4);
+        const uint32_t words[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {         // tokens 4 kb .. 4 kb + 3 of the word row
+          uint32_t a01[8], a23[8];              // channel c: (token 0, 1) and (token 2, 3)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t bt = (words[c] >> (8 * kb)) & 0xFFu;
+            uint32_t x = (bt | (bt << 12)) & 0x000F000Fu;
+            x = (x | (x << 6)) & 0x03030303u;   // code of token j in byte j
+            const uint32_t sel = x * 0x22u + 0x10101010u;
+            a01[c] = __byte_perm(lo[c], hi[c], sel);
+            a23[c] = __byte_perm(lo[c], hi[c], sel >> 16);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int64_t t = t0 + wr * W + 4 * kb + j;
+            if (t >= p.rows) break;
+            const uint32_t *src = j < 2 ? a01 : a23;
+            const uint32_t pick = (j & 1) ? 0x7632u : 0x5410u;   // high or low halves
+            uint32_t out[4];
+#pragma unroll
+            for (int cp = 0; cp < 4; ++cp) out[cp] = __byte_perm(src[2 * cp], src[2 * cp + 1], pick);
+            st_stream(y + t * D, make_uint4(out[0], out[1], out[2], out[3]));
+          }
+        }
+      }
+      continue;
+    }
 #pragma unroll 1
     for (int wr = 0; wr < TPU / W; ++wr) {
       const uint4 ca = ld_stream(cw + static_cast<int64_t>(wr) * D);
