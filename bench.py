@@ -299,10 +299,12 @@ class PrefillFlush:
         self.e2e_graph = None
         return h2d, d2h
 
-    # measured on the llama prefill step (GB/s end to end): 7 equal chunks
-    # 295, with a (1, 1, 2) ramp 301.5, 5 chunks with a (1, 1, 2, 2) ramp 303
-    E2E_CHUNKS = 5
-    E2E_RAMP = (1, 1, 2, 2)
+    # measured end to end (GB/s, llama3_2_3b_prefill / qwen2_5_7b_long): 7
+    # equal chunks 295 / 317, with a (1, 1, 2) ramp 301 / 325; 5 chunks with a
+    # (1, 1, 2, 2) ramp 303 / 178 (the 5.5-layer chunks of the long prompt
+    # copy slowly)
+    E2E_CHUNKS = 7
+    E2E_RAMP = (1, 1, 2)
 
     def e2e_step(self, stream):
         import torch
