@@ -163,9 +163,10 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
   constexpr int WPT = TPT / W;               // words per channel per thread
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
   // split-major units with the shared-memory exchange: with the fused
-  // reconstruction (whose row pieces would otherwise be 128 / T bytes); the
-  // plain quantize keeps the shuffle order, measured 2-7% faster without it
-  constexpr bool XCH = RECON && DC == 128 && T > 1;
+  // reconstruction (whose row pieces would otherwise be 128 / T bytes) and
+  // the plain 2-bit quantize (+1% at G = 64, +3% at G = 128); the plain 4-
+  // and 8-bit quantize keep the shuffle order, measured 5-9% faster
+  constexpr bool XCH = (RECON || (MODE == kQuantPlain && BITS == 2)) && DC == 128 && T > 1;
   const float qf = static_cast<float>(Q);
   __shared__ uint2 xch[XCH ? 2 : 1][XCH ? kKeyThreads : 1];
   int parity = 0;
