@@ -307,7 +307,9 @@ typedef struct {
 } kivi_sink_layer;
 
 /* batch: sequences (cache->bh / batch KV heads each); k_top: 0..64;
- * sink_cap: sink store capacity per sequence; reserved must be 0. */
+ * sink_cap: sink store capacity per sequence; reserved must be 0.  Every
+ * sink call also requires n_layers * batch * r_cap and
+ * n_layers * bh * sink_cap * d / 8 to stay below 2^31 (KIVI_ERR_INVAL). */
 typedef struct {
     int64_t batch;
     int32_t k_top;

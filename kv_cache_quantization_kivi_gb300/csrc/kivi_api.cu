@@ -627,6 +627,11 @@ static kivi_status check_sinks(const kivi_sink_layer *sinks, int n_layers, const
   if (cfg->batch < 1 || c->bh % cfg->batch != 0 || cfg->k_top < 0 ||
       cfg->k_top > kivi_impl::kMaxSinkTop || cfg->sink_cap < 0 || cfg->reserved != 0)
     return KIVI_ERR_INVAL;
+  // launch sizes of the sink kernels: the update's score blocks (32 tokens)
+  // and tokens over all layers and sequences, the restore's 16-byte pieces
+  if (sat_mul(sat_mul(n_layers, cfg->batch), c->r_cap) > kMaxUnits ||
+      sat_mul(sat_mul(sat_mul(n_layers, c->bh), cfg->sink_cap), c->d / 8) > kMaxUnits)
+    return KIVI_ERR_INVAL;
   for (int l = 0; l < n_layers; ++l) {
     const kivi_sink_layer &S = sinks[l];
     const void *ptrs[9] = {S.top_pos, S.top_score, S.top_count, S.sink_pos,

@@ -351,6 +351,15 @@ def test_sink_validation():
     assert upd(c, _sinks(), cfg(), 30, 11) == 1                 # past the residual
     assert upd(c, _sinks(), cfg(), 0, 0) == 0                   # nothing to score
     assert upd(c, _sinks(), cfg(k_top=0), 0, 8) == 0            # no top-k kept
+    # launch sizes beyond 2^31 - 1 units are refused before any launch: 128
+    # layers x 2^16 sequences x 2^10 ring rows of tokens to score, and 128 x
+    # 2^16 sequence-heads x 2^10 sink slots x 4 pieces to restore
+    upd128 = lambda cc, cf: L.kivi_sink_update(_layers(128), _sinks(128), 128,  # noqa
+                                                C.byref(cc), C.byref(cf), 0, 8, None)
+    big = _cache(bh=1 << 16, d=32, r_cap=1 << 10, cap=0, n_res=40)
+    assert upd128(big, cfg(batch=1 << 16, sink_cap=0)) == 1
+    mid = _cache(bh=1 << 10, d=32, r_cap=32, cap=0, n_res=32)
+    assert upd128(mid, cfg(batch=1 << 10, sink_cap=1 << 14)) == 1
     out = C.c_int64(-1)
     c2 = _cache(n_res=63)                                       # nothing to flush
     assert L.kivi_flush_sink(_layers(2), _sinks(), 2, C.byref(c2), C.byref(cfg()),
