@@ -153,8 +153,8 @@ kivi_status kivi_quantize_keys(const void *x, int64_t bh, int64_t s, int64_t d,
   p.x_bh_stride = x_bh_stride;
   p.codes_bh_stride = codes_bh_stride;
   p.sz_bh_stride = sz_bh_stride;
-  p.jobs[0] = {x, codes, scale, zero};
-  return cuda_status(kivi_impl::launch_key_quant(p, group, bits, false, stream));
+  p.jobs[0] = {x, codes, scale, zero, nullptr, nullptr};
+  return cuda_status(kivi_impl::launch_key_quant(p, group, bits, kivi_impl::kQuantPlain, stream));
 }
 
 kivi_status kivi_quantize_values(const void *x, int64_t bh, int64_t s, int64_t d,
@@ -182,8 +182,8 @@ kivi_status kivi_quantize_values(const void *x, int64_t bh, int64_t s, int64_t d
   p.x_bh_stride = x_bh_stride;
   p.codes_bh_stride = codes_bh_stride;
   p.sz_bh_stride = sz_bh_stride;
-  p.jobs[0] = {x, codes, scale, zero};
-  return cuda_status(kivi_impl::launch_value_quant(p, group, bits, false, stream));
+  p.jobs[0] = {x, codes, scale, zero, nullptr, nullptr};
+  return cuda_status(kivi_impl::launch_value_quant(p, group, bits, kivi_impl::kQuantPlain, stream));
 }
 
 // Fused quantize + dequantize: the same kernels with the reconstruction
@@ -219,8 +219,8 @@ kivi_status kivi_fakequant_keys(const void *x, int64_t bh, int64_t s, int64_t d,
   p.codes_bh_stride = store ? codes_bh_stride : 0;
   p.sz_bh_stride = store ? sz_bh_stride : 0;
   p.y_bh_stride = y_bh_stride;
-  p.jobs[0] = {x, codes, scale, zero, y};
-  return cuda_status(kivi_impl::launch_key_quant(p, group, bits, true, stream));
+  p.jobs[0] = {x, codes, scale, zero, y, nullptr};
+  return cuda_status(kivi_impl::launch_key_quant(p, group, bits, kivi_impl::kQuantRecon, stream));
 }
 
 kivi_status kivi_fakequant_values(const void *x, int64_t bh, int64_t s, int64_t d,
@@ -254,8 +254,8 @@ kivi_status kivi_fakequant_values(const void *x, int64_t bh, int64_t s, int64_t 
   p.codes_bh_stride = store ? codes_bh_stride : 0;
   p.sz_bh_stride = store ? sz_bh_stride : 0;
   p.y_bh_stride = y_bh_stride;
-  p.jobs[0] = {x, codes, scale, zero, y};
-  return cuda_status(kivi_impl::launch_value_quant(p, group, bits, true, stream));
+  p.jobs[0] = {x, codes, scale, zero, y, nullptr};
+  return cuda_status(kivi_impl::launch_value_quant(p, group, bits, kivi_impl::kQuantRecon, stream));
 }
 
 kivi_status kivi_dequantize_keys(const uint32_t *codes, int64_t codes_bh_stride,
@@ -412,17 +412,18 @@ static kivi_status flush_impl(const kivi_layer *layers, int n_layers, kivi_cache
   vp.out0 = cache->s_q;
   for (int l = 0; l < n_layers; ++l) {
     const kivi_layer &L = layers[l];
-    kp.jobs[l] = {L.k_res, L.k_codes, L.k_scale, L.k_zero, recon ? k_hat[l] : nullptr};
-    vp.jobs[l] = {L.v_res, L.v_codes, L.v_scale, L.v_zero, recon ? v_hat[l] : nullptr};
+    kp.jobs[l] = {L.k_res, L.k_codes, L.k_scale, L.k_zero, recon ? k_hat[l] : nullptr, nullptr};
+    vp.jobs[l] = {L.v_res, L.v_codes, L.v_scale, L.v_zero, recon ? v_hat[l] : nullptr, nullptr};
   }
   cudaStream_t s = stream;
   kivi_status r = cuda_status(record(events, 0, s));
   if (r != KIVI_OK) return r;
-  r = cuda_status(kivi_impl::launch_key_quant(kp, cache->group, cache->bits, recon, s));
+  const int mode = recon ? kivi_impl::kQuantRecon : kivi_impl::kQuantPlain;
+  r = cuda_status(kivi_impl::launch_key_quant(kp, cache->group, cache->bits, mode, s));
   if (r != KIVI_OK) return r;
   r = cuda_status(record(events, 1, s));
   if (r != KIVI_OK) return r;
-  r = cuda_status(kivi_impl::launch_value_quant(vp, cache->group, cache->bits, recon, s));
+  r = cuda_status(kivi_impl::launch_value_quant(vp, cache->group, cache->bits, mode, s));
   if (r != KIVI_OK) return r;
   r = cuda_status(record(events, 2, s));
   if (r != KIVI_OK) return r;
@@ -571,7 +572,7 @@ static kivi_status attn_prepare(const kivi_layer *layers, int n_layers, const ki
   for (int l = 0; l < n_layers; ++l) {
     const kivi_layer &L = layers[l];
     p->jobs[l] = {L.k_codes, L.k_scale, L.k_zero, L.v_codes, L.v_scale, L.v_zero,
-                  L.k_res, L.v_res, q[l], out[l]};
+                  L.k_res, L.v_res, q[l], out[l], nullptr, nullptr, nullptr, nullptr};
   }
   return KIVI_OK;
 }

@@ -461,27 +461,27 @@ __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant_
           }
         }
       }
-      continue;
-    }
+    } else {
 #pragma unroll 1
-    for (int wr = 0; wr < TPU / W; ++wr) {
-      const uint4 ca = ld_stream(cw + static_cast<int64_t>(wr) * D);
-      const uint4 cb = ld_stream(cw + static_cast<int64_t>(wr) * D + 4);
-      const uint32_t words[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+      for (int wr = 0; wr < TPU / W; ++wr) {
+        const uint4 ca = ld_stream(cw + static_cast<int64_t>(wr) * D);
+        const uint4 cb = ld_stream(cw + static_cast<int64_t>(wr) * D + 4);
+        const uint32_t words[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
 #pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const int64_t t = t0 + wr * W + k;
-        if (t >= p.rows) break;
-        uint32_t out[4];
+        for (int k = 0; k < W; ++k) {
+          const int64_t t = t0 + wr * W + k;
+          if (t >= p.rows) break;
+          uint32_t out[4];
 #pragma unroll
-        for (int c = 0; c < 8; c += 2) {
-          const uint32_t q0 = (words[c] >> (k * BITS)) & Q;
-          const uint32_t q1 = (words[c + 1] >> (k * BITS)) & Q;
-          const float r0 = recon_f32(q0, sc[c], nsc[c], ze[c]);
-          const float r1 = recon_f32(q1, sc[c + 1], nsc[c + 1], ze[c + 1]);
-          out[c >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
+          for (int c = 0; c < 8; c += 2) {
+            const uint32_t q0 = (words[c] >> (k * BITS)) & Q;
+            const uint32_t q1 = (words[c + 1] >> (k * BITS)) & Q;
+            const float r0 = recon_f32(q0, sc[c], nsc[c], ze[c]);
+            const float r1 = recon_f32(q1, sc[c + 1], nsc[c + 1], ze[c + 1]);
+            out[c >> 1] = h2_as_u32(__floats2half2_rn(r0, r1));
+          }
+          st_stream(y + t * D, make_uint4(out[0], out[1], out[2], out[3]));
         }
-        st_stream(y + t * D, make_uint4(out[0], out[1], out[2], out[3]));
       }
     }
   }
