@@ -55,6 +55,48 @@ CSRC_FILES = {
 }
 
 
+def spread_us(ms: list) -> dict:
+    """Per-step times of one kernel (ms) -> median, min, max and the
+    interquartile range relative to the median (the run-to-run noise of an
+    unchanged kernel), in microseconds and percent."""
+    v = sorted(ms)
+    n = len(v)
+
+    def q(f):                       # linear interpolation between order statistics
+        x = f * (n - 1)
+        i = int(x)
+        return v[i] if i + 1 >= n else v[i] + (v[i + 1] - v[i]) * (x - i)
+
+    med = q(0.5)
+    return {"median_us": round(med * 1e3, 2), "min_us": round(v[0] * 1e3, 2),
+            "max_us": round(v[-1] * 1e3, 2),
+            "iqr_pct": round((q(0.75) - q(0.25)) / med * 100, 2) if med > 0 else None}
+
+
+def host_cpu() -> dict:
+    """Logical CPUs and the CPU model of the host (for the CPU baselines)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
 def e2e_bounds(layers: int, n_chunks: int, ramp=()) -> list:
     """Layer bounds of the end-to-end pipeline's chunks: about n_chunks equal
     chunks, the first of them split into the ramp's smaller sizes (the
@@ -1166,7 +1208,8 @@ def run_kivi(args):
         gbs = wl.kernel_bytes[k] / (avg * 1e-3) / 1e9
         kernels[k] = {"avg_us": round(avg * 1e3, 2), "gbs": round(gbs, 1),
                       "frac_of_measured": round(gbs / peak, 4),
-                      "share": round(sum(k_ms[k]) / total_kernel_ms, 4)}
+                      "share": round(sum(k_ms[k]) / total_kernel_ms, 4),
+                      **spread_us(k_ms[k])}
     dom = max(wl.kernels, key=lambda k: sum(k_ms[k]))
     dom_avg_s = sum(k_ms[dom]) / len(k_ms[dom]) * 1e-3
     achieved = wl.kernel_bytes[dom] / dom_avg_s / 1e9
@@ -1205,7 +1248,7 @@ def run_kivi(args):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cb, cs, what = wl.cpu_sample(args.cpu_seconds)
         cpu = {"value": round(cb / cs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{what}; {cs:.1f} s single-threaded on the host"}
+               "sample": f"{what}; {cs:.1f} s single-threaded on the host", **host_cpu()}
 
     config = wl.config()
     config["bytes_per_step"] = wl.step_bytes
@@ -1291,7 +1334,7 @@ def run_reference(args):
                        "head_dim": w.head_dim, "bits": w.bits, "group": w.group,
                        "residual": w.residual},
             "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, **host_cpu()},
             "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

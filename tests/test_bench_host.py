@@ -39,3 +39,19 @@ def test_e2e_bounds_of_the_benchmarked_prefill():
     bench = load_bench()
     b = bench.e2e_bounds(28, bench.PrefillFlush.E2E_CHUNKS, bench.PrefillFlush.E2E_RAMP)
     assert b == [0, 1, 2, 4, 8, 12, 16, 20, 24, 28]
+
+
+def test_kernel_time_spread():
+    """Median, extremes and interquartile range of per-step kernel times."""
+    bench = load_bench()
+    ms = [0.050, 0.051, 0.049, 0.052, 0.050, 0.060, 0.048]   # sorted: 48 49 50 50 51 52 60 us
+    s = bench.spread_us(ms)
+    assert s["median_us"] == 50.0 and s["min_us"] == 48.0 and s["max_us"] == 60.0
+    assert s["iqr_pct"] == 4.0                                 # (51.5 - 49.5) / 50
+    assert bench.spread_us([0.1]) == {"median_us": 100.0, "min_us": 100.0, "max_us": 100.0,
+                                      "iqr_pct": 0.0}
+
+
+def test_host_cpu_description():
+    info = load_bench().host_cpu()
+    assert info["nproc"] >= 1 and isinstance(info["cpu_model"], str) and info["cpu_model"]
