@@ -646,7 +646,7 @@ class DecodeFlush:
                 "store_tokens": w.store_prefill, "tokens_flushed_per_step": w.new_per_step,
                 "consecutive_flushes": self.cycle,
                 "residual_compaction_bytes_per_step": 0,
-                "residual": "a ring of 2R rows: the flush advances its head, copies nothing",
+                "residual_storage": "a ring of 2R rows: the flush advances its head, copies nothing",
                 "step": "one decode flush of every layer (keys and values)"}
 
     def step(self, stream, ev=None):
