@@ -55,3 +55,15 @@ def test_kernel_time_spread():
 def test_host_cpu_description():
     info = load_bench().host_cpu()
     assert info["nproc"] >= 1 and isinstance(info["cpu_model"], str) and info["cpu_model"]
+
+
+def test_decode_config_reports_residual_and_compaction():
+    """The decode flush's config keeps the residual length as a number and
+    states the compaction bytes (none: the residual is a ring)."""
+    bench = load_bench()
+    import workloads as W
+    d = bench.DecodeFlush.__new__(bench.DecodeFlush)
+    d.w, d.cycle = W.CONFIGS["batched_decode"], 100
+    c = d.config()
+    assert c["residual"] == 32 and c["residual_compaction_bytes_per_step"] == 0
+    assert c["workload"] == "batched_decode" and c["tokens_flushed_per_step"] == 32
