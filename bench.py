@@ -400,21 +400,30 @@ class PrefillFlush:
         done_bytes, t_total, layers = 0.0, 0.0, 0
         elems = w.bh * self.n * w.head_dim
         W_ = 32 // w.bits
+        t_fn = {"flush": 0.0, "dequantize_keys": 0.0, "dequantize_values": 0.0}
         for l in range(w.layers):
             st = O.Store(w.bh, w.head_dim, w.seq, w.group, w.bits)
             k, v = self.k_host[l], self.v_host[l]
             t0 = time.perf_counter()
             n, _, _, _ = O.flush(k, v, st, w.residual, 0, 0, w.seq)
+            t1 = time.perf_counter()
             O.dequantize_keys(st.k_codes[:, :n // W_], st.k_scale[:, :n // w.group],
                               st.k_zero[:, :n // w.group], n, w.group, w.bits)
+            t2 = time.perf_counter()
             O.dequantize_values(st.v_codes[:, :n], st.v_scale[:, :n], st.v_zero[:, :n],
                                 w.group, w.bits)
-            t_total += time.perf_counter() - t0
+            t3 = time.perf_counter()
+            t_fn["flush"] += t1 - t0
+            t_fn["dequantize_keys"] += t2 - t1
+            t_fn["dequantize_values"] += t3 - t2
+            t_total += t3 - t0
             done_bytes += 4 * elems * bytes_per_elem(w.bits, w.group)
             layers += 1
             if t_total >= budget_s:
                 break
-        return done_bytes, t_total, f"{layers} of {w.layers} layers (flush + dequantize, keys and values)"
+        per_fn = ", ".join(f"{k} {v / layers * 1e3:.0f} ms" for k, v in t_fn.items())
+        return done_bytes, t_total, (f"{layers} of {w.layers} layers (flush + dequantize, keys "
+                                     f"and values; per layer: {per_fn})")
 
 
 class SinkPrefillFlush(PrefillFlush):

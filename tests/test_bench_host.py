@@ -67,3 +67,27 @@ def test_decode_config_reports_residual_and_compaction():
     c = d.config()
     assert c["residual"] == 32 and c["residual_compaction_bytes_per_step"] == 0
     assert c["workload"] == "batched_decode" and c["tokens_flushed_per_step"] == 32
+
+
+def test_cpu_sample_times_each_oracle_function():
+    """The benchmark's CPU leg (the oracle's flush and both dequantizations of
+    whole layers) on the tiny workload: bytes, time and a per-function
+    breakdown."""
+    import numpy as np
+    import oracle as O
+    import workloads as W
+    bench = load_bench()
+    w = W.CONFIGS["tiny_flush"]
+    pf = bench.PrefillFlush.__new__(bench.PrefillFlush)
+    pf.w = w
+    pf.n = O.flush_size(w.seq, w.residual, w.group)
+    shape = (w.layers, w.bh, w.seq, w.head_dim)
+    pf.k_host = np.zeros(shape, np.uint16)
+    pf.v_host = np.zeros(shape, np.uint16)
+    for l in range(w.layers):
+        W.fill(w, l, "k", pf.k_host[l])
+        W.fill(w, l, "v", pf.v_host[l])
+    done, secs, what = pf.cpu_sample(0.0)                 # stops after one layer
+    elems = w.bh * pf.n * w.head_dim
+    assert done == 4 * elems * bench.bytes_per_elem(w.bits, w.group) and secs > 0
+    assert what.startswith("1 of 1 layers") and "dequantize_values" in what
