@@ -93,6 +93,9 @@ def lib():
                                             _u32p, _f32p, _f32p, _u32p, _f32p, _f32p,
                                             _i64p, _i64p, _i64p]
             L.kivi_oracle_flush.restype = _i64
+            L.kivi_oracle_append.argtypes = [_u16p, _u16p, _i64, _i64, _i64, _i64, _i64p,
+                                             _u16p, _u16p, _i64]
+            L.kivi_oracle_append.restype = C.c_int
             L.kivi_oracle_attention.argtypes = [_u16p, _i64, _u16p, _u16p, _i64, _i64,
                                                 C.c_double, _f64p]
             L.kivi_oracle_attention.restype = C.c_int
@@ -247,6 +250,21 @@ class Store:
         self.v_codes = np.zeros((bh, cap, d // w), np.uint32)
         self.v_scale = np.zeros((bh, cap, d // group), np.float32)
         self.v_zero = np.zeros((bh, cap, d // group), np.float32)
+
+
+def append(k_res: np.ndarray, v_res: np.ndarray, res_head: int, n_res: int,
+           k_new: np.ndarray, v_new: np.ndarray) -> int:
+    """Writes new tokens k_new, v_new [bh, n, d] (fp16 bits) behind the
+    residual of the rings k_res, v_res [bh, r_cap, d] (in place); returns the
+    new residual count."""
+    bh, r_cap, d = k_res.shape
+    assert k_res.flags.c_contiguous and v_res.flags.c_contiguous
+    k_new = np.ascontiguousarray(k_new, dtype=np.uint16)
+    v_new = np.ascontiguousarray(v_new, dtype=np.uint16)
+    cnt = C.c_int64(n_res)
+    _check(lib().kivi_oracle_append(k_res, v_res, bh, d, r_cap, res_head, C.byref(cnt), k_new,
+                                    v_new, k_new.shape[1]), "append")
+    return int(cnt.value)
 
 
 def flush(k_res: np.ndarray, v_res: np.ndarray, store: Store, residual: int,

@@ -293,6 +293,27 @@ int64_t kivi_oracle_flush_size(int64_t n_res, int residual, int group)
     return ((n_res - residual) / group) * group;
 }
 
+int kivi_oracle_append(uint16_t *k_res, uint16_t *v_res, int64_t bh, int64_t d, int64_t r_cap,
+                       int64_t res_head, int64_t *n_res, const uint16_t *k_new,
+                       const uint16_t *v_new, int64_t n)
+{
+    if (bh < 0 || d <= 0 || r_cap <= 0 || n < 0) return -1;
+    if (res_head < 0 || res_head >= r_cap || *n_res < 0 || *n_res > r_cap) return -1;
+    if (*n_res + n > r_cap) return -3;
+    for (int64_t b = 0; b < bh; ++b) {
+        for (int64_t i = 0; i < n; ++i) {
+            /* new token i becomes logical residual token n_res + i */
+            const int64_t row = (res_head + *n_res + i) % r_cap;
+            for (int64_t c = 0; c < d; ++c) {
+                k_res[(b * r_cap + row) * d + c] = k_new[(b * n + i) * d + c];
+                v_res[(b * r_cap + row) * d + c] = v_new[(b * n + i) * d + c];
+            }
+        }
+    }
+    *n_res += n;
+    return 0;
+}
+
 int64_t kivi_oracle_flush(const uint16_t *k_res, const uint16_t *v_res,
                           int64_t bh, int64_t d, int64_t r_cap, int64_t cap,
                           int group, int bits, int residual,

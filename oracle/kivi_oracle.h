@@ -99,6 +99,17 @@ int kivi_oracle_value_row(const uint16_t *x_row, int64_t d, int group, int bits,
  *   n_flush = floor((n_res - R) / G) * G  if n_res >= R + G, else 0. */
 int64_t kivi_oracle_flush_size(int64_t n_res, int residual, int group);
 
+/* Append of n new tokens behind the residual of one layer ([POST] "What
+ * we're actually optimizing": the newest tokens enter the fp16 residual
+ * window and age out of it by flushes).  New token i of k_new, v_new
+ * (fp16 [bh][n][d]) becomes logical residual token *n_res + i, stored at
+ * ring row (res_head + *n_res + i) % r_cap of k_res, v_res ([bh][r_cap][d]);
+ * then *n_res += n.  Returns 0, -1 (invalid arguments) or -3 (the ring
+ * would hold more than r_cap tokens; nothing written). */
+int kivi_oracle_append(uint16_t *k_res, uint16_t *v_res, int64_t bh, int64_t d, int64_t r_cap,
+                       int64_t res_head, int64_t *n_res, const uint16_t *k_new,
+                       const uint16_t *v_new, int64_t n);
+
 /* Flush of one layer (keys and values) from an fp16 residual ring into the
  * quantized store.
  *   k_res, v_res   fp16 [bh][r_cap][d]; logical residual token i (0 = oldest)

@@ -6,7 +6,8 @@ with the oracle's own flags, and runs the pin file that should catch it
 against that build (``KIVI_ORACLE_LIB``).  The pins must fail.  The
 mistakes: the rounding rule, a fused reconstruction, zero padding, a sign,
 signed-zero handling, bit order, the level count, the flush size, a
-reciprocal for the division, truncating fp16 conversion, a group index;
+reciprocal for the division, truncating fp16 conversion, a group index,
+the ring row and the count of an append;
 for KIVI-Sink the calibration exclusion, a sink's code, the tie rule, the
 mean over heads, the square root, the restore row, the value row and the
 store capacity; for attention the maximum subtraction, the scale, the key
@@ -51,6 +52,9 @@ MUTANTS = {
                              "return ((n_res - residual + group - 1) / group) * group;"),
     "reciprocal": (PINS, "const float u = t / scale;", "const float u = t * (1.0f / scale);"),
     "truncating_fp16": (PINS, "float n = nearbyintf(units);", "float n = truncf(units);"),
+    "append_row": (PINS, "const int64_t row = (res_head + *n_res + i) % r_cap;",
+                   "const int64_t row = (res_head + i) % r_cap;"),
+    "append_count": (PINS, "    *n_res += n;\n    return 0;", "    return 0;"),
     "key_dequant_group_index": (PINS, "const int64_t p = (b * ng + t / group) * d + c;",
                                 "const int64_t p = (b * ng + t / w / group) * d + c;"),
     # KIVI-Sink

@@ -571,6 +571,62 @@ def test_flush_sequence_g16_odd_ring_equals_full_quantization():
     assert np.array_equal(st.v_scale[:, :s_q], sv) and np.array_equal(st.v_zero[:, :s_q], zv)
 
 
+def test_append_places_tokens_in_ring_order():
+    """The oracle's append against a token-by-token placement written here
+    (the sequence's token j at ring row (head + its residual index) mod
+    r_cap), over chunk sizes that wrap the ring mid-chunk, interleaved with
+    flushes; the flushed store ends up holding exactly the full quantization
+    of every flushed token, and the residual the newest tokens in order."""
+    G, R, bits, bh, d = 32, 32, 4, 2, 64
+    chunks = [64, 16, 16, 5, 27, 16, 30, 2, 40, 1, 31, 33]
+    total = sum(chunks)
+    w = W.custom(seed=29, batch=1, kv_heads=bh, seq=total, head_dim=d)
+    K = W.generate(w, 0, "k")
+    V = W.generate(w, 0, "v")
+    r_cap, cap = 96, 512
+    k_res = np.zeros((bh, r_cap, d), np.uint16)
+    v_res = np.zeros((bh, r_cap, d), np.uint16)
+    k_ref, v_ref = k_res.copy(), v_res.copy()
+    st = O.Store(bh, d, cap, G, bits)
+    s_q, head, n_res, pos = 0, 0, 0, 0
+    wrapped = False
+    for n_new in chunks:
+        assert n_res + n_new <= r_cap
+        for j in range(n_new):                      # the placement by its definition
+            row = (head + n_res + j) % r_cap
+            wrapped |= row < (head + n_res) % r_cap
+            k_ref[:, row] = K[:, pos + j]
+            v_ref[:, row] = V[:, pos + j]
+        n_res2 = O.append(k_res, v_res, head, n_res, K[:, pos:pos + n_new], V[:, pos:pos + n_new])
+        assert n_res2 == n_res + n_new
+        assert np.array_equal(k_res, k_ref) and np.array_equal(v_res, v_ref)
+        n_res, pos = n_res2, pos + n_new
+        _, s_q, head, n_res = O.flush(k_res, v_res, st, R, s_q, head, n_res)
+    assert wrapped and s_q >= 192
+    ck, sk, zk = O.quantize_keys(np.ascontiguousarray(K[:, :s_q]), G, bits)
+    cv, sv, zv = O.quantize_values(np.ascontiguousarray(V[:, :s_q]), G, bits)
+    w_ = 32 // bits
+    assert np.array_equal(st.k_codes[:, :s_q // w_], ck)
+    assert np.array_equal(st.k_scale[:, :s_q // G], sk) and np.array_equal(st.k_zero[:, :s_q // G], zk)
+    assert np.array_equal(st.v_codes[:, :s_q], cv)
+    assert np.array_equal(st.v_scale[:, :s_q], sv) and np.array_equal(st.v_zero[:, :s_q], zv)
+    rows = (head + np.arange(n_res)) % r_cap
+    assert np.array_equal(k_res[:, rows], K[:, s_q:total])
+    assert np.array_equal(v_res[:, rows], V[:, s_q:total])
+
+
+def test_append_rejects_ring_overflow():
+    bh, d, r_cap = 1, 32, 64
+    k = np.zeros((bh, r_cap, d), np.uint16)
+    v = np.zeros((bh, r_cap, d), np.uint16)
+    new = np.ones((bh, 40, d), np.uint16)
+    assert O.append(k, v, 0, 20, new, new) == 60
+    with pytest.raises(ValueError):
+        O.append(k, v, 0, 30, new, new)           # 70 tokens in a 64-row ring
+    with pytest.raises(ValueError):
+        O.append(k, v, 64, 0, new, new)           # head outside the ring
+
+
 def test_flush_rejects_overflowing_store_and_bad_state():
     bh, d = 1, 32
     k = np.zeros((bh, 128, d), np.uint16)
