@@ -12,18 +12,23 @@ the definition of the operation) per second:
                               scale and zero)
     dequantize b/8 + 8/G + 2  bytes per fp16 element
 
-Default workload: 28 layers x 8 KV heads x 4096 tokens x head_dim 128
-(Llama-3.2-3B shape), 2-bit, G = 32, residual 32, so each layer flushes 4064
-tokens.  Inputs are seeded synthetic tensors (``workloads``), resident in HBM
-before the timed region; one step moves ~1.2 GB, more than the 129 MB L2, so
-no L2 flush is needed between steps.
+Default workload: 28 layers x 4 KV heads x 32768 tokens x head_dim 128
+(Qwen2.5-7B shape, long context), 4-bit, G = 64, residual 64, so each layer
+flushes 32704 tokens; one step moves ~4.9 GB.  The same line then carries the
+nine (bits, G) cells of the large store sweep ([128 x 16384 x 128] keys and
+values, full quantize then full dequantize; ``--no-sweep`` leaves them out),
+each timed the same way.  Inputs are seeded synthetic tensors
+(``workloads``), resident in HBM before the timed region; every kernel pass
+moves more than the 129 MB L2, so no L2 flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...     # the CPU oracle on the same metric
 
-Under torchrun (N > 1) every rank runs the same workload on its own GPU
-(independent shards, no collective on the data path); the step time is the
-maximum over ranks and ``value`` counts the bytes of all ranks.
+With ``--gpus N`` (N > 1) outside torchrun the script relaunches itself
+under ``torch.distributed.run`` with N processes; under torchrun every rank
+runs the same workload on its own GPU (independent shards, no collective on
+the data path); the step time is the maximum over ranks and ``value`` counts
+the bytes of all ranks.
 """
 from __future__ import annotations
 
@@ -37,12 +42,15 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "quantize+dequant HBM GB/s (bytes in+out) and % of GB300 HBM peak"
 NOMINAL_HBM_GBS = 8000.0
+DEFAULT_WORKLOAD = "qwen2_5_7b_long"
 FALLBACK_HBM_GBS = 6800.0
 # Kernel sources behind each kind of workload: a committed ncu traffic figure
 # stays valid while these files hash to the value stored with it.
@@ -614,73 +622,108 @@ class FusedPrefillFlush(PrefillFlush):
 
 class DecodeFlush:
     """Batched decode: every layer's store already holds 2048 tokens per
-    sequence; a step flushes the 32 oldest of the 64 residual tokens of every
-    layer (keys and values) into the store.  The residual ring holds 64
-    tokens (written by the attention layer, untimed); the flushed half
-    alternates, and the store offset cycles over 100 consecutive flushes."""
+    sequence and its residual ring (2R = 64 rows) the R = 32 newest tokens;
+    one step appends the next 32 tokens of every layer (keys and values,
+    written behind the residual by the library's append) and flushes the 32
+    oldest into the store, so the residual is back at R.  The store offset
+    cycles over 100 consecutive flushes; the new tokens come from two
+    device-resident sets used alternately."""
 
-    kernels = ("key_quant", "value_quant")
-    events_per_step = 3
+    kernels = ("append", "key_quant", "value_quant")
+    events_per_step = 4
+    RECON = False
 
     def __init__(self, w, device):
         import torch
         import kv_cache_quantization_kivi_gb300 as K
         import workloads as W
         self.w, self.K = w, K
-        L, bh, d, G = w.layers, w.bh, w.head_dim, w.group
-        self.r_cap = 2 * w.residual
+        L, bh, d, G, R = w.layers, w.bh, w.head_dim, w.group, w.residual
+        n = w.new_per_step
+        self.r_cap = 2 * R
         self.cycle = w.steps
-        cap = w.store_prefill + w.new_per_step * self.cycle
+        cap = w.store_prefill + n * self.cycle
         self.cache = K.KiviCache(L, bh, d, r_cap=self.r_cap, cap=cap, group=G, bits=w.bits,
-                                 residual=w.residual, device=device)
+                                 residual=R, device=device, recon=self.RECON)
+        # the ring's residual (tokens 2048 .. 2048+R-1) and two sets of new tokens
         self.k_host_t, self.k_host = pinned_u16((L, bh, self.r_cap, d))
         self.v_host_t, self.v_host = pinned_u16((L, bh, self.r_cap, d))
         for l in range(L):
             W.fill(w, l, "k", self.k_host[l], tok0=w.store_prefill)
             W.fill(w, l, "v", self.v_host[l], tok0=w.store_prefill)
-        self.cache.k_res_all.copy_(self.k_host_t.to(device))
-        self.cache.v_res_all.copy_(self.v_host_t.to(device))
+        self.cache.k_res_all[:, :, :R].copy_(self.k_host_t[:, :, :R].to(device))
+        self.cache.v_res_all[:, :, :R].copy_(self.v_host_t[:, :, :R].to(device))
+        # new-token sets: set 0 = tokens 2048+R .., set 1 = tokens 2048+2R ..
+        self.new_host, self.new_host_u16 = [], []
+        for s in range(2):
+            kt, kh = pinned_u16((L, bh, n, d))
+            vt, vh = pinned_u16((L, bh, n, d))
+            for l in range(L):
+                W.fill(w, l, "k", kh[l], tok0=w.store_prefill + R + s * n)
+                W.fill(w, l, "v", vh[l], tok0=w.store_prefill + R + s * n)
+            self.new_host.append((kt, vt))
+            self.new_host_u16.append((kh, vh))
+        self.new_dev = [(kt.to(device), vt.to(device)) for kt, vt in self.new_host]
+        self.new_ptrs = [(K._ptr_array(list(kd.unbind(0)), L), K._ptr_array(list(vd.unbind(0)), L))
+                         for kd, vd in self.new_dev]
+        self.new_bh_stride = n * d
+        self.cache.reset(s_q=w.store_prefill, res_head=0, n_res=R)
         self.i = 0
-        elems = L * bh * w.new_per_step * d
-        bpe = bytes_per_elem(w.bits, G)
-        self.kernel_bytes = {k: elems * bpe for k in self.kernels}
-        self.step_bytes = 2 * elems * bpe
+        elems = L * bh * n * d
+        bpe = (fused_bytes_per_elem if self.RECON else bytes_per_elem)(w.bits, G)
+        qk = "key_fakequant" if self.RECON else "key_quant"
+        qv = "value_fakequant" if self.RECON else "value_quant"
+        # append: read the new fp16 tokens, write them into the ring (keys and values)
+        self.kernel_bytes = {"append": 2 * elems * 4.0, qk: elems * bpe, qv: elems * bpe}
+        self.step_bytes = sum(self.kernel_bytes.values())
         self.step_elems = 2 * elems
-        self.launches_per_step = 2
+        self.launches_per_step = 3
 
     def config(self):
         w = self.w
         return {"workload": w.name, "layers": w.layers, "bh": w.bh, "head_dim": w.head_dim,
                 "bits": w.bits, "group": w.group, "residual": w.residual,
-                "store_tokens": w.store_prefill, "tokens_flushed_per_step": w.new_per_step,
+                "store_tokens": w.store_prefill, "tokens_appended_per_step": w.new_per_step,
+                "tokens_flushed_per_step": w.new_per_step,
                 "consecutive_flushes": self.cycle,
                 "residual_compaction_bytes_per_step": 0,
-                "residual_storage": "a ring of 2R rows: the flush advances its head, copies nothing",
-                "step": "one decode flush of every layer (keys and values)"}
+                "residual_storage": "a ring of 2R rows: the append writes behind the residual, "
+                                    "the flush advances its head, nothing is copied",
+                "step": "one decode step of every layer: append of the new tokens (keys and "
+                        "values) and the flush of the oldest residual tokens",
+                "bytes": "append 8 B per new fp16 element pair (read + ring write, K and V); "
+                         "flush 2 + b/8 + 8/G per element"}
+
+    def _flush(self, stream, ev):
+        return self.cache.flush(stream, ev)
 
     def step(self, stream, ev=None):
         w, c = self.w, self.cache
-        j = self.i % self.cycle
-        c.reset(s_q=w.store_prefill + w.new_per_step * j,
-                res_head=(w.new_per_step * self.i) % self.r_cap, n_res=self.r_cap)
+        if self.i % self.cycle == 0:     # the store offset cycles; the ring runs on
+            c.state.s_q = w.store_prefill
+        kp, vp = self.new_ptrs[self.i % 2]
         self.i += 1
-        n = c.flush(stream, ev)
+        if ev is not None:
+            ev[0].record(stream)
+        self.K.kivi_append(c.layers, c.n_layers, c.state, kp, vp, w.new_per_step,
+                           new_bh_stride=self.new_bh_stride, stream=stream)
+        n = self._flush(stream, None if ev is None else ev[1])
         assert n == w.new_per_step
 
     def step_events(self, evs):
-        return self.K.event_handles(evs[0:3])
+        return (evs[0], self.K.event_handles(evs[1:4]))
 
     def kernel_times(self, e):
-        return {"key_quant": e[0].elapsed_time(e[1]), "value_quant": e[1].elapsed_time(e[2])}
+        names = self.kernels
+        return {names[0]: e[0].elapsed_time(e[1]), names[1]: e[1].elapsed_time(e[2]),
+                names[2]: e[2].elapsed_time(e[3])}
 
     def e2e_setup(self):
         import torch
         w = self.w
-        # per step: the 32 new tokens of every layer in, the flushed store slice out
+        # per step: the new tokens of every layer in, the flushed store slice out
         L, bh, d, G = w.layers, w.bh, w.head_dim, w.group
         n = w.new_per_step
-        self.new_k = self.k_host_t[:, :, :n].clone().pin_memory()
-        self.new_v = self.v_host_t[:, :, :n].clone().pin_memory()
         Wd = 32 // w.bits
         self.back = [torch.empty((L, bh, n // Wd, d), dtype=torch.int32, pin_memory=True),
                      torch.empty((L, bh, n // G, d), dtype=torch.float32, pin_memory=True),
@@ -688,23 +731,26 @@ class DecodeFlush:
                      torch.empty((L, bh, n, d // Wd), dtype=torch.int32, pin_memory=True),
                      torch.empty((L, bh, n, d // G), dtype=torch.float32, pin_memory=True),
                      torch.empty((L, bh, n, d // G), dtype=torch.float32, pin_memory=True)]
-        h2d = 2 * self.new_k.numel() * 2
+        h2d = 2 * self.new_host[0][0].numel() * 2
         d2h = sum(t.numel() * t.element_size() for t in self.back)
         return h2d, d2h
 
-    def e2e_step(self, stream):
-        w, c = self.w, self.cache
-        n, G = w.new_per_step, w.group
-        Wd = 32 // w.bits
-        head_new = (w.new_per_step * (self.i + 1)) % self.r_cap  # the half not flushed now
-        c.k_res_all[:, :, head_new:head_new + n].copy_(self.new_k, non_blocking=True)
-        c.v_res_all[:, :, head_new:head_new + n].copy_(self.new_v, non_blocking=True)
-        s_q = w.store_prefill + n * (self.i % self.cycle)
-        self.step(stream)
-        srcs = [c.k_codes_all[:, :, s_q // Wd:(s_q + n) // Wd], c.k_scale_all[:, :, s_q // G:(s_q + n) // G],
+    def _store_slices(self, s_q):
+        c, w = self.cache, self.w
+        n, G, Wd = w.new_per_step, w.group, 32 // w.bits
+        return [c.k_codes_all[:, :, s_q // Wd:(s_q + n) // Wd],
+                c.k_scale_all[:, :, s_q // G:(s_q + n) // G],
                 c.k_zero_all[:, :, s_q // G:(s_q + n) // G], c.v_codes_all[:, :, s_q:s_q + n],
                 c.v_scale_all[:, :, s_q:s_q + n], c.v_zero_all[:, :, s_q:s_q + n]]
-        for dst, src in zip(self.back, srcs):
+
+    def e2e_step(self, stream):
+        w, c = self.w, self.cache
+        s = self.i % 2
+        self.new_dev[s][0].copy_(self.new_host[s][0], non_blocking=True)
+        self.new_dev[s][1].copy_(self.new_host[s][1], non_blocking=True)
+        s_q = w.store_prefill if self.i % self.cycle == 0 else c.s_q
+        self.step(stream)
+        for dst, src in zip(self.back, self._store_slices(s_q)):
             dst.copy_(src, non_blocking=True)
 
     def cpu_sample(self, budget_s: float):
@@ -712,72 +758,44 @@ class DecodeFlush:
         w = self.w
         done, t_total, layers = 0.0, 0.0, 0
         cap = w.store_prefill + w.new_per_step
+        R, n = w.residual, w.new_per_step
+        per_layer = self.step_bytes / w.layers
         for l in range(w.layers):
             st = O.Store(w.bh, w.head_dim, cap, w.group, w.bits)
+            k_ring = np.ascontiguousarray(self.k_host[l])
+            v_ring = np.ascontiguousarray(self.v_host[l])
+            kn, vn = self.new_host_u16[0][0][l], self.new_host_u16[0][1][l]
             t0 = time.perf_counter()
-            n, _, _, _ = O.flush(self.k_host[l], self.v_host[l], st, w.residual,
-                                 w.store_prefill, 0, self.r_cap)
+            n_res = O.append(k_ring, v_ring, 0, R, kn, vn)
+            m, _, _, _ = O.flush(k_ring, v_ring, st, R, w.store_prefill, 0, n_res)
             t_total += time.perf_counter() - t0
-            done += 2 * w.bh * n * w.head_dim * bytes_per_elem(w.bits, w.group)
+            assert m == n
+            done += per_layer
             layers += 1
             if t_total >= budget_s:
                 break
-        return done, t_total, f"{layers} of {w.layers} layers (one decode flush, keys and values)"
+        return done, t_total, (f"{layers} of {w.layers} layers (one decode step: append + "
+                               "flush, keys and values)")
 
 
 class FusedDecodeFlush(DecodeFlush):
-    """The batched decode flush in its fused fake-quant form: each step
-    quantizes the 32 oldest residual tokens of every layer into the store and
-    writes their fp16 reconstruction into the fp16 cache [bh, cap, d] in the
-    same pass."""
+    """The batched decode step in its fused fake-quant form: the append, then
+    a flush that quantizes the 32 oldest residual tokens of every layer into
+    the store and writes their fp16 reconstruction into the fp16 cache
+    [bh, cap, d] in the same pass."""
 
-    kernels = ("key_fakequant", "value_fakequant")
-
-    def __init__(self, w, device):
-        import torch
-        import kv_cache_quantization_kivi_gb300 as K
-        import workloads as W
-        self.w, self.K = w, K
-        L, bh, d, G = w.layers, w.bh, w.head_dim, w.group
-        self.r_cap = 2 * w.residual
-        self.cycle = w.steps
-        cap = w.store_prefill + w.new_per_step * self.cycle
-        self.cache = K.KiviCache(L, bh, d, r_cap=self.r_cap, cap=cap, group=G, bits=w.bits,
-                                 residual=w.residual, device=device, recon=True)
-        self.k_host_t, self.k_host = pinned_u16((L, bh, self.r_cap, d))
-        self.v_host_t, self.v_host = pinned_u16((L, bh, self.r_cap, d))
-        for l in range(L):
-            W.fill(w, l, "k", self.k_host[l], tok0=w.store_prefill)
-            W.fill(w, l, "v", self.v_host[l], tok0=w.store_prefill)
-        self.cache.k_res_all.copy_(self.k_host_t.to(device))
-        self.cache.v_res_all.copy_(self.v_host_t.to(device))
-        self.i = 0
-        elems = L * bh * w.new_per_step * d
-        bpe = fused_bytes_per_elem(w.bits, G)
-        self.kernel_bytes = {k: elems * bpe for k in self.kernels}
-        self.step_bytes = 2 * elems * bpe
-        self.step_elems = 2 * elems
-        self.launches_per_step = 2
+    kernels = ("append", "key_fakequant", "value_fakequant")
+    RECON = True
 
     def config(self):
         c = super().config()
-        c["step"] = ("one fused fake-quant decode flush of every layer: store and fp16 "
-                     "reconstruction of the flushed tokens in one pass")
+        c["step"] = ("one fused fake-quant decode step of every layer: append of the new tokens, "
+                     "then store and fp16 reconstruction of the flushed tokens in one pass")
         c["bytes_per_elem"] = fused_bytes_per_elem(self.w.bits, self.w.group)
         return c
 
-    def step(self, stream, ev=None):
-        w, c = self.w, self.cache
-        j = self.i % self.cycle
-        c.reset(s_q=w.store_prefill + w.new_per_step * j,
-                res_head=(w.new_per_step * self.i) % self.r_cap, n_res=self.r_cap)
-        self.i += 1
-        n = c.flush_fakequant(stream, ev)
-        assert n == w.new_per_step
-
-    def kernel_times(self, e):
-        return {"key_fakequant": e[0].elapsed_time(e[1]),
-                "value_fakequant": e[1].elapsed_time(e[2])}
+    def _flush(self, stream, ev):
+        return self.cache.flush_fakequant(stream, ev)
 
     def e2e_setup(self):
         import torch
@@ -791,7 +809,7 @@ class FusedDecodeFlush(DecodeFlush):
     def e2e_step(self, stream):
         w, c = self.w, self.cache
         n = w.new_per_step
-        s_q = w.store_prefill + n * (self.i % self.cycle)
+        s_q = w.store_prefill if self.i % self.cycle == 0 else c.s_q
         super().e2e_step(stream)
         self.hat_back[0].copy_(c.k_hat_all[:, :, s_q:s_q + n], non_blocking=True)
         self.hat_back[1].copy_(c.v_hat_all[:, :, s_q:s_q + n], non_blocking=True)
@@ -802,24 +820,28 @@ class FusedDecodeFlush(DecodeFlush):
         done, t_total, layers = 0.0, 0.0, 0
         cap = w.store_prefill + w.new_per_step
         Wd = 32 // w.bits
-        s0 = w.store_prefill
+        s0, R = w.store_prefill, w.residual
+        per_layer = self.step_bytes / w.layers
         for l in range(w.layers):
             st = O.Store(w.bh, w.head_dim, cap, w.group, w.bits)
+            k_ring = np.ascontiguousarray(self.k_host[l])
+            v_ring = np.ascontiguousarray(self.v_host[l])
+            kn, vn = self.new_host_u16[0][0][l], self.new_host_u16[0][1][l]
             t0 = time.perf_counter()
-            n, _, _, _ = O.flush(self.k_host[l], self.v_host[l], st, w.residual, s0, 0,
-                                 self.r_cap)
+            n_res = O.append(k_ring, v_ring, 0, R, kn, vn)
+            n, _, _, _ = O.flush(k_ring, v_ring, st, R, s0, 0, n_res)
             O.dequantize_keys(st.k_codes[:, s0 // Wd:(s0 + n) // Wd],
                               st.k_scale[:, s0 // w.group:(s0 + n) // w.group],
                               st.k_zero[:, s0 // w.group:(s0 + n) // w.group], n, w.group, w.bits)
             O.dequantize_values(st.v_codes[:, s0:s0 + n], st.v_scale[:, s0:s0 + n],
                                 st.v_zero[:, s0:s0 + n], w.group, w.bits)
             t_total += time.perf_counter() - t0
-            done += 2 * w.bh * n * w.head_dim * fused_bytes_per_elem(w.bits, w.group)
+            done += per_layer
             layers += 1
             if t_total >= budget_s:
                 break
-        return done, t_total, (f"{layers} of {w.layers} layers (one decode flush + "
-                               "dequantize of the flushed tokens, keys and values)")
+        return done, t_total, (f"{layers} of {w.layers} layers (one decode step: append + flush "
+                               "+ dequantize of the flushed tokens, keys and values)")
 
 
 class DecodeAttention:
@@ -952,6 +974,18 @@ class DecodeAttention:
         return done, t_total, f"{pairs} (layer, sequence) pairs"
 
 
+def sweep_inputs(w, device):
+    """Keys and values of the store sweep: ((pinned tensor, uint16 view,
+    device tensor) for keys, the same for values)."""
+    import workloads as W
+    out = []
+    for kind in ("k", "v"):
+        t, h = pinned_u16((w.bh, w.seq, w.head_dim))
+        W.fill(w, 0, kind, h)
+        out.append((t, h, t.to(device)))
+    return tuple(out)
+
+
 class StoreSweep:
     """Full-tensor quantize of keys and values, then full dequantize, of a
     [bh, S, d] store at one (bits, group) point of the sweep."""
@@ -959,18 +993,17 @@ class StoreSweep:
     kernels = ("key_quant", "value_quant", "key_dequant", "value_dequant")
     events_per_step = 5
 
-    def __init__(self, w, device, bits, group):
+    def __init__(self, w, device, bits, group, inputs=None):
         import torch
         import kv_cache_quantization_kivi_gb300 as K
         import workloads as W
         self.w, self.K, self.bits, self.group = w, K, bits, group
         bh, S, d = w.bh, w.seq, w.head_dim
-        self.k_host_t, self.k_host = pinned_u16((bh, S, d))
-        self.v_host_t, self.v_host = pinned_u16((bh, S, d))
-        W.fill(w, 0, "k", self.k_host)
-        W.fill(w, 0, "v", self.v_host)
-        self.k = self.k_host_t.to(device)
-        self.v = self.v_host_t.to(device)
+        if inputs is None:
+            inputs = sweep_inputs(w, device)
+        # the store's keys and values do not depend on (bits, G): every cell of
+        # the sweep shares one pinned host copy and one device copy
+        (self.k_host_t, self.k_host, self.k), (self.v_host_t, self.v_host, self.v) = inputs
         self.kc, self.ks, self.kz = K.kivi_quantize_keys(self.k, group, bits)
         self.vc, self.vs, self.vz = K.kivi_quantize_values(self.v, group, bits)
         self.ky = torch.empty_like(self.k)
@@ -1056,8 +1089,8 @@ class FusedStoreSweep(StoreSweep):
     kernels = ("key_fakequant", "value_fakequant")
     events_per_step = 3
 
-    def __init__(self, w, device, bits, group):
-        super().__init__(w, device, bits, group)
+    def __init__(self, w, device, bits, group, inputs=None):
+        super().__init__(w, device, bits, group, inputs)
         elems = w.bh * w.seq * w.head_dim
         bpe = fused_bytes_per_elem(bits, group)
         self.kernel_bytes = {k: elems * bpe for k in self.kernels}
@@ -1158,6 +1191,107 @@ def ncu_traffic(workload: str, kernel: str):
 # arms
 # ---------------------------------------------------------------------------
 
+def time_steps(wl, steps: int, warmup: int, stream, device, sampler=None):
+    """W untimed warm-up steps, then exactly K steps between a barrier and a
+    synchronize on both sides, with CUDA events on the launching stream
+    around the whole region and around every kernel of every step.  Returns
+    (elapsed ms of the K steps, max over ranks; the per-step event lists)."""
+    import torch
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)
+        return evs
+
+    for _ in range(warmup):
+        wl.step(stream)
+    torch.cuda.synchronize(device)
+    evs = [new_events(wl.events_per_step) for _ in range(steps)]
+    handles = [wl.step_events(e) for e in evs]
+    start, end = new_events(2)
+    torch.cuda.synchronize(device)
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)  # let the sampler start before the load
+    barrier()
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    for i in range(steps):
+        wl.step(stream, handles[i])
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    return reduce_max(start.elapsed_time(end), device), evs
+
+
+def kernel_stats(wl, evs, peak: float) -> dict:
+    """Per kernel: average event time, algorithmic GB/s, fraction of the
+    measured copy peak and of the nominal 8 TB/s, share of the step's kernel
+    time and the spread of the per-step times."""
+    k_ms = {k: [] for k in wl.kernels}
+    for e in evs:
+        for k, t in wl.kernel_times(e).items():
+            k_ms[k].append(t)
+    total_kernel_ms = sum(sum(v) for v in k_ms.values())
+    out = {}
+    for k in wl.kernels:
+        avg = sum(k_ms[k]) / len(k_ms[k])
+        gbs = wl.kernel_bytes[k] / (avg * 1e-3) / 1e9
+        out[k] = {"avg_us": round(avg * 1e3, 2), "gbs": round(gbs, 1),
+                  "frac_of_measured": round(gbs / peak, 4),
+                  "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                  "share": round(sum(k_ms[k]) / total_kernel_ms, 4),
+                  **spread_us(k_ms[k])}
+    return out
+
+
+def run_sweep(args, device, stream, peak: float) -> dict:
+    """Every (bits, G) cell of the large store sweep, timed like the main
+    workload (W warm-up steps, K timed steps, CUDA events per kernel), with
+    the SM clocks sampled over the whole sweep."""
+    import torch
+    import workloads as W
+    w = W.CONFIGS["large_store_sweep"]
+    inputs = sweep_inputs(w, device)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    if not args.no_clocks:
+        sampler.start()
+        time.sleep(0.3)
+    cells = {}
+    floor = None
+    for bits in w.sweep_bits:
+        for group in w.sweep_groups:
+            cell = (FusedStoreSweep if args.fused else StoreSweep)(w, device, bits, group, inputs)
+            ms, evs = time_steps(cell, args.steps, args.warmup, stream, device)
+            ks = kernel_stats(cell, evs, peak)
+            step_gbs = cell.step_bytes * args.steps / (ms * 1e-3) / 1e9
+            cells[f"b{bits}_g{group}"] = {
+                "step_gbs": round(step_gbs, 1),
+                "ms_per_step": round(ms / args.steps, 5),
+                "kernels": {k: {"gbs": v["gbs"], "avg_us": v["avg_us"],
+                                "frac_of_measured": v["frac_of_measured"],
+                                "frac_of_nominal": v["frac_of_nominal"]}
+                            for k, v in ks.items()}}
+            lo = min(v["frac_of_nominal"] for v in ks.values())
+            floor = lo if floor is None else min(floor, lo)
+            del cell
+            torch.cuda.synchronize(device)
+    clocks = sampler.stop() if not args.no_clocks else None
+    kinds = sorted(next(iter(cells.values()))["kernels"])
+    at_bar = sum(1 for c in cells.values() for k in c["kernels"].values()
+                 if k["frac_of_nominal"] >= 0.70)
+    return {"workload": w.name, "bh": w.bh, "seq": w.seq, "head_dim": w.head_dim,
+            "step": ("fused fake quantization of keys and values" if args.fused else
+                     "full quantize of keys and values, then full dequantize"),
+            "cells": cells, "kernels_per_cell": kinds,
+            "min_kernel_frac_of_nominal": floor,
+            "kernel_cells_at_70pct_of_nominal": f"{at_bar} of {len(cells) * len(kinds)}",
+            "clocks": clocks,
+            "l2": "no flush: each kernel pass reads and writes 0.6-0.9 GB, more than the "
+                  "129 MB L2"}
+
+
 def run_kivi(args):
     import torch
     ws, rank, local = dist_env()
@@ -1171,58 +1305,20 @@ def run_kivi(args):
     wl = make_workload(args.workload, device, args.layers, args.bits, args.group, args.fused,
                        args.attention, args.sink)
     stream = torch.cuda.current_stream(device)
-
-    def new_events(n):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        for e in evs:
-            e.record(stream)
-        return evs
-
-    for _ in range(args.warmup):
-        wl.step(stream)
-    torch.cuda.synchronize(device)
-
-    evs = [new_events(wl.events_per_step) for _ in range(args.steps)]
-    handles = [wl.step_events(e) for e in evs]
-    start, end = new_events(2)
-    torch.cuda.synchronize(device)
+    peak, peak_kind = measured_peaks()
 
     sampler = ClockSampler(device.index if device.index is not None else 0)
-    if not args.no_clocks:
-        sampler.start()
-        time.sleep(0.3)  # let the sampler start before the load
-    barrier()
-    torch.cuda.synchronize(device)
-    start.record(stream)
-    for i in range(args.steps):
-        wl.step(stream, handles[i])
-    end.record(stream)
-    torch.cuda.synchronize(device)
-    barrier()
+    elapsed_ms, evs = time_steps(wl, args.steps, args.warmup, stream, device,
+                                 None if args.no_clocks else sampler)
     clocks = sampler.stop() if not args.no_clocks else None
-
-    elapsed_ms = start.elapsed_time(end)
-    elapsed_ms = reduce_max(elapsed_ms, device)
     ms_per_step = elapsed_ms / args.steps
     total_bytes = reduce_sum(wl.step_bytes * args.steps, device)
     value = total_bytes / (elapsed_ms * 1e-3) / 1e9
 
-    k_ms = {k: [] for k in wl.kernels}
-    for e in evs:
-        for k, t in wl.kernel_times(e).items():
-            k_ms[k].append(t)
-    peak, peak_kind = measured_peaks()
-    total_kernel_ms = sum(sum(v) for v in k_ms.values())
-    kernels = {}
-    for k in wl.kernels:
-        avg = sum(k_ms[k]) / len(k_ms[k])
-        gbs = wl.kernel_bytes[k] / (avg * 1e-3) / 1e9
-        kernels[k] = {"avg_us": round(avg * 1e3, 2), "gbs": round(gbs, 1),
-                      "frac_of_measured": round(gbs / peak, 4),
-                      "share": round(sum(k_ms[k]) / total_kernel_ms, 4),
-                      **spread_us(k_ms[k])}
-    dom = max(wl.kernels, key=lambda k: sum(k_ms[k]))
-    dom_avg_s = sum(k_ms[dom]) / len(k_ms[dom]) * 1e-3
+    kernels = kernel_stats(wl, evs, peak)
+    k_total = {k: v["avg_us"] for k, v in kernels.items()}
+    dom = max(wl.kernels, key=lambda k: k_total[k])
+    dom_avg_s = kernels[dom]["avg_us"] * 1e-6
     achieved = wl.kernel_bytes[dom] / dom_avg_s / 1e9
     traffic = ncu_traffic(args.workload + ("+fused" if args.fused else "")
                           + ("+attention" if args.attention else "")
@@ -1239,7 +1335,7 @@ def run_kivi(args):
         h2d, d2h = wl.e2e_setup()
         wl.e2e_step(stream)
         torch.cuda.synchronize(device)
-        a, b = new_events(2)
+        a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
         barrier()
         torch.cuda.synchronize(device)
         a.record(stream)
@@ -1261,24 +1357,39 @@ def run_kivi(args):
         cpu = {"value": round(cb / cs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{what}; {cs:.1f} s single-threaded on the host", **host_cpu()}
 
+    # what the line reports about the main workload, taken before its buffers
+    # are released for the sweep
     config = wl.config()
     config["bytes_per_step"] = wl.step_bytes
     config["fp16_elements_per_step"] = wl.step_elems
     config["l2"] = ("no flush: each step reads and writes ~%.2f GB, more than the 129 MB L2"
                     % (wl.step_bytes / 1e9))
     config["parallelism"] = f"independent replicas x{ws}" if ws > 1 else "single GPU"
+    launches = wl.launches_per_step * args.steps
+    elems = reduce_sum(wl.step_elems * args.steps, device)
+
+    sweep = None
+    if not args.no_sweep and args.workload == DEFAULT_WORKLOAD and not args.attention \
+            and not args.sink:
+        del wl
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+        sweep = run_sweep(args, device, stream, peak)
+        launches += sum(len(c["kernels"]) for c in sweep["cells"].values()) * args.steps
+
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16",
+        "formats": {"inputs_and_reconstructions": "fp16", "codes": "u32 (packed)",
+                    "scale_zero": "f32"},
         "data": "synthetic (seeded counter-based generator, shapes of the pages' models)",
         "config": config,
         "pct_of_hbm_peak": {"measured_copy": round(value / ws / peak * 100, 2),
                             "nominal_8tbs": round(value / ws / NOMINAL_HBM_GBS * 100, 2)},
-        "elements_per_s": round(reduce_sum(wl.step_elems * args.steps, device)
-                                / (elapsed_ms * 1e-3), 1),
+        "elements_per_s": round(elems / (elapsed_ms * 1e-3), 1),
         "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
+        "sweep": sweep, "gpu_launches": launches, "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -1340,7 +1451,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
             "config": {"workload": w.name, "layers": w.layers, "bh": w.bh, "seq": w.seq,
                        "head_dim": w.head_dim, "bits": w.bits, "group": w.group,
                        "residual": w.residual},
@@ -1351,13 +1462,29 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def relaunch_distributed(n: int, argv) -> int:
+    """Runs this script under torch.distributed.run with one process per GPU
+    (rendezvous on 127.0.0.1); returns its exit status."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=None,
+                    help="GPUs (processes, one per GPU); default: WORLD_SIZE under torchrun, "
+                         "else 1")
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("kivi", "reference"), default="kivi")
-    ap.add_argument("--workload", default="llama3_2_3b_prefill")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="time budget of the oracle CPU-baseline sample")
@@ -1365,6 +1492,9 @@ def main(argv=None):
                     help="total oracle time budget of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="leave out the nine (bits, G) cells of the large store sweep that "
+                         "follow the default workload in the same line")
     ap.add_argument("--json-out", default=None)
     ap.add_argument("--bits", type=int, default=None, help="large_store_sweep: code width")
     ap.add_argument("--group", type=int, default=None, help="large_store_sweep: group size")
@@ -1382,6 +1512,16 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    ws = int(os.environ.get("WORLD_SIZE", "0"))
+    if args.gpus is None:
+        args.gpus = ws or 1
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if ws == 0 and args.gpus > 1:
+        # not under torchrun yet: one process per GPU, launched the same way
+        sys.exit(relaunch_distributed(args.gpus, sys.argv[1:] if argv is None else argv))
+    if ws not in (0, args.gpus):
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {ws}")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -178,6 +178,7 @@ KIVI_API kivi_status kivi_fakequant_values(const void *x, int64_t bh, int64_t s,
 /* One layer's buffers (all device, caller-owned, contiguous per bh):
  *   k_res, v_res   fp16 [bh][r_cap][d] residual rings: logical residual
  *                  token i (0 = oldest) lives at ring row (res_head + i) % r_cap
+ *                  (written by kivi_append, read by the flushes)
  *   k_codes        u32 [bh][cap/W][d]      store, key layout with s = cap
  *   k_scale,k_zero f32 [bh][cap/G][d]
  *   v_codes        u32 [bh][cap][d/W]      store, value layout with s = cap
@@ -215,6 +216,28 @@ typedef struct {
  * "Generation 1" table fixes the rule).  Returns -1 for a negative argument
  * or group <= 0. */
 KIVI_API int64_t kivi_flush_size(int64_t n_res, int residual, int group);
+
+/* Append: n new tokens of every layer enter the fp16 residual window behind
+ * the tokens already there (fused-kernel post, "What we're actually
+ * optimizing": the newest tokens stay fp16 until whole groups of them age
+ * out).  Token i (0 <= i < n) of bh slice b of layer l is read from
+ * k_new[l] + b * new_bh_stride + i * d (likewise v_new[l]) and written to
+ * ring row (res_head + n_res + i) % r_cap of layers[l].k_res (v_res); then
+ * n_res += n.  Nothing else moves: rows of the ring wrap, tokens are never
+ * shifted.  One launch covers every layer.
+ *   k_new, v_new    host arrays of n_layers device pointers, each fp16
+ *                   [bh][n][d] rows with bh stride new_bh_stride >= n*d
+ *                   elements (a multiple of 8); they must not overlap the
+ *                   rings
+ *   cache           host memory, updated in place on success (n_res)
+ * The store pointers of `layers` are not used (they may be NULL).
+ * n == 0 (or bh == 0) launches nothing and only advances n_res.
+ * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN, KIVI_ERR_CAPACITY (the
+ * ring would hold more than r_cap tokens; nothing launched, state
+ * unchanged) or KIVI_ERR_CUDA. */
+KIVI_API kivi_status kivi_append(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                                 const void *const *k_new, const void *const *v_new,
+                                 int64_t new_bh_stride, int64_t n, kivi_stream_t stream);
 
 /* Flush: quantize the oldest kivi_flush_size(n_res, residual, group) residual
  * tokens of every layer (keys per channel, values per token) into the store
@@ -331,8 +354,11 @@ KIVI_API kivi_status kivi_sink_update(const kivi_layer *layers, const kivi_sink_
  * are left out of the key groups' min/max (a group of sinks only gets scale
  * and zero 0) with code 0, their value rows get codes, scales and zeros 0,
  * and their positions and fp16 key / value rows (every head) are appended
- * to the sink store.  A sink store that would overflow keeps what fits and
- * sets bit 1 of the device fault word (kivi_device_fault).
+ * to the sink store.  A sink store that would overflow keeps the earliest
+ * flushed sinks that fit and sets bit 1 of the device fault word
+ * (kivi_device_fault); the flushed top-k tokens that did not fit are
+ * quantized as plain tokens (codes, scales and zeros of plain KIVI), so no
+ * token's value is lost.
  * Returns as kivi_flush. */
 KIVI_API kivi_status kivi_flush_sink(const kivi_layer *layers, const kivi_sink_layer *sinks,
                                      int n_layers, kivi_cache *cache,
@@ -395,12 +421,20 @@ KIVI_API int32_t kivi_decode_attention_splits(const kivi_cache *cache, int n_lay
 KIVI_API int64_t kivi_decode_attention_workspace(const kivi_cache *cache, int n_layers,
                                                  int64_t batch, int32_t h_q, int32_t n_split);
 
-/* kivi_decode_attention without a caller workspace and without allocating:
- * with n_split > 1 the partial results go to a fixed device array inside
- * the library (2^24 floats, 64 MiB, one per device; its address is looked
- * up once per device).  A call whose kivi_decode_attention_workspace size
- * exceeds it returns KIVI_ERR_CAPACITY before any CUDA call.  Every partial
- * a call reads is written earlier in the same call, so the array is never
+/* kivi_decode_attention without a caller workspace and without allocating,
+ * for callers that cannot obtain device memory at the point of the call: a
+ * plug-in handed only the cache's pointers and no allocator, a runtime
+ * whose memory is planned once up front, or a decode loop that must not
+ * pay cudaMalloc's implicit device synchronisation.  The paper has no
+ * counterpart; this is a deployment variant of the call above.  With
+ * n_split > 1 the partial results go to a fixed device array inside the
+ * library (2^24 floats = 64 MiB, held on every device that loads the
+ * library until the process exits).  Its device address is looked up on
+ * the first call on a device (and again after that device is reset); that
+ * first call makes runtime calls, so it should come before any stream
+ * capture.  A call whose kivi_decode_attention_workspace size exceeds the
+ * array returns KIVI_ERR_CAPACITY before any CUDA call.  Every partial a
+ * call reads is written earlier in the same call, so the array is never
  * cleared.  Calls that overlap on the device (different streams, or
  * different host threads without ordering) share the array and race: order
  * them on one stream.  Otherwise identical to kivi_decode_attention,

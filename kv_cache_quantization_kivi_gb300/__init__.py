@@ -24,6 +24,7 @@ from . import _build
 __all__ = [
     "KiviError", "lib", "library_path", "kivi_quantize_keys", "kivi_quantize_values",
     "kivi_dequantize_keys", "kivi_dequantize_values", "kivi_flush", "kivi_flush_size",
+    "kivi_append",
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
     "kivi_fakequant_keys", "kivi_fakequant_values", "kivi_flush_fakequant",
     "kivi_decode_attention", "kivi_decode_attention_splits", "kivi_decode_attention_workspace",
@@ -108,6 +109,9 @@ def lib():
             L.kivi_flush.argtypes = [C.POINTER(kivi_layer), _int, C.POINTER(kivi_cache),
                                      C.POINTER(_i64), _vp]
             L.kivi_flush.restype = _int
+            L.kivi_append.argtypes = [C.POINTER(kivi_layer), _int, C.POINTER(kivi_cache),
+                                      C.POINTER(_vp), C.POINTER(_vp), _i64, _i64, _vp]
+            L.kivi_append.restype = _int
             L.kivi_dequantize_cache.argtypes = [C.POINTER(kivi_layer), _int,
                                                 C.POINTER(kivi_cache), C.POINTER(_vp),
                                                 C.POINTER(_vp), _vp]
@@ -370,6 +374,24 @@ def _ptr_array(ts, n: int):
     return ts if isinstance(ts, C.Array) else (C.c_void_p * n)(*[t.data_ptr() for t in ts])
 
 
+def kivi_append(layers, n_layers: int, cache: kivi_cache, k_new, v_new, n: int,
+                new_bh_stride: Optional[int] = None, stream=None) -> None:
+    """Raw C call: new tokens of every layer into the residual rings behind the
+    residual (``cache.n_res`` advances by n).  ``k_new``/``v_new``: sequences
+    of fp16 [bh, n, d] tensors (last two dims contiguous) or prepared ctypes
+    pointer arrays (then ``new_bh_stride``, in elements, is required)."""
+    if new_bh_stride is None:
+        t = k_new[0]
+        for x in list(k_new) + list(v_new):
+            _fp16_3d(x, "kivi_append")
+            if _bh_stride(x) != _bh_stride(t):
+                raise ValueError("kivi_append: every new-token tensor needs the same bh stride")
+        new_bh_stride = _bh_stride(t)
+    _check(lib().kivi_append(layers, n_layers, C.byref(cache), _ptr_array(k_new, n_layers),
+                             _ptr_array(v_new, n_layers), new_bh_stride, n,
+                             _stream_handle(stream)), "kivi_append")
+
+
 def kivi_flush_fakequant(layers, n_layers: int, cache: kivi_cache, k_hat, v_hat, stream=None,
                          events=None) -> int:
     """Raw C call of the fused fake-quant flush: as :func:`kivi_flush`, and the
@@ -541,23 +563,31 @@ class KiviCache:
     def reset(self, s_q: int = 0, res_head: int = 0, n_res: int = 0) -> None:
         self.state.s_q, self.state.res_head, self.state.n_res = s_q, res_head, n_res
 
-    def ring_rows(self, start: int, n: int):
-        """Ring rows of logical residual tokens start .. start+n-1."""
-        import torch
-        r_cap = int(self.state.r_cap)
-        return (torch.arange(start, start + n, device=self.k_res[0].device) + self.res_head) % r_cap
-
-    def append(self, layer: int, k_new, v_new) -> None:
-        """Writes new tokens [bh, n, d] behind the residual of one layer (a
-        caller-side copy; call :meth:`advance` once every layer has its tokens)."""
-        rows = self.ring_rows(self.n_res, k_new.shape[1])
-        self.k_res[layer].index_copy_(1, rows, k_new)
-        self.v_res[layer].index_copy_(1, rows, v_new)
+    def append(self, layer: int, k_new, v_new, stream=None) -> None:
+        """Writes new tokens [bh, n, d] behind the residual of one layer (the
+        library's append kernel on that layer alone; the cache's residual count
+        is left as it is: call :meth:`advance` once every layer has its
+        tokens)."""
+        n = int(k_new.shape[1])
+        if self.n_res + n > int(self.state.r_cap):
+            raise ValueError("residual ring overflow")
+        st = kivi_cache.from_buffer_copy(self.state)   # the count advances in the copy only
+        kivi_append((kivi_layer * 1)(self.layers[layer]), 1, st, [k_new], [v_new], n,
+                    stream=stream)
 
     def advance(self, n: int) -> None:
         if self.n_res + n > int(self.state.r_cap):
             raise ValueError("residual ring overflow")
         self.state.n_res += n
+
+    def append_all(self, k_new, v_new, stream=None) -> None:
+        """New tokens of every layer (fp16 [n_layers, bh, n, d] tensors or
+        per-layer lists of [bh, n, d]) behind the residual, in one launch; the
+        residual count advances by n."""
+        ks = list(k_new.unbind(0)) if hasattr(k_new, "unbind") else list(k_new)
+        vs = list(v_new.unbind(0)) if hasattr(v_new, "unbind") else list(v_new)
+        kivi_append(self.layers, self.n_layers, self.state, ks, vs, int(ks[0].shape[1]),
+                    stream=stream)
 
     # hot path --------------------------------------------------------------
     def flush(self, stream=None, events=None) -> int:

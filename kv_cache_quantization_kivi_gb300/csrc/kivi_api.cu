@@ -358,6 +358,42 @@ static cudaError_t record(void *const *events, int i, cudaStream_t s) {
   return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
 }
 
+kivi_status kivi_append(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                        const void *const *k_new, const void *const *v_new,
+                        int64_t new_bh_stride, int64_t n, kivi_stream_t stream) {
+  const kivi_status st = check_cache(layers, n_layers, cache, /*allow_no_store=*/true);
+  if (st != KIVI_OK) return st;
+  if (n < 0 || !k_new || !v_new) return KIVI_ERR_INVAL;
+  if (cache->n_res + n > cache->r_cap) return KIVI_ERR_CAPACITY;
+  const int64_t d = cache->d;
+  if (n > 0 && cache->bh > 0) {
+    if (new_bh_stride < n * d) return KIVI_ERR_INVAL;
+    if (sat_mul(sat_mul(sat_mul(n_layers, cache->bh), n), d / 8) > kMaxUnits)
+      return KIVI_ERR_INVAL;
+    for (int l = 0; l < n_layers; ++l) {
+      if (!k_new[l] || !v_new[l]) return KIVI_ERR_INVAL;
+      if (!aligned16(k_new[l]) || !aligned16(v_new[l])) return KIVI_ERR_ALIGN;
+    }
+    if (!bytes16(new_bh_stride, 2)) return KIVI_ERR_ALIGN;
+    kivi_impl::AppendParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.n_jobs = n_layers;
+    p.d = static_cast<int32_t>(d);
+    p.bh = cache->bh;
+    p.n = n;
+    p.r_cap = cache->r_cap;
+    p.row0 = (cache->res_head + cache->n_res) % cache->r_cap;
+    p.new_bh_stride = new_bh_stride;
+    for (int l = 0; l < n_layers; ++l)
+      p.jobs[l] = {k_new[l], v_new[l], const_cast<void *>(layers[l].k_res),
+                   const_cast<void *>(layers[l].v_res)};
+    const kivi_status r = cuda_status(kivi_impl::launch_append(p, stream));
+    if (r != KIVI_OK) return r;
+  }
+  cache->n_res += n;
+  return KIVI_OK;
+}
+
 kivi_status kivi_flush(const kivi_layer *layers, int n_layers, kivi_cache *cache,
                        int64_t *n_flushed, kivi_stream_t stream) {
   return kivi_flush_timed(layers, n_layers, cache, n_flushed, stream, nullptr);

@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
@@ -856,21 +857,80 @@ int attention_splits(int64_t items, int64_t tiles_store, int group, int bits) {
   return static_cast<int>(std::max<int64_t>(1, std::min(want, most)));
 }
 
-cudaError_t attention_scratch(float **ptr, int64_t *max_floats) {
-  // the symbol's address, looked up once per device
-  constexpr int kMaxDevices = 64;
-  static float *addr[kMaxDevices] = {};
+// Addresses of this file's device symbols as host code must pass them to
+// kernels (the symbol's name in host code is a host-side stand-in, not a
+// device address).  The lookup runs once per device and context: entries
+// are keyed by the device and the unique id of the context current on it,
+// so a device that was reset (a new context, its modules loaded again) gets
+// a fresh lookup, and a mutex serialises concurrent host threads.  The
+// first call on a device (and the first after a reset) makes the runtime
+// calls of the lookup, so it should come before any stream capture.
+namespace {
+
+using CtxGetCurrentFn = int (*)(void **);                      // cuCtxGetCurrent
+using CtxGetIdFn = int (*)(void *, unsigned long long *);      // cuCtxGetId
+
+// Unique id of the context current on the calling thread (0 if none or if
+// the driver does not provide the query).
+unsigned long long current_context_id() {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  void *ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != 0 || ctx == nullptr || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+struct SymbolSlot {
+  unsigned long long ctx_id;
+  void *addr;
+};
+
+// The device address of `symbol` on the current device.
+cudaError_t symbol_address(const void *symbol, SymbolSlot (&slots)[64], void **out) {
+  static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!addr[dev]) {
-    void *a = nullptr;
-    e = cudaGetSymbolAddress(&a, g_attn_scratch);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<float *>(a);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  const unsigned long long id = current_context_id();
+  if (id != 0 && slots[dev].ctx_id == id && slots[dev].addr != nullptr) {
+    *out = slots[dev].addr;
+    return cudaSuccess;
   }
-  *ptr = addr[dev];
+  void *a = nullptr;
+  e = cudaGetSymbolAddress(&a, symbol);   // creates the context if there is none yet
+  if (e != cudaSuccess) return e;
+  slots[dev] = {current_context_id(), a};
+  *out = a;
+  return cudaSuccess;
+}
+
+SymbolSlot g_scratch_slots[64];
+SymbolSlot g_fault_slots[64];
+
+}  // namespace
+
+cudaError_t attention_scratch(float **ptr, int64_t *max_floats) {
+  void *a = nullptr;
+  const cudaError_t e = symbol_address(reinterpret_cast<const void *>(&g_attn_scratch),
+                                       g_scratch_slots, &a);
+  if (e != cudaSuccess) return e;
+  *ptr = static_cast<float *>(a);
   *max_floats = kAttnScratchFloats;
   return cudaSuccess;
 }
@@ -878,19 +938,11 @@ cudaError_t attention_scratch(float **ptr, int64_t *max_floats) {
 int64_t attention_scratch_floats() { return kAttnScratchFloats; }
 
 cudaError_t fault_word_address(unsigned int **ptr) {
-  constexpr int kMaxDevices = 64;
-  static unsigned int *addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *a = nullptr;
+  const cudaError_t e = symbol_address(reinterpret_cast<const void *>(&g_fault_word),
+                                       g_fault_slots, &a);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!addr[dev]) {
-    void *a = nullptr;
-    e = cudaGetSymbolAddress(&a, g_fault_word);
-    if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<unsigned int *>(a);
-  }
-  *ptr = addr[dev];
+  *ptr = static_cast<unsigned int *>(a);
   return cudaSuccess;
 }
 

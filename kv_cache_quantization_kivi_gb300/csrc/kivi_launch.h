@@ -92,6 +92,28 @@ struct DequantParams {
   DequantJob jobs[KIVI_MAX_LAYERS];
 };
 
+// Append of n new tokens of every layer behind its residual: token i of
+// bh slice b of job l goes from new[b * new_bh_stride + i * d ..] to ring row
+// (row0 + i) % r_cap of the layer's rings (row0 = (res_head + n_res) % r_cap).
+struct AppendJob {
+  const void *k_new;   // fp16 [bh][n][d] (bh stride new_bh_stride)
+  const void *v_new;
+  void *k_res;         // fp16 rings [bh][r_cap][d]
+  void *v_res;
+};
+struct AppendParams {
+  int32_t n_jobs;
+  int32_t d;
+  int64_t bh;
+  int64_t n;
+  int64_t r_cap;
+  int64_t row0;
+  int64_t new_bh_stride;  // fp16 elements
+  FastDiv div_chunks, div_n, div_bh;  // filled by the launcher
+  AppendJob jobs[KIVI_MAX_LAYERS];
+};
+cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
+
 // Decode attention over one layer's cache: the packed store (key and value
 // codes, scales, zeros) and the fp16 residual rings, queries fp16
 // [batch][h_q][d], output fp32 [batch][h_q][d].

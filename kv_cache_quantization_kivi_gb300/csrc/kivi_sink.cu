@@ -348,8 +348,10 @@ __global__ void __launch_bounds__(NT) sink_select_kernel(const __grid_constant__
 // (in the top-k or not), read by the quantize kernels' sink mode; the sinks'
 // positions and fp16 key / value rows of every head appended to the sink
 // store (the quantize kernels read neither the store nor its count).  An
-// overflowing store keeps what fits and sets bit 1 of the device fault
-// word; the mask still flags every flushed top-k token.
+// overflowing store keeps what fits (the earliest flushed sinks) and sets
+// bit 1 of the device fault word; the mask flags only the sinks it kept, so
+// the flushed top-k tokens that did not fit are quantized as plain tokens
+// rather than lost.
 __global__ void __launch_bounds__(kThreads) sink_prepare_kernel(const __grid_constant__ SinkParams p) {
   kivi_dev::grid_dependency_wait();
   kivi_dev::grid_launch_dependents();
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kThreads) sink_prepare_kernel(const __grid_con
   const int64_t seq = blockIdx.x - static_cast<int64_t>(job) * p.batch;
   const SinkJob &J = p.jobs[job];
   __shared__ int64_t pos[kMaxSinkTop];
-  __shared__ int slot0, m, cnt_all;
+  __shared__ int slot0, m;
   if (threadIdx.x == 0) {
     int cnt = 0;
     const int tn = J.top_count[seq];
@@ -371,7 +373,6 @@ __global__ void __launch_bounds__(kThreads) sink_prepare_kernel(const __grid_con
       }
       pos[i] = q;
     }
-    cnt_all = cnt;
     const int have = J.sink_count[seq];
     if (have + cnt > p.sink_cap) {   // the store is full: record it, keep what fits
       atomicOr(p.fault, 2u);
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(kThreads) sink_prepare_kernel(const __grid_con
   for (int64_t w = threadIdx.x; w < words; w += kThreads) {
     const int64_t lo = p.s_q + 32 * w;
     uint32_t bits = 0u;
-    for (int e = 0; e < cnt_all; ++e)
+    for (int e = 0; e < m; ++e)   // the stored sinks only
       if (pos[e] >= lo && pos[e] < lo + 32) bits |= 1u << (pos[e] - lo);
     J.mask[seq * p.mask_words + w] = bits;
   }

@@ -391,3 +391,42 @@ def test_decode_attention_sinks_validation():
     assert call(_cache(), _sinks(), cfg(), n_split=2) == 1      # no workspace
     assert L.kivi_decode_attention_sinks(_layers(2), None, 2, C.byref(_cache()), C.byref(cfg()),
                                          2, 8, 0.1, q, out, 1, None, 0, None) == 1
+
+
+def _append(layers, n_layers, cache, n, stride=None, k_new=FAKE, v_new=FAKE + 65536):
+    kp = (C.c_void_p * max(n_layers, 1))(*([k_new] * max(n_layers, 1)))
+    vp = (C.c_void_p * max(n_layers, 1))(*([v_new] * max(n_layers, 1)))
+    stride = n * int(cache.d) if stride is None else stride
+    return K.lib().kivi_append(layers, n_layers, C.byref(cache), kp, vp, stride, n, None)
+
+
+def test_append_validation_leaves_state():
+    """Argument errors of kivi_append launch nothing and leave n_res alone."""
+    cases = [
+        (dict(n_res=100), dict(n=40), 3),                 # 140 tokens in a 128-row ring
+        (dict(n_res=0), dict(n=-1), 1),
+        (dict(n_res=0), dict(n=8, stride=8 * 128 - 8), 1),   # stride below n * d
+        (dict(n_res=0), dict(n=8, stride=8 * 128 + 4), 2),   # stride not 16-byte aligned
+        (dict(n_res=0), dict(n=8, k_new=FAKE + 8), 2),
+        (dict(n_res=0), dict(n=8, v_new=0), 1),
+        (dict(n_res=0, res_head=128), dict(n=8), 1),       # head outside the ring
+    ]
+    for ckw, akw, status in cases:
+        c = _cache(**ckw)
+        before = (c.s_q, c.res_head, c.n_res)
+        assert _append(_layers(), 2, c, **akw) == status, (ckw, akw)
+        assert (c.s_q, c.res_head, c.n_res) == before
+
+
+def test_append_of_nothing_advances_nothing():
+    c = _cache(n_res=5)
+    assert _append(_layers(), 2, c, 0) == 0 and c.n_res == 5
+    c = _cache(bh=0, n_res=5)                              # no sequences: the count advances
+    assert _append(_layers(), 2, c, 40) == 0 and c.n_res == 45
+
+
+def test_append_accepts_layers_without_store():
+    c = _cache(bh=0, n_res=0)
+    L = _layers(k_codes=None, k_scale=None, k_zero=None, v_codes=None, v_scale=None,
+                v_zero=None)
+    assert _append(L, 2, c, 16) == 0 and c.n_res == 16

@@ -63,3 +63,23 @@ def test_reference_arm_prints_on_rank_zero_only():
     (rc0, o0, e0), (rc1, o1, e1) = outs
     assert rc0 == 0 and rc1 == 0, (e0, e1)
     assert '"impl": "reference"' in o0 and o1.strip() == ""
+
+
+def test_gpus_flag_must_match_the_launch():
+    """--gpus that contradicts torchrun's WORLD_SIZE is an error, not ignored."""
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", "3", "--impl", "reference"],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr
+
+
+def test_gpus_flag_relaunches_under_torchrun():
+    """--gpus 2 outside torchrun starts two ranks (gloo-free: the reference arm
+    prints on rank 0 only)."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--impl", "reference",
+                        "--steps", "3", "--warmup", "3", "--reference-seconds", "3"],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=240)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.count('"impl": "reference"') == 1

@@ -156,22 +156,51 @@ def test_no_top_k_is_plain_kivi():
     assert_same("plain value codes", host_u32(pair.cache.v_codes[0]), st.v_codes)
 
 
-def test_sink_store_overflow_is_recorded():
-    batch, heads, d, group, bits = 1, 2, 128, 32, 4
+def test_sink_store_overflow_keeps_the_earliest_sinks():
+    """A flush whose sinks do not all fit the sink store records the overflow
+    (bit 1 of the fault word), stores the earliest flushed sinks that fit,
+    and quantizes the other flushed top-k tokens as plain tokens: store, sink
+    store and restored reconstruction equal the oracle's flush over a top-k
+    cut down to the sinks that fit."""
+    batch, heads, d, group, bits, cap_sinks = 2, 2, 128, 32, 4, 3
     pair = SinkPair(1, batch, heads, d, bits, group, group, r_cap=256, cap=256, k_top=8,
-                    sink_cap=3, seed=9, plant_every=20)
-    pair.sinks.update(0, 0)
-    rows = np.arange(256)
+                    sink_cap=cap_sinks, seed=9, plant_every=20)
     k = pair.tokens(0, "k", 256)
     v = pair.tokens(0, "v", 256)
+    pair.ring_k[0][:] = k
+    pair.ring_v[0][:] = v
     pair.cache.append(0, to_dev(k), to_dev(v))
     pair.cache.advance(256)
+    full = pair.states[0]
+    full.update(O.sink_scores(k, heads), 0)
     pair.sinks.update(0, 256)
-    pair.sinks.flush()
+    n = pair.sinks.flush()
     torch.cuda.synchronize()
     assert K.kivi_device_fault() == 2
-    assert int(pair.sinks.sink_count[0, 0]) == 3
-    del rows
+    assert (pair.sinks.sink_count[0].cpu().numpy() == cap_sinks).all()
+    # the oracle refuses an overflowing flush; its expectation is the flush
+    # over the top-k cut down to the earliest flushed positions that fit
+    cut = O.SinkState(batch, heads, d, 8, cap_sinks)
+    excess = []
+    for b in range(batch):
+        flushed = sorted(int(p) for p in full.top_pos[b, :full.top_count[b]] if p < n)
+        assert len(flushed) > cap_sinks, flushed     # every sequence overflows
+        cut.top_pos[b, :cap_sinks] = flushed[:cap_sinks]
+        cut.top_count[b] = cap_sinks
+        excess += [(b, p) for p in flushed[cap_sinks:]]
+    n_o, s_q, head, n_res = O.flush_sink(pair.ring_k[0], pair.ring_v[0], pair.stores[0], group,
+                                         0, 0, 256, cut)
+    assert n_o == n
+    pair.s_q, pair.head, pair.n_res = s_q, head, n_res
+    # the running top-k itself is untouched by the flush
+    cut.top_pos[:], cut.top_score[:], cut.top_count[:] = (full.top_pos, full.top_score,
+                                                           full.top_count)
+    pair.states[0] = cut
+    pair.check()
+    # the excess top-k tokens kept their values: quantized rows, not zeroed ones
+    vs = pair.cache.v_scale[0].cpu().numpy()
+    for b, p in excess:
+        assert (vs[b * heads:(b + 1) * heads, p] > 0).all(), (b, p)
 
 
 def attention_bound_check(q16, k, v, got, sm_scale, batch):
