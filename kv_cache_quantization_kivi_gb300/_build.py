@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(OUT_DIR, "libkivi.so")
 HEADER = os.path.join(ROOT, "include", "kivi.h")
 
 SOURCES = ["kivi_api.cu", "kivi_keys.cu", "kivi_values.cu", "kivi_attention.cu", "kivi_sink.cu",
-           "kivi_ring.cu"]
+           "kivi_ring.cu", "kivi_staged.cu"]
 HEADERS = ["kivi_device.cuh", "kivi_arith.cuh", "kivi_launch.h", "kivi_dispatch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -91,6 +91,24 @@ __device__ __forceinline__ uint32_t exact_code(float x, const GroupQ &g, float q
 }
 
 // ---------------------------------------------------------------------------
+// Half-precision min / max.  binary16 -> binary32 conversion is exact and
+// monotone, so min/max taken in binary16 equal min/max of the converted
+// values; only the sign of a zero extreme can differ, and make_group
+// canonicalises it.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
+  __half2 h;
+  memcpy(&h, &u, 4);
+  return h;
+}
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
+}
+
+// ---------------------------------------------------------------------------
 // Packed binary32 pairs (Blackwell f32x2 arithmetic: two IEEE operations,
 // each rounded on its own, per instruction).  A pair is a 64-bit value with
 // the first element in the low 32 bits.
@@ -120,6 +138,7 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ uint64_t f2_const(float c) { return f2_pack(c, c); }
 __device__ __forceinline__ uint64_t h2_to_f2(__half2 h) {
   const float2 f = __half22float2(h);
   return f2_pack(f.x, f.y);
@@ -204,12 +223,126 @@ __device__ __forceinline__ uint64_t codes2_nobranch(uint64_t x, const GroupQ2 &g
   return n;
 }
 
+// ---------------------------------------------------------------------------
+// Fast path from the binary16 input ("difference first")
+// ---------------------------------------------------------------------------
+//
+// The definition's first step, t = RN(x - zero), is one mixed-precision add
+// from the binary16 input (add.rn.f32.f16: the exact binary16 -> binary32
+// conversion and one rounded addition of -zero), so no separate conversion
+// is needed.  Then v = RN(t * r) with r = RN(1/scale).  With eps = 2^-24,
+// T = t / scale (exact) and u = RN(T) (the quotient the definition rounds):
+//   t * r = T (1 + a),   v = T (1 + a)(1 + b),   u = T (1 + g),  |a|,|b|,|g| <= eps
+//   0 <= T <= Q (1 + 2 eps)       (t <= RN(max - min), scale >= (max - min)(1 - eps) / Q)
+// so |v - u| <= Q (1 + 2 eps)(3 eps + 3 eps^2) <= 3.0001 Q eps =: E, a bound
+// that depends on the code width alone.  As for the fast path above, if
+// |v - n| < 1/2 - E for n = rint(v) then rint(u) = n (and u < Q + 1/2, so
+// no clip is needed); the test is run against 1/2 - 2E, here a compile-time
+// constant per code width.  A group with scale == 0 has r = 0: v = 0 and
+// every code 0, as defined.
+
+struct GroupD2 {
+  uint64_t r;    // (RN(1/scale0), RN(1/scale1)), 0 for a zero scale
+  float nz0;     // -zero0
+  float nz1;     // -zero1
+};
+
+__host__ __device__ constexpr double diff_thr(double q) {
+  return 0.5 - 2.0 * 3.0001 * q * 5.9604644775390625e-8;   // 1/2 - 2E, E = 3.0001 Q 2^-24
+}
+// -(thr')^2 with thr' = thr (1 - 2^-20): the float rounding of the square
+// (relative 2^-24) stays far inside the 2^-20 margin, so d^2 < thr'^2
+// implies |d| < thr.
+template <int BITS>
+__host__ __device__ constexpr float diff_neg_thr2() {
+  return -static_cast<float>(diff_thr((1 << BITS) - 1) * (1.0 - 9.5367431640625e-7) *
+                             diff_thr((1 << BITS) - 1) * (1.0 - 9.5367431640625e-7));
+}
+
+// A group's scale, zero and reciprocal only (the difference-first path
+// needs no other constant); the same arithmetic as make_group.
+__device__ __forceinline__ GroupQ make_group_szr(float mn, float mx, float qf) {
+  GroupQ g;
+  mn = __fadd_rn(mn, 0.0f);
+  mx = __fadd_rn(mx, 0.0f);
+  g.zero = mn;
+  g.scale = div_by_q(__fsub_rn(mx, mn), qf);
+  g.r = g.scale > 0.0f ? rcp_rn(g.scale) : 0.0f;
+  g.c = 0.0f;
+  g.thr = 0.0f;
+  return g;
+}
+
+__device__ __forceinline__ GroupD2 make_group_d2(const GroupQ &a, const GroupQ &b) {
+  GroupD2 g;
+  g.r = f2_pack(a.r, b.r);
+  g.nz0 = -a.zero;
+  g.nz1 = -b.zero;
+  return g;
+}
+
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// (RN(x0 - zero0), RN(x1 - zero1)) from a pair of binary16 values.
+__device__ __forceinline__ uint64_t diff_pair(uint32_t x2, float nz0, float nz1) {
+  float t0, t1;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
+      : "=f"(t0), "=f"(t1)
+      : "r"(x2), "f"(nz0), "f"(nz1));
+  return f2_pack(t0, t1);
+}
+
+// Codes of a pair as integer-valued floats, branch-free; the sign bits of the
+// acceptance test are AND-ed into neg_acc (its top bit ends clear if some
+// element needs the literal division).
+template <int BITS>
+__device__ __forceinline__ uint64_t codes2_diff_nobranch(uint32_t x2, const GroupD2 &g,
+                                                         uint32_t &neg_acc) {
+  const uint64_t magic = f2_pack(kRoundMagic, kRoundMagic);
+  const uint64_t v = f2_mul(diff_pair(x2, g.nz0, g.nz1), g.r);
+  const uint64_t y = f2_add(v, magic);
+  const uint64_t n = f2_sub(y, magic);
+  const uint64_t d = f2_sub(v, n);
+  const uint64_t e = f2_fma(d, d, f2_const(diff_neg_thr2<BITS>()));
+  neg_acc &= f2_lo_bits(e) & f2_hi_bits(e);
+  return n;
+}
+
+// The defined codes of a pair with the literal division, from the groups'
+// scale and zero (the rare pairs the difference-first path declines).
+__device__ __noinline__ inline uint64_t exact_pair_sz(uint32_t x2, float s0, float z0, float s1,
+                                                      float z1, float qf) {
+  GroupQ a, b;
+  a.scale = s0;
+  a.zero = z0;
+  b.scale = s1;
+  b.zero = z1;
+  const float2 x = __half22float2(u32_as_h2(x2));
+  return f2_pack(static_cast<float>(exact_code(x.x, a, qf)),
+                 static_cast<float>(exact_code(x.y, b, qf)));
+}
+
+// Codes of a pair: the difference-first fast path, or the literal division
+// behind a branch per pair (almost never taken).
+template <int BITS>
+__device__ __forceinline__ uint64_t codes2_diff(uint32_t x2, const GroupD2 &g, float s0, float z0,
+                                                float s1, float z1, float qf) {
+  uint32_t ok = 0xFFFFFFFFu;
+  const uint64_t n = codes2_diff_nobranch<BITS>(x2, g, ok);
+  if (ok >> 31) return n;
+  return exact_pair_sz(x2, s0, z0, s1, z1, qf);
+}
+
 // Packing.  Codes are small integers held exactly in binary32, so sums
 // q_a + q_b * 2^k (k a multiple of the code width) below 2^24 are exact; a
 // binary tree of such fused multiply-adds assembles a 16-bit half-word of
 // codes, y = half + 2^23 then holds it in its low 16 mantissa bits, and one
 // byte permute joins two half-words into a 32-bit code word (LSB first).
-__device__ __forceinline__ uint64_t f2_const(float c) { return f2_pack(c, c); }
 
 // Two 16-bit halves (as integer-valued floats) -> one word: lo | hi << 16.
 __device__ __forceinline__ uint32_t join_halves(float lo, float hi) {
@@ -268,24 +401,6 @@ __device__ __forceinline__ uint64_t neg_scale_2p23_pair(float s0, float s1) {
 }
 
 // ---------------------------------------------------------------------------
-// Half-precision min / max.  binary16 -> binary32 conversion is exact and
-// monotone, so min/max taken in binary16 equal min/max of the converted
-// values; only the sign of a zero extreme can differ, and make_group
-// canonicalises it.
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) {
-  __half2 h;
-  memcpy(&h, &u, 4);
-  return h;
-}
-__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) {
-  uint32_t u;
-  memcpy(&u, &h, 4);
-  return u;
-}
-
-// ---------------------------------------------------------------------------
 // Streaming global loads / stores (data touched once)
 // ---------------------------------------------------------------------------
 
@@ -338,6 +453,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {

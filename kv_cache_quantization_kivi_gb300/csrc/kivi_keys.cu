@@ -12,11 +12,12 @@
 // min(G, 32) tokens (a whole group at G = 16); for G = 64 and 128 the G/32
 // threads of a column are adjacent lanes that combine their extremes with
 // two-step shuffles.  The arithmetic is the
-// packed binary32 fast path of kivi_device.cuh with the exact-division
+// difference-first fast path of kivi_device.cuh with the exact-division
 // fallback; codes are packed along tokens in registers and stored as 8-byte
-// words pairs.  (A variant that staged each G x d tile into shared memory with
-// bulk asynchronous copies ran at a third of this throughput: its per-tile
-// CTA barrier and waits cost more than the copies saved.)
+// words pairs.  At head_dim 128 and G >= 32 the plain quantize takes the
+// staged kernel instead (kivi_staged.cu: whole tiles streamed into shared
+// memory by a producer warp); this kernel serves G = 16, other head dims,
+// the fused reconstruction and the sink mode.
 //
 // Dequantize: one thread per (layer, bh, group, 8 channels); 16-byte loads of
 // codes, scales and zeros, 16-byte streaming stores.
@@ -294,14 +295,19 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
                                  (p.y_row0 + static_cast<int64_t>(k.g) * G + k.split * TPT) * D +
                                  2 * k.col
                            : nullptr;
-      GroupQ2 gq;
+      GroupD2 gq;
+      float s0, z0, s1, z1;
       uint64_t sc2 = 0, nsc2 = 0, ze2 = 0;
       const float2 mnf = __half22float2(gmn);
       const float2 mxf = __half22float2(gmx);
       {
-        const GroupQ g0 = make_group(mnf.x, mxf.x, qf);
-        const GroupQ g1 = make_group(mnf.y, mxf.y, qf);
-        gq = make_group2(g0, g1);
+        const GroupQ g0 = make_group_szr(mnf.x, mxf.x, qf);
+        const GroupQ g1 = make_group_szr(mnf.y, mxf.y, qf);
+        gq = make_group_d2(g0, g1);
+        s0 = g0.scale;
+        z0 = g0.zero;
+        s1 = g1.scale;
+        z1 = g1.zero;
         if (RECON) {
           sc2 = f2_pack(g0.scale, g1.scale);
           nsc2 = neg_scale_2p23_pair(g0.scale, g1.scale);
@@ -340,17 +346,18 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
             if constexpr (BF) {
               uint32_t ok = 0xFFFFFFFFu;
 #pragma unroll
-              for (int j = 0; j < H; ++j) n[j] = codes2_nobranch(h2_to_f2(h[t0 + j]), gq, ok);
+              for (int j = 0; j < H; ++j)
+                n[j] = codes2_diff_nobranch<BITS>(h2_as_u32(h[t0 + j]), gq, ok);
               if (!(ok >> 31)) {   // rare: redo this half pair by pair from registers
 #pragma unroll
                 for (int j = 0; j < H; ++j)
-                  n[j] = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
+                  n[j] = codes2_diff<BITS>(h2_as_u32(h[t0 + j]), gq, s0, z0, s1, z1, qf);
               }
             }
 #pragma unroll
             for (int j = 0; j < H; ++j) {
               if constexpr (!BF)
-                n[j] = codes2<BITS, true>(h2_to_f2(h[t0 + j]), gq, mnf.x, mxf.x, mnf.y, mxf.y);
+                n[j] = codes2_diff<BITS>(h2_as_u32(h[t0 + j]), gq, s0, z0, s1, z1, qf);
               half[hh] = j == 0 ? n[j]
                                 : f2_fma(n[j], f2_const(static_cast<float>(1u << (BITS * j))),
                                          half[hh]);
@@ -537,6 +544,9 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
 
 cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, int mode,
                              cudaStream_t stream) {
+  bool handled = false;
+  const cudaError_t e = launch_key_quant_staged(p, group, bits, mode, stream, &handled);
+  if (handled) return e;
   KIVI_DISPATCH_MODE(key_quant_launch, p, group, bits, mode, stream);
 }
 

@@ -67,6 +67,8 @@ struct QuantParams {
   int64_t y_row0;           // row of the reconstruction of logical row 0
   int64_t heads;            // sink mode: bh slices per sequence (sequence = bh / heads)
   int64_t mask_words;       // sink mode: mask words per sequence
+  unsigned int *fault;      // staged kernels: the device fault word (bit 3: a pipeline wait
+                            // timed out); filled by their launcher
   // filled by the launchers: divisors of the kernels' unit index
   FastDiv div_chunks, div_rows, div_bh;
   QuantJob jobs[KIVI_MAX_LAYERS];
@@ -210,6 +212,11 @@ cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, int mode
 cudaError_t launch_value_quant(const QuantParams &p, int group, int bits, int mode,
                                cudaStream_t stream);
 cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits, cudaStream_t stream);
+// The staged key quantizer (head_dim 128, G >= 32, plain and fused modes):
+// whole G x 128 tiles streamed into a shared-memory ring by bulk copies.
+// Sets *handled = false (and launches nothing) for arguments it does not take.
+cudaError_t launch_key_quant_staged(const QuantParams &p, int group, int bits, int mode,
+                                    cudaStream_t stream, bool *handled);
 // Decode attention (head_dim 128): the main kernel, then (n_split > 1) the
 // combine kernel.
 cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits,
@@ -229,11 +236,11 @@ int current_sm_count();
 // moment it completes (the ordering is that of a plain launch).
 template <typename P>
 cudaError_t launch_dependent(void (*kern)(P), int64_t grid, int threads, cudaStream_t stream,
-                             const P &params) {
+                             const P &params, size_t dynamic_smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(static_cast<unsigned>(threads));
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dynamic_smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -207,12 +207,15 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
         }
         continue;
       }
-      GroupQ2 gq[SUB];
+      GroupD2 gq[SUB];
+      float gsc[SUB], gze[SUB];
       uint64_t sc2[SUB], nsc2[SUB], ze2[SUB];
 #pragma unroll
       for (int sg = 0; sg < SUB; ++sg) {
-        const GroupQ g = make_group(gmn[sg], gmx[sg], qf);
-        gq[sg] = make_group2(g, g);
+        const GroupQ g = make_group_szr(gmn[sg], gmx[sg], qf);
+        gq[sg] = make_group_d2(g, g);
+        gsc[sg] = g.scale;
+        gze[sg] = g.zero;
         sc2[sg] = nsc2[sg] = ze2[sg] = 0;
         if (RECON) {
           sc2[sg] = f2_pack(g.scale, g.scale);
@@ -244,12 +247,12 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
           uint64_t n[H / 2];
 #pragma unroll
           for (int j = 0; j < H / 2; ++j)
-            n[j] = codes2_nobranch(h2_to_f2(h[p0 + j]), gq[sg], neg_acc);
+            n[j] = codes2_diff_nobranch<BITS>(h2_as_u32(h[p0 + j]), gq[sg], neg_acc);
           if (!(neg_acc >> 31)) {  // rare: redo this half pair by pair, exactly where needed
 #pragma unroll
             for (int j = 0; j < H / 2; ++j)
-              n[j] = codes2<BITS, false>(h2_to_f2(h[p0 + j]), gq[sg], gmn[sg], gmx[sg], gmn[sg],
-                                         gmx[sg]);
+              n[j] = codes2_diff<BITS>(h2_as_u32(h[p0 + j]), gq[sg], gsc[sg], gze[sg], gsc[sg],
+                                       gze[sg], qf);
           }
           acc[hh] = n[0];
 #pragma unroll

@@ -2,9 +2,11 @@
 kernels' own headers: the group reciprocal (kivi_arith.cuh) is bit-identical
 to the correctly rounded reciprocal for every normal float in [2^-126,
 2^126), the whole range a group scale can take and more; the per-element
-code (kivi_device.cuh, codes2: the error-bounded fast path and its exact
-fallback) equals the literal definition with the IEEE division on random
-binary16 groups and on elements next to a rounding midpoint."""
+code of both fast paths (kivi_device.cuh: codes2, the fused multiply-add
+form with its exact fallback, and codes2_diff_nobranch, difference first,
+whose declined pairs the kernels redo exactly) equals the literal definition
+with the IEEE division on random binary16 groups and on elements next to a
+rounding midpoint."""
 from __future__ import annotations
 
 import os
@@ -40,4 +42,9 @@ def test_codes_equal_the_literal_definition(tmp_path):
     r = build_and_run(tmp_path, "quot_check")
     assert r.returncode == 0, r.stdout + r.stderr
     lines = r.stdout.strip().splitlines()
-    assert len(lines) == 2 and all("mismatches=0" in l for l in lines), r.stdout
+    assert len(lines) == 4 and all("mismatches=0" in l for l in lines), r.stdout
+    # the difference-first path declines few random pairs (its bound does not
+    # grow with the group's distance from zero)
+    rnd = [l for l in lines if "difference-first" in l and "mode=random" in l][0]
+    samples = int(rnd.split("samples=")[1].split()[0])
+    assert int(rnd.split("declined=")[1]) < samples // 1000, rnd

@@ -6,7 +6,9 @@ tiles, ragged tails, every (bits, group) pair, odd head dims and the
 degenerate inputs the method has (constant groups, signed zeros, exact .5
 ties, subnormals, extremes, groups far from zero).  Full-size workloads run
 in the launch configuration the benchmark times and are checked on sampled
-groups that the oracle computes one by one.
+groups that the oracle computes one by one, plus one complete layer (the
+last) of each prefill and one complete bh slice (the last) of every store
+sweep cell, for all four kernels and the fused forms.
 """
 from __future__ import annotations
 
@@ -278,6 +280,25 @@ def test_prefill_flush_full_size_sampled(name):
         sample_values(np.ascontiguousarray(v[:, :n]), host_u32(cache.v_codes[l]),
                       host_f32_bits(cache.v_scale[l]), host_f32_bits(cache.v_zero[l]),
                       host_u16(vy[l]), w.group, w.bits, 200, rng)
+    # the last layer complete, every group and element: its tiles are among the
+    # last each grid takes (late grid-stride iterations, the ring's last rows)
+    l = w.layers - 1
+    k, v = (np.ascontiguousarray(a[:, :n]) for a in hosts[l])
+    oc, os_, oz = O.quantize_keys(k, w.group, w.bits)
+    Wd = 32 // w.bits
+    assert_same("last layer key codes", host_u32(cache.k_codes[l])[:, :n // Wd], oc)
+    assert_same("last layer key scale", host_f32_bits(cache.k_scale[l])[:, :n // w.group],
+                bits32(os_))
+    assert_same("last layer key zero", host_f32_bits(cache.k_zero[l])[:, :n // w.group],
+                bits32(oz))
+    assert_same("last layer key recon", host_u16(ky[l]),
+                O.dequantize_keys(oc, os_, oz, n, w.group, w.bits))
+    oc, os_, oz = O.quantize_values(v, w.group, w.bits)
+    assert_same("last layer value codes", host_u32(cache.v_codes[l])[:, :n], oc)
+    assert_same("last layer value scale", host_f32_bits(cache.v_scale[l])[:, :n], bits32(os_))
+    assert_same("last layer value zero", host_f32_bits(cache.v_zero[l])[:, :n], bits32(oz))
+    assert_same("last layer value recon", host_u16(vy[l]),
+                O.dequantize_values(oc, os_, oz, w.group, w.bits))
 
 
 @pytest.mark.slow
@@ -287,20 +308,44 @@ def test_large_store_sweep_full_size_sampled():
     v = W.generate(w, 0, "v")
     kd, vd = to_dev(k), to_dev(v)
     rng = np.random.default_rng(6)
+    last = w.bh - 1            # one complete bh slice per cell: the grid's last tiles
+    kl, vl = np.ascontiguousarray(k[last:]), np.ascontiguousarray(v[last:])
     for bits in w.sweep_bits:
         for group in w.sweep_groups:
             c, s, z = K.kivi_quantize_keys(kd, group, bits)
             y = K.kivi_dequantize_keys(c, s, z, w.seq, group, bits)
+            fy, fc, fs, fz = K.kivi_fakequant_keys(kd, group, bits)
             torch.cuda.synchronize()
             sample_keys(k, host_u32(c), host_f32_bits(s), host_f32_bits(z), host_u16(y),
                         group, bits, 60, rng)
-            del c, s, z, y
+            oc, os_, oz = O.quantize_keys(kl, group, bits)
+            oy = O.dequantize_keys(oc, os_, oz, w.seq, group, bits)
+            for name, got, want in (("key codes", host_u32(c[last:]), oc),
+                                    ("key scale", host_f32_bits(s[last:]), bits32(os_)),
+                                    ("key zero", host_f32_bits(z[last:]), bits32(oz)),
+                                    ("key recon", host_u16(y[last:]), oy),
+                                    ("fused key recon", host_u16(fy[last:]), oy),
+                                    ("fused key codes", host_u32(fc[last:]), oc),
+                                    ("fused key scale", host_f32_bits(fs[last:]), bits32(os_))):
+                assert_same(f"{name} b{bits} g{group}", got, want)
+            del c, s, z, y, fy, fc, fs, fz
             c, s, z = K.kivi_quantize_values(vd, group, bits)
             y = K.kivi_dequantize_values(c, s, z, group, bits)
+            fy, fc, fs, fz = K.kivi_fakequant_values(vd, group, bits)
             torch.cuda.synchronize()
             sample_values(v, host_u32(c), host_f32_bits(s), host_f32_bits(z), host_u16(y),
                           group, bits, 60, rng)
-            del c, s, z, y
+            oc, os_, oz = O.quantize_values(vl, group, bits)
+            oy = O.dequantize_values(oc, os_, oz, group, bits)
+            for name, got, want in (("value codes", host_u32(c[last:]), oc),
+                                    ("value scale", host_f32_bits(s[last:]), bits32(os_)),
+                                    ("value zero", host_f32_bits(z[last:]), bits32(oz)),
+                                    ("value recon", host_u16(y[last:]), oy),
+                                    ("fused value recon", host_u16(fy[last:]), oy),
+                                    ("fused value codes", host_u32(fc[last:]), oc),
+                                    ("fused value zero", host_f32_bits(fz[last:]), bits32(oz))):
+                assert_same(f"{name} b{bits} g{group}", got, want)
+            del c, s, z, y, fy, fc, fs, fz
 
 
 @pytest.mark.slow
@@ -342,4 +387,19 @@ def test_batched_decode_flushes_full_size_sampled():
             sample_values(v, host_u32(cache.v_codes[l]), host_f32_bits(cache.v_scale[l]),
                           host_f32_bits(cache.v_zero[l]), None, w.group, w.bits, 100, rng,
                           out_r0=s_q0)
+        # the last layer's flushed tokens complete (every sequence, head, channel)
+        l = w.layers - 1
+        n, G, Wd = w.new_per_step, w.group, 32 // w.bits
+        k = W.generate(w, l, "k", tok0=t_flushed, n_tok=n)
+        v = W.generate(w, l, "v", tok0=t_flushed, n_tok=n)
+        oc, os_, oz = O.quantize_keys(k, G, w.bits)
+        assert_same("key codes", host_u32(cache.k_codes[l])[:, s_q0 // Wd:(s_q0 + n) // Wd], oc)
+        assert_same("key scale", host_f32_bits(cache.k_scale[l])[:, s_q0 // G:(s_q0 + n) // G],
+                    bits32(os_))
+        assert_same("key zero", host_f32_bits(cache.k_zero[l])[:, s_q0 // G:(s_q0 + n) // G],
+                    bits32(oz))
+        oc, os_, oz = O.quantize_values(v, G, w.bits)
+        assert_same("value codes", host_u32(cache.v_codes[l])[:, s_q0:s_q0 + n], oc)
+        assert_same("value scale", host_f32_bits(cache.v_scale[l])[:, s_q0:s_q0 + n], bits32(os_))
+        assert_same("value zero", host_f32_bits(cache.v_zero[l])[:, s_q0:s_q0 + n], bits32(oz))
     assert cache.s_q == w.store_prefill + steps * w.new_per_step
