@@ -22,7 +22,7 @@ from typing import List, Optional, Sequence, Tuple
 from . import _build
 
 __all__ = [
-    "KiviError", "lib", "library_path", "kivi_quantize_keys", "kivi_quantize_values",
+    "KiviError", "lib", "library_path", "debug_bounds", "kivi_quantize_keys", "kivi_quantize_values",
     "kivi_dequantize_keys", "kivi_dequantize_values", "kivi_flush", "kivi_flush_size",
     "kivi_append",
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
@@ -83,16 +83,22 @@ _lib = None
 _i64, _int, _vp = C.c_int64, C.c_int, C.c_void_p
 
 
+def debug_bounds() -> bool:
+    """True when ``KIVI_DEBUG_BOUNDS=1``: the index-checking build is loaded."""
+    return os.environ.get("KIVI_DEBUG_BOUNDS") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if debug_bounds() else _build.LIB_PATH
 
 
 def lib():
-    """The loaded ``libkivi.so`` (built from source first if missing)."""
+    """The loaded ``libkivi.so`` (built from source first if missing; with
+    ``KIVI_DEBUG_BOUNDS=1`` the index-checking ``libkivi_debug.so``)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            path = _build.build(debug_bounds=debug_bounds())
             L = C.CDLL(path)
             q_args = [_vp, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _vp, _vp, _i64, _vp]
             dq_args = [_vp, _i64, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int, _vp, _i64, _vp]

@@ -15,6 +15,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libkivi.so")
+# the index-checking build (KIVI_DEBUG_BOUNDS: every global access of the
+# flush and full-tensor kernels checked against its bh slice, failures
+# recorded in the device fault word), loaded when KIVI_DEBUG_BOUNDS=1
+DEBUG_LIB_PATH = os.path.join(OUT_DIR, "libkivi_debug.so")
 HEADER = os.path.join(ROOT, "include", "kivi.h")
 
 SOURCES = ["kivi_api.cu", "kivi_keys.cu", "kivi_values.cu", "kivi_attention.cu", "kivi_sink.cu",
@@ -36,23 +40,29 @@ def _inputs():
             [os.path.join(CSRC, h) for h in HEADERS] + [HEADER, os.path.abspath(__file__)])
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link ``libkivi.so`` if missing or older than its sources."""
-    if not force and not is_stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug_bounds: bool = False) -> str:
+    """Compile and link ``libkivi.so`` (``libkivi_debug.so`` with
+    ``debug_bounds``) if missing or older than its sources."""
+    lib_path = DEBUG_LIB_PATH if debug_bounds else LIB_PATH
+    if not force and not is_stale(lib_path):
+        return lib_path
     os.makedirs(OUT_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug_bounds:
+        extra.append("-DKIVI_DEBUG_BOUNDS")
     pid = os.getpid()
+    tag = "dbg" if debug_bounds else "rel"
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, f"{os.path.splitext(src)[0]}.{pid}.o")
+        obj = os.path.join(OUT_DIR, f"{os.path.splitext(src)[0]}.{tag}.{pid}.o")
         cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,8 +71,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             print(r.stdout + r.stderr)
         return obj
 
-    objs = [os.path.join(OUT_DIR, f"{os.path.splitext(s)[0]}.{pid}.o") for s in SOURCES]
-    tmp = LIB_PATH + f".{pid}.tmp"
+    objs = [os.path.join(OUT_DIR, f"{os.path.splitext(s)[0]}.{tag}.{pid}.o") for s in SOURCES]
+    tmp = lib_path + f".{pid}.tmp"
     try:
         with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
             list(ex.map(compile_one, SOURCES))
@@ -76,8 +86,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                 pass
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

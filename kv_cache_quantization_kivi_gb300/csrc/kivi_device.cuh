@@ -10,6 +10,22 @@
 
 namespace kivi_dev {
 
+// Index checks of the debug build (compiled with -DKIVI_DEBUG_BOUNDS): every
+// global access of the flush and full-tensor kernels first checks its offset
+// against the extent of its bh slice that the host validated (and its slice
+// and layer against the launch); a failed check records bit 4 of the device
+// fault word and the access is skipped.  Release builds compile every check
+// to `true`.
+#ifdef KIVI_DEBUG_BOUNDS
+__device__ __forceinline__ bool bound_check(bool ok, unsigned int *fault) {
+  if (!ok && fault != nullptr) atomicOr(fault, 16u);
+  return ok;
+}
+#define KIVI_BOUND(fault, cond) (::kivi_dev::bound_check((cond), (fault)))
+#else
+#define KIVI_BOUND(fault, cond) (true)
+#endif
+
 // ---------------------------------------------------------------------------
 // Group quantizer
 // ---------------------------------------------------------------------------

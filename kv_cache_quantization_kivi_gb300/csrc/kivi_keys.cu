@@ -199,6 +199,13 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
                              static_cast<int64_t>(k.b) * p.x_bh_stride + row0 * D) +
                          k.col + static_cast<int64_t>(k.split) * TPT * (D / 2);
     const bool full = active && rows_here >= TPT;
+    // debug builds: every row this thread reads (padded rows included) lies
+    // inside its bh slice
+    const int64_t r_first = row0 + static_cast<int64_t>(k.split) * TPT;
+    const bool x_ok = KIVI_BOUND(
+        p.fault, !active || (k.b < p.bh && r_first + min(0, rows_here - 1) >= 0 &&
+                             (r_first + (rows_here >= 1 ? min(rows_here, TPT) : rows_here)) * D <=
+                                 p.x_bh_stride));
 
     // sink mode: bit t = token t of this split is a sink (left out of the
     // group's min / max, code 0); the flush only moves whole groups.  Mask
@@ -213,7 +220,7 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
     // TPT tokens of this thread's channel pair; min / max in four chains
     __half2 h[TPT];
     __half2 gmn, gmx;
-    if (full) {
+    if (full && x_ok) {
 #pragma unroll
       for (int t = 0; t < TPT; ++t) h[t] = __ldcs(src + t * (D / 2));
       if (SINK && sink_bits != 0u) {   // a group holding sinks (rare)
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
         gmn = __hmin2(__hmin2(mn[0], mn[1]), __hmin2(mn[2], mn[3]));
         gmx = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
       }
-    } else if (active) {  // ragged last group: padded by repeating the last row
+    } else if (active && x_ok) {  // ragged last group: padded by repeating the last row
       const uint2 e = key_partial_ragged<TPT>(src, rows_here, D);
       gmn = u32_as_h2(e.x);
       gmx = u32_as_h2(e.y);
@@ -285,12 +292,22 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
 
     if (active) {
       const int64_t out_g = p.out0 + k.g;
-      const bool codes_out = !RECON || job.codes != nullptr;
+      // debug builds: the code words, scale / zero and reconstruction rows this
+      // thread writes lie inside its bh slice
+      const bool codes_out =
+          (!RECON || job.codes != nullptr) &&
+          KIVI_BOUND(p.fault, (out_g * (G / W) + k.split * WPT + WPT - 1) * D + 2 * k.col + 2 <=
+                                  p.codes_bh_stride &&
+                              out_g * D + 2 * k.col + 2 <= p.sz_bh_stride);
+      const bool y_ok = KIVI_BOUND(
+          p.fault, !RECON || rows_here <= 0 ||
+                       (p.y_row0 + static_cast<int64_t>(k.g) * G + k.split * TPT +
+                        min(rows_here, TPT) - 1) * D + 2 * k.col + 2 <= p.y_bh_stride);
       uint32_t *cdst = codes_out ? job.codes + static_cast<int64_t>(k.b) * p.codes_bh_stride +
                                        (out_g * (G / W) + k.split * WPT) * D + 2 * k.col
                                  : nullptr;
       // reconstruction: column (2 col, 2 col + 1) of the first token of the split
-      __half *ycol = RECON ? static_cast<__half *>(job.y) +
+      __half *ycol = RECON && y_ok ? static_cast<__half *>(job.y) +
                                  static_cast<int64_t>(k.b) * p.y_bh_stride +
                                  (p.y_row0 + static_cast<int64_t>(k.g) * G + k.split * TPT) * D +
                                  2 * k.col
@@ -321,7 +338,9 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
       }
       if (!full) {
         // ragged group: literal division, rows read again from memory
-        key_exact_store<BITS, TPT>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst, ycol);
+        if (x_ok)
+          key_exact_store<BITS, TPT>(src, rows_here, D, h2_as_u32(gmn), h2_as_u32(gmx), cdst,
+                                     ycol);
       } else {
         // Quantize and pack along tokens: WPT words per channel, word wi holds
         // tokens [wi*W, wi*W + W) of this thread's TPT (token wi*W + j at bits
@@ -361,7 +380,7 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
               half[hh] = j == 0 ? n[j]
                                 : f2_fma(n[j], f2_const(static_cast<float>(1u << (BITS * j))),
                                          half[hh]);
-              if (RECON)
+              if (RECON && y_ok)
                 __stcs(reinterpret_cast<unsigned int *>(ycol + static_cast<int64_t>(t0 + j) * D),
                        recon_pair(n[j], sc2, nsc2, ze2));
             }
@@ -405,6 +424,14 @@ __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant_
     const int64_t b = jb - job * p.div_bh.d;
     const DequantJob &J = p.jobs[job];
 
+    // debug builds: the unit's reads and writes stay inside its bh slice
+    if (!KIVI_BOUND(p.fault,
+                    b < p.bh && g * D + ch * 8 + 8 <= p.sz_bh_stride &&
+                        (g * (G / W) + split * (TPU / W) + TPU / W - 1) * D + ch * 8 + 8 <=
+                            p.codes_bh_stride &&
+                        (min(p.rows, g * G + split * TPU + TPU) - 1) * D + ch * 8 + 8 <=
+                            p.y_bh_stride))
+      continue;
     const int64_t so = b * p.sz_bh_stride + g * D + ch * 8;
     const uint4 s_a = ld_stream(J.scale + so), s_b = ld_stream(J.scale + so + 4);
     const uint4 z_a = ld_stream(J.zero + so), z_b = ld_stream(J.zero + so + 4);
@@ -520,6 +547,8 @@ cudaError_t key_quant_launch(const QuantParams &p, cudaStream_t stream) {
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 2));
   q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));
   q.div_bh = FastDiv::make(static_cast<uint32_t>(p.bh));
+  cudaError_t e = debug_fault_word(&q.fault);
+  if (e != cudaSuccess) return e;
   return launch_dependent(kern, grid, threads, stream, q);
 }
 
@@ -535,6 +564,8 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   q.div_chunks = FastDiv::make(static_cast<uint32_t>(p.d / 8));
   q.div_rows = FastDiv::make(static_cast<uint32_t>(ng));
   q.div_bh = FastDiv::make(static_cast<uint32_t>(p.bh));
+  const cudaError_t e = debug_fault_word(&q.fault);
+  if (e != cudaSuccess) return e;
   return launch_dependent(kern, grid, threads, stream, q);
 }
 

@@ -67,8 +67,9 @@ struct QuantParams {
   int64_t y_row0;           // row of the reconstruction of logical row 0
   int64_t heads;            // sink mode: bh slices per sequence (sequence = bh / heads)
   int64_t mask_words;       // sink mode: mask words per sequence
-  unsigned int *fault;      // staged kernels: the device fault word (bit 3: a pipeline wait
-                            // timed out); filled by their launcher
+  unsigned int *fault;      // the device fault word (staged kernels, bit 3: a pipeline wait
+                            // timed out; debug builds, bit 4: an index check failed);
+                            // filled by the launchers that use it
   // filled by the launchers: divisors of the kernels' unit index
   FastDiv div_chunks, div_rows, div_bh;
   QuantJob jobs[KIVI_MAX_LAYERS];
@@ -91,6 +92,7 @@ struct DequantParams {
   int64_t sz_bh_stride;
   int64_t y_bh_stride;
   FastDiv div_chunks, div_rows, div_bh;  // filled by the launcher
+  unsigned int *fault;                  // debug builds: the device fault word (bit 4)
   DequantJob jobs[KIVI_MAX_LAYERS];
 };
 
@@ -112,6 +114,7 @@ struct AppendParams {
   int64_t row0;
   int64_t new_bh_stride;  // fp16 elements
   FastDiv div_chunks, div_n, div_bh;  // filled by the launcher
+  unsigned int *fault;                // debug builds: the device fault word (bit 4)
   AppendJob jobs[KIVI_MAX_LAYERS];
 };
 cudaError_t launch_append(const AppendParams &p, cudaStream_t stream);
@@ -258,6 +261,16 @@ inline int64_t flat_grid(int64_t units, int threads) {
 // Address of the device fault word on the current device (looked up once
 // per device), for kernels of other translation units.
 cudaError_t fault_word_address(unsigned int **ptr);
+// The fault word for the index checks of the debug build; nullptr (and no
+// lookup) in release builds.
+inline cudaError_t debug_fault_word(unsigned int **ptr) {
+#ifdef KIVI_DEBUG_BOUNDS
+  return fault_word_address(ptr);
+#else
+  *ptr = nullptr;
+  return cudaSuccess;
+#endif
+}
 // Reads and clears the device word in which kernels record a pipeline wait
 // that timed out (bit 0: decode attention).
 cudaError_t read_and_clear_fault(uint32_t *fault);

@@ -44,6 +44,10 @@ __global__ void __launch_bounds__(kAppendThreads)
     const int64_t src = static_cast<int64_t>(b) * p.new_bh_stride +
                         static_cast<int64_t>(i) * p.d + 8 * c;
     const int64_t dst = (static_cast<int64_t>(b) * p.r_cap + row) * p.d + 8 * c;
+    // debug builds: both rows lie inside their bh slices
+    if (!KIVI_BOUND(p.fault, b < p.bh && static_cast<int64_t>(i) * p.d + 8 * c + 8 <=
+                                 p.new_bh_stride && row >= 0 && row < p.r_cap))
+      continue;
     const uint4 kv = kivi_dev::ld_stream(static_cast<const uint16_t *>(J.k_new) + src);
     const uint4 vv = kivi_dev::ld_stream(static_cast<const uint16_t *>(J.v_new) + src);
     *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(J.k_res) + dst) = kv;
@@ -59,6 +63,8 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t stream) {
   q.div_n = FastDiv::make(static_cast<uint32_t>(p.n));
   q.div_bh = FastDiv::make(static_cast<uint32_t>(p.bh));
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.n * (p.d / 8);
+  const cudaError_t e = debug_fault_word(&q.fault);
+  if (e != cudaSuccess) return e;
   return launch_dependent(append_kernel, flat_grid(units, kAppendThreads), kAppendThreads,
                           stream, q);
 }

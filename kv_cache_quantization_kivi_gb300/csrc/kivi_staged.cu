@@ -160,7 +160,7 @@ __device__ __forceinline__ void key_half(uint32_t row_addr, int row_first, int r
       h01 = j == 0 ? n01[jj] : f2_fma(n01[jj], m, h01);
       h23 = j == 0 ? n23[jj] : f2_fma(n23[jj], m, h23);
       if constexpr (RECON) {
-        if (FULL || row_first + j < rows_here)
+        if ((FULL || row_first + j < rows_here) && ydst != nullptr)
           __stcs(reinterpret_cast<uint2 *>(ydst + static_cast<int64_t>(y_first + j) * kD),
                  make_uint2(recon_pair(n01[jj], sc01, nsc01, ze01),
                             recon_pair(n23[jj], sc23, nsc23, ze23)));
@@ -258,9 +258,16 @@ __global__ void __launch_bounds__(KeyStaged<G>::kThreads, 1)
                         static_cast<int64_t>(k.b) * p.x_bh_stride + row0 * kD;
       const uint32_t bytes = static_cast<uint32_t>(rows_here) * kRowBytes;
       *reinterpret_cast<volatile uint32_t *>(&stage_tile[s]) = j;
-      mbar_arrive_expect_tx(smem_addr(&full_bar[s]), bytes);
-      bulk_load(ring0 + static_cast<uint32_t>(s) * C::kTile, src, bytes,
-                smem_addr(&full_bar[s]), pol);
+      // debug builds: the tile lies inside its bh slice (else the stage's phase
+      // completes without a copy)
+      if (KIVI_BOUND(p.fault, k.b < p.bh && rows_here > 0 && rows_here <= G &&
+                                  (row0 + rows_here) * kD <= p.x_bh_stride)) {
+        mbar_arrive_expect_tx(smem_addr(&full_bar[s]), bytes);
+        bulk_load(ring0 + static_cast<uint32_t>(s) * C::kTile, src, bytes,
+                  smem_addr(&full_bar[s]), pol);
+      } else {
+        mbar_arrive(smem_addr(&full_bar[s]));
+      }
     }
     // every issued copy has landed before the CTA may end
     for (int s = 0; s < S && static_cast<uint32_t>(s) < j; ++s) {
@@ -375,7 +382,17 @@ __global__ void __launch_bounds__(KeyStaged<G>::kThreads, 1)
     const float4 sc = make_float4(g0.scale, g1.scale, g2.scale, g3.scale);
     const float4 ze = make_float4(g0.zero, g1.zero, g2.zero, g3.zero);
     const int64_t out_g = p.out0 + k.g;
-    const bool codes_out = !RECON || job.codes != nullptr;
+    // debug builds: the code words, scales, zeros and reconstruction rows this
+    // lane writes lie inside its bh slice
+    const bool codes_out =
+        (!RECON || job.codes != nullptr) &&
+        KIVI_BOUND(p.fault, (out_g * (G / W) + pw * (kWarpRows / W) + kWarpRows / W - 1) * kD +
+                                    4 * lane + 4 <= p.codes_bh_stride &&
+                                out_g * kD + 4 * lane + 4 <= p.sz_bh_stride);
+    const bool y_ok = KIVI_BOUND(
+        p.fault, !RECON || rows_here <= r0 ||
+                     (p.y_row0 + lr0 + min(rows_here, r0 + kWarpRows) - 1) * kD + 4 * lane + 4 <=
+                         p.y_bh_stride);
     if (pw == 0 && codes_out) {
       const int64_t o = static_cast<int64_t>(k.b) * p.sz_bh_stride + out_g * kD + 4 * lane;
       __stcs(reinterpret_cast<float4 *>(job.scale + o), sc);
@@ -384,7 +401,7 @@ __global__ void __launch_bounds__(KeyStaged<G>::kThreads, 1)
     uint32_t *cdst = codes_out ? job.codes + static_cast<int64_t>(k.b) * p.codes_bh_stride +
                                      (out_g * (G / W) + pw * (kWarpRows / W)) * kD + 4 * lane
                                : nullptr;
-    __half *ydst = RECON ? static_cast<__half *>(job.y) + static_cast<int64_t>(k.b) * p.y_bh_stride +
+    __half *ydst = RECON && y_ok ? static_cast<__half *>(job.y) + static_cast<int64_t>(k.b) * p.y_bh_stride +
                                (p.y_row0 + lr0 + r0) * kD + 4 * lane
                          : nullptr;
 

@@ -81,7 +81,12 @@ __device__ __forceinline__ void warp_store_units(uint32_t *blk, uint32_t lane, b
     const uint32_t j = lane + 32u * i;      // chunk of the warp block
     const uint32_t owner = j >> 2;          // unit (lane) that produced it
     const unsigned long long d = __shfl_sync(0xffffffffu, dbits, owner);
-    if (base + owner < total) {
+#ifdef KIVI_DEBUG_BOUNDS
+    const bool owner_valid = __shfl_sync(0xffffffffu, valid ? 1 : 0, owner) != 0;
+#else
+    constexpr bool owner_valid = true;      // valid == (the lane's unit exists)
+#endif
+    if (base + owner < total && owner_valid) {
       const uint4 v = *reinterpret_cast<const uint4 *>(blk + unit_slot(owner, j & 3u));
       st_stream(reinterpret_cast<__half *>(d) + 8 * (j & 3), v);
     }
@@ -126,8 +131,11 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
     }
     const __half *src = static_cast<const __half *>(job.x) + t.b * p.x_bh_stride + phys * D +
                         t.k * 32;
+    // debug builds: the unit's input and outputs lie inside its bh slice
+    const bool x_ok =
+        KIVI_BOUND(p.fault, !active || (t.b < p.bh && phys * D + t.k * 32 + 32 <= p.x_bh_stride));
     uint4 v[4] = {};
-    if (active) {
+    if (active && x_ok) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) v[i] = ld_stream(src + 8 * i);
     }
@@ -175,6 +183,9 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
     __half *ydst = RECON ? static_cast<__half *>(job.y) + t.b * p.y_bh_stride +
                                (p.y_row0 + static_cast<int64_t>(t.r)) * D + t.k * 32
                          : nullptr;
+    const bool y_ok = KIVI_BOUND(
+        p.fault, !RECON || !active ||
+                     (p.y_row0 + static_cast<int64_t>(t.r)) * D + t.k * 32 + 32 <= p.y_bh_stride);
     if (!RECON && !active) continue;
     uint32_t out[16];  // reconstruction of the 32 channels (RECON)
     if (active) {
@@ -185,12 +196,16 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
         gmx[sg] = -__high2float(ext[sg]);
       }
       const int64_t out_row = p.out0 + t.r;
-      const bool codes_out = !RECON || job.codes != nullptr;
+      const bool codes_out =
+          (!RECON || job.codes != nullptr) &&
+          KIVI_BOUND(p.fault, out_row * (D / W) + t.k * BITS + BITS <= p.codes_bh_stride &&
+                                  out_row * (D / G) + t.k * SUB / L + SUB <= p.sz_bh_stride);
       // (scale, zero) of this thread's first group: row out_row, entry k SUB / L
       const int64_t so = t.b * p.sz_bh_stride + out_row * (D / G) + t.k * SUB / L;
       // sink mode: a sink token's row is not quantized (codes, scales, zeros 0)
       if (SINK && ((job.mask[static_cast<int64_t>(t.b / p.heads) * p.mask_words + (t.r >> 5)] >>
                     (t.r & 31)) & 1u)) {
+        if (!codes_out) continue;
         if (t.k % L == 0) {
 #pragma unroll
           for (int sg = 0; sg < SUB; ++sg) {
@@ -285,7 +300,7 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
         }
       }
     }  // active
-    if (RECON) warp_store_units(blk, lane, active, out, ydst, base, total);
+    if (RECON) warp_store_units(blk, lane, active && y_ok, out, ydst, base, total);
   }
 }
 
@@ -319,7 +334,15 @@ __global__ void __launch_bounds__(kBlockThreads)
     __half *y = static_cast<__half *>(J.y) + t.b * p.y_bh_stride + static_cast<int64_t>(t.r) * D +
                 t.k * 32;
     uint32_t out[16];
-    if (active) {
+    // debug builds: the unit's reads and its output row lie inside its bh slice
+    const bool ok = KIVI_BOUND(
+        p.fault, !active || (t.b < p.bh &&
+                             static_cast<int64_t>(t.r) * (D / W) + t.k * BITS + BITS <=
+                                 p.codes_bh_stride &&
+                             static_cast<int64_t>(t.r) * (D / G) + t.k * SUB / L + SUB <=
+                                 p.sz_bh_stride &&
+                             static_cast<int64_t>(t.r) * D + t.k * 32 + 32 <= p.y_bh_stride));
+    if (active && ok) {
       const uint32_t *src = J.codes + t.b * p.codes_bh_stride +
                             static_cast<int64_t>(t.r) * (D / W) + t.k * BITS;
       uint32_t w[BITS];
@@ -387,7 +410,7 @@ __global__ void __launch_bounds__(kBlockThreads)
         }
       }
     }
-    warp_store_units(blk, lane, active, out, y, base, total);
+    warp_store_units(blk, lane, active && ok, out, y, base, total);
   }
 }
 
@@ -426,7 +449,10 @@ cudaError_t value_quant_launch(const QuantParams &p, cudaStream_t stream) {
   // fused reconstruction at G = 16, where the flat grid is 12% faster.
   const int64_t flat = flat_grid(units, threads);
   grid = (MODE == kQuantRecon && G == 16) ? flat : std::min<int64_t>(flat, 3 * grid);
-  return launch_dependent(kern, grid, threads, stream, with_dividers(p));
+  QuantParams q = with_dividers(p);
+  err = debug_fault_word(&q.fault);
+  if (err != cudaSuccess) return err;
+  return launch_dependent(kern, grid, threads, stream, q);
 }
 
 // The dequantize kernels take one block per kBlockThreads units rather than a
@@ -441,7 +467,10 @@ cudaError_t value_dequant_launch(const DequantParams &p, cudaStream_t stream) {
   auto kern = value_dequant_kernel<BITS, G, DC>;
   const int64_t units = static_cast<int64_t>(p.n_jobs) * p.bh * p.rows * (p.d / 32);
   const int64_t grid = flat_grid(units, threads);
-  return launch_dependent(kern, grid, threads, stream, with_dividers(p));
+  DequantParams q = with_dividers(p);
+  const cudaError_t e = debug_fault_word(&q.fault);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(kern, grid, threads, stream, q);
 }
 
 }  // namespace
