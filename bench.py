@@ -694,24 +694,23 @@ class DecodeFlush:
                 "bytes": "append 8 B per new fp16 element pair (read + ring write, K and V); "
                          "flush 2 + b/8 + 8/G per element"}
 
-    def _flush(self, stream, ev):
-        return self.cache.flush(stream, ev)
-
     def step(self, stream, ev=None):
         w, c = self.w, self.cache
         if self.i % self.cycle == 0:     # the store offset cycles; the ring runs on
             c.state.s_q = w.store_prefill
         kp, vp = self.new_ptrs[self.i % 2]
         self.i += 1
-        if ev is not None:
-            ev[0].record(stream)
-        self.K.kivi_append(c.layers, c.n_layers, c.state, kp, vp, w.new_per_step,
-                           new_bh_stride=self.new_bh_stride, stream=stream)
-        n = self._flush(stream, None if ev is None else ev[1])
+        self._append_flush(stream, kp, vp, ev)
+
+    def _append_flush(self, stream, kp, vp, ev):
+        # one call: the flush's launches overlap the append's tail
+        w, c = self.w, self.cache
+        n = self.K.kivi_append_flush(c.layers, c.n_layers, c.state, kp, vp, w.new_per_step,
+                                     self.new_bh_stride, stream, ev)
         assert n == w.new_per_step
 
     def step_events(self, evs):
-        return (evs[0], self.K.event_handles(evs[1:4]))
+        return (C_void_p_array(evs))
 
     def kernel_times(self, e):
         names = self.kernels
@@ -794,8 +793,19 @@ class FusedDecodeFlush(DecodeFlush):
         c["bytes_per_elem"] = fused_bytes_per_elem(self.w.bits, self.w.group)
         return c
 
-    def _flush(self, stream, ev):
-        return self.cache.flush_fakequant(stream, ev)
+    def _append_flush(self, stream, kp, vp, ev):
+        # the fused flush has no combined call: append, then the flush
+        w, c = self.w, self.cache
+        if ev is not None:
+            ev_torch, handles = ev
+            ev_torch.record(stream)
+        self.K.kivi_append(c.layers, c.n_layers, c.state, kp, vp, w.new_per_step,
+                           new_bh_stride=self.new_bh_stride, stream=stream)
+        n = c.flush_fakequant(stream, None if ev is None else handles)
+        assert n == w.new_per_step
+
+    def step_events(self, evs):
+        return (evs[0], self.K.event_handles(evs[1:4]))
 
     def e2e_setup(self):
         import torch
@@ -1127,6 +1137,12 @@ class FusedStoreSweep(StoreSweep):
                 (2 * bytes_per_elem(self.bits, self.group)), t, what)
 
 
+def C_void_p_array(evs):
+    """ctypes array of the cudaEvent_t handles of torch events (each recorded once)."""
+    import ctypes as C
+    return (C.c_void_p * len(evs))(*[e.cuda_event for e in evs])
+
+
 def make_workload(name, device, layers=None, bits=None, group=None, fused=False,
                   attention=False, sink=False):
     import dataclasses
@@ -1194,8 +1210,11 @@ def ncu_traffic(workload: str, kernel: str):
 def time_steps(wl, steps: int, warmup: int, stream, device, sampler=None):
     """W untimed warm-up steps, then exactly K steps between a barrier and a
     synchronize on both sides, with CUDA events on the launching stream
-    around the whole region and around every kernel of every step.  Returns
-    (elapsed ms of the K steps, max over ranks; the per-step event lists)."""
+    around the whole region only (an event recorded between two launches
+    would end the overlap of a launch with its predecessor's tail); then K
+    more steps, outside the timed region, with events around every kernel of
+    every step for the per-kernel breakdown.  Returns (elapsed ms of the
+    timed K steps, max over ranks; the per-step event lists)."""
     import torch
 
     def new_events(n):
@@ -1207,8 +1226,6 @@ def time_steps(wl, steps: int, warmup: int, stream, device, sampler=None):
     for _ in range(warmup):
         wl.step(stream)
     torch.cuda.synchronize(device)
-    evs = [new_events(wl.events_per_step) for _ in range(steps)]
-    handles = [wl.step_events(e) for e in evs]
     start, end = new_events(2)
     torch.cuda.synchronize(device)
     if sampler is not None:
@@ -1217,12 +1234,19 @@ def time_steps(wl, steps: int, warmup: int, stream, device, sampler=None):
     barrier()
     torch.cuda.synchronize(device)
     start.record(stream)
-    for i in range(steps):
-        wl.step(stream, handles[i])
+    for _ in range(steps):
+        wl.step(stream)
     end.record(stream)
     torch.cuda.synchronize(device)
     barrier()
-    return reduce_max(start.elapsed_time(end), device), evs
+    elapsed = reduce_max(start.elapsed_time(end), device)
+    evs = [new_events(wl.events_per_step) for _ in range(steps)]
+    handles = [wl.step_events(e) for e in evs]
+    torch.cuda.synchronize(device)
+    for i in range(steps):
+        wl.step(stream, handles[i])
+    torch.cuda.synchronize(device)
+    return elapsed, evs
 
 
 def kernel_stats(wl, evs, peak: float) -> dict:

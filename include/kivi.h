@@ -268,6 +268,24 @@ KIVI_API kivi_status kivi_flush_fakequant(const kivi_layer *layers, int n_layers
                                           void *const *v_hat, int64_t *n_flushed,
                                           kivi_stream_t stream, void *const events[3]);
 
+/* A decode step's append and flush in one call: kivi_append of the n new
+ * tokens of every layer, then kivi_flush (same arguments, results, state
+ * updates and errors; every argument of both steps is checked before the
+ * first launch, so an error launches nothing and changes no state).  When
+ * the tokens the flush moves were all in the ring before the append (the
+ * usual decode step: n_res >= the flush size), the flush's kernels do not
+ * read what the append writes, and their launches overlap the append's tail
+ * on the GPU (programmatic dependent launch) instead of waiting for it;
+ * stream order is kept: the call's work is complete when the stream reaches
+ * its end.  The store pointers of `layers` must be given (no NULL store).
+ * events: NULL, or 4 cudaEvent_t recorded before the append, before the key
+ * launch, between the key and the value launch and after it (NULL entries
+ * skipped); when the flush moves nothing only the first is recorded. */
+KIVI_API kivi_status kivi_append_flush(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                                       const void *const *k_new, const void *const *v_new,
+                                       int64_t new_bh_stride, int64_t n, int64_t *n_flushed,
+                                       kivi_stream_t stream, void *const events[4]);
+
 /* Dequantize the first cache->s_q tokens of every layer's store into
  * k_out[l], v_out[l] (host arrays of n_layers device pointers, each fp16
  * [bh][s_q][d] contiguous).  Equivalent to kivi_dequantize_keys and

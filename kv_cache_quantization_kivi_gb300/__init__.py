@@ -24,7 +24,7 @@ from . import _build
 __all__ = [
     "KiviError", "lib", "library_path", "debug_bounds", "kivi_quantize_keys", "kivi_quantize_values",
     "kivi_dequantize_keys", "kivi_dequantize_values", "kivi_flush", "kivi_flush_size",
-    "kivi_append",
+    "kivi_append", "kivi_append_flush",
     "kivi_dequantize_cache", "kivi_key_code_words", "kivi_value_code_words",
     "kivi_fakequant_keys", "kivi_fakequant_values", "kivi_flush_fakequant",
     "kivi_decode_attention", "kivi_decode_attention_splits", "kivi_decode_attention_workspace",
@@ -118,6 +118,10 @@ def lib():
             L.kivi_append.argtypes = [C.POINTER(kivi_layer), _int, C.POINTER(kivi_cache),
                                       C.POINTER(_vp), C.POINTER(_vp), _i64, _i64, _vp]
             L.kivi_append.restype = _int
+            L.kivi_append_flush.argtypes = [C.POINTER(kivi_layer), _int, C.POINTER(kivi_cache),
+                                            C.POINTER(_vp), C.POINTER(_vp), _i64, _i64,
+                                            C.POINTER(_i64), _vp, C.POINTER(_vp)]
+            L.kivi_append_flush.restype = _int
             L.kivi_dequantize_cache.argtypes = [C.POINTER(kivi_layer), _int,
                                                 C.POINTER(kivi_cache), C.POINTER(_vp),
                                                 C.POINTER(_vp), _vp]
@@ -380,6 +384,21 @@ def _ptr_array(ts, n: int):
     return ts if isinstance(ts, C.Array) else (C.c_void_p * n)(*[t.data_ptr() for t in ts])
 
 
+def kivi_append_flush(layers, n_layers: int, cache: kivi_cache, k_new, v_new, n: int,
+                      new_bh_stride: int, stream=None, events=None) -> int:
+    """Raw C call: append + flush in one call (``k_new``/``v_new`` prepared
+    ctypes pointer arrays or per-layer tensors, ``new_bh_stride`` in
+    elements); ``events`` None or four cudaEvent handles / torch events.
+    Returns the tokens flushed."""
+    out = C.c_int64(0)
+    if events is not None and not isinstance(events, C.Array):
+        events = (C.c_void_p * 4)(*[e.cuda_event if e is not None else None for e in events])
+    _check(lib().kivi_append_flush(layers, n_layers, C.byref(cache), _ptr_array(k_new, n_layers),
+                                   _ptr_array(v_new, n_layers), new_bh_stride, n, C.byref(out),
+                                   _stream_handle(stream), events), "kivi_append_flush")
+    return int(out.value)
+
+
 def kivi_append(layers, n_layers: int, cache: kivi_cache, k_new, v_new, n: int,
                 new_bh_stride: Optional[int] = None, stream=None) -> None:
     """Raw C call: new tokens of every layer into the residual rings behind the
@@ -585,6 +604,19 @@ class KiviCache:
         if self.n_res + n > int(self.state.r_cap):
             raise ValueError("residual ring overflow")
         self.state.n_res += n
+
+    def append_flush(self, k_new, v_new, stream=None) -> int:
+        """New tokens of every layer (fp16 [n_layers, bh, n, d] or per-layer
+        lists of [bh, n, d], one bh stride) behind the residual, then the
+        flush, in one call; returns the tokens flushed."""
+        ks = list(k_new.unbind(0)) if hasattr(k_new, "unbind") else list(k_new)
+        vs = list(v_new.unbind(0)) if hasattr(v_new, "unbind") else list(v_new)
+        for x in ks + vs:
+            _fp16_3d(x, "append_flush")
+            if _bh_stride(x) != _bh_stride(ks[0]):
+                raise ValueError("append_flush: every new-token tensor needs the same bh stride")
+        return kivi_append_flush(self.layers, self.n_layers, self.state, ks, vs,
+                                 int(ks[0].shape[1]), _bh_stride(ks[0]), stream)
 
     def append_all(self, k_new, v_new, stream=None) -> None:
         """New tokens of every layer (fp16 [n_layers, bh, n, d] tensors or

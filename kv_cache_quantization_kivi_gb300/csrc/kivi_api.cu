@@ -358,10 +358,10 @@ static cudaError_t record(void *const *events, int i, cudaStream_t s) {
   return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s);
 }
 
-kivi_status kivi_append(const kivi_layer *layers, int n_layers, kivi_cache *cache,
-                        const void *const *k_new, const void *const *v_new,
-                        int64_t new_bh_stride, int64_t n, kivi_stream_t stream) {
-  const kivi_status st = check_cache(layers, n_layers, cache, /*allow_no_store=*/true);
+static kivi_status check_append(const kivi_layer *layers, int n_layers, const kivi_cache *cache,
+                                const void *const *k_new, const void *const *v_new,
+                                int64_t new_bh_stride, int64_t n, bool allow_no_store) {
+  const kivi_status st = check_cache(layers, n_layers, cache, allow_no_store);
   if (st != KIVI_OK) return st;
   if (n < 0 || !k_new || !v_new) return KIVI_ERR_INVAL;
   if (cache->n_res + n > cache->r_cap) return KIVI_ERR_CAPACITY;
@@ -375,6 +375,16 @@ kivi_status kivi_append(const kivi_layer *layers, int n_layers, kivi_cache *cach
       if (!aligned16(k_new[l]) || !aligned16(v_new[l])) return KIVI_ERR_ALIGN;
     }
     if (!bytes16(new_bh_stride, 2)) return KIVI_ERR_ALIGN;
+  }
+  return KIVI_OK;
+}
+
+// The append's launch (arguments already checked) and the state update.
+static kivi_status append_impl(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                               const void *const *k_new, const void *const *v_new,
+                               int64_t new_bh_stride, int64_t n, kivi_stream_t stream) {
+  const int64_t d = cache->d;
+  if (n > 0 && cache->bh > 0) {
     kivi_impl::AppendParams p;
     std::memset(&p, 0, sizeof(p));
     p.n_jobs = n_layers;
@@ -394,14 +404,28 @@ kivi_status kivi_append(const kivi_layer *layers, int n_layers, kivi_cache *cach
   return KIVI_OK;
 }
 
+kivi_status kivi_append(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                        const void *const *k_new, const void *const *v_new,
+                        int64_t new_bh_stride, int64_t n, kivi_stream_t stream) {
+  const kivi_status st =
+      check_append(layers, n_layers, cache, k_new, v_new, new_bh_stride, n, true);
+  if (st != KIVI_OK) return st;
+  return append_impl(layers, n_layers, cache, k_new, v_new, new_bh_stride, n, stream);
+}
+
 kivi_status kivi_flush(const kivi_layer *layers, int n_layers, kivi_cache *cache,
                        int64_t *n_flushed, kivi_stream_t stream) {
   return kivi_flush_timed(layers, n_layers, cache, n_flushed, stream, nullptr);
 }
 
+// defer_key: the key launch's inputs do not depend on the previous launch in
+// the stream (the flushed rows were not written by it), so it may defer its
+// dependency wait (QuantParams::defer_wait); the value launch never depends
+// on the key launch and always defers.
 static kivi_status flush_impl(const kivi_layer *layers, int n_layers, kivi_cache *cache,
                               void *const *k_hat, void *const *v_hat, int64_t *n_flushed,
-                              kivi_stream_t stream, void *const *events) {
+                              kivi_stream_t stream, void *const *events,
+                              bool defer_key = false) {
   const bool recon = k_hat != nullptr;
   const kivi_status st = check_cache(layers, n_layers, cache, recon);
   if (st != KIVI_OK) return st;
@@ -443,9 +467,11 @@ static kivi_status flush_impl(const kivi_layer *layers, int n_layers, kivi_cache
   kp.codes_bh_stride = cache->cap / W * d;
   kp.sz_bh_stride = cache->cap / G * d;
   kp.out0 = cache->s_q / G;
+  kp.defer_wait = defer_key ? 1 : 0;
   vp.codes_bh_stride = cache->cap * (d / W);
   vp.sz_bh_stride = cache->cap * (d / G);
   vp.out0 = cache->s_q;
+  vp.defer_wait = 1;
   for (int l = 0; l < n_layers; ++l) {
     const kivi_layer &L = layers[l];
     kp.jobs[l] = {L.k_res, L.k_codes, L.k_scale, L.k_zero, recon ? k_hat[l] : nullptr, nullptr};
@@ -483,6 +509,27 @@ kivi_status kivi_flush_fakequant(const kivi_layer *layers, int n_layers, kivi_ca
   return flush_impl(layers, n_layers, cache, k_hat, v_hat, n_flushed, stream, events);
 }
 
+kivi_status kivi_append_flush(const kivi_layer *layers, int n_layers, kivi_cache *cache,
+                              const void *const *k_new, const void *const *v_new,
+                              int64_t new_bh_stride, int64_t n, int64_t *n_flushed,
+                              kivi_stream_t stream, void *const events[4]) {
+  // every check of both steps before the first launch
+  kivi_status st = check_append(layers, n_layers, cache, k_new, v_new, new_bh_stride, n, false);
+  if (st != KIVI_OK) return st;
+  const int64_t n_res_before = cache->n_res;
+  const int64_t n_flush = kivi_flush_size(n_res_before + n, cache->residual, cache->group);
+  if (n_flush > 0 && cache->s_q + n_flush > cache->cap) return KIVI_ERR_CAPACITY;
+  cudaStream_t s = stream;
+  kivi_status r = cuda_status(record(events, 0, s));
+  if (r != KIVI_OK) return r;
+  r = append_impl(layers, n_layers, cache, k_new, v_new, new_bh_stride, n, stream);
+  if (r != KIVI_OK) return r;
+  // the flushed rows are residual tokens 0 .. n_flush - 1; when they were all
+  // in the ring before the append, the quantizers do not read what it wrote
+  return flush_impl(layers, n_layers, cache, nullptr, nullptr, n_flushed, stream,
+                    events ? events + 1 : nullptr, n_flush <= n_res_before);
+}
+
 kivi_status kivi_dequantize_cache(const kivi_layer *layers, int n_layers, const kivi_cache *cache,
                                   void *const *k_out, void *const *v_out, kivi_stream_t stream) {
   return kivi_dequantize_cache_timed(layers, n_layers, cache, k_out, v_out, stream, nullptr);
@@ -515,6 +562,7 @@ kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n_layers,
   kp.sz_bh_stride = cache->cap / G * d;
   vp.codes_bh_stride = cache->cap * (d / W);
   vp.sz_bh_stride = cache->cap * (d / G);
+  vp.defer_wait = 1;   // the value store does not depend on the key launch
   for (int l = 0; l < n_layers; ++l) {
     const kivi_layer &L = layers[l];
     kp.jobs[l] = {L.k_codes, L.k_scale, L.k_zero, k_out[l]};
@@ -771,6 +819,7 @@ kivi_status kivi_flush_sink(const kivi_layer *layers, const kivi_sink_layer *sin
   vp.codes_bh_stride = cache->cap * (d / W);
   vp.sz_bh_stride = cache->cap * (d / G);
   vp.out0 = cache->s_q;
+  vp.defer_wait = 1;   // reads the mask, complete before the key launch began its work
   for (int l = 0; l < n_layers; ++l) {
     const kivi_layer &L = layers[l];
     kp.jobs[l] = {L.k_res, L.k_codes, L.k_scale, L.k_zero, nullptr, sinks[l].mask};

@@ -154,7 +154,9 @@ __host__ __device__ constexpr int key_min_blocks() { return BITS >= 4 ? 3 : 4; }
 
 template <int BITS, int G, int DC, int MODE>
 __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant_kernel(const __grid_constant__ QuantParams p) {
-  kivi_dev::grid_dependency_wait();
+  // a launch whose inputs do not depend on the previous grid in the stream
+  // (defer_wait) starts at once and waits for it only before it ends
+  if (!p.defer_wait) kivi_dev::grid_dependency_wait();
   kivi_dev::grid_launch_dependents();
   constexpr bool RECON = MODE == kQuantRecon;
   constexpr bool SINK = MODE == kQuantSink;
@@ -392,6 +394,7 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
     }
 
   }
+  if (p.defer_wait) kivi_dev::grid_dependency_wait();
 }
 
 // One thread: channels [8*chunk, 8*chunk + 8) of group g of one bh slice.
@@ -399,7 +402,9 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
 // p.div_chunks, p.div_rows and p.div_bh divide by d/8, ng and bh.
 template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant__ DequantParams p) {
-  kivi_dev::grid_dependency_wait();
+  // a launch whose inputs do not depend on the previous grid in the stream
+  // (defer_wait) starts at once and waits for it only before it ends
+  if (!p.defer_wait) kivi_dev::grid_dependency_wait();
   kivi_dev::grid_launch_dependents();
   constexpr int W = CodeFmt<BITS>::W;
   constexpr uint32_t Q = CodeFmt<BITS>::Q;
@@ -519,6 +524,7 @@ __global__ void __launch_bounds__(256) key_dequant_kernel(const __grid_constant_
       }
     }
   }
+  if (p.defer_wait) kivi_dev::grid_dependency_wait();
 }
 
 

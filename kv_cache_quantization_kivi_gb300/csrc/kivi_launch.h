@@ -55,6 +55,12 @@ struct QuantJob {
 struct QuantParams {
   int32_t n_jobs;
   int32_t d;
+  // 1: the launch's inputs do not depend on the previous grid in the stream
+  // (programmatic dependent launch): the kernel starts its work at once and
+  // waits for that grid only before it ends, so its blocks fill the SMs the
+  // previous grid's tail leaves idle while stream order is kept
+  int32_t defer_wait;
+  int32_t pad0;
   int64_t bh;
   int64_t rows;
   int64_t x_bh_stride;      // fp16 elements
@@ -86,6 +92,8 @@ struct DequantJob {
 struct DequantParams {
   int32_t n_jobs;
   int32_t d;
+  int32_t defer_wait;   // as QuantParams::defer_wait
+  int32_t pad0;
   int64_t bh;
   int64_t rows;
   int64_t codes_bh_stride;

@@ -213,7 +213,9 @@ __global__ void __launch_bounds__(KeyStaged<G>::kThreads, 1)
   // producer before it issues the copy
   __shared__ uint32_t stage_tile[S];
 
-  grid_dependency_wait();
+  // a launch whose inputs do not depend on the previous grid in the stream
+  // (defer_wait) starts at once and waits for it only before it ends
+  if (!p.defer_wait) grid_dependency_wait();
   grid_launch_dependents();
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31u);
@@ -235,7 +237,10 @@ __global__ void __launch_bounds__(KeyStaged<G>::kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ---------------- producer: local tile j = global tile blockIdx.x + j * gridDim.x
-    if (lane != 0) return;
+    if (lane != 0) {
+      if (p.defer_wait) grid_dependency_wait();
+      return;
+    }
     const uint64_t pol = policy_evict_first();
     uint32_t j = 0;
     for (; j < mine; ++j) {
@@ -274,6 +279,7 @@ __global__ void __launch_bounds__(KeyStaged<G>::kThreads, 1)
       const uint32_t last = static_cast<uint32_t>(s) + ((j - 1u - s) / S) * S;
       mbar_wait_bounded(smem_addr(&full_bar[s]), (last / S) & 1u, kWaitLimitNs);
     }
+    if (p.defer_wait) grid_dependency_wait();
     return;
   }
 
@@ -414,6 +420,7 @@ __global__ void __launch_bounds__(KeyStaged<G>::kThreads, 1)
     if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
     j = j_next;
   }
+  if (p.defer_wait) grid_dependency_wait();
 }
 
 template <int BITS, int G, int MODE>

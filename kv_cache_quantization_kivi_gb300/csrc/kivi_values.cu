@@ -97,7 +97,9 @@ __device__ __forceinline__ void warp_store_units(uint32_t *blk, uint32_t lane, b
 template <int BITS, int G, int DC, int MODE>
 __global__ void __launch_bounds__(kBlockThreads, 4)
     value_quant_kernel(const __grid_constant__ QuantParams p) {
-  kivi_dev::grid_dependency_wait();
+  // a launch whose inputs do not depend on the previous grid in the stream
+  // (defer_wait) starts at once and waits for it only before it ends
+  if (!p.defer_wait) kivi_dev::grid_dependency_wait();
   kivi_dev::grid_launch_dependents();
   constexpr bool RECON = MODE == kQuantRecon;
   constexpr bool SINK = MODE == kQuantSink;
@@ -302,6 +304,7 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
     }  // active
     if (RECON) warp_store_units(blk, lane, active && y_ok, out, ydst, base, total);
   }
+  if (p.defer_wait) kivi_dev::grid_dependency_wait();
 }
 
 // Dequantize: a thread reconstructs the 32 channels of one (row, chunk) unit
@@ -310,7 +313,9 @@ __global__ void __launch_bounds__(kBlockThreads, 4)
 template <int BITS, int G, int DC>
 __global__ void __launch_bounds__(kBlockThreads)
     value_dequant_kernel(const __grid_constant__ DequantParams p) {
-  kivi_dev::grid_dependency_wait();
+  // a launch whose inputs do not depend on the previous grid in the stream
+  // (defer_wait) starts at once and waits for it only before it ends
+  if (!p.defer_wait) kivi_dev::grid_dependency_wait();
   kivi_dev::grid_launch_dependents();
   constexpr int L = G < 32 ? 1 : G / 32;  // lanes per group
   constexpr int SUB = G < 32 ? 32 / G : 1; // groups per thread
@@ -412,6 +417,7 @@ __global__ void __launch_bounds__(kBlockThreads)
     }
     warp_store_units(blk, lane, active && ok, out, y, base, total);
   }
+  if (p.defer_wait) kivi_dev::grid_dependency_wait();
 }
 
 

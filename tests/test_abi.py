@@ -430,3 +430,33 @@ def test_append_accepts_layers_without_store():
     L = _layers(k_codes=None, k_scale=None, k_zero=None, v_codes=None, v_scale=None,
                 v_zero=None)
     assert _append(L, 2, c, 16) == 0 and c.n_res == 16
+
+
+def _append_flush(layers, n_layers, cache, n, stride=None, events=None):
+    kp = (C.c_void_p * n_layers)(*([FAKE] * n_layers))
+    vp = (C.c_void_p * n_layers)(*([FAKE + 65536] * n_layers))
+    stride = n * int(cache.d) if stride is None else stride
+    out = C.c_int64(-7)
+    rc = K.lib().kivi_append_flush(layers, n_layers, C.byref(cache), kp, vp, stride, n,
+                                   C.byref(out), None, events)
+    return rc, out.value
+
+
+def test_append_flush_checks_both_steps_before_launching():
+    """A flush that would overrun the store is refused before the append
+    launches: the state (residual count included) is unchanged."""
+    c = _cache(cap=64, s_q=32, n_res=40)      # 40 + 60 tokens -> flush of 64 into 32 free
+    assert _append_flush(_layers(), 2, c, 60)[0] == 3
+    assert (c.s_q, c.res_head, c.n_res) == (32, 0, 40)
+    c = _cache(n_res=100)
+    assert _append_flush(_layers(), 2, c, 40)[0] == 3          # ring overflow
+    assert c.n_res == 100
+    c = _cache(n_res=0)
+    assert _append_flush(_layers(v_codes=None, v_scale=None, v_zero=None), 2, c, 8)[0] == 1
+    assert _append_flush(_layers(), 2, c, 8, stride=8 * 128 + 4)[0] == 2
+
+
+def test_append_flush_without_sequences_advances_both_steps():
+    c = _cache(bh=0, n_res=32)
+    rc, n = _append_flush(_layers(), 2, c, 64)                 # 96 in the residual -> flush 64
+    assert (rc, n) == (0, 64) and (c.s_q, c.res_head, c.n_res) == (64, 64, 32)

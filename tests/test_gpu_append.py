@@ -21,7 +21,7 @@ if not torch.cuda.is_available():  # pragma: no cover - CPU-only machines
 import kv_cache_quantization_kivi_gb300 as K  # noqa: E402
 
 
-def run_sequence(layers, bh, d, group, bits, r_cap, chunks, strided, seed):
+def run_sequence(layers, bh, d, group, bits, r_cap, chunks, strided, seed, fused=False):
     cap = (sum(chunks) // group + 1) * group
     cache = K.KiviCache(layers, bh, d, r_cap=r_cap, cap=cap, group=group, bits=bits,
                         residual=group)
@@ -49,16 +49,21 @@ def run_sequence(layers, bh, d, group, bits, r_cap, chunks, strided, seed):
             kd = [to_dev(x) for x in ks]
             vd = [to_dev(x) for x in vs]
         wrapped |= (head + n_res) % r_cap + n > r_cap
-        cache.append_all(kd, vd)
         n_res2 = n_res
         for l in range(layers):
             n_res2 = O.append(rings[l][0], rings[l][1], head, n_res, ks[l], vs[l])
+        if fused:
+            # append and flush in one call (the flush's launches overlap the
+            # append's tail when the flushed rows were in the ring before it)
+            n_gpu = cache.append_flush(kd, vd)
+        else:
+            cache.append_all(kd, vd)
+            assert cache.n_res == n_res2
+            for l in range(layers):
+                assert_same(f"key ring {l}", host_u16(cache.k_res[l]), rings[l][0])
+                assert_same(f"value ring {l}", host_u16(cache.v_res[l]), rings[l][1])
+            n_gpu = cache.flush()
         n_res = n_res2
-        assert cache.n_res == n_res
-        for l in range(layers):
-            assert_same(f"key ring {l}", host_u16(cache.k_res[l]), rings[l][0])
-            assert_same(f"value ring {l}", host_u16(cache.v_res[l]), rings[l][1])
-        n_gpu = cache.flush()
         for l in range(layers):
             n_o, s_q2, head2, n_res2 = O.flush(rings[l][0], rings[l][1], stores[l], group,
                                                s_q, head, n_res)
@@ -101,3 +106,24 @@ def test_decode_step_shape():
     flushed one step later, 40 steps."""
     _, s_q = run_sequence(2, 16, 128, 32, 2, 64, [32] * 40, False, seed=311)
     assert s_q == 32 * 39          # the ring's head went round 20 times
+
+
+@pytest.mark.parametrize("bits,group,r_groups", [(2, 32, 3), (4, 64, 4), (8, 16, 5)])
+def test_append_flush_matches_oracle(bits, group, r_groups):
+    """kivi_append_flush over decode-like steps (the flushed rows precede the
+    appended ones: overlapped launches) and prefill-like chunks (some
+    appended tokens flushed at once: the flush waits for the append)."""
+    r_cap = r_groups * group
+    rng = np.random.default_rng(bits + group)
+    chunks, n_res, kinds = [], 0, set()
+    while (len(chunks) < 14 or not {True, False} <= kinds) and len(chunks) < 200:
+        room = r_cap - n_res
+        n = int(rng.choice([group, room, 1 + int(rng.integers(room))]))
+        f = O.flush_size(n_res + n, group, group)
+        kinds.add(f <= n_res if f > 0 else None)
+        chunks.append(n)
+        n_res += n - f
+    assert True in kinds and False in kinds
+    _, s_q = run_sequence(2, 6, 128, group, bits, r_cap, chunks, False, seed=400 + bits + group,
+                          fused=True)
+    assert s_q >= 3 * group
