@@ -169,6 +169,7 @@ struct AttnParams {
   float scale_log2;   // softmax scale * log2(e)
   int32_t sink_cap;   // > 0: the jobs' sink stores are read (see AttnJob)
   float *ws;          // n_split > 1: partial results, see kivi_attention.cu
+  unsigned int *fault;   // device fault word (filled by the launchers)
   AttnJob jobs[KIVI_MAX_LAYERS];
 };
 
@@ -229,9 +230,19 @@ cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits, cuda
 cudaError_t launch_key_quant_staged(const QuantParams &p, int group, int bits, int mode,
                                     cudaStream_t stream, bool *handled);
 // Decode attention (head_dim 128): the main kernel, then (n_split > 1) the
-// combine kernel.
+// combine kernel.  The register-MMA kernel (kivi_attention.cu) serves every
+// call; with KIVI_ATTENTION_KERNEL=tcgen05 in the environment the
+// tensor-memory kernel (kivi_attention_tc.cu) serves the calls without a sink
+// store at G >= 32.
 cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits,
                                     cudaStream_t stream);
+// The tensor-memory kernel: sets *handled = false (and launches nothing)
+// for arguments it does not take.
+cudaError_t launch_decode_attention_tc(const AttnParams &p, int group, int bits,
+                                       cudaStream_t stream, bool *handled);
+// The split combine (n_split > 1): out = sum_s e^(m_s - M) o_s / sum_s
+// e^(m_s - M) l_s per (layer, sequence, query head, channel) from p.ws.
+cudaError_t launch_attention_combine(const AttnParams &p, cudaStream_t stream);
 // Recommended number of splits for `items` (job, bh) pairs of `tiles_store`
 // store tiles each on the current device.
 int attention_splits(int64_t items, int64_t tiles_store, int group, int bits);

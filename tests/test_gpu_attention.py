@@ -39,6 +39,16 @@ import kv_cache_quantization_kivi_gb300 as K  # noqa: E402
 D = 128
 
 
+@pytest.fixture(autouse=True, params=["mma", "tcgen05"])
+def attention_kernel(request, monkeypatch):
+    """Every test runs on both decode-attention kernels: the default
+    register-operand one and the tensor-memory one that
+    KIVI_ATTENTION_KERNEL=tcgen05 selects (read by the library at each call;
+    it takes the calls at G >= 32, the default kernel keeps G = 16)."""
+    monkeypatch.setenv("KIVI_ATTENTION_KERNEL", request.param)
+    return request.param
+
+
 class Pair:
     """A GPU cache and the oracle's mirror of it, filled with the same tokens."""
 
