@@ -420,10 +420,11 @@ KIVI_API kivi_status kivi_sink_restore(const kivi_sink_layer *sinks, int n_layer
  *                   n_split > 1 the partial results go to `workspace`
  *                   (device, kivi_decode_attention_workspace floats) and a
  *                   second launch combines them
- * Supported: d == 128.  s_q + n_res must be at least 1.
+ * Supported: d in {64, 128, 256} (G dividing d).  s_q + n_res must be at
+ * least 1.
  * Kernel: matrix products on the register-operand tensor-core path by
  * default.  With the environment variable KIVI_ATTENTION_KERNEL=tcgen05
- * (read at every call) calls at G >= 32 without a sink store run on the
+ * (read at every call) calls at d == 128 and G >= 32 without a sink store run on the
  * tensor-memory kernel instead (tcgen05 matrix multiplies, accumulators in
  * tensor memory); the results agree to the same bound, and on a GB300 it
  * measured slower at every bits x G, so it is not the default.

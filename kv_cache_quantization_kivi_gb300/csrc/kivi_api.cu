@@ -584,7 +584,6 @@ kivi_status kivi_dequantize_cache_timed(const kivi_layer *layers, int n_layers,
 // decode attention over the packed cache
 // ---------------------------------------------------------------------------
 
-static constexpr int kAttnD = 128;
 static constexpr int kAttnTile = 32;
 static constexpr int kAttnMaxSplit = 64;
 
@@ -592,8 +591,13 @@ struct AttnGeom {
   int64_t h_kv, r, tiles_store, tiles_res;
 };
 
+// head dims of the decode-attention kernels (the value groups must tile the head)
+static bool attn_dim(const kivi_cache *c) {
+  return (c->d == 64 || c->d == 128 || c->d == 256) && c->d % c->group == 0;
+}
+
 static kivi_status attn_geom(const kivi_cache *c, int64_t batch, int32_t h_q, AttnGeom *g) {
-  if (c->d != kAttnD || batch < 1 || c->bh % batch != 0) return KIVI_ERR_INVAL;
+  if (!attn_dim(c) || batch < 1 || c->bh % batch != 0) return KIVI_ERR_INVAL;
   g->h_kv = c->bh / batch;
   if (g->h_kv < 1 || h_q < 1 || h_q % g->h_kv != 0) return KIVI_ERR_INVAL;
   g->r = h_q / g->h_kv;
@@ -616,7 +620,7 @@ int64_t kivi_decode_attention_workspace(const kivi_cache *cache, int n_layers, i
   if (!cache || n_layers < 1 || n_split < 1 || n_split > kAttnMaxSplit) return -1;
   if (attn_geom(cache, batch, h_q, &g) != KIVI_OK) return -1;
   if (n_split == 1) return 0;
-  return sat_mul(sat_mul(sat_mul(n_layers, cache->bh), n_split), g.r * (kAttnD + 2));
+  return sat_mul(sat_mul(sat_mul(n_layers, cache->bh), n_split), g.r * (cache->d + 2));
 }
 
 // Validation and parameter block of a decode-attention call; the workspace
@@ -640,6 +644,7 @@ static kivi_status attn_prepare(const kivi_layer *layers, int n_layers, const ki
 
   std::memset(p, 0, sizeof(*p));
   p->n_jobs = n_layers;
+  p->d = static_cast<int32_t>(cache->d);
   p->r = static_cast<int32_t>(g.r);
   p->h_kv = static_cast<int32_t>(g.h_kv);
   p->n_split = n_split;

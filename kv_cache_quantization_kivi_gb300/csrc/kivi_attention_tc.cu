@@ -676,7 +676,7 @@ cudaError_t tc_launch(const AttnParams &p, cudaStream_t stream) {
 cudaError_t launch_decode_attention_tc(const AttnParams &p, int group, int bits,
                                        cudaStream_t stream, bool *handled) {
   *handled = false;
-  if (p.sink_cap > 0 || p.r > kMaxR || group < 32) return cudaSuccess;
+  if (p.d != kD || p.sink_cap > 0 || p.r > kMaxR || group < 32) return cudaSuccess;
   *handled = true;
   switch (bits * 1000 + group) {
     case 2032: return tc_launch<2, 32>(p, stream);

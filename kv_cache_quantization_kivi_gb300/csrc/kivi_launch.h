@@ -154,6 +154,7 @@ struct AttnJob {
 // split also the residual tiles.
 struct AttnParams {
   int32_t n_jobs;
+  int32_t d;          // head_dim: 64, 128 or 256
   int32_t r;          // query heads per KV head
   int32_t h_kv;       // KV heads per sequence (bh = batch * h_kv)
   int32_t n_split;
@@ -236,8 +237,14 @@ cudaError_t launch_key_quant_staged(const QuantParams &p, int group, int bits, i
 // store at G >= 32.
 cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits,
                                     cudaStream_t stream);
-// The tensor-memory kernel: sets *handled = false (and launches nothing)
-// for arguments it does not take.
+// The register-operand kernels at head_dim 64 and 256 (each in its own
+// translation unit; 128 is in kivi_attention.cu).
+cudaError_t launch_decode_attention_d64(const AttnParams &p, int group, int bits,
+                                        cudaStream_t stream);
+cudaError_t launch_decode_attention_d256(const AttnParams &p, int group, int bits,
+                                         cudaStream_t stream);
+// The tensor-memory kernel (head_dim 128): sets *handled = false (and
+// launches nothing) for arguments it does not take.
 cudaError_t launch_decode_attention_tc(const AttnParams &p, int group, int bits,
                                        cudaStream_t stream, bool *handled);
 // The split combine (n_split > 1): out = sum_s e^(m_s - M) o_s / sum_s

@@ -277,7 +277,12 @@ def _attn(cache, layers=None, n=2, batch=2, h_q=8, scale=0.1, q=None, out=None, 
 
 def test_decode_attention_validation():
     # bh = 4: batch 2 -> h_kv 2; h_q 8 -> r = 4
-    assert _attn(_cache(d=64)) == 1                         # only head_dim 128
+    assert _attn(_cache(d=96)) == 1                         # head_dim 64, 128 or 256 only
+    assert _attn(_cache(d=32)) == 1
+    assert K.lib().kivi_decode_attention_workspace(C.byref(_cache(d=96)), 2, 2, 8, 2) == -1
+    for d in (64, 256):                                      # partials of d + 2 floats
+        assert K.lib().kivi_decode_attention_workspace(C.byref(_cache(d=d)), 2, 2, 8, 2) == \
+            2 * 4 * 2 * 4 * (d + 2)
     assert _attn(_cache(), batch=3) == 1                    # bh % batch
     assert _attn(_cache(), h_q=7) == 1                      # h_q % h_kv
     assert _attn(_cache(), h_q=18) == 1                     # r = 9 > 8
@@ -387,7 +392,7 @@ def test_decode_attention_sinks_validation():
     assert call(_cache(), _sinks(sink_pos=None), cfg()) == 1
     assert call(_cache(), _sinks(sink_k=FAKE + 4), cfg()) == 2
     assert call(_cache(), _sinks(), cfg(reserved=1)) == 1
-    assert call(_cache(d=64), _sinks(), cfg()) == 1             # attention needs head_dim 128
+    assert call(_cache(d=96), _sinks(), cfg()) == 1             # head_dim 64, 128 or 256 only
     assert call(_cache(), _sinks(), cfg(), n_split=2) == 1      # no workspace
     assert L.kivi_decode_attention_sinks(_layers(2), None, 2, C.byref(_cache()), C.byref(cfg()),
                                          2, 8, 0.1, q, out, 1, None, 0, None) == 1

@@ -52,16 +52,16 @@ def attention_kernel(request, monkeypatch):
 class Pair:
     """A GPU cache and the oracle's mirror of it, filled with the same tokens."""
 
-    def __init__(self, layers, bh, bits, group, residual, r_cap, cap, seed, kdist=None):
+    def __init__(self, layers, bh, bits, group, residual, r_cap, cap, seed, kdist=None, d=D):
         self.layers, self.bh, self.bits, self.group = layers, bh, bits, group
         self.residual, self.r_cap, self.cap = residual, r_cap, cap
-        self.cache = K.KiviCache(layers, bh, D, r_cap=r_cap, cap=cap, group=group, bits=bits,
+        self.cache = K.KiviCache(layers, bh, d, r_cap=r_cap, cap=cap, group=group, bits=bits,
                                  residual=residual)
-        self.w = W.custom(seed=seed, batch=1, kv_heads=bh, seq=cap + r_cap, head_dim=D,
+        self.w = W.custom(seed=seed, batch=1, kv_heads=bh, seq=cap + r_cap, head_dim=d,
                           keys=kdist or W.Dist(W.NORMAL, 1.0, n_outliers=4, outlier_mult=15.0))
-        self.ring_k = [np.zeros((bh, r_cap, D), np.uint16) for _ in range(layers)]
-        self.ring_v = [np.zeros((bh, r_cap, D), np.uint16) for _ in range(layers)]
-        self.stores = [O.Store(bh, D, cap, group, bits) for _ in range(layers)]
+        self.ring_k = [np.zeros((bh, r_cap, d), np.uint16) for _ in range(layers)]
+        self.ring_v = [np.zeros((bh, r_cap, d), np.uint16) for _ in range(layers)]
+        self.stores = [O.Store(bh, d, cap, group, bits) for _ in range(layers)]
         self.s_q = self.head = self.n_res = self.pos = 0
 
     def append(self, n_new, flush=True):
@@ -92,9 +92,9 @@ class Pair:
                           self.n_res)
 
 
-def queries(layers, batch, h_q, seed, scale=1.0):
+def queries(layers, batch, h_q, seed, scale=1.0, d=D):
     rng = np.random.default_rng(seed)
-    return (rng.standard_normal((layers, batch, h_q, D)) * scale).astype(np.float16)
+    return (rng.standard_normal((layers, batch, h_q, d)) * scale).astype(np.float16)
 
 
 def run_gpu(pair, q16, batch, n_split=None, sm_scale=None):
@@ -148,6 +148,25 @@ def test_attention_store_and_residual(bits, group):
     assert pair.s_q > 0 and pair.n_res > 0
     q = queries(1, batch, h_kv * r, 7)
     sc = 1.0 / math.sqrt(D)
+    for n_split in (1, 2, 3):
+        check(pair, q, batch, run_gpu(pair, q, batch, n_split=n_split, sm_scale=sc), sc)
+
+
+@pytest.mark.parametrize("d,bits,group", [(64, 2, 16), (64, 2, 32), (64, 4, 64), (64, 8, 32),
+                                          (64, 8, 16), (256, 2, 16), (256, 2, 32), (256, 4, 64),
+                                          (256, 2, 128), (256, 8, 128), (256, 8, 16)])
+def test_attention_head_dims(d, bits, group):
+    """head_dim 64 and 256 (each width, G = 16 with its half-tile store end,
+    the shared 2-bit key tables at G >= 32, and at 256 / 8 bits / G = 16 the
+    one-stage ring): store and residual under 1 to 3 splits, as at 128."""
+    batch, h_kv, r = 2, 2, 4
+    pair = Pair(1, batch * h_kv, bits, group, residual=group, r_cap=4 * group, cap=8 * group,
+                seed=700 + d + bits + group, d=d)
+    for n in (3 * group // 2, group + 5, 2 * group - 3, group + 11):
+        pair.append(n)
+    assert pair.s_q > 0 and pair.n_res > 0
+    q = queries(1, batch, h_kv * r, 17, d=d)
+    sc = 1.0 / math.sqrt(d)
     for n_split in (1, 2, 3):
         check(pair, q, batch, run_gpu(pair, q, batch, n_split=n_split, sm_scale=sc), sc)
 
@@ -256,8 +275,13 @@ def test_attention_rejects_bad_arguments():
         K.kivi_decode_attention(c.layers, 1, c.state, 1, 18, 0.1, [q[0]], [out[0]])  # r > 8
     with pytest.raises(K.KiviError):
         K.kivi_decode_attention(c.layers, 1, c.state, 2, 8, 0.1, [q[0]], [out[0]], n_split=2)
+    c96 = K.KiviCache(1, 2, 96, r_cap=64, cap=128, group=32, bits=2, residual=32)
+    q96 = torch.zeros((2, 8, 96), dtype=torch.float16, device="cuda")
+    o96 = torch.zeros((2, 8, 96), dtype=torch.float32, device="cuda")
+    with pytest.raises(K.KiviError):                                     # head_dim 96
+        K.kivi_decode_attention(c96.layers, 1, c96.state, 2, 8, 0.1, [q96], [o96])
     torch.cuda.synchronize()
-    assert not out.any()
+    assert not out.any() and not o96.any()
 
 
 def fill_decode_store(w, cache, r_cap):

@@ -226,13 +226,14 @@ def attention_bound_check(q16, k, v, got, sm_scale, batch):
     return ref
 
 
-@pytest.mark.parametrize("bits,group", [(2, 32), (4, 64), (8, 16)])
-def test_attention_over_sink_protected_cache(bits, group):
+@pytest.mark.parametrize("bits,group,d", [(2, 32, 128), (4, 64, 128), (8, 16, 128), (2, 16, 64),
+                                          (4, 32, 256)])
+def test_attention_over_sink_protected_cache(bits, group, d):
     """Decode attention over a sink-protected cache equals the oracle's
     attention over the restored cache (store dequantized, sinks' fp16 rows
     put back, residual appended), within the attention bound; without the
     sink store the stored sinks' zeroed slots would be attended instead."""
-    batch, heads, d = 2, 2, 128
+    batch, heads = 2, 2
     pair = SinkPair(2, batch, heads, d, bits, group, group, r_cap=4 * group, cap=16 * group,
                     k_top=6, sink_cap=40, seed=90 + bits + group, plant_every=50)
     pair.append(3 * group)
