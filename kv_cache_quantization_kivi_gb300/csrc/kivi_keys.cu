@@ -14,10 +14,10 @@
 // two-step shuffles.  The arithmetic is the
 // difference-first fast path of kivi_device.cuh with the exact-division
 // fallback; codes are packed along tokens in registers and stored as 8-byte
-// words pairs.  At head_dim 128 and G >= 32 the plain quantize takes the
-// staged kernel instead (kivi_staged.cu: whole tiles streamed into shared
-// memory by a producer warp); this kernel serves G = 16, other head dims,
-// the fused reconstruction and the sink mode.
+// words pairs.  With KIVI_KEY_QUANTIZER=staged in the environment the plain
+// quantize at head_dim 128 and G >= 32 takes the staged kernel instead
+// (kivi_staged.cu: whole tiles streamed into shared memory by a producer
+// warp; see launch_key_quant for why it is not the default).
 //
 // Dequantize: one thread per (layer, bh, group, 8 channels); 16-byte loads of
 // codes, scales and zeros, 16-byte streaming stores.
@@ -25,6 +25,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
@@ -579,11 +581,27 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
 
 #include "kivi_dispatch.h"
 
+// The staged key quantizer (kivi_staged.cu) runs when the environment
+// variable KIVI_KEY_QUANTIZER reads "staged" (read at every call).  Alone it
+// is the faster kernel (28-layer x 4-head x 32 K-token flush: 6281 vs 6060
+// GB/s), but it holds every SM's shared memory and most of its registers, so
+// the value quantizer launched behind it cannot overlap it and the next
+// kernel waits for it to drain: whole flush + dequantize steps measured
+// 3-12% faster on the register kernel (the same flush, the store sweep's
+// nine cells, a 28-layer x 8-head x 4 K-token prefill flush, a 32-token
+// decode flush), so that is the default.
+static bool staged_key_quantizer_selected() {
+  const char *v = std::getenv("KIVI_KEY_QUANTIZER");
+  return v && std::strcmp(v, "staged") == 0;
+}
+
 cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, int mode,
                              cudaStream_t stream) {
-  bool handled = false;
-  const cudaError_t e = launch_key_quant_staged(p, group, bits, mode, stream, &handled);
-  if (handled) return e;
+  if (staged_key_quantizer_selected()) {
+    bool handled = false;
+    const cudaError_t e = launch_key_quant_staged(p, group, bits, mode, stream, &handled);
+    if (handled) return e;
+  }
   KIVI_DISPATCH_MODE(key_quant_launch, p, group, bits, mode, stream);
 }
 

@@ -77,8 +77,18 @@ def _x(bh, s, d, seed, kind, keys=None):
     return W.generate(w, 0, kind)
 
 
+@pytest.fixture(params=["register", "staged"])
+def key_quantizer(request, monkeypatch):
+    """Runs a test on both key quantizers: the default register kernel and
+    the staged one that KIVI_KEY_QUANTIZER=staged selects (read by the
+    library at each call; it takes head_dim 128 at G >= 32 in plain mode,
+    the register kernel keeps the rest)."""
+    monkeypatch.setenv("KIVI_KEY_QUANTIZER", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("bits,group", COMBOS)
-def test_keys_several_tiles_ragged_tail(bits, group):
+def test_keys_several_tiles_ragged_tail(bits, group, key_quantizer):
     check_keys(_x(3, 3 * group + 5, 128, 1000 + bits * group, "k"), group, bits)
 
 
@@ -92,7 +102,7 @@ def test_values_several_rows(bits, group):
     (1, 129, 256, 128, 2), (4, 64, 256, 32, 4), (2, 300, 16, 128, 8), (5, 31, 128, 32, 2),
     (2, 37, 64, 16, 2), (1, 17, 8, 16, 8), (3, 100, 40, 16, 4), (1, 1, 256, 16, 2),
 ], ids=str)
-def test_keys_odd_shapes(shape):
+def test_keys_odd_shapes(shape, key_quantizer):
     bh, s, d, g, b = shape
     check_keys(_x(bh, s, d, 3000 + s + d, "k"), g, b)
 
@@ -107,10 +117,11 @@ def test_values_odd_shapes(shape):
     check_values(_x(bh, s, d, 4000 + s + d, "v"), g, b)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("bits,group", COMBOS)
-def test_keys_degenerate_and_tie_groups(bits, group):
-    rng = np.random.default_rng(bits * 7 + group)
-    bh, d = 2, 64
+def test_keys_degenerate_and_tie_groups(bits, group, d, key_quantizer):
+    rng = np.random.default_rng(bits * 7 + group + d)
+    bh = 2
     blocks = [hard_block(rng, group, d) for _ in range(bh * 3)]
     x = np.stack([np.concatenate(blocks[3 * b:3 * b + 3], axis=0) for b in range(bh)])
     check_keys(x.astype(np.float16).view(np.uint16), group, bits)
@@ -125,7 +136,7 @@ def test_values_degenerate_and_tie_groups(bits, group):
     check_values(x.astype(np.float16).view(np.uint16), group, bits)
 
 
-def test_strided_inputs_and_outputs():
+def test_strided_inputs_and_outputs(key_quantizer):
     bh, s, d, g, b = 3, 96, 128, 32, 4
     x = _x(bh, s, d, 55, "k")
     big = torch.zeros((bh, s + 40, d), dtype=torch.float16, device="cuda")
@@ -165,7 +176,7 @@ def test_determinism():
         assert np.array_equal(u, v)
 
 
-def test_tiny_flush_config_end_to_end():
+def test_tiny_flush_config_end_to_end(key_quantizer):
     """The tiny flush workload: 8 heads x 128 tokens, 2-bit, G=R=32; the flush
     moves 96 tokens and keeps 32 in fp16; keys and values also quantized as
     full tensors."""
@@ -205,7 +216,7 @@ def compare_store(cache, layer: int, st) -> None:
 
 @pytest.mark.parametrize("bits,group,residual", [(4, 32, 32), (8, 64, 64), (2, 128, 32),
                                                   (2, 16, 16), (8, 16, 32)])
-def test_multi_layer_flush_sequence_with_ring_wrap(bits, group, residual):
+def test_multi_layer_flush_sequence_with_ring_wrap(bits, group, residual, key_quantizer):
     layers, bh, d = 3, 4, 128
     r_cap = 3 * group + (residual // group + 1) * group
     cap = 16 * group
@@ -252,7 +263,7 @@ def test_multi_layer_flush_sequence_with_ring_wrap(bits, group, residual):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["llama3_2_3b_prefill", "qwen2_5_7b_long"])
-def test_prefill_flush_full_size_sampled(name):
+def test_prefill_flush_full_size_sampled(name, key_quantizer):
     """All layers' residual windows hold the whole prompt; one flush (one
     launch per tensor kind over every layer) moves all but the newest
     tokens; the store is then dequantized in one launch per kind."""
@@ -302,7 +313,7 @@ def test_prefill_flush_full_size_sampled(name):
 
 
 @pytest.mark.slow
-def test_large_store_sweep_full_size_sampled():
+def test_large_store_sweep_full_size_sampled(key_quantizer):
     w = W.CONFIGS["large_store_sweep"]
     k = W.generate(w, 0, "k")
     v = W.generate(w, 0, "v")
@@ -349,7 +360,7 @@ def test_large_store_sweep_full_size_sampled():
 
 
 @pytest.mark.slow
-def test_batched_decode_flushes_full_size_sampled():
+def test_batched_decode_flushes_full_size_sampled(key_quantizer):
     """32 layers x 512 sequences: a store already holding 2048 tokens per
     sequence, a 64-token ring holding 32 fp16 tokens; each step appends 32
     tokens and the flush (one launch per kind over all layers) moves the 32
