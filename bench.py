@@ -57,9 +57,13 @@ FALLBACK_HBM_GBS = 6800.0
 _COMMON_FILES = ("kivi_api.cu", "kivi_device.cuh", "kivi_arith.cuh", "kivi_launch.h",
                  "kivi_dispatch.h")
 CSRC_FILES = {
-    "flush": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu"),
-    "attention": _COMMON_FILES + ("kivi_attention.cu",),
-    "sink": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu", "kivi_sink.cu"),
+    "flush": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu", "kivi_staged.cu",
+                              "kivi_ring.cu"),
+    "attention": _COMMON_FILES + ("kivi_expand.cuh", "kivi_attention_kernel.cuh",
+                                  "kivi_attention.cu", "kivi_attention_d64.cu",
+                                  "kivi_attention_d256.cu", "kivi_attention_tc.cu"),
+    "sink": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu", "kivi_staged.cu",
+                             "kivi_sink.cu"),
 }
 
 

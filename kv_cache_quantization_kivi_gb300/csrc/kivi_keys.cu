@@ -14,10 +14,9 @@
 // two-step shuffles.  The arithmetic is the
 // difference-first fast path of kivi_device.cuh with the exact-division
 // fallback; codes are packed along tokens in registers and stored as 8-byte
-// words pairs.  With KIVI_KEY_QUANTIZER=staged in the environment the plain
-// quantize at head_dim 128 and G >= 32 takes the staged kernel instead
-// (kivi_staged.cu: whole tiles streamed into shared memory by a producer
-// warp; see launch_key_quant for why it is not the default).
+// words pairs.  The plain quantize at head_dim 128 takes the staged kernel
+// instead (kivi_staged.cu: whole tiles streamed into shared memory by a
+// producer warp) at G = 128 and at 2-bit G = 64 (see launch_key_quant).
 //
 // Dequantize: one thread per (layer, bh, group, 8 channels); 16-byte loads of
 // codes, scales and zeros, 16-byte streaming stores.
@@ -581,23 +580,29 @@ cudaError_t key_dequant_launch(const DequantParams &p, cudaStream_t stream) {
 
 #include "kivi_dispatch.h"
 
-// The staged key quantizer (kivi_staged.cu) runs when the environment
-// variable KIVI_KEY_QUANTIZER reads "staged" (read at every call).  Alone it
-// is the faster kernel (28-layer x 4-head x 32 K-token flush: 6281 vs 6060
-// GB/s), but it holds every SM's shared memory and most of its registers, so
-// the value quantizer launched behind it cannot overlap it and the next
-// kernel waits for it to drain: whole flush + dequantize steps measured
-// 3-12% faster on the register kernel (the same flush, the store sweep's
-// nine cells, a 28-layer x 8-head x 4 K-token prefill flush, a 32-token
-// decode flush), so that is the default.
-static bool staged_key_quantizer_selected() {
+// Which key quantizer a plain quantize takes.  By measurement of whole flush
+// + dequantize steps on a GB300, each pair on one box: the staged kernel
+// (kivi_staged.cu) at G = 128, and at G = 64 with 2-bit codes (store sweep
+// cells 2/64 +1.5%, 2/128 +3%, 4/128 and 8/128 level), the register kernel
+// everywhere else (4-bit G = 64 flush of 28 layers x 4 heads x 32 K tokens
+// +0.6%, 2-bit G = 32 prefill flush +3.3% and decode flush +4%, the G = 32
+// and 4/8-bit G = 64 sweep cells +0.6-1.2%).  The staged kernel is the
+// faster one alone at every G >= 32 but holds every SM's shared memory and
+// most of its registers, so the kernels around it cannot overlap it; the
+// register kernel's cost grows with G (G / 32 lanes per column exchanging
+// extremes), so the staged one gains where G is large and the codes narrow.
+// KIVI_KEY_QUANTIZER=staged or =register in the environment (read at every
+// call) takes that kernel wherever it applies.
+static bool staged_key_quantizer(int group, int bits) {
   const char *v = std::getenv("KIVI_KEY_QUANTIZER");
-  return v && std::strcmp(v, "staged") == 0;
+  if (v && std::strcmp(v, "staged") == 0) return true;
+  if (v && std::strcmp(v, "register") == 0) return false;
+  return group == 128 || (bits == 2 && group >= 64);
 }
 
 cudaError_t launch_key_quant(const QuantParams &p, int group, int bits, int mode,
                              cudaStream_t stream) {
-  if (staged_key_quantizer_selected()) {
+  if (staged_key_quantizer(group, bits)) {
     bool handled = false;
     const cudaError_t e = launch_key_quant_staged(p, group, bits, mode, stream, &handled);
     if (handled) return e;

@@ -79,10 +79,11 @@ def _x(bh, s, d, seed, kind, keys=None):
 
 @pytest.fixture(params=["register", "staged"])
 def key_quantizer(request, monkeypatch):
-    """Runs a test on both key quantizers: the default register kernel and
-    the staged one that KIVI_KEY_QUANTIZER=staged selects (read by the
-    library at each call; it takes head_dim 128 at G >= 32 in plain mode,
-    the register kernel keeps the rest)."""
+    """Runs a test on both key quantizers, forced by KIVI_KEY_QUANTIZER
+    (read by the library at each call): the register kernel and the staged
+    one (which takes head_dim 128 at G >= 32 in plain mode; the register
+    kernel keeps the rest).  Without the variable the library picks by G and
+    width."""
     monkeypatch.setenv("KIVI_KEY_QUANTIZER", request.param)
     return request.param
 
