@@ -27,7 +27,8 @@
 // then:
 //   S^T = K Q^T     m16n8k16 tensor-core MMAs: A = key tile (16 tokens x 16
 //                   channels, ldmatrix), B = the query heads
-//   online softmax  per head column, base-2 exponent with the scale folded in
+//   online softmax  per head column, base-2 exponent with the scale folded in;
+//                   the reference moves only when a score exceeds it by > 2^3
 //   O^T += V^T P^T  A = value tile (16 channels x 16 tokens, ldmatrix), B =
 //                   P^T from the score accumulators through movmatrix
 // P is scaled by 2^12 and split into fp16 high and low parts (two MMAs), so
@@ -59,6 +60,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kTile = 32;          // tokens per tile (one pipeline stage)
 constexpr int kHalf = 16;          // tokens expanded and attended at a time
 constexpr float kPScale = 4096.0f; // P * 2^12 stays a normal fp16 down to P = 2^-26
+constexpr float kTau = 3.0f;       // a score at most 2^3 above the reference: P * 2^12 <= 2^15
 constexpr uint64_t kWaitLimitNs = 200000000ull;  // 0.2 s per pipeline wait
 
 // Shared-memory stage of one store tile (byte offsets).
@@ -349,30 +351,48 @@ template <int D>
 __device__ __forceinline__ void half_softmax(SoftState<D> &st, float (&s)[4], float scale_log2,
                                              int valid, int g, uint32_t (&phi)[2],
                                              uint32_t (&plo)[2]) {
-  float mt[2] = {-INFINITY, -INFINITY};
+  // The reference m of a head column moves only when a score of the half
+  // exceeds it by more than kTau (one warp vote; always at the first half):
+  // then it becomes the running maximum and the output and sum are
+  // rescaled.  P = 2^(s - m) * 2^12 <= 2^15 stays a finite fp16, and o and l
+  // are relative to the same m, so the result is that of any reference.
+  bool over = false;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int tok = g + (i >= 2 ? 8 : 0);
     const float v = tok < valid ? s[i] * scale_log2 : -INFINITY;
     s[i] = v;
-    mt[i & 1] = fmaxf(mt[i & 1], v);
+    over |= v > st.m[i & 1] + kTau;
   }
+  if (__any_sync(0xffffffffu, over)) {
+    float mt[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mt[0] = fmaxf(mt[0], __shfl_xor_sync(0xffffffffu, mt[0], off));
-    mt[1] = fmaxf(mt[1], __shfl_xor_sync(0xffffffffu, mt[1], off));
-  }
-  float mn[2], alpha[2];
+    for (int i = 0; i < 4; ++i) mt[i & 1] = fmaxf(mt[i & 1], s[i]);
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    mn[j] = fmaxf(st.m[j], mt[j]);
-    alpha[j] = mn[j] == -INFINITY ? 1.0f : exp2f(st.m[j] - mn[j]);
-    st.m[j] = mn[j];
+    for (int off = 4; off < 32; off <<= 1) {
+      mt[0] = fmaxf(mt[0], __shfl_xor_sync(0xffffffffu, mt[0], off));
+      mt[1] = fmaxf(mt[1], __shfl_xor_sync(0xffffffffu, mt[1], off));
+    }
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float mn = fmaxf(st.m[j], mt[j]);
+      alpha[j] = mn == -INFINITY ? 1.0f : exp2f(st.m[j] - mn);
+      st.m[j] = mn;
+      st.l[j] *= alpha[j];
+    }
+#pragma unroll
+    for (int mc = 0; mc < D / 16; ++mc) {
+      st.o[mc][0] *= alpha[0];
+      st.o[mc][1] *= alpha[1];
+      st.o[mc][2] *= alpha[0];
+      st.o[mc][3] *= alpha[1];
+    }
   }
   float p[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float m = mn[i & 1];
+    const float m = st.m[i & 1];
     p[i] = m == -INFINITY ? 0.0f : exp2f(s[i] - m) * kPScale;
   }
   const __half2 h0 = __floats2half2_rn(p[0], p[1]);   // token g: heads 2t, 2t+1
@@ -383,18 +403,8 @@ __device__ __forceinline__ void half_softmax(SoftState<D> &st, float (&s)[4], fl
   phi[1] = movmatrix_trans(h2_as_u32(h1));
   plo[0] = movmatrix_trans(h2_as_u32(l0));
   plo[1] = movmatrix_trans(h2_as_u32(l1));
-  st.l[0] = st.l[0] * alpha[0] + (p[0] + p[2]);
-  st.l[1] = st.l[1] * alpha[1] + (p[1] + p[3]);
-  // once the running maximum settles most steps leave it unchanged (alpha 1)
-  if (__any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
-#pragma unroll
-    for (int mc = 0; mc < D / 16; ++mc) {
-      st.o[mc][0] *= alpha[0];
-      st.o[mc][1] *= alpha[1];
-      st.o[mc][2] *= alpha[0];
-      st.o[mc][3] *= alpha[1];
-    }
-  }
+  st.l[0] += p[0] + p[2];
+  st.l[1] += p[1] + p[3];
 }
 
 // O^T += V^T P^T from the row-major value half tile in `buf`.
