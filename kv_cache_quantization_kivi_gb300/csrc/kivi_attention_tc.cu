@@ -2,7 +2,7 @@
 // fifth-generation tensor cores (tcgen05 matrix multiply with the
 // accumulators in tensor memory).
 //
-// What it computes is that of decode_attention_kernel (kivi_attention.cu):
+// What it computes is that of decode_attention_kernel (kivi_attention_kernel.cuh):
 // for every layer, sequence and query head, softmax(scale * q K^T) V over the
 // cache's store tokens (dequantized on chip, bit-identical to the dequantize
 // kernels' fp16 reconstructions) followed by its fp16 residual tokens, query

@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kKeyThreads, key_min_blocks<BITS>()) key_quant
     const bool full = active && rows_here >= TPT;
     // debug builds: every row this thread reads (padded rows included) lies
     // inside its bh slice
-    const int64_t r_first = row0 + static_cast<int64_t>(k.split) * TPT;
+    [[maybe_unused]] const int64_t r_first = row0 + static_cast<int64_t>(k.split) * TPT;
     const bool x_ok = KIVI_BOUND(
         p.fault, !active || (k.b < p.bh && r_first + min(0, rows_here - 1) >= 0 &&
                              (r_first + (rows_here >= 1 ? min(rows_here, TPT) : rows_here)) * D <=

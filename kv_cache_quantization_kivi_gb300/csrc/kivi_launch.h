@@ -169,7 +169,7 @@ struct AttnParams {
   int64_t n_res;
   float scale_log2;   // softmax scale * log2(e)
   int32_t sink_cap;   // > 0: the jobs' sink stores are read (see AttnJob)
-  float *ws;          // n_split > 1: partial results, see kivi_attention.cu
+  float *ws;          // n_split > 1: partial results, see kivi_attention_kernel.cuh
   unsigned int *fault;   // device fault word (filled by the launchers)
   AttnJob jobs[KIVI_MAX_LAYERS];
 };
@@ -230,10 +230,11 @@ cudaError_t launch_key_dequant(const DequantParams &p, int group, int bits, cuda
 // Sets *handled = false (and launches nothing) for arguments it does not take.
 cudaError_t launch_key_quant_staged(const QuantParams &p, int group, int bits, int mode,
                                     cudaStream_t stream, bool *handled);
-// Decode attention (head_dim 128): the main kernel, then (n_split > 1) the
-// combine kernel.  The register-MMA kernel (kivi_attention.cu) serves every
-// call; with KIVI_ATTENTION_KERNEL=tcgen05 in the environment the
-// tensor-memory kernel (kivi_attention_tc.cu) serves the calls without a sink
+// Decode attention (head_dim 64, 128 or 256): the main kernel, then
+// (n_split > 1) the combine kernel.  The register-MMA kernel
+// (kivi_attention_kernel.cuh) serves every call; with
+// KIVI_ATTENTION_KERNEL=tcgen05 in the environment the tensor-memory kernel
+// (kivi_attention_tc.cu) serves the calls at head_dim 128 without a sink
 // store at G >= 32.
 cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits,
                                     cudaStream_t stream);

@@ -200,7 +200,6 @@ __global__ void __launch_bounds__(KeyStaged<G>::kThreads, 1)
   constexpr int P = C::P, U = C::U, S = C::S;
   constexpr bool RECON = MODE == kQuantRecon;
   constexpr int W = CodeFmt<BITS>::W;   // codes per word
-  constexpr int H = 16 / BITS;          // rows per half-word
   const float qf = static_cast<float>(CodeFmt<BITS>::Q);
 
   extern __shared__ __align__(128) uint8_t ring[];
