@@ -333,3 +333,56 @@ def test_sink_prefill_full_size_as_benchmarked():
         O.sink_restore(kref, vref, st)
         assert_same("restored keys", host_u16(wl.k_out[l]), kref)
         assert_same("restored values", host_u16(wl.v_out[l]), vref)
+
+
+class TiedPair(SinkPair):
+    """Key rows copied: in each sequence the tokens at `ties[b]` get the same
+    high-norm key row in every head, so their scores are equal bit for bit
+    and the ranking falls to the positions."""
+
+    def __init__(self, *args, ties, **kw):
+        super().__init__(*args, **kw)
+        self.ties = ties
+
+    def tokens(self, l, kind, n):
+        x = super().tokens(l, kind, n)
+        if kind == "k":
+            f = x.view(np.float16).astype(np.float32)
+            for b, pos in enumerate(self.ties):
+                hs = slice(b * self.heads, (b + 1) * self.heads)
+                row = f[hs, pos[0] - self.pos] * 20.0
+                for t in pos:
+                    f[hs, t - self.pos] = row
+            x = np.ascontiguousarray(f.astype(np.float16).view(np.uint16))
+        return x
+
+
+def test_sink_top_k_ties_across_and_within_tiles():
+    """Seven tokens with the same score and k = 5: the five earliest win.
+    Sequence 0 spreads them over three 32-token score tiles (two, three and
+    two of them), sequence 1 puts all seven in one tile, sequence 2 puts one
+    in each of seven tiles; the ranked top-k and everything after it equal
+    the oracle's."""
+    ties = [(5, 6, 33, 40, 63, 100, 127), (64, 65, 66, 67, 68, 69, 70),
+            (3, 35, 67, 99, 131, 163, 195)]
+    pair = TiedPair(2, len(ties), 2, 128, 2, 32, 32, r_cap=256, cap=256, k_top=5, sink_cap=8,
+                    seed=31, ties=ties)
+    pair.append(256)
+    for l in range(pair.layers):
+        tp = pair.sinks.top_pos[l].cpu().numpy()
+        for b, pos in enumerate(ties):
+            assert list(tp[b, :5]) == list(pos[:5]), (l, b, tp[b])
+    pair.check()
+
+
+@pytest.mark.parametrize("k_top,plant_every", [(8, 6), (20, 10), (64, 4)])
+def test_sink_many_tiles_dense_candidates(k_top, plant_every):
+    """Many high-norm tokens (one in `plant_every`) over 16 score tiles per
+    sequence, so that most tiles hold several of the sequence's top-k: k = 8
+    (the score blocks select), 20 and 64 (the select kernel); a second update
+    and flush merge into the kept top-k."""
+    pair = SinkPair(2, 2, 2, 128, 4, 64, 64, r_cap=512, cap=1024, k_top=k_top,
+                    sink_cap=2 * k_top + 8, seed=k_top, plant_every=plant_every)
+    pair.append(512)
+    pair.append(448)
+    pair.check()
