@@ -252,10 +252,33 @@ struct RegTop8 {
   }
 };
 
+// A list head as a ranking key: sb = the score's bits + 1 (scores are
+// finite and non-negative, so their bit patterns order as unsigned
+// integers; 0 = no candidate) and the position.
+struct HeadKey {
+  uint32_t sb;
+  int64_t pos;
+};
+
+// The best key over the 32 lanes of a warp (largest score, then smallest
+// position), by three warp reductions: the largest score, then among the
+// lanes holding it the smallest high and low position words (positions are
+// non-negative).
+__device__ __forceinline__ HeadKey warp_best(uint32_t sb, int64_t pos) {
+  const uint32_t best = __reduce_max_sync(0xffffffffu, sb);
+  const uint32_t hi = static_cast<uint32_t>(static_cast<uint64_t>(pos) >> 32);
+  const uint32_t lo = static_cast<uint32_t>(static_cast<uint64_t>(pos));
+  const bool in = sb == best;
+  const uint32_t bhi = __reduce_min_sync(0xffffffffu, in ? hi : 0xFFFFFFFFu);
+  const uint32_t blo = __reduce_min_sync(0xffffffffu, in && hi == bhi ? lo : 0xFFFFFFFFu);
+  return {best, static_cast<int64_t>((static_cast<uint64_t>(bhi) << 32) | blo)};
+}
+
 // block = (job, sequence): the new scores and the kept top-k merged.  Each
 // of the NT threads keeps the best k of its strided share; k rounds of a
-// block-wide argmax over the threads' list heads (shuffles within each warp,
-// then across the warps' winners in warp 0) give the k best overall.
+// block-wide argmax over the threads' list heads (warp reductions within
+// each warp, then across the warps' winners in warp 0) give the k best
+// overall.
 template <typename List, int NT>
 __global__ void __launch_bounds__(NT) sink_select_kernel(const __grid_constant__ SinkParams p) {
   kivi_dev::grid_dependency_wait();
@@ -266,10 +289,8 @@ __global__ void __launch_bounds__(NT) sink_select_kernel(const __grid_constant__
   const SinkJob &J = p.jobs[job];
   __shared__ float new_s[kMaxSinkTop];
   __shared__ int64_t new_p[kMaxSinkTop];
-  __shared__ float red_s[NW];
+  __shared__ uint32_t red_sb[NW];
   __shared__ int64_t red_p[NW];
-  __shared__ int red_i[NW];
-  __shared__ int winner;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = p.k_top;
   List lt;
@@ -294,47 +315,30 @@ __global__ void __launch_bounds__(NT) sink_select_kernel(const __grid_constant__
       if (i < p.n) lt.offer(v[b], p.s_q + p.i0 + i, k);
     }
   }
-  // best of (bs, bp, owner) over the 32 lanes of a warp; owner < 0: none
-  auto warp_best = [](float &bs, int64_t &bp, int &owner) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-      const int64_t op = __shfl_xor_sync(0xffffffffu, bp, off);
-      const int oo = __shfl_xor_sync(0xffffffffu, owner, off);
-      if (oo >= 0 && (owner < 0 || ranks_before(os, op, bs, bp))) {
-        bs = os; bp = op; owner = oo;
-      }
-    }
-  };
   const int64_t avail = tn + p.n;
   const int keep = avail < k ? static_cast<int>(avail) : k;
   for (int j = 0; j < keep; ++j) {
     const bool have = lt.has();
-    float bs = have ? lt.hs() : 0.0f;
-    int64_t bp = have ? lt.hq() : 0;
-    int owner = have ? tid : -1;
-    warp_best(bs, bp, owner);
+    const uint32_t sb = have ? __float_as_uint(lt.hs()) + 1u : 0u;
+    const int64_t hp = have ? lt.hq() : INT64_MAX;
+    const HeadKey wk = warp_best(sb, hp);
     if (lane == 0) {
-      red_s[warp] = bs;
-      red_p[warp] = bp;
-      red_i[warp] = owner;
+      red_sb[warp] = wk.sb;
+      red_p[warp] = wk.pos;
     }
     __syncthreads();
     if (warp == 0) {
-      float ws = lane < NW ? red_s[lane] : 0.0f;
-      int64_t wp = lane < NW ? red_p[lane] : 0;
-      int wo = lane < NW ? red_i[lane] : -1;
-      warp_best(ws, wp, wo);
+      const HeadKey bk = warp_best(lane < NW ? red_sb[lane] : 0u, lane < NW ? red_p[lane] : INT64_MAX);
       if (lane == 0) {
-        new_s[j] = ws;
-        new_p[j] = wp;
-        winner = wo;
+        new_s[j] = __uint_as_float(bk.sb - 1u);
+        new_p[j] = bk.pos;
       }
     }
     __syncthreads();
-    // every thread reads `winner` here, before it reaches the next round's
-    // first barrier, after which alone warp 0 writes it again
-    if (winner == tid) lt.pop();
+    // the one thread whose list head is the winner (positions are unique)
+    // takes it off; warp 0 writes the next round's entry only after the
+    // next barrier
+    if (have && sb == __float_as_uint(new_s[j]) + 1u && hp == new_p[j]) lt.pop();
   }
   if (tid < keep) {
     J.top_score[seq * p.k_top + tid] = new_s[tid];
