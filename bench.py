@@ -61,7 +61,8 @@ CSRC_FILES = {
                               "kivi_ring.cu"),
     "attention": _COMMON_FILES + ("kivi_expand.cuh", "kivi_attention_kernel.cuh",
                                   "kivi_attention.cu", "kivi_attention_d64.cu",
-                                  "kivi_attention_d256.cu", "kivi_attention_tc.cu"),
+                                  "kivi_attention_d256.cu", "kivi_tc_common.cuh",
+                                  "kivi_attention_ws.cu"),
     "sink": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu", "kivi_staged.cu",
                              "kivi_sink.cu"),
 }

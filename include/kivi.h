@@ -424,10 +424,12 @@ KIVI_API kivi_status kivi_sink_restore(const kivi_sink_layer *sinks, int n_layer
  * least 1.
  * Kernel: matrix products on the register-operand tensor-core path by
  * default.  With the environment variable KIVI_ATTENTION_KERNEL=tcgen05
- * (read at every call) calls at d == 128 and G >= 32 without a sink store run on the
- * tensor-memory kernel instead (tcgen05 matrix multiplies, accumulators in
- * tensor memory); the results agree to the same bound, and on a GB300 it
- * measured slower at every bits x G, so it is not the default.
+ * (read at every call) calls at d == 128 and G >= 32 with at most 8 query
+ * heads per KV head and without a sink store run on the tensor-memory
+ * kernel instead (warp-specialised and persistent: tcgen05 matrix
+ * multiplies issued by one thread, accumulators in tensor memory); the
+ * results agree to the same bound, and on a GB300 it measured slower than
+ * the default at every bits x G, so it is not the default.
  * Returns KIVI_OK, KIVI_ERR_INVAL, KIVI_ERR_ALIGN or KIVI_ERR_CUDA. */
 KIVI_API kivi_status kivi_decode_attention(const kivi_layer *layers, int n_layers,
                                            const kivi_cache *cache, int64_t batch, int32_t h_q,

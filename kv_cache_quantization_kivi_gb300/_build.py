@@ -22,10 +22,11 @@ DEBUG_LIB_PATH = os.path.join(OUT_DIR, "libkivi_debug.so")
 HEADER = os.path.join(ROOT, "include", "kivi.h")
 
 SOURCES = ["kivi_api.cu", "kivi_keys.cu", "kivi_values.cu", "kivi_attention.cu",
-           "kivi_attention_d64.cu", "kivi_attention_d256.cu", "kivi_attention_tc.cu", "kivi_sink.cu",
+           "kivi_attention_d64.cu", "kivi_attention_d256.cu", "kivi_attention_ws.cu",
+           "kivi_sink.cu",
            "kivi_ring.cu", "kivi_staged.cu"]
 HEADERS = ["kivi_device.cuh", "kivi_arith.cuh", "kivi_launch.h", "kivi_dispatch.h",
-           "kivi_expand.cuh", "kivi_attention_kernel.cuh"]
+           "kivi_expand.cuh", "kivi_attention_kernel.cuh", "kivi_tc_common.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -72,8 +72,9 @@ cudaError_t launch_attention_combine(const AttnParams &p, cudaStream_t stream) {
 
 // The kernel the environment variable KIVI_ATTENTION_KERNEL selects: the
 // register-operand kernel unless it reads "tcgen05", which selects the
-// tensor-memory kernel (kivi_attention_tc.cu) for the calls that kernel
-// takes.  Read at every call, so a process can switch between calls.
+// warp-specialised tensor-memory kernel (kivi_attention_ws.cu) for the calls
+// that kernel takes.  Read at every call, so a process can switch between
+// calls.
 static bool tensor_memory_kernel_selected() {
   const char *v = std::getenv("KIVI_ATTENTION_KERNEL");
   return v && std::strcmp(v, "tcgen05") == 0;
@@ -82,7 +83,7 @@ static bool tensor_memory_kernel_selected() {
 cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits, cudaStream_t stream) {
   if (tensor_memory_kernel_selected()) {
     bool handled = false;
-    const cudaError_t e = launch_decode_attention_tc(p, group, bits, stream, &handled);
+    const cudaError_t e = launch_decode_attention_ws(p, group, bits, stream, &handled);
     if (handled) return e;
   }
   switch (p.d) {

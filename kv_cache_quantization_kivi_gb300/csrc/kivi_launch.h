@@ -234,7 +234,7 @@ cudaError_t launch_key_quant_staged(const QuantParams &p, int group, int bits, i
 // (n_split > 1) the combine kernel.  The register-MMA kernel
 // (kivi_attention_kernel.cuh) serves every call; with
 // KIVI_ATTENTION_KERNEL=tcgen05 in the environment the tensor-memory kernel
-// (kivi_attention_tc.cu) serves the calls at head_dim 128 without a sink
+// (kivi_attention_ws.cu) serves the calls at head_dim 128 without a sink
 // store at G >= 32.
 cudaError_t launch_decode_attention(const AttnParams &p, int group, int bits,
                                     cudaStream_t stream);
@@ -244,9 +244,10 @@ cudaError_t launch_decode_attention_d64(const AttnParams &p, int group, int bits
                                         cudaStream_t stream);
 cudaError_t launch_decode_attention_d256(const AttnParams &p, int group, int bits,
                                          cudaStream_t stream);
-// The tensor-memory kernel (head_dim 128): sets *handled = false (and
+// The warp-specialised persistent tensor-memory kernel (kivi_attention_ws.cu;
+// head_dim 128, G >= 32, no sink store, r <= 8): sets *handled = false (and
 // launches nothing) for arguments it does not take.
-cudaError_t launch_decode_attention_tc(const AttnParams &p, int group, int bits,
+cudaError_t launch_decode_attention_ws(const AttnParams &p, int group, int bits,
                                        cudaStream_t stream, bool *handled);
 // The split combine (n_split > 1): out = sum_s e^(m_s - M) o_s / sum_s
 // e^(m_s - M) l_s per (layer, sequence, query head, channel) from p.ws.

@@ -42,7 +42,7 @@ D = 128
 @pytest.fixture(autouse=True, params=["mma", "tcgen05"])
 def attention_kernel(request, monkeypatch):
     """Every test runs on both decode-attention kernels: the default
-    register-operand one and the tensor-memory one that
+    register-operand one and the warp-specialised tensor-memory one that
     KIVI_ATTENTION_KERNEL=tcgen05 selects (read by the library at each call;
     it takes the calls at G >= 32, the default kernel keeps G = 16)."""
     monkeypatch.setenv("KIVI_ATTENTION_KERNEL", request.param)
