@@ -147,14 +147,20 @@ struct Item {
   int pc0, n_pc;     // store pieces [pc0, pc0 + n_pc)
   int n_st, n_rt;    // store tiles (four pieces each) and residual tiles
 };
+// (32-bit divisions: layers x bh x splits < 2^31, host-checked)
 __device__ __forceinline__ Item item_of(const AttnParams &p, int64_t item) {
   Item it;
-  const int split = static_cast<int>(item % p.n_split);
-  const int64_t pair = item / p.n_split;
-  it.job = static_cast<int>(pair / p.bh);
-  it.bhi = pair - static_cast<int64_t>(it.job) * p.bh;
-  it.b = it.bhi / p.h_kv;
-  it.kvh = it.bhi - it.b * p.h_kv;
+  const uint32_t u = static_cast<uint32_t>(item), ns = static_cast<uint32_t>(p.n_split);
+  const uint32_t bh = static_cast<uint32_t>(p.bh), hkv = static_cast<uint32_t>(p.h_kv);
+  const uint32_t pair = u / ns;
+  const int split = static_cast<int>(u - pair * ns);
+  const uint32_t job = pair / bh;
+  const uint32_t bhi = pair - job * bh;
+  const uint32_t b = bhi / hkv;
+  it.job = static_cast<int>(job);
+  it.bhi = bhi;
+  it.b = b;
+  it.kvh = bhi - b * hkv;
   it.pc0 = split * p.tiles_per_split;
   it.n_pc = max(0, min(it.pc0 + p.tiles_per_split, p.tiles_store) - it.pc0);
   it.n_st = (it.n_pc + 3) / 4;
@@ -426,6 +432,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
   } else {
     // ---------------- softmax, output (warps 2..5; 128 threads)
     const int sw = warp - kSoftWarp0;            // 0..3
+    const int r = p.r;
     const int quarter = warp & 3;                // tensor-memory lanes 32 quarter ..
     const int slot = 32 * quarter + lane;        // token slot (scores), channel slot (output)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
@@ -463,8 +470,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
         const bool real = slot < valid && ok;
         bool vote = false;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          sc[j] = real ? sc[j] * p.scale_log2 : -INFINITY;
+        for (int j = 0; j < 8; ++j) {   // heads past r: zero query rows, P = 0
+          sc[j] = real && j < r ? sc[j] * p.scale_log2 : -INFINITY;
           vote |= sc[j] > m_ref[j] + kTau;
         }
         if (soft_any(!ok)) {
@@ -523,13 +530,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_attention_ws_kernel(cons
         float pf[8];
 #pragma unroll
         for (int j = 0; j < 8; j += 2) {
-          pf[j] = sc[j] == -INFINITY ? 0.0f : ex2_approx(sc[j] - m_ref[j] + kLog2PScale);
-          pf[j + 1] = sc[j + 1] == -INFINITY ? 0.0f : ex2_approx(sc[j + 1] - m_ref[j + 1] + kLog2PScale);
-          const __half2 hh = __floats2half2_rn(pf[j], pf[j + 1]);
-          const float2 hf = __half22float2(hh);
-          const __half2 ll = __floats2half2_rn(pf[j] - hf.x, pf[j + 1] - hf.y);
-          hi2[j / 2] = h2_as_u32(hh);
-          lo2[j / 2] = h2_as_u32(ll);
+          if (j < r) {   // (r is uniform: pairs past it skip the exponentials)
+            pf[j] = sc[j] == -INFINITY ? 0.0f : ex2_approx(sc[j] - m_ref[j] + kLog2PScale);
+            pf[j + 1] = sc[j + 1] == -INFINITY ? 0.0f : ex2_approx(sc[j + 1] - m_ref[j + 1] + kLog2PScale);
+            const __half2 hh = __floats2half2_rn(pf[j], pf[j + 1]);
+            const float2 hf = __half22float2(hh);
+            const __half2 ll = __floats2half2_rn(pf[j] - hf.x, pf[j + 1] - hf.y);
+            hi2[j / 2] = h2_as_u32(hh);
+            lo2[j / 2] = h2_as_u32(ll);
+          } else {
+            pf[j] = pf[j + 1] = 0.0f;
+            hi2[j / 2] = lo2[j / 2] = 0u;
+          }
         }
         const uint32_t row = pop_(b) + p_row(slot);
         sts128(row, make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]));
