@@ -58,13 +58,13 @@ _COMMON_FILES = ("kivi_api.cu", "kivi_device.cuh", "kivi_arith.cuh", "kivi_launc
                  "kivi_dispatch.h")
 CSRC_FILES = {
     "flush": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu", "kivi_staged.cu",
-                              "kivi_ring.cu"),
+                              "kivi_ring.cu", "kivi_expand.cuh"),
     "attention": _COMMON_FILES + ("kivi_expand.cuh", "kivi_attention_kernel.cuh",
                                   "kivi_attention.cu", "kivi_attention_d64.cu",
                                   "kivi_attention_d256.cu", "kivi_tc_common.cuh",
                                   "kivi_attention_ws.cu"),
     "sink": _COMMON_FILES + ("kivi_keys.cu", "kivi_values.cu", "kivi_staged.cu",
-                             "kivi_sink.cu"),
+                             "kivi_sink.cu", "kivi_expand.cuh"),
 }
 
 

@@ -427,16 +427,19 @@ __global__ void __launch_bounds__(kThreads) sink_restore_kernel(const __grid_con
   const SinkJob &J = p.jobs[job];
   const int64_t c = r % chunks, hj = r / chunks;
   const int64_t h = hj % p.heads, j = hj / p.heads;
-  if (j >= J.sink_count[seq]) return;
-  const int64_t t = J.sink_pos[seq * p.sink_cap + j];
-  if (t < 0 || t >= p.out_rows) return;
+  // the count, the slot's position and its rows are read together (slot j <
+  // sink_cap lies inside every array whether or not it is in use), so the
+  // thread waits for one round trip instead of three
   const int64_t bb = seq * p.heads + h;
   const int64_t src = (bb * p.sink_cap + j) * p.d + 8 * c;
+  const int cnt = J.sink_count[seq];
+  const int64_t t = J.sink_pos[seq * p.sink_cap + j];
+  const uint4 kv = *reinterpret_cast<const uint4 *>(static_cast<const __half *>(J.sink_k) + src);
+  const uint4 vv = *reinterpret_cast<const uint4 *>(static_cast<const __half *>(J.sink_v) + src);
+  if (j >= cnt || t < 0 || t >= p.out_rows) return;
   const int64_t dst = (bb * p.out_rows + t) * p.d + 8 * c;
-  *reinterpret_cast<uint4 *>(static_cast<__half *>(J.k_out) + dst) =
-      *reinterpret_cast<const uint4 *>(static_cast<const __half *>(J.sink_k) + src);
-  *reinterpret_cast<uint4 *>(static_cast<__half *>(J.v_out) + dst) =
-      *reinterpret_cast<const uint4 *>(static_cast<const __half *>(J.sink_v) + src);
+  *reinterpret_cast<uint4 *>(static_cast<__half *>(J.k_out) + dst) = kv;
+  *reinterpret_cast<uint4 *>(static_cast<__half *>(J.v_out) + dst) = vv;
 }
 
 unsigned blocks_for(int64_t threads) {

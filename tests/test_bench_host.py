@@ -91,3 +91,36 @@ def test_cpu_sample_times_each_oracle_function():
     elems = w.bh * pf.n * w.head_dim
     assert done == 4 * elems * bench.bytes_per_elem(w.bits, w.group) and secs > 0
     assert what.startswith("1 of 1 layers") and "dequantize_values" in what
+
+
+def test_every_kernel_source_is_built_and_hashed():
+    """Every file under csrc/ is compiled (a translation unit) or tracked as
+    a header by the build, and every file the kernels of a workload family
+    include is in that family's hash (bench.py CSRC_FILES), so a committed
+    ncu traffic figure goes stale whenever a kernel it measured changes."""
+    import re
+    import kv_cache_quantization_kivi_gb300._build as B
+    bench = load_bench()
+    csrc = B.CSRC
+    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    assert sorted(B.SOURCES + B.HEADERS) == files
+    inc = re.compile(r'#include "([^"/]+)"')
+
+    def closure(names):
+        seen, todo = set(), list(names)
+        while todo:
+            f = todo.pop()
+            if f in seen or not os.path.exists(os.path.join(csrc, f)):
+                continue
+            seen.add(f)
+            todo += inc.findall(open(os.path.join(csrc, f)).read())
+        return seen
+
+    fams = bench.CSRC_FILES
+    for fam, tus in {"flush": ["kivi_keys.cu", "kivi_values.cu", "kivi_staged.cu", "kivi_ring.cu"],
+                     "attention": ["kivi_attention.cu", "kivi_attention_d64.cu",
+                                   "kivi_attention_d256.cu", "kivi_attention_ws.cu"],
+                     "sink": ["kivi_sink.cu", "kivi_keys.cu", "kivi_values.cu",
+                              "kivi_staged.cu"]}.items():
+        missing = closure(tus) - set(fams[fam])
+        assert not missing, (fam, missing)
