@@ -35,12 +35,20 @@ struct RowRef {
   uint32_t k;  // 32-channel chunk within the row
 };
 
-// unit = ((job * bh + b) * rows + r) * chunks + k   (all < 2^31, host-checked)
-template <typename P>
+// unit = ((job * bh + b) * rows + r) * chunks + k   (all < 2^31, host-checked);
+// DC > 0: head_dim DC known at compile time, chunks = DC / 32
+template <int DC = 0, typename P>
 __device__ __forceinline__ RowRef decode_unit(uint32_t u, const P &p) {
   RowRef t;
-  const uint32_t row = p.div_chunks.div(u);
-  t.k = u - row * p.div_chunks.d;
+  uint32_t row;
+  if constexpr (DC > 0 && ((DC / 32) & (DC / 32 - 1)) == 0) {   // a power of two
+    constexpr uint32_t CH = DC / 32;
+    row = u / CH;
+    t.k = u % CH;
+  } else {
+    row = p.div_chunks.div(u);
+    t.k = u - row * p.div_chunks.d;
+  }
   const uint32_t jb = p.div_rows.div(row);
   t.r = row - jb * p.div_rows.d;
   const uint32_t job = p.div_bh.div(jb);
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(kBlockThreads, PF ? 3 : 4)
   auto fetch = [&](uint32_t b0) {
     const uint32_t u = b0 + lane;
     an = u < total;
-    tn = decode_unit(an ? u : b0, p);
+    tn = decode_unit<DC>(an ? u : b0, p);
     int64_t phys = tn.r;
     if (p.ring > 0) {
       phys += p.head;
